@@ -1,0 +1,112 @@
+"""Token-balanced split-KV schedule, restated with plain loops.
+
+The pages split each row's cache into ``num_kv_splits`` contiguous ranges and
+combine the partials afterwards (submission 722089, ``_mla_multihead_stage1``:
+``tokens_per_split = ceil(kv_len / NUM_SPLITS)``, split s covers
+``[s * tps, min((s + 1) * tps, kv_len))``; submission 663509 and 738050 build
+"work" and "reduce" maps for a persistent kernel with ``get_mla_metadata_v1``
+from ``qo_indptr`` / ``kv_indptr`` at a token granularity ``kv_granularity``).
+
+The schedule here is the persistent, token-balanced form of that split, fixed
+as follows (the pages print no formula for their persistent work map):
+
+* every row is cut into tiles of ``TILE_TOKENS`` tokens, ``ceil(L_b / 128)``
+  tiles, the last one partial; the tiles of all rows, row after row, form one
+  global sequence of ``T`` tiles;
+* the grid has ``G = max(1, min(num_sms, B * ceil(max_kv_len / 128)))`` workers;
+  worker c takes the contiguous tile range ``[floor(c T / G), floor((c+1) T / G))``;
+* the part of a row inside one worker's range is a segment; a row covered by a
+  single worker is "whole", otherwise "split" and each of its segments writes a
+  partial (normalised output and base-2 log-sum-exp) to a workspace slot:
+  slot ``2c`` when worker c's range begins inside that row, else ``2c + 1``.
+
+This module is the restatement the CUDA path's schedule must match bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+TILE_TOKENS = 128
+
+
+def ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def plan_grid(batch: int, max_kv_len: int, num_sms: int) -> int:
+    """Number of persistent workers for a batch of ``batch`` rows."""
+    upper = batch * ceil_div(max(0, max_kv_len), TILE_TOKENS)
+    return max(1, min(num_sms, upper))
+
+
+def row_tiles(kv_indptr) -> list[int]:
+    """Tiles per row; a decreasing indptr counts as an empty row."""
+    out = []
+    for b in range(len(kv_indptr) - 1):
+        length = int(kv_indptr[b + 1]) - int(kv_indptr[b])
+        out.append(ceil_div(length, TILE_TOKENS) if length > 0 else 0)
+    return out
+
+
+def schedule(kv_indptr, grid: int) -> dict:
+    """Per-worker ranges, per-row covers and segment list, by enumeration."""
+    tiles = row_tiles(kv_indptr)
+    prefix = [0]
+    for n in tiles:
+        prefix.append(prefix[-1] + n)
+    total = prefix[-1]
+
+    workers = []
+    for c in range(grid):
+        t0 = (c * total) // grid
+        t1 = ((c + 1) * total) // grid
+        workers.append({"t0": t0, "t1": t1, "first_row": -1, "last_row": -1})
+
+    # Which workers touch which row: enumerate every tile.
+    owner = []                       # owner[t] = worker holding global tile t
+    for c, w in enumerate(workers):
+        owner.extend([c] * (w["t1"] - w["t0"]))
+    assert len(owner) == total
+
+    covers = {}                      # row -> ordered list of workers
+    segments = []
+    for b, n in enumerate(tiles):
+        ws = []
+        for t in range(prefix[b], prefix[b] + n):
+            if not ws or ws[-1] != owner[t]:
+                ws.append(owner[t])
+        covers[b] = ws
+    for c, w in enumerate(workers):
+        rows = [b for b in range(len(tiles)) if c in covers[b]]
+        if rows:
+            w["first_row"], w["last_row"] = rows[0], rows[-1]
+        for b in rows:
+            j0 = max(w["t0"], prefix[b]) - prefix[b]
+            j1 = min(w["t1"], prefix[b + 1]) - prefix[b]
+            split = len(covers[b]) > 1
+            slot = -1
+            if split:
+                slot = 2 * c if w["t0"] >= prefix[b] else 2 * c + 1
+            segments.append({"worker": c, "row": b, "tile_begin": j0, "tile_end": j1,
+                             "split": split, "slot": slot})
+    return {"grid": grid, "total_tiles": total, "prefix": prefix, "workers": workers,
+            "covers": covers, "segments": segments}
+
+
+def token_segments(kv_indptr, grid: int) -> dict:
+    """Row -> list of row-local token ranges, in the form ``mla_decode_split_ref`` takes."""
+    sch = schedule(kv_indptr, grid)
+    out = {}
+    for s in sch["segments"]:
+        b = s["row"]
+        length = int(kv_indptr[b + 1]) - int(kv_indptr[b])
+        out.setdefault(b, []).append((s["tile_begin"] * TILE_TOKENS,
+                                      min(length, s["tile_end"] * TILE_TOKENS)))
+    return out
+
+
+def worker_table(kv_indptr, grid: int) -> np.ndarray:
+    """int64 ``[grid, 4]``: (t0, t1, first_row, last_row) per worker."""
+    sch = schedule(kv_indptr, grid)
+    return np.array([[w["t0"], w["t1"], w["first_row"], w["last_row"]] for w in sch["workers"]],
+                    dtype=np.int64).reshape(grid, 4)
