@@ -1,0 +1,164 @@
+/*
+ * libmla_decode — decode step of DeepSeek-R1-style Multi-head Latent Attention
+ * (forward_absorb path) over an FP8 per-tensor-scaled latent cache, for sm_103a.
+ *
+ * What one call computes (kernelbot-amd-mixed-mla submission 738050, comment
+ * block above its mla_decode_fwd call; constants of submission 663509):
+ *
+ *     out[t, h, :] = softmax_j( q[t, h, :] . K[j, :] / sqrt(576) ) @ V[j, :]
+ *
+ * for every batch row b with its single query token t = qo_indptr[b], over the
+ * cached tokens j of that row.  q has 16 heads of 576 dims (512 latent + 64
+ * rope); the one shared KV head stores 576 e4m3fn codes per token with a single
+ * float32 scale (value = code * scale); K is all 576 dims of a cache row and V
+ * its first 512.  The output is bf16 [T, 16, 512].
+ *
+ * All pointers named "device" are CUDA device pointers; every buffer is owned
+ * and allocated by the caller.  The library never allocates, frees or
+ * synchronises on the forward path: all work is ordered on `stream`.
+ * Functions return MLA_OK or an mla_status_t describing a host-detected error,
+ * in which case nothing was launched.  Errors that need the data to detect are
+ * recorded as bits in the workspace error word (MLA_DERR_*), readable with
+ * mla_decode_read_error.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_NUM_HEADS 16
+#define MLA_QK_HEAD_DIM 576
+#define MLA_V_HEAD_DIM 512
+#define MLA_TILE_TOKENS 128
+#define MLA_ABI_VERSION 1
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,         /* null / misaligned pointer, bad size, plan mismatch  */
+  MLA_ERR_UNSUPPORTED = 2,         /* device is not sm_103 / lacks the shared memory      */
+  MLA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < plan->ws_bytes                    */
+  MLA_ERR_CUDA = 4                 /* a CUDA runtime or driver call failed                */
+} mla_status_t;
+
+/* Bits of the device-side error word (sticky until cleared). */
+#define MLA_DERR_QO_INDPTR 1  /* a row does not hold exactly one query token in [0, batch) */
+#define MLA_DERR_KV_INDPTR 2  /* kv_indptr decreases, or its end exceeds kv_rows / kv_indices_len */
+#define MLA_DERR_KV_INDEX 4   /* a page-table entry lies outside [0, kv_rows)                */
+#define MLA_DERR_TIMEOUT 8    /* a pipeline wait ran past its time limit; the call gave up  */
+
+/*
+ * Launch plan for a batch shape.  The split-KV schedule (flash-decoding split,
+ * submission 722089 `_mla_multihead_stage1`; the persistent work maps of
+ * submissions 663509 and 738050) is fixed analytically here: rows are cut into
+ * tiles of 128 tokens, the tiles of all rows form one sequence of T tiles, and
+ * `grid` persistent workers take equal contiguous ranges of it.  A row covered
+ * by more than one worker is combined by the second stage.
+ */
+typedef struct {
+  int32_t batch;       /* B, rows (one query token each)                          */
+  int32_t max_kv_len;  /* upper bound on any row's cached tokens (sizes the grid)  */
+  int32_t num_sms;     /* SMs the grid is sized for                               */
+  int32_t grid;        /* persistent stage-1 workers: max(1, min(num_sms, B*ceil(max_kv_len/128))) */
+  int32_t tile_tokens; /* 128                                                      */
+  int32_t abi_version; /* MLA_ABI_VERSION                                          */
+  uint64_t ws_bytes;   /* workspace bytes mla_decode_fwd needs                      */
+  uint64_t ws_prefix_offset;  /* int32[B+1]   tile prefix over rows                 */
+  uint64_t ws_workers_offset; /* int32[grid*4] (t0, t1, first_row, last_row) / worker */
+  uint64_t ws_lse_offset;     /* float[2*grid*16] base-2 log-sum-exp of partials    */
+  uint64_t ws_partial_offset; /* float[2*grid*16*512] normalised split partials     */
+} mla_plan_t;
+
+/*
+ * mla_decode_plan — pure host function, re-entrant.
+ *   batch >= 1, max_kv_len >= 0.  num_sms > 0 sizes the grid for that many SMs;
+ *   num_sms <= 0 queries the current device's SM count.
+ *   Fills *plan.  Returns MLA_ERR_INVALID_ARG for bad sizes / null plan.
+ */
+mla_status_t mla_decode_plan(int32_t batch, int32_t max_kv_len, int32_t num_sms, mla_plan_t* plan);
+
+/*
+ * mla_decode_fwd — the decode step: stage 1 (split attention) then stage 2
+ * (log-sum-exp combine of split rows), both on `stream`.
+ *   q_bf16     device, bf16 [B, 16, 576] row-major, 16-byte aligned.
+ *   kv_fp8     device, e4m3fn codes [kv_rows, 576] (= [kv_rows, 1, 576]), 16-byte aligned.
+ *              Codes must be finite (0x7F / 0xFF never appear).
+ *   kv_scale   device, float[1]; a code's value is code * (*kv_scale).
+ *   qo_indptr  device, int32 [B+1]; row b's query token is qo_indptr[b], and
+ *              qo_indptr[b+1] - qo_indptr[b] must be 1 (decode, qseqlen 1).
+ *   kv_indptr  device, int32 [B+1], non-decreasing; row b owns the flattened
+ *              tokens [kv_indptr[b], kv_indptr[b+1]).  A row with no token
+ *              yields an all-zero output row.
+ *   out_bf16   device, bf16 [B, 16, 512], 16-byte aligned.  Fully overwritten.
+ *   stream     CUDA stream (0 = legacy default stream).
+ *   plan       from mla_decode_plan for this batch size.
+ *   kv_indices device int32 page table (page size 1): flattened token j lives in
+ *              cache row kv_indices[j].  NULL means row j (identity).
+ *   kv_indices_len  entries in kv_indices (ignored when it is NULL).
+ *   kv_rows    rows in the cache pool kv_fp8 (>= 1).
+ *   workspace  device scratch of at least plan->ws_bytes, 256-byte aligned.
+ *              Zero it once after allocating (mla_decode_workspace_init) so the
+ *              error word starts clear.  Calls sharing a workspace must not
+ *              overlap on the GPU.
+ * Output is deterministic for a given plan.  Returns MLA_OK after launching.
+ */
+mla_status_t mla_decode_fwd(const void* q_bf16, const void* kv_fp8, const float* kv_scale,
+                            const int32_t* qo_indptr, const int32_t* kv_indptr, void* out_bf16,
+                            cudaStream_t stream, const mla_plan_t* plan,
+                            const int32_t* kv_indices, int64_t kv_indices_len, int64_t kv_rows,
+                            void* workspace, size_t workspace_bytes);
+
+/* The two stages of mla_decode_fwd launched separately (same arguments); the
+ * pair is equivalent to one mla_decode_fwd call.  Used to time stage 1 alone. */
+mla_status_t mla_decode_stage1(const void* q_bf16, const void* kv_fp8, const float* kv_scale,
+                               const int32_t* qo_indptr, const int32_t* kv_indptr, void* out_bf16,
+                               cudaStream_t stream, const mla_plan_t* plan,
+                               const int32_t* kv_indices, int64_t kv_indices_len, int64_t kv_rows,
+                               void* workspace, size_t workspace_bytes);
+mla_status_t mla_decode_stage2(const int32_t* qo_indptr, void* out_bf16, cudaStream_t stream,
+                               const mla_plan_t* plan, void* workspace, size_t workspace_bytes);
+
+/*
+ * mla_fp8_quantize_per_tensor — per-tensor absmax quantisation of a bf16 tensor
+ * to e4m3fn (input preparation; the pages' harness supplies the cache already
+ * quantised this way: submission 722089 `quantize_fp8`, submission 738050
+ * `_quantize_fp8`):  scale = max(max|x|, 1e-12) / 448 and
+ * code = e4m3fn_rn_satfinite(x / scale), both divisions IEEE float32.
+ *   src_bf16  device bf16 [n];  dst_fp8 device uint8 [n];
+ *   scale_out device float[1];  tmp device scratch of >= 16 bytes.
+ * Two kernels and one 4-byte memset on `stream`.
+ */
+mla_status_t mla_fp8_quantize_per_tensor(const void* src_bf16, int64_t n, void* dst_fp8,
+                                         float* scale_out, void* tmp, size_t tmp_bytes,
+                                         cudaStream_t stream);
+
+/* Zero a workspace (cudaMemsetAsync of ws_bytes on `stream`). */
+mla_status_t mla_decode_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Read (and, when clear != 0, reset) the device error word of a workspace.
+ * Synchronises `stream`; off the hot path. */
+mla_status_t mla_decode_read_error(void* workspace, int32_t* err_host, int32_t clear,
+                                   cudaStream_t stream);
+
+/*
+ * mla_decode_schedule_host — the stage-1 schedule computed on the host from a
+ * host copy of kv_indptr, with the same integer formulas the kernel uses.
+ *   workers_out int32 [grid*4]: (t0, t1, first_row, last_row) per worker
+ *   (first_row = last_row = -1 for an empty range); prefix_out int32 [B+1]:
+ *   tiles before each row.  Pure host; for tests and tools.
+ */
+mla_status_t mla_decode_schedule_host(const int32_t* kv_indptr_host, int32_t batch, int32_t grid,
+                                      int32_t* workers_out, int32_t* prefix_out);
+
+const char* mla_status_string(mla_status_t status);
+int32_t mla_decode_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_DECODE_H */

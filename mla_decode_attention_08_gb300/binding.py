@@ -1,0 +1,196 @@
+"""ctypes binding of libmla_decode (argument marshalling only).
+
+Every function here forwards to the C ABI declared in ``include/mla_decode.h``
+under the same name.  Tensors must already live on a CUDA device: there is no
+CPU path, and a missing library raises instead of falling back.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB as LIB_PATH
+
+NUM_HEADS, QK_HEAD_DIM, V_HEAD_DIM, TILE_TOKENS = 16, 576, 512, 128
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported device", 3: "workspace too small",
+          4: "CUDA call failed"}
+DERR = {1: "qo_indptr", 2: "kv_indptr", 4: "kv_index", 8: "timeout"}
+
+
+class MlaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+class mla_plan_t(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("max_kv_len", ctypes.c_int32),
+                ("num_sms", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("tile_tokens", ctypes.c_int32), ("abi_version", ctypes.c_int32),
+                ("ws_bytes", ctypes.c_uint64), ("ws_prefix_offset", ctypes.c_uint64),
+                ("ws_workers_offset", ctypes.c_uint64), ("ws_lse_offset", ctypes.c_uint64),
+                ("ws_partial_offset", ctypes.c_uint64)]
+
+
+_VP, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+_PLANP = ctypes.POINTER(mla_plan_t)
+_FWD_ARGS = [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _PLANP, _VP, _I64, _I64, _VP, _SZ]
+SIGNATURES = {
+    "mla_decode_plan": (ctypes.c_int, [_I32, _I32, _I32, _PLANP]),
+    "mla_decode_fwd": (ctypes.c_int, _FWD_ARGS),
+    "mla_decode_stage1": (ctypes.c_int, _FWD_ARGS),
+    "mla_decode_stage2": (ctypes.c_int, [_VP, _VP, _VP, _PLANP, _VP, _SZ]),
+    "mla_fp8_quantize_per_tensor": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP, _SZ, _VP]),
+    "mla_decode_workspace_init": (ctypes.c_int, [_VP, _SZ, _VP]),
+    "mla_decode_read_error": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int32), _I32, _VP]),
+    "mla_decode_schedule_host": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP]),
+    "mla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "mla_decode_abi_version": (ctypes.c_int32, []),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmla_decode.so (raises when it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                               "(python -m mla_decode_attention_08_gb300.build)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise MlaError(fn, status)
+
+
+def _dev_ptr(t: Optional[torch.Tensor], name: str, dtype=None) -> Optional[int]:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def mla_decode_plan(batch: int, max_kv_len: int, num_sms: int = 0) -> mla_plan_t:
+    plan = mla_plan_t()
+    _check("mla_decode_plan", load_library().mla_decode_plan(batch, max_kv_len, num_sms,
+                                                            ctypes.byref(plan)))
+    return plan
+
+
+def _fwd_args(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream, plan, kv_indices,
+              workspace):
+    if kv_fp8.dim() == 3:
+        kv_fp8 = kv_fp8.reshape(kv_fp8.shape[0], -1)
+    kv_rows = int(kv_fp8.shape[0])
+    return (_dev_ptr(q, "q", torch.bfloat16), _dev_ptr(kv_fp8, "kv_fp8"),
+            _dev_ptr(kv_scale, "kv_scale", torch.float32),
+            _dev_ptr(qo_indptr, "qo_indptr", torch.int32),
+            _dev_ptr(kv_indptr, "kv_indptr", torch.int32), _dev_ptr(out, "out", torch.bfloat16),
+            _stream(stream), ctypes.byref(plan),
+            _dev_ptr(kv_indices, "kv_indices", torch.int32),
+            0 if kv_indices is None else int(kv_indices.numel()), kv_rows,
+            _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size())
+
+
+def mla_decode_fwd(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream=None, *, plan,
+                   workspace, kv_indices=None) -> torch.Tensor:
+    """Decode step; writes ``out`` (bf16 [B, 16, 512]) and returns it."""
+    _check("mla_decode_fwd", load_library().mla_decode_fwd(
+        *_fwd_args(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream, plan, kv_indices,
+                   workspace)))
+    return out
+
+
+def mla_decode_stage1(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream=None, *, plan,
+                      workspace, kv_indices=None) -> None:
+    _check("mla_decode_stage1", load_library().mla_decode_stage1(
+        *_fwd_args(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream, plan, kv_indices,
+                   workspace)))
+
+
+def mla_decode_stage2(qo_indptr, out, stream=None, *, plan, workspace) -> None:
+    _check("mla_decode_stage2", load_library().mla_decode_stage2(
+        _dev_ptr(qo_indptr, "qo_indptr", torch.int32), _dev_ptr(out, "out", torch.bfloat16),
+        _stream(stream), ctypes.byref(plan), _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size()))
+
+
+def mla_fp8_quantize_per_tensor(src_bf16, dst_fp8, scale_out, tmp, stream=None) -> None:
+    """e4m3fn codes of a bf16 tensor with a per-tensor absmax scale (float32 [1])."""
+    _check("mla_fp8_quantize_per_tensor", load_library().mla_fp8_quantize_per_tensor(
+        _dev_ptr(src_bf16, "src", torch.bfloat16), src_bf16.numel(), _dev_ptr(dst_fp8, "dst"),
+        _dev_ptr(scale_out, "scale_out", torch.float32), _dev_ptr(tmp, "tmp"),
+        tmp.numel() * tmp.element_size(), _stream(stream)))
+
+
+def mla_decode_workspace_init(workspace, stream=None) -> None:
+    _check("mla_decode_workspace_init", load_library().mla_decode_workspace_init(
+        _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def mla_decode_read_error(workspace, clear: bool = True, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _check("mla_decode_read_error", load_library().mla_decode_read_error(
+        _dev_ptr(workspace, "workspace"), ctypes.byref(v), int(clear), _stream(stream)))
+    return int(v.value)
+
+
+def mla_decode_schedule_host(kv_indptr, grid: int):
+    """(workers int32 [grid, 4], prefix int32 [B + 1]) from a host kv_indptr."""
+    import numpy as np
+    ind = np.ascontiguousarray(np.asarray(kv_indptr, dtype=np.int32))
+    batch = ind.shape[0] - 1
+    workers = np.zeros((grid, 4), dtype=np.int32)
+    prefix = np.zeros(batch + 1, dtype=np.int32)
+    _check("mla_decode_schedule_host", load_library().mla_decode_schedule_host(
+        ind.ctypes.data, batch, grid, workers.ctypes.data, prefix.ctypes.data))
+    return workers, prefix
+
+
+def new_workspace(plan: mla_plan_t, device=None) -> torch.Tensor:
+    """A zeroed uint8 workspace of plan.ws_bytes on ``device`` (256-byte aligned)."""
+    ws = torch.zeros(int(plan.ws_bytes), dtype=torch.uint8, device=device or "cuda")
+    assert ws.data_ptr() % 256 == 0
+    return ws
+
+
+def workspace_views(plan: mla_plan_t, ws: torch.Tensor) -> dict:
+    """Typed views of the workspace regions (for tests and tools)."""
+    g, b = int(plan.grid), int(plan.batch)
+
+    def view(off, n, dtype):
+        size = torch.tensor([], dtype=dtype).element_size()
+        return ws[off:off + n * size].view(dtype)
+
+    return {"err": view(0, 1, torch.int32),
+            "prefix": view(plan.ws_prefix_offset, b + 1, torch.int32),
+            "workers": view(plan.ws_workers_offset, 4 * g, torch.int32).view(g, 4),
+            "lse": view(plan.ws_lse_offset, 2 * g * 16, torch.float32).view(2 * g, 16),
+            "partial": view(plan.ws_partial_offset, 2 * g * 16 * 512,
+                            torch.float32).view(2 * g, 16, 512)}

@@ -1,0 +1,338 @@
+// Host side of libmla_decode: plan, argument checks, TMA descriptors, launches.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mla_decode.h"
+#include "kernels.h"
+#include "schedule.h"
+
+namespace {
+
+using mla::kNumHeads;
+using mla::kQkDim;
+using mla::kTileTokens;
+using mla::kVDim;
+
+constexpr uint64_t kAlign = 256;
+uint64_t round_up(uint64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Rows of the [kv_rows, 576] uint8 cache: box_w bytes wide, box_h rows high.
+bool encode_kv_map(CUtensorMap* map, const void* kv, int64_t rows, uint32_t box_w, uint32_t box_h,
+                   CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kQkDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kQkDim)};
+  const cuuint32_t box[2] = {box_w, box_h};
+  const cuuint32_t estride[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), gdim, gstride, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Small per-thread cache of encoded descriptors: the same cache pool is
+// normally decoded step after step.
+struct MapEntry {
+  const void* kv = nullptr;
+  int64_t rows = 0;
+  bool gather = false;
+  int device = -1;
+  CUtensorMap v, r;
+};
+
+bool kv_maps(const void* kv, int64_t rows, bool gather, int device, CUtensorMap* v, CUtensorMap* r) {
+  constexpr int kEntries = 8;
+  thread_local MapEntry cache[kEntries];
+  thread_local int next = 0;
+  for (auto& e : cache) {
+    if (e.kv == kv && e.rows == rows && e.gather == gather && e.device == device) {
+      *v = e.v;
+      *r = e.r;
+      return true;
+    }
+  }
+  MapEntry e;
+  e.kv = kv;
+  e.rows = rows;
+  e.gather = gather;
+  e.device = device;
+  const uint32_t h = gather ? 1u : static_cast<uint32_t>(kTileTokens);
+  if (!encode_kv_map(&e.v, kv, rows, 128, h, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
+  if (!encode_kv_map(&e.r, kv, rows, 64, h, CU_TENSOR_MAP_SWIZZLE_64B)) return false;
+  cache[next] = e;
+  next = (next + 1) % kEntries;
+  *v = e.v;
+  *r = e.r;
+  return true;
+}
+
+// Checks the current device is an sm_103 part and sets the kernels' shared
+// memory limit once per device.
+mla_status_t prepare_device(int* device_out) {
+  static std::atomic<int> ready[64];
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return MLA_ERR_CUDA;
+  if (device < 0 || device >= 64) return MLA_ERR_UNSUPPORTED;
+  *device_out = device;
+  if (ready[device].load(std::memory_order_acquire) == 1) return MLA_OK;
+  int major = 0, minor = 0, smem = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (major != 10 || minor != 3) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<size_t>(smem) < mla::stage1_smem_bytes()) return MLA_ERR_UNSUPPORTED;
+  if (mla::stage1_prepare(device) != cudaSuccess) return MLA_ERR_CUDA;
+  ready[device].store(1, std::memory_order_release);
+  return MLA_OK;
+}
+
+mla_status_t check_plan(const mla_plan_t* plan) {
+  if (plan == nullptr || plan->abi_version != MLA_ABI_VERSION || plan->batch < 1 ||
+      plan->grid < 1 || plan->tile_tokens != kTileTokens || plan->max_kv_len < 0)
+    return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+mla_status_t check_workspace(const mla_plan_t* plan, void* workspace, size_t workspace_bytes) {
+  if (workspace == nullptr || !aligned(workspace, kAlign)) return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->ws_bytes) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  return MLA_OK;
+}
+
+mla::Stage2Params stage2_params(const int32_t* qo_indptr, void* out, const mla_plan_t* plan,
+                                void* workspace) {
+  auto* ws = static_cast<uint8_t*>(workspace);
+  mla::Stage2Params s;
+  s.qo_indptr = qo_indptr;
+  s.out = static_cast<uint16_t*>(out);
+  s.err = reinterpret_cast<int32_t*>(ws);
+  s.prefix = reinterpret_cast<const int32_t*>(ws + plan->ws_prefix_offset);
+  s.lse = reinterpret_cast<const float*>(ws + plan->ws_lse_offset);
+  s.partial = reinterpret_cast<const float*>(ws + plan->ws_partial_offset);
+  s.batch = plan->batch;
+  s.grid = plan->grid;
+  return s;
+}
+
+mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
+                        const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
+                        cudaStream_t stream, const mla_plan_t* plan, const int32_t* kv_indices,
+                        int64_t kv_indices_len, int64_t kv_rows, void* workspace,
+                        size_t workspace_bytes) {
+  mla_status_t st = check_plan(plan);
+  if (st != MLA_OK) return st;
+  if (q == nullptr || kv == nullptr || kv_scale == nullptr || qo_indptr == nullptr ||
+      kv_indptr == nullptr || out == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16)) return MLA_ERR_INVALID_ARG;
+  if (kv_rows < 1 || kv_rows > INT32_MAX) return MLA_ERR_INVALID_ARG;
+  if (kv_indices != nullptr && (kv_indices_len < 0 || kv_indices_len > INT32_MAX))
+    return MLA_ERR_INVALID_ARG;
+  st = check_workspace(plan, workspace, workspace_bytes);
+  if (st != MLA_OK) return st;
+  int device = 0;
+  st = prepare_device(&device);
+  if (st != MLA_OK) return st;
+
+  const bool gather = kv_indices != nullptr;
+  CUtensorMap map_v, map_r;
+  if (!kv_maps(kv, kv_rows, gather, device, &map_v, &map_r)) return MLA_ERR_CUDA;
+
+  auto* ws = static_cast<uint8_t*>(workspace);
+  mla::Stage1Params p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.kv_scale = kv_scale;
+  p.qo_indptr = qo_indptr;
+  p.kv_indptr = kv_indptr;
+  p.kv_indices = kv_indices;
+  p.out = static_cast<uint16_t*>(out);
+  p.err = reinterpret_cast<int32_t*>(ws);
+  p.prefix = reinterpret_cast<int32_t*>(ws + plan->ws_prefix_offset);
+  p.workers = reinterpret_cast<int32_t*>(ws + plan->ws_workers_offset);
+  p.lse = reinterpret_cast<float*>(ws + plan->ws_lse_offset);
+  p.partial = reinterpret_cast<float*>(ws + plan->ws_partial_offset);
+  p.kv_rows = kv_rows;
+  p.kv_indices_len = gather ? kv_indices_len : 0;
+  p.batch = plan->batch;
+  p.grid = plan->grid;
+  return mla::launch_stage1(p, map_v, map_r, gather, stream) == cudaSuccess ? MLA_OK
+                                                                           : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(mla_status_t status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported device (needs sm_103 with 227 KB shared memory per block)";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MLA_ERR_CUDA: return "CUDA call failed";
+  }
+  return "unknown status";
+}
+
+int32_t mla_decode_abi_version(void) { return MLA_ABI_VERSION; }
+
+mla_status_t mla_decode_plan(int32_t batch, int32_t max_kv_len, int32_t num_sms, mla_plan_t* plan) {
+  if (plan == nullptr || batch < 1 || max_kv_len < 0) return MLA_ERR_INVALID_ARG;
+  if (num_sms <= 0) {
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  mla_plan_t p;
+  std::memset(&p, 0, sizeof(p));
+  p.batch = batch;
+  p.max_kv_len = max_kv_len;
+  p.num_sms = num_sms;
+  p.grid = mla::plan_grid(batch, max_kv_len, num_sms);
+  p.tile_tokens = kTileTokens;
+  p.abi_version = MLA_ABI_VERSION;
+  const uint64_t g = static_cast<uint64_t>(p.grid);
+  uint64_t off = kAlign;  // error word + reserved header
+  p.ws_prefix_offset = off;
+  off += round_up((static_cast<uint64_t>(batch) + 1) * sizeof(int32_t));
+  p.ws_workers_offset = off;
+  off += round_up(g * 4 * sizeof(int32_t));
+  p.ws_lse_offset = off;
+  off += round_up(2 * g * kNumHeads * sizeof(float));
+  p.ws_partial_offset = off;
+  off += round_up(2 * g * kNumHeads * kVDim * sizeof(float));
+  p.ws_bytes = off;
+  *plan = p;
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_stage1(const void* q_bf16, const void* kv_fp8, const float* kv_scale,
+                               const int32_t* qo_indptr, const int32_t* kv_indptr, void* out_bf16,
+                               cudaStream_t stream, const mla_plan_t* plan,
+                               const int32_t* kv_indices, int64_t kv_indices_len, int64_t kv_rows,
+                               void* workspace, size_t workspace_bytes) {
+  return run_stage1(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream, plan,
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes);
+}
+
+mla_status_t mla_decode_stage2(const int32_t* qo_indptr, void* out_bf16, cudaStream_t stream,
+                               const mla_plan_t* plan, void* workspace, size_t workspace_bytes) {
+  mla_status_t st = check_plan(plan);
+  if (st != MLA_OK) return st;
+  if (qo_indptr == nullptr || out_bf16 == nullptr || !aligned(out_bf16, 16))
+    return MLA_ERR_INVALID_ARG;
+  st = check_workspace(plan, workspace, workspace_bytes);
+  if (st != MLA_OK) return st;
+  return mla::launch_stage2(stage2_params(qo_indptr, out_bf16, plan, workspace), false, stream) ==
+                 cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+mla_status_t mla_decode_fwd(const void* q_bf16, const void* kv_fp8, const float* kv_scale,
+                            const int32_t* qo_indptr, const int32_t* kv_indptr, void* out_bf16,
+                            cudaStream_t stream, const mla_plan_t* plan,
+                            const int32_t* kv_indices, int64_t kv_indices_len, int64_t kv_rows,
+                            void* workspace, size_t workspace_bytes) {
+  mla_status_t st = run_stage1(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream,
+                               plan, kv_indices, kv_indices_len, kv_rows, workspace,
+                               workspace_bytes);
+  if (st != MLA_OK) return st;
+  return mla::launch_stage2(stage2_params(qo_indptr, out_bf16, plan, workspace), true, stream) ==
+                 cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+mla_status_t mla_fp8_quantize_per_tensor(const void* src_bf16, int64_t n, void* dst_fp8,
+                                         float* scale_out, void* tmp, size_t tmp_bytes,
+                                         cudaStream_t stream) {
+  if (src_bf16 == nullptr || dst_fp8 == nullptr || scale_out == nullptr || tmp == nullptr ||
+      n < 1 || tmp_bytes < 16 || !aligned(tmp, 4) || !aligned(src_bf16, 2))
+    return MLA_ERR_INVALID_ARG;
+  int device = 0;
+  mla_status_t st = prepare_device(&device);
+  if (st != MLA_OK) return st;
+  return mla::launch_fp8_quantize(static_cast<const uint16_t*>(src_bf16), n,
+                                  static_cast<uint8_t*>(dst_fp8), scale_out,
+                                  static_cast<uint32_t*>(tmp), stream) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+mla_status_t mla_decode_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (workspace == nullptr || workspace_bytes < sizeof(int32_t)) return MLA_ERR_INVALID_ARG;
+  return cudaMemsetAsync(workspace, 0, workspace_bytes, stream) == cudaSuccess ? MLA_OK
+                                                                               : MLA_ERR_CUDA;
+}
+
+mla_status_t mla_decode_read_error(void* workspace, int32_t* err_host, int32_t clear,
+                                   cudaStream_t stream) {
+  if (workspace == nullptr || err_host == nullptr) return MLA_ERR_INVALID_ARG;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  *err_host = v;
+  if (clear && cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_schedule_host(const int32_t* kv_indptr_host, int32_t batch, int32_t grid,
+                                      int32_t* workers_out, int32_t* prefix_out) {
+  if (kv_indptr_host == nullptr || workers_out == nullptr || prefix_out == nullptr || batch < 1 ||
+      grid < 1)
+    return MLA_ERR_INVALID_ARG;
+  bool bad = kv_indptr_host[0] < 0;
+  for (int32_t b = 0; b < batch; ++b)
+    if (kv_indptr_host[b + 1] < kv_indptr_host[b]) bad = true;
+  int32_t a = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    prefix_out[b] = a;
+    if (!bad) a += mla::tiles_of_length(static_cast<int64_t>(kv_indptr_host[b + 1]) - kv_indptr_host[b]);
+  }
+  prefix_out[batch] = a;
+  const int32_t total = a;
+  for (int32_t c = 0; c < grid; ++c) {
+    const int32_t t0 = mla::worker_begin(c, total, grid);
+    const int32_t t1 = mla::worker_begin(c + 1, total, grid);
+    int32_t first = -1, last = -1;
+    if (t1 > t0) {
+      for (int32_t b = 0; b < batch; ++b) {
+        const int32_t nt = prefix_out[b + 1] - prefix_out[b];
+        if (nt <= 0) continue;
+        if (prefix_out[b] <= t0 && t0 < prefix_out[b] + nt) first = b;
+        if (prefix_out[b] <= t1 - 1 && t1 - 1 < prefix_out[b] + nt) last = b;
+      }
+    }
+    workers_out[4 * c + 0] = t0;
+    workers_out[4 * c + 1] = t1;
+    workers_out[4 * c + 2] = first;
+    workers_out[4 * c + 3] = last;
+  }
+  return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+// Kernel parameter blocks and launchers (internal to libmla_decode).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace mla {
+
+// Stage 1 ring / layout constants.
+constexpr int kNumVSlots = 10;      // 16 KB slots: tokens x 128 latent dims (swizzle 128B)
+constexpr int kNumRSlots = 3;       // 8 KB slots: tokens x 64 rope dims (swizzle 64B)
+constexpr int kVPanelBytes = 128 * 128;
+constexpr int kRPanelBytes = 128 * 64;
+constexpr int kStage1Threads = 192; // warps 0-3 softmax/epilogue, 4 TMA producer, 5 MMA issuer
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
+
+struct Stage1Params {
+  const uint16_t* q;          // bf16 bits [B, 16, 576]
+  const float* kv_scale;      // [1]
+  const int32_t* qo_indptr;   // [B+1]
+  const int32_t* kv_indptr;   // [B+1]
+  const int32_t* kv_indices;  // [kv_indices_len] or null
+  uint16_t* out;              // bf16 bits [B, 16, 512]
+  int32_t* err;               // workspace error word
+  int32_t* prefix;            // [B+1]
+  int32_t* workers;           // [grid*4]
+  float* lse;                 // [2*grid*16]
+  float* partial;             // [2*grid*16*512]
+  int64_t kv_rows;
+  int64_t kv_indices_len;
+  int32_t batch;
+  int32_t grid;
+};
+
+struct Stage2Params {
+  const int32_t* qo_indptr;
+  uint16_t* out;
+  int32_t* err;
+  const int32_t* prefix;
+  const float* lse;
+  const float* partial;
+  int32_t batch;
+  int32_t grid;
+};
+
+size_t stage1_smem_bytes();
+cudaError_t stage1_prepare(int device);  // sets the dynamic shared memory limit once
+cudaError_t launch_stage1(const Stage1Params& p, const CUtensorMap& map_v,
+                          const CUtensorMap& map_r, bool gather, cudaStream_t stream);
+cudaError_t launch_stage2(const Stage2Params& p, bool programmatic, cudaStream_t stream);
+cudaError_t launch_fp8_quantize(const uint16_t* src, int64_t n, uint8_t* dst, float* scale_out,
+                                uint32_t* amax_bits, cudaStream_t stream);
+
+}  // namespace mla

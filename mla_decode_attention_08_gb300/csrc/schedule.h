@@ -1,0 +1,51 @@
+// Integer formulas of the token-balanced split-KV schedule, shared by the host
+// planner and the kernels so both compute the same ranges.
+//
+// Rows are cut into tiles of kTileTokens tokens; all rows' tiles, row after
+// row, form one sequence of T tiles; worker c of a grid of G takes the tiles
+// [floor(c*T/G), floor((c+1)*T/G)).  This is the persistent form of the
+// flash-decoding split (kernelbot-amd-mixed-mla submission 722089,
+// `_mla_multihead_stage1` splits each row into contiguous ranges; submissions
+// 663509 and 738050 hand a persistent kernel precomputed work maps).
+#pragma once
+#include <cstdint>
+
+#ifdef __CUDACC__
+#define MLA_HD __host__ __device__ __forceinline__
+#else
+#define MLA_HD inline
+#endif
+
+namespace mla {
+
+constexpr int kNumHeads = 16;
+constexpr int kQkDim = 576;
+constexpr int kVDim = 512;
+constexpr int kTileTokens = 128;
+
+MLA_HD int32_t tiles_of_length(int64_t len) {
+  return len > 0 ? static_cast<int32_t>((len + kTileTokens - 1) / kTileTokens) : 0;
+}
+
+MLA_HD int32_t plan_grid(int32_t batch, int32_t max_kv_len, int32_t num_sms) {
+  int64_t upper = static_cast<int64_t>(batch) * tiles_of_length(max_kv_len);
+  int64_t g = upper < num_sms ? upper : num_sms;
+  return g < 1 ? 1 : static_cast<int32_t>(g);
+}
+
+MLA_HD int32_t worker_begin(int32_t c, int32_t total, int32_t grid) {
+  return static_cast<int32_t>((static_cast<int64_t>(c) * total) / grid);
+}
+
+// Worker holding global tile t (0 <= t < total).
+MLA_HD int32_t worker_of_tile(int32_t t, int32_t total, int32_t grid) {
+  return static_cast<int32_t>(((static_cast<int64_t>(t) + 1) * grid - 1) / total);
+}
+
+// Workspace slot of worker c's partial for a split row whose tiles start at
+// prefix_b: slot 2c when c's range begins inside that row, else 2c + 1.
+MLA_HD int32_t partial_slot(int32_t c, int32_t worker_t0, int32_t prefix_b) {
+  return worker_t0 >= prefix_b ? 2 * c : 2 * c + 1;
+}
+
+}  // namespace mla

@@ -1,0 +1,870 @@
+// Stage 1 of the MLA forward_absorb decode step on sm_103a: split attention.
+//
+// One persistent CTA per worker of the token-balanced schedule walks its tile
+// range.  Per 128-token tile of the FP8 latent cache:
+//   * warp 4 streams the tile once through TMA into a ring of swizzled panels
+//     (four 128-dim latent panels + one 64-dim rope panel; page-table rows are
+//     fetched with tile::gather4),
+//   * warp 5 issues tcgen05 MMAs: S^T[128 tok x 32] = K_tile . [Q_hi;Q_lo]^T
+//     and O^T[512 x 32] += V_tile^T . [P_hi;P_lo]^T, accumulators in TMEM,
+//   * warps 0-3 run the exp2 online softmax on S read from TMEM, write P, and
+//     at the end of a segment write either the bf16 output (row fully inside
+//     this worker) or a normalised partial plus its base-2 log-sum-exp.
+// The same shared-memory tile feeds both products and all 16 heads, which is
+// the pages' multi-head KV reuse (kernelbot-amd-mixed-mla submission 722089,
+// module docstring and `_mla_multihead_stage1`).
+//
+// Both operands of each product are FP8 e4m3 (kind::f8f6f4).  Q and P keep
+// bf16-level precision by a two-term split x ~= hi + lo / 16 with both terms
+// e4m3: the 16 "hi" heads and 16 "lo" heads form N = 32.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "../../include/mla_decode.h"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "schedule.h"
+
+namespace mla {
+namespace {
+
+// ------------------------------------------------------------ layout
+constexpr int kQPanelBytes = 32 * 128;   // 32 operand rows x 128 dims (swizzle 128B)
+constexpr int kQRopeBytes = 32 * 64;     // 32 operand rows x 64 dims (swizzle 64B)
+constexpr int kPBytes = 128 * 32;        // 128 tokens x 32 operand columns (swizzle 32B)
+
+constexpr int kOffV = 0;
+constexpr int kOffR = kOffV + kNumVSlots * kVPanelBytes;
+constexpr int kOffQ = kOffR + kNumRSlots * kRPanelBytes;
+constexpr int kOffQRope = kOffQ + 4 * kQPanelBytes;
+constexpr int kOffP = kOffQRope + kQRopeBytes;
+constexpr int kOffMisc = kOffP + 2 * kPBytes;
+
+struct Misc {
+  uint64_t v_full[kNumVSlots];
+  uint64_t v_empty[kNumVSlots];
+  uint64_t r_full[kNumRSlots];
+  uint64_t r_empty[kNumRSlots];
+  uint64_t s_full[2];
+  uint64_t p_full;
+  uint64_t pv_done;
+  uint64_t q_full;
+  uint64_t q_empty;
+  uint64_t o_empty;
+  uint64_t mma_done;
+  float red_max[2][4][16];
+  float red_sum[4][16];
+  uint32_t red_u32[8];
+  int32_t scan[8];
+  uint32_t tmem_base;
+  volatile int32_t abort_flag;
+  int32_t total_tiles;
+  int32_t t0, t1;
+  int32_t first_row, first_prefix, last_row;
+  int32_t bad;
+};
+
+constexpr int kSmemUsed = kOffMisc + static_cast<int>(sizeof(Misc));
+constexpr int kSmemAlloc = kSmemUsed + 1024;  // room to align the base to 1024 B
+static_assert(kSmemAlloc <= 232448, "stage-1 shared memory exceeds the per-CTA limit");
+
+// TMEM columns: two S buffers (32 each) then O (4 chunks x 32).
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 64;
+
+constexpr int kSoftmaxThreads = 128;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kBarSoftmax = 1;  // named barrier id of warps 0-3
+
+// Operand descriptors (layout codes: 2 = 128B swizzle, 4 = 64B, 6 = 32B).
+constexpr uint32_t kLayoutSw128 = 2, kLayoutSw64 = 4, kLayoutSw32 = 6;
+constexpr uint32_t kIdescQK = idesc_e4m3(128, 32, false, false);  // K-major A and B
+constexpr uint32_t kIdescPV = idesc_e4m3(128, 32, true, true);    // MN-major A and B
+
+// log2(e) / sqrt(576): converts a dot product to base-2 softmax exponent units.
+constexpr float kSmScaleLog2 = 1.4426950408889634f / 24.0f;
+// A new row maximum above the running reference by more than this many base-2
+// units triggers a rescale; below it, P values up to 2^8 still fit e4m3.
+constexpr float kRescaleThreshold = 8.0f;
+
+__device__ __forceinline__ int32_t ldg_i32(const int32_t* p) { return __ldg(p); }
+
+__device__ __forceinline__ void set_error(int32_t* err, int32_t bits) { atomicOr(err, bits); }
+
+// Bounded wait on an mbarrier phase.  Returns false when the call is being
+// abandoned (this or another role timed out); never spins without limit.
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, Misc* ms, int32_t* err) {
+  if (ms->abort_flag) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t start = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 31) == 0) {
+      if (ms->abort_flag) return false;
+      if (global_timer_ns() - start > kWaitLimitNs) {
+        ms->abort_flag = 1;
+        set_error(err, MLA_DERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ segment cursor
+// Walks the rows intersecting this worker's tile range [t0, t1).
+struct Cursor {
+  int32_t b;        // current row
+  int32_t next_a;   // prefix of row b + 1
+  int32_t row_a;    // prefix of row b
+  int32_t kb, len;  // first flattened token and token count of row b
+  int32_t j, j0, j1;  // current tile and this worker's tile range inside row b
+  int32_t seg;      // segment counter (0-based)
+  bool whole;       // row b lies entirely inside this worker
+  bool live;
+};
+
+// Advance to the next row holding tiles of [t0, t1).
+__device__ bool cursor_next_segment(Cursor& c, const int32_t* kv_indptr, int32_t batch,
+                                    int32_t t0, int32_t t1) {
+  while (c.next_a < t1) {
+    const int32_t b = ++c.b;
+    if (b >= batch) return false;
+    const int32_t kb = ldg_i32(kv_indptr + b);
+    const int32_t ke = ldg_i32(kv_indptr + b + 1);
+    const int32_t len = ke > kb ? ke - kb : 0;
+    const int32_t nt = tiles_of_length(len);
+    const int32_t a = c.next_a;
+    c.next_a = a + nt;
+    if (nt == 0) continue;
+    c.row_a = a;
+    c.kb = kb;
+    c.len = len;
+    c.j0 = (t0 > a ? t0 : a) - a;
+    c.j1 = (t1 < a + nt ? t1 : a + nt) - a;
+    c.j = c.j0;
+    c.whole = a >= t0 && a + nt <= t1;
+    ++c.seg;
+    return true;
+  }
+  return false;
+}
+
+__device__ void cursor_start(Cursor& c, const Misc* ms, const int32_t* kv_indptr, int32_t batch) {
+  c.b = ms->first_row - 1;
+  c.next_a = ms->first_prefix;
+  c.seg = -1;
+  c.live = ms->t1 > ms->t0 && ms->first_row >= 0 &&
+           cursor_next_segment(c, kv_indptr, batch, ms->t0, ms->t1);
+}
+
+// Step to the next tile; returns false when the worker's range is exhausted.
+__device__ bool cursor_next_tile(Cursor& c, const Misc* ms, const int32_t* kv_indptr,
+                                 int32_t batch) {
+  if (++c.j < c.j1) return true;
+  c.live = cursor_next_segment(c, kv_indptr, batch, ms->t0, ms->t1);
+  return c.live;
+}
+
+// Bounded wait used only while draining after an abandoned call.
+__device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity) {
+  const uint64_t start = global_timer_ns();
+  for (uint32_t n = 0;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 31) == 31 && global_timer_ns() - start > kWaitLimitNs) return false;
+  }
+}
+
+// ------------------------------------------------------------ schedule prologue
+// All threads.  Tile counts of every row, their prefix, this worker's range
+// [t0, t1) and the rows holding its first and last tile.  Worker 0 also stores
+// the prefix for stage 2; every worker stores its (t0, t1, first, last) record.
+__device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int32_t batch = p.batch;
+  const int32_t per = (batch + nthreads - 1) / nthreads;
+  const int32_t r0 = min(tid * per, batch), r1 = min(r0 + per, batch);
+
+  int32_t local = 0;
+  int bad = 0;
+  if (r0 < r1) {
+    int32_t prev = ldg_i32(p.kv_indptr + r0);
+    for (int32_t b = r0; b < r1; ++b) {
+      const int32_t next = ldg_i32(p.kv_indptr + b + 1);
+      if (next < prev) bad = 1;
+      local += tiles_of_length(static_cast<int64_t>(next) - prev);
+      prev = next;
+    }
+  }
+  if (tid == 0) {
+    const int64_t limit = p.kv_indices != nullptr ? p.kv_indices_len : p.kv_rows;
+    if (ldg_i32(p.kv_indptr) < 0 || ldg_i32(p.kv_indptr + batch) > limit) bad = 1;
+  }
+  int32_t incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) ms->scan[warp] = incl;
+  bad = __syncthreads_or(bad);
+
+  int32_t warp_off = 0, total = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    const int32_t s = ms->scan[w];
+    if (w < warp) warp_off += s;
+    total += s;
+  }
+  if (bad) total = 0;
+  const int32_t c = static_cast<int32_t>(blockIdx.x);
+  const int32_t t0 = worker_begin(c, total, p.grid);
+  const int32_t t1 = worker_begin(c + 1, total, p.grid);
+  if (tid == 0) {
+    ms->total_tiles = total;
+    ms->t0 = t0;
+    ms->t1 = t1;
+    ms->first_row = -1;
+    ms->last_row = -1;
+    ms->first_prefix = 0;
+    ms->bad = bad;
+    if (bad) set_error(p.err, MLA_DERR_KV_INDPTR);
+  }
+  __syncthreads();
+
+  int32_t a = bad ? 0 : warp_off + incl - local;
+  if (r0 < r1) {
+    int32_t prev = ldg_i32(p.kv_indptr + r0);
+    for (int32_t b = r0; b < r1; ++b) {
+      const int32_t next = ldg_i32(p.kv_indptr + b + 1);
+      const int32_t nt = bad ? 0 : tiles_of_length(static_cast<int64_t>(next) - prev);
+      if (c == 0) p.prefix[b] = a;
+      if (nt > 0 && t1 > t0) {
+        if (a <= t0 && t0 < a + nt) {
+          ms->first_row = b;
+          ms->first_prefix = a;
+        }
+        if (a <= t1 - 1 && t1 - 1 < a + nt) ms->last_row = b;
+      }
+      a += nt;
+      prev = next;
+    }
+  }
+  if (c == 0 && tid == 0) p.prefix[batch] = total;
+  __syncthreads();
+  if (tid == 0) {
+    int32_t* w = p.workers + 4 * c;
+    w[0] = t0;
+    w[1] = t1;
+    w[2] = ms->first_row;
+    w[3] = ms->last_row;
+  }
+}
+
+// ------------------------------------------------------------ producer (warp 4)
+// Streams each tile once: the rope panel (64 dims) then four latent panels.
+template <bool kGather>
+__device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
+                             const CUtensorMap* map_r, Misc* ms, uint32_t sbase) {
+  const int lane = threadIdx.x & 31;
+  int32_t last_r[kNumRSlots], last_v[kNumVSlots];  // last fill issued per slot (-1: none)
+#pragma unroll
+  for (int s = 0; s < kNumRSlots; ++s) last_r[s] = -1;
+#pragma unroll
+  for (int s = 0; s < kNumVSlots; ++s) last_v[s] = -1;
+
+  Cursor cur;
+  cursor_start(cur, ms, p.kv_indptr, p.batch);
+  uint32_t tile = 0;
+  while (cur.live) {
+    const int32_t tok0 = cur.kb + cur.j * kTileTokens;
+    const int32_t valid = min(kTileTokens, cur.len - cur.j * kTileTokens);
+    int32_t rows[4] = {0, 0, 0, 0};
+    if (kGather) {
+      // Lane l gathers tokens 4l..4l+3; tokens past the end repeat the last one.
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int32_t t = min(4 * lane + k, valid - 1);
+        int32_t idx = ldg_i32(p.kv_indices + tok0 + t);
+        if (idx < 0 || static_cast<int64_t>(idx) >= p.kv_rows) {
+          set_error(p.err, MLA_DERR_KV_INDEX);
+          idx = 0;
+        }
+        rows[k] = idx;
+      }
+    }
+    // rope panel
+    {
+      const uint32_t slot = tile % kNumRSlots, use = tile / kNumRSlots;
+      int ok = 1;
+      if (lane == 0 && use > 0)
+        ok = wait_phase(smem_u32(&ms->r_empty[slot]), (use - 1) & 1, ms, p.err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok) {
+        const uint32_t dst = sbase + kOffR + slot * kRPanelBytes;
+        const uint32_t bar = smem_u32(&ms->r_full[slot]);
+        if (lane == 0) mbar_arrive_expect_tx(bar, kRPanelBytes);
+        __syncwarp();
+        if (kGather)
+          tma_gather4(dst + lane * 4 * 64, map_r, kVDim, rows[0], rows[1], rows[2], rows[3], bar);
+        else if (lane == 0)
+          tma_load_2d(dst, map_r, kVDim, tok0, bar);
+        last_r[slot] = static_cast<int32_t>(use);
+      }
+    }
+    // latent panels
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t g = tile * 4 + c;
+      const uint32_t slot = g % kNumVSlots, use = g / kNumVSlots;
+      int ok = 1;
+      if (lane == 0 && use > 0)
+        ok = wait_phase(smem_u32(&ms->v_empty[slot]), (use - 1) & 1, ms, p.err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok) {
+        const uint32_t dst = sbase + kOffV + slot * kVPanelBytes;
+        const uint32_t bar = smem_u32(&ms->v_full[slot]);
+        if (lane == 0) mbar_arrive_expect_tx(bar, kVPanelBytes);
+        __syncwarp();
+        if (kGather)
+          tma_gather4(dst + lane * 4 * 128, map_v, 128 * c, rows[0], rows[1], rows[2], rows[3], bar);
+        else if (lane == 0)
+          tma_load_2d(dst, map_v, 128 * c, tok0, bar);
+        last_v[slot] = static_cast<int32_t>(use);
+      }
+    }
+    ++tile;
+    if (!cursor_next_tile(cur, ms, p.kv_indptr, p.batch)) break;
+  }
+  // An abandoned call must not leave copies landing in shared memory after exit.
+  if (ms->abort_flag && lane == 0) {
+    for (int s = 0; s < kNumRSlots; ++s)
+      if (last_r[s] >= 0) drain_phase(smem_u32(&ms->r_full[s]), last_r[s] & 1);
+    for (int s = 0; s < kNumVSlots; ++s)
+      if (last_v[s] >= 0) drain_phase(smem_u32(&ms->v_full[s]), last_v[s] & 1);
+  }
+}
+
+// ------------------------------------------------------------ MMA issuer (warp 5, lane 0)
+// S^T[tile & 1] = K_tile . [Q_hi; Q_lo]^T : 4 latent panels x 4 k-steps of 32
+// dims (128-byte swizzle) plus the rope panel's 2 k-steps (64-byte swizzle).
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t sbase, uint32_t tile) {
+  const uint32_t d = tmem + kColS + 32 * (tile & 1);
+  const uint32_t qb = sbase + kOffQ;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint32_t g = tile * 4 + p;
+    const uint32_t vs = sbase + kOffV + (g % kNumVSlots) * kVPanelBytes;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      umma_f8(d, smem_desc(vs + 32 * kk, 1024, 1024, kLayoutSw128),
+              smem_desc(qb + p * kQPanelBytes + 32 * kk, 1024, 1024, kLayoutSw128), kIdescQK,
+              (p | kk) != 0);
+    }
+  }
+  const uint32_t rs = sbase + kOffR + (tile % kNumRSlots) * kRPanelBytes;
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    umma_f8(d, smem_desc(rs + 32 * kk, 512, 512, kLayoutSw64),
+            smem_desc(sbase + kOffQRope + 32 * kk, 512, 512, kLayoutSw64), kIdescQK, 1);
+  }
+}
+
+// O^T[chunk c] (+)= V_c^T . [P_hi; P_lo]^T over the tile's 128 tokens: V panel c
+// read MN-major (dims contiguous), P read MN-major (operand columns contiguous).
+// Each latent panel is released as soon as its four MMAs complete.
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, uint32_t tile, bool first,
+                                         Misc* ms) {
+  const uint32_t pb = sbase + kOffP + (tile & 1) * kPBytes;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t g = tile * 4 + c;
+    const uint32_t slot = g % kNumVSlots;
+    const uint32_t vs = sbase + kOffV + slot * kVPanelBytes;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      umma_f8(tmem + kColO + 32 * c, smem_desc(vs + kk * 4096, 1024, 1024, kLayoutSw128),
+              smem_desc(pb + kk * 1024, 256, 256, kLayoutSw32), kIdescPV, !(first && kk == 0));
+    }
+    umma_commit(smem_u32(&ms->v_empty[slot]));
+  }
+}
+
+__device__ void run_mma(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
+  Cursor qc, pc;
+  cursor_start(qc, ms, p.kv_indptr, p.batch);
+  cursor_start(pc, ms, p.kv_indptr, p.batch);
+  uint32_t qk_n = 0, pv_n = 0;  // tiles whose QK / PV have been issued
+  uint32_t qk_stage = 0;        // preconditions of the next QK already observed
+  uint64_t last_progress = global_timer_ns();
+
+  while (pc.live) {
+    bool progressed = false;
+    // QK of tile qk_n: its rope + 4 latent panels landed, its Q operand is
+    // written (first tile of a segment), and the S buffer it overwrites has
+    // been read (PV of tile qk_n - 2 issued implies that softmax finished it).
+    if (qc.live && qk_n <= pv_n + 1) {
+      while (qk_stage < 6) {
+        uint32_t bar, parity;
+        if (qk_stage == 0) {
+          bar = smem_u32(&ms->r_full[qk_n % kNumRSlots]);
+          parity = (qk_n / kNumRSlots) & 1;
+        } else if (qk_stage <= 4) {
+          const uint32_t g = qk_n * 4 + (qk_stage - 1);
+          bar = smem_u32(&ms->v_full[g % kNumVSlots]);
+          parity = (g / kNumVSlots) & 1;
+        } else {
+          if (qc.j != qc.j0) {
+            qk_stage = 6;
+            break;
+          }
+          bar = smem_u32(&ms->q_full);
+          parity = qc.seg & 1;
+        }
+        if (!mbar_test_wait(bar, parity)) break;
+        ++qk_stage;
+      }
+      if (qk_stage == 6) {
+        tc_fence_after();
+        issue_qk(tmem, sbase, qk_n);
+        umma_commit(smem_u32(&ms->s_full[qk_n & 1]));
+        umma_commit(smem_u32(&ms->r_empty[qk_n % kNumRSlots]));
+        if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
+        ++qk_n;
+        qk_stage = 0;
+        progressed = true;
+        cursor_next_tile(qc, ms, p.kv_indptr, p.batch);
+      }
+    }
+    // PV of tile pv_n: its P is published, and (first tile of a later segment)
+    // the previous segment's epilogue has read O out of TMEM.
+    if (pv_n < qk_n) {
+      const bool first = pc.j == pc.j0;
+      bool ready = mbar_test_wait(smem_u32(&ms->p_full), pv_n & 1);
+      if (ready && first && pc.seg > 0)
+        ready = mbar_test_wait(smem_u32(&ms->o_empty), (pc.seg - 1) & 1);
+      if (ready) {
+        tc_fence_after();
+        issue_pv(tmem, sbase, pv_n, first, ms);
+        umma_commit(smem_u32(&ms->pv_done));
+        ++pv_n;
+        progressed = true;
+        cursor_next_tile(pc, ms, p.kv_indptr, p.batch);
+      }
+    }
+    if (progressed) {
+      last_progress = global_timer_ns();
+    } else {
+      if (ms->abort_flag) break;
+      if (global_timer_ns() - last_progress > kWaitLimitNs) {
+        ms->abort_flag = 1;
+        set_error(p.err, MLA_DERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(20);
+    }
+  }
+  // Every MMA issued by this thread completes before TMEM is released.
+  umma_commit(smem_u32(&ms->mma_done));
+  drain_phase(smem_u32(&ms->mma_done), 0);
+}
+
+// ------------------------------------------------------------ softmax warps (0-3)
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Sum of v[h] over the 32 lanes of the warp, returned for head (lane >> 1) & 15:
+// four halving exchanges move half of the heads to the partner lane each time.
+__device__ __forceinline__ float warp_transpose_sum16(float (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int half = 8, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
+    const bool up = (lane & bit) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = up ? v[k] : v[k + half];
+      const float keep = up ? v[k + half] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+// Byte address of 16-byte chunk `cc` of operand row `row` in the Q operand:
+// latent dims in four 128-byte-swizzled panels, rope dims in one 64-byte panel.
+__device__ __forceinline__ uint32_t q_chunk_addr(uint32_t sq, int row, int ch) {
+  if (ch < 32) {
+    const int panel = ch >> 3, cc = ch & 7;
+    return sq + panel * kQPanelBytes + row * 128 + ((cc ^ (row & 7)) << 4);
+  }
+  const int cc = ch - 32;
+  return sq + 4 * kQPanelBytes + row * 64 + ((cc ^ ((row >> 1) & 3)) << 4);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d) : "memory");
+}
+
+// Two-term e4m3 split of 16 floats x (|x| <= 448): hi = e4m3(x), lo = e4m3(16 (x - hi)),
+// so x ~= hi + lo / 16 with about 8 significant bits.  Packs codes 4 per word.
+__device__ __forceinline__ void split_e4m3_16(const float (&x)[16], uint32_t (&hi)[4],
+                                              uint32_t (&lo)[4]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint16_t h2 = cvt_e4m3x2(x[2 * k], x[2 * k + 1]);
+    const uint32_t hf = cvt_e4m3x2_to_f16x2(h2);
+    const float2 hv = __half22float2(*reinterpret_cast<const __half2*>(&hf));
+    const uint16_t l2 = cvt_e4m3x2((x[2 * k] - hv.x) * 16.0f, (x[2 * k + 1] - hv.y) * 16.0f);
+    if (k & 1) {
+      hi[k >> 1] |= static_cast<uint32_t>(h2) << 16;
+      lo[k >> 1] |= static_cast<uint32_t>(l2) << 16;
+    } else {
+      hi[k >> 1] = h2;
+      lo[k >> 1] = l2;
+    }
+  }
+}
+
+// Loads query token tq (16 heads x 576 bf16), scales it by a power of two so the
+// largest magnitude lands in (224, 448], and writes the hi / lo e4m3 operand rows
+// (rows 0-15 hi, 16-31 lo).  Returns the factor turning the QK accumulator into
+// base-2 softmax exponent units.  tq < 0 writes a zero query.
+__device__ float prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq,
+                           float kv_scale) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  uint4 raw[5][2];
+  uint32_t amax = 0;
+#pragma unroll
+  for (int r = 0; r < 5; ++r) {
+    const int job = t + 128 * r;
+    raw[r][0] = raw[r][1] = make_uint4(0, 0, 0, 0);
+    if (job < 576 && tq >= 0) {
+      const int head = job / 36, ch = job % 36;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + (static_cast<size_t>(tq) * kNumHeads + head) * kQkDim + ch * 16);
+      raw[r][0] = __ldg(src);
+      raw[r][1] = __ldg(src + 1);
+    }
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(&raw[r][0]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      amax = max(amax, w[i] & 0x7FFFu);
+      amax = max(amax, (w[i] >> 16) & 0x7FFFu);
+    }
+  }
+  amax = __reduce_max_sync(0xffffffffu, amax);
+  if (lane == 0) ms->red_u32[warp] = amax;
+  named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+  amax = max(max(ms->red_u32[0], ms->red_u32[1]), max(ms->red_u32[2], ms->red_u32[3]));
+  const float a = __uint_as_float(amax << 16);
+  int k2 = 0;
+  if (a > 0.0f) {
+    int e;
+    const float f = frexpf(a, &e);  // a = f * 2^e, f in [0.5, 1)
+    k2 = (f <= 0.875f) ? 9 - e : 8 - e;
+    k2 = min(max(k2, -126), 126);
+  }
+  const float up = __int_as_float((k2 + 127) << 23);
+  const float down = __int_as_float((127 - k2) << 23);
+
+#pragma unroll
+  for (int r = 0; r < 5; ++r) {
+    const int job = t + 128 * r;
+    if (job < 576) {
+      const int head = job / 36, ch = job % 36;
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(&raw[r][0]);
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = u2f(w[i] << 16) * up;
+        x[2 * i + 1] = u2f(w[i] & 0xFFFF0000u) * up;
+      }
+      uint32_t hi[4], lo[4];
+      split_e4m3_16(x, hi, lo);
+      st_shared_v4(q_chunk_addr(sq, head, ch), hi[0], hi[1], hi[2], hi[3]);
+      st_shared_v4(q_chunk_addr(sq, 16 + head, ch), lo[0], lo[1], lo[2], lo[3]);
+    }
+  }
+  fence_proxy_async_smem();
+  named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+  if (t == 0) mbar_arrive(smem_u32(&ms->q_full));
+  return down * kv_scale * kSmScaleLog2;
+}
+
+__device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem,
+                            float kv_scale) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;  // TMEM lane quarter
+  const int token = warp * 32 + lane;  // S row (token) / O row (dim within a chunk) of this thread
+  const int32_t c = static_cast<int32_t>(blockIdx.x);
+
+  Cursor cur;
+  cursor_start(cur, ms, p.kv_indptr, p.batch);
+  uint32_t tile = 0;     // tiles processed by this CTA
+  uint32_t pv_seen = 0;  // pv_done phases consumed
+
+  auto wait_pv_through = [&](uint32_t k) {
+    while (pv_seen <= k) {
+      wait_phase(smem_u32(&ms->pv_done), pv_seen & 1, ms, p.err);
+      ++pv_seen;
+    }
+  };
+
+  while (cur.live) {
+    // ------------------------------------------------ segment start
+    const int32_t b = cur.b;
+    const int32_t tq = ldg_i32(p.qo_indptr + b);
+    const bool row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == 1 && tq >= 0 && tq < p.batch;
+    if (!row_ok && t == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
+    if (cur.seg > 0) wait_phase(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
+    const float qk_scale = prepare_q(p, ms, sbase + kOffQ, row_ok ? tq : -1, kv_scale);
+
+    float m_ref[16], l[16];
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+      m_ref[h] = -INFINITY;
+      l[h] = 0.0f;
+    }
+    const uint32_t seg_first_tile = tile;
+
+    // ------------------------------------------------ tiles
+    for (;;) {
+      const int32_t valid = min(kTileTokens, cur.len - cur.j * kTileTokens);
+      const uint32_t sb = tile & 1;
+      wait_phase(smem_u32(&ms->s_full[sb]), (tile >> 1) & 1, ms, p.err);
+      tc_fence_after();
+      uint32_t r[32];
+      tmem_ld32(tmem + lane_base + kColS + 32 * sb, r);
+      tmem_wait_ld();
+
+      const bool tok_ok = token < valid;
+      float s[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        s[h] = tok_ok ? (u2f(r[h]) + u2f(r[16 + h]) * 0.0625f) * qk_scale : -INFINITY;
+
+      // Row maximum of this tile, per head, over the 128 tokens.
+      float mx[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) mx[h] = warp_max(s[h]);
+      if (lane == 0) {
+        float4* dst = reinterpret_cast<float4*>(&ms->red_max[sb][warp][0]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          dst[k] = make_float4(mx[4 * k], mx[4 * k + 1], mx[4 * k + 2], mx[4 * k + 3]);
+      }
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float4 m4 = reinterpret_cast<const float4*>(&ms->red_max[sb][0][0])[k];
+#pragma unroll
+        for (int w = 1; w < 4; ++w) {
+          const float4 o4 = reinterpret_cast<const float4*>(&ms->red_max[sb][w][0])[k];
+          m4.x = fmaxf(m4.x, o4.x); m4.y = fmaxf(m4.y, o4.y);
+          m4.z = fmaxf(m4.z, o4.z); m4.w = fmaxf(m4.w, o4.w);
+        }
+        mx[4 * k] = m4.x; mx[4 * k + 1] = m4.y; mx[4 * k + 2] = m4.z; mx[4 * k + 3] = m4.w;
+      }
+
+      // Lazy reference maximum: move it only when the tile maximum exceeds it by
+      // more than the threshold (always on a segment's first tile).
+      float alpha[16];
+      bool moved = false;
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        alpha[h] = 1.0f;
+        if (mx[h] > m_ref[h] + kRescaleThreshold) {
+          alpha[h] = exp2f(m_ref[h] - mx[h]);
+          m_ref[h] = mx[h];
+          l[h] *= alpha[h];
+          moved = true;
+        }
+      }
+      const bool rescale_o = moved && tile != seg_first_tile;
+
+      float pr[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        pr[h] = tok_ok ? exp2f(s[h] - m_ref[h]) : 0.0f;
+        l[h] += pr[h];
+      }
+      uint32_t phi[4], plo[4];
+      split_e4m3_16(pr, phi, plo);
+      {
+        const uint32_t pa = sbase + kOffP + sb * kPBytes + token * 32;
+        const uint32_t sw = (token >> 2) & 1;
+        st_shared_v4(pa + ((0 ^ sw) << 4), phi[0], phi[1], phi[2], phi[3]);
+        st_shared_v4(pa + ((1 ^ sw) << 4), plo[0], plo[1], plo[2], plo[3]);
+      }
+      fence_proxy_async_smem();
+
+      // PV of the previous tile must be complete before this tile's P is
+      // published (and before O is rescaled).
+      if (tile > 0) wait_pv_through(tile - 1);
+      if (rescale_o) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          const uint32_t addr = tmem + lane_base + kColO + 32 * cc;
+          tmem_ld32(addr, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(u2f(o[j]) * alpha[j & 15]);
+          tmem_st32(addr, o);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+      if (t == 0) mbar_arrive(smem_u32(&ms->p_full));
+      ++tile;
+      if (cur.j + 1 == cur.j1) break;
+      ++cur.j;
+    }
+
+    // ------------------------------------------------ segment epilogue
+    float l_tot[16];
+    {
+      float v[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) v[h] = l[h];
+      const float ws = warp_transpose_sum16(v);
+      if ((lane & 1) == 0) ms->red_sum[warp][lane >> 1] = ws;
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        l_tot[h] = (ms->red_sum[0][h] + ms->red_sum[1][h]) + (ms->red_sum[2][h] + ms->red_sum[3][h]);
+    }
+    wait_pv_through(tile - 1);
+    tc_fence_after();
+    const bool write = row_ok && !ms->abort_flag;
+    const int32_t slot = cur.whole ? -1 : partial_slot(c, ms->t0, cur.row_a);
+    float inv[16];
+#pragma unroll
+    for (int h = 0; h < 16; ++h) inv[h] = kv_scale / l_tot[h];
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t o[32];
+      tmem_ld32(tmem + lane_base + kColO + 32 * cc, o);
+      tmem_wait_ld();
+      const int dim = 128 * cc + token;
+      if (write) {
+        if (cur.whole) {
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                               static_cast<size_t>(tq) * kNumHeads * kVDim + dim;
+#pragma unroll
+          for (int h = 0; h < 16; ++h)
+            dst[h * kVDim] = __float2bfloat16_rn((u2f(o[h]) + u2f(o[16 + h]) * 0.0625f) * inv[h]);
+        } else {
+          float* dst = p.partial + static_cast<size_t>(slot) * kNumHeads * kVDim + dim;
+#pragma unroll
+          for (int h = 0; h < 16; ++h)
+            dst[h * kVDim] = (u2f(o[h]) + u2f(o[16 + h]) * 0.0625f) * inv[h];
+        }
+      }
+    }
+    if (write && !cur.whole) {
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        if (t == h) p.lse[slot * kNumHeads + h] = m_ref[h] + log2f(l_tot[h]);
+    }
+    tc_fence_before();
+    named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+    if (t == 0) mbar_arrive(smem_u32(&ms->o_empty));
+    cursor_next_tile(cur, ms, p.kv_indptr, p.batch);
+  }
+}
+
+// ------------------------------------------------------------ kernel
+template <bool kGather>
+__global__ void __launch_bounds__(kStage1Threads, 1)
+    mla_decode_stage1_kernel(const __grid_constant__ CUtensorMap map_v,
+                             const __grid_constant__ CUtensorMap map_r, const Stage1Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Misc* ms = reinterpret_cast<Misc*>(smem + kOffMisc);
+  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(&ms->tmem_base), kTmemCols);
+  if (tid == kProducerWarp * 32) {
+    for (int s = 0; s < kNumVSlots; ++s) {
+      mbar_init(smem_u32(&ms->v_full[s]), 1);
+      mbar_init(smem_u32(&ms->v_empty[s]), 1);
+    }
+    for (int s = 0; s < kNumRSlots; ++s) {
+      mbar_init(smem_u32(&ms->r_full[s]), 1);
+      mbar_init(smem_u32(&ms->r_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&ms->s_full[0]), 1);
+    mbar_init(smem_u32(&ms->s_full[1]), 1);
+    mbar_init(smem_u32(&ms->p_full), 1);
+    mbar_init(smem_u32(&ms->pv_done), 1);
+    mbar_init(smem_u32(&ms->q_full), 1);
+    mbar_init(smem_u32(&ms->q_empty), 1);
+    mbar_init(smem_u32(&ms->o_empty), 1);
+    mbar_init(smem_u32(&ms->mma_done), 1);
+    ms->abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&map_v);
+    prefetch_tensormap(&map_r);
+  }
+  // Stage 2 may start launching now; it waits for this grid's completion
+  // before it reads anything this grid writes.
+  pdl_launch_dependents();
+  schedule_prologue(p, ms);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ms->tmem_base;
+
+  if (warp < 4) {
+    run_softmax(p, ms, sbase, tmem, __ldg(p.kv_scale));
+  } else if (warp == kProducerWarp) {
+    run_producer<kGather>(p, &map_v, &map_r, ms, sbase);
+  } else if (lane == 0) {
+    run_mma(p, ms, sbase, tmem);
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t stage1_smem_bytes() { return static_cast<size_t>(kSmemAlloc); }
+
+cudaError_t stage1_prepare(int device) {
+  (void)device;
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_stage1_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mla_decode_stage1_kernel<true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+}
+
+cudaError_t launch_stage1(const Stage1Params& p, const CUtensorMap& map_v,
+                          const CUtensorMap& map_r, bool gather, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(p.grid)), block(kStage1Threads);
+  if (gather)
+    mla_decode_stage1_kernel<true><<<grid, block, kSmemAlloc, stream>>>(map_v, map_r, p);
+  else
+    mla_decode_stage1_kernel<false><<<grid, block, kSmemAlloc, stream>>>(map_v, map_r, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -28,3 +28,10 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def built_library():
+    """Path of libmla_decode.so, compiled in-tree if missing or stale."""
+    from mla_decode_attention_08_gb300.build import build
+    return build()

@@ -1,0 +1,109 @@
+"""The C ABI on the CPU: exports, plan, host schedule vs the oracle, host-side errors."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from mla_decode_attention_08_gb300 import binding
+from mla_decode_attention_08_gb300.build import ROOT
+from oracle.schedule import plan_grid, worker_table
+from oracle.schedule import schedule as oracle_schedule
+
+HEADER = os.path.join(ROOT, "include", "mla_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib(built_library):
+    return binding.load_library(built_library)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert "mla_decode_fwd" in names and len(names) >= 9
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(binding.SIGNATURES)
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.mla_decode_abi_version() == 1
+    for s in range(5):
+        assert lib.mla_status_string(s)
+
+
+@pytest.mark.parametrize("batch,max_len,sms", [(4, 1024, 152), (32, 1024, 152), (64, 8192, 152),
+                                               (256, 8192, 152), (128, 8192, 148), (1, 0, 152),
+                                               (7, 129, 10)])
+def test_plan_matches_oracle_grid(lib, batch, max_len, sms):
+    plan = binding.mla_decode_plan(batch, max_len, sms)
+    assert plan.grid == plan_grid(batch, max_len, sms)
+    assert plan.tile_tokens == 128 and plan.batch == batch
+    g = plan.grid
+    assert plan.ws_prefix_offset >= 4 and plan.ws_prefix_offset % 256 == 0
+    assert plan.ws_workers_offset >= plan.ws_prefix_offset + 4 * (batch + 1)
+    assert plan.ws_lse_offset >= plan.ws_workers_offset + 16 * g
+    assert plan.ws_partial_offset >= plan.ws_lse_offset + 4 * 32 * g
+    assert plan.ws_bytes >= plan.ws_partial_offset + 4 * 2 * g * 16 * 512
+    assert all(o % 256 == 0 for o in (plan.ws_workers_offset, plan.ws_lse_offset,
+                                      plan.ws_partial_offset, plan.ws_bytes))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_host_schedule_bit_exact_vs_oracle(lib, seed):
+    rng = np.random.default_rng(100 + seed)
+    batch = int(rng.integers(1, 300))
+    lengths = rng.integers(0, int(rng.integers(1, 9000)) + 1, size=batch)
+    lengths[rng.random(batch) < 0.15] = 0
+    indptr = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    grid = int(rng.integers(1, 200))
+    workers, prefix = binding.mla_decode_schedule_host(indptr, grid)
+    assert np.array_equal(workers, worker_table(indptr, grid))
+    assert prefix.tolist() == oracle_schedule(indptr, grid)["prefix"]
+
+
+def test_host_schedule_workload_shapes(lib):
+    for batch, length in [(4, 1024), (32, 1024), (64, 8192), (256, 8192)]:
+        indptr = np.arange(batch + 1, dtype=np.int32) * length
+        grid = plan_grid(batch, length, 152)
+        workers, _ = binding.mla_decode_schedule_host(indptr, grid)
+        assert np.array_equal(workers, worker_table(indptr, grid))
+
+
+def test_host_side_argument_errors(lib):
+    plan = binding.mla_decode_plan(4, 1024, 152)
+    p = ctypes.byref(plan)
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the checks fail first
+    assert lib.mla_decode_fwd(None, fake, fake, fake, fake, fake, None, p, None, 0, 4096,
+                              fake, plan.ws_bytes) == 1
+    bad = binding.mla_plan_t.from_buffer_copy(plan)
+    bad.abi_version = 99
+    assert lib.mla_decode_fwd(fake, fake, fake, fake, fake, fake, None, ctypes.byref(bad), None,
+                              0, 4096, fake, plan.ws_bytes) == 1
+    # misaligned q
+    assert lib.mla_decode_fwd(ctypes.c_void_p((1 << 20) + 2), fake, fake, fake, fake, fake, None,
+                              p, None, 0, 4096, fake, plan.ws_bytes) == 1
+    # kv_rows out of range
+    assert lib.mla_decode_fwd(fake, fake, fake, fake, fake, fake, None, p, None, 0, 0,
+                              fake, plan.ws_bytes) == 1
+    # workspace too small
+    assert lib.mla_decode_fwd(fake, fake, fake, fake, fake, fake, None, p, None, 0, 4096,
+                              fake, plan.ws_bytes - 1) == 3
+    assert lib.mla_decode_plan(0, 10, 152, ctypes.byref(binding.mla_plan_t())) == 1
+    assert lib.mla_decode_plan(3, -1, 152, ctypes.byref(binding.mla_plan_t())) == 1
+    assert lib.mla_decode_schedule_host(None, 3, 3, None, None) == 1
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    plan = binding.mla_decode_plan(1, 128, 152)
+    q = torch.zeros(1, 16, 576, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        binding.mla_decode_fwd(q, q, q, q, q, q, plan=plan, workspace=q)

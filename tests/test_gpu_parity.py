@@ -1,0 +1,209 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from mla_decode_attention_08_gb300 import binding
+from mla_decode_attention_08_gb300.inputs import WORKLOADS, make_from_lengths, make_inputs
+from oracle.fp8 import e4m3fn_decode
+from oracle.schedule import plan_grid, worker_table
+from oracle.schedule import schedule as oracle_schedule
+
+from .gpu_util import DeviceCase, OracleCase, assert_close, num_sms
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(built_library):
+    binding.load_library(built_library)
+
+
+# ------------------------------------------------------------------ small shapes
+SMALL = [
+    ("one_tile", [128], False),
+    ("tails", [1, 127, 128, 129, 255, 257, 1000], False),
+    ("empty_rows", [0, 300, 0, 1, 0], False),
+    ("paged_tails", [3, 129, 700, 64, 1], True),
+    ("long_row", [5000], False),
+    ("many_rows", list(range(1, 400, 13)), True),
+]
+
+
+@pytest.mark.parametrize("name,lengths,paged", SMALL, ids=[s[0] for s in SMALL])
+@pytest.mark.parametrize("sms", [1, 5, None])
+def test_small_shapes(name, lengths, paged, sms):
+    inp = make_from_lengths(lengths, seed=777 + len(lengths), paged=paged)
+    dev = DeviceCase(inp)
+    gpu, err, plan, ws = dev.run(sms=sms)
+    assert err == 0
+    ref = OracleCase(inp).reference()
+    assert_close(gpu, ref)
+    # the schedule the kernel used, bit for bit
+    views = binding.workspace_views(plan, ws)
+    assert np.array_equal(views["workers"].cpu().numpy(), worker_table(inp.kv_indptr, plan.grid))
+    assert views["prefix"].cpu().numpy().tolist() == oracle_schedule(inp.kv_indptr, plan.grid)["prefix"]
+
+
+def test_grid_larger_than_tile_count():
+    # 3 tiles over a grid of 8: most workers have empty ranges.
+    inp = make_from_lengths([130, 1, 0, 120], seed=5)
+    gpu, err, plan, _ = DeviceCase(inp).run(plan=binding.mla_decode_plan(4, 8192, 8))
+    assert plan.grid == 8 and err == 0
+    assert_close(gpu, OracleCase(inp).reference())
+
+
+def test_all_rows_empty():
+    inp = make_from_lengths([0, 0, 0], seed=6, max_kv_len=64)
+    gpu, err, _, _ = DeviceCase(inp).run()
+    assert err == 0 and np.all(gpu == 0)
+
+
+def test_sharp_scores_exercise_rescaling():
+    inp = make_from_lengths([2000, 517, 4096], seed=8)
+    inp.q_bits = (inp.q_bits.view(np.uint16).astype(np.uint32) + (4 << 7)).astype(np.uint16)  # q x 16
+    gpu, err, _, _ = DeviceCase(inp).run(sms=3)
+    assert err == 0
+    assert_close(gpu, OracleCase(inp).reference())
+
+
+def test_one_token_rows_return_v():
+    inp = make_from_lengths([1, 1, 1], seed=9, paged=True)
+    dev = DeviceCase(inp)
+    gpu, err, _, _ = dev.run()
+    assert err == 0
+    codes = dev.kv_codes.cpu().numpy()
+    scale = np.float32(dev.kv_scale.item())
+    for b in range(3):
+        slot = inp.kv_indices[b]
+        v32 = (e4m3fn_decode(codes[slot, :512]).astype(np.float32) * scale).astype(np.float32)
+        want = torch.from_numpy(v32).to(torch.bfloat16).float().numpy()
+        assert np.array_equal(gpu[b], np.broadcast_to(want, (16, 512))), b
+
+
+def test_constant_scores_return_mean_of_v():
+    inp = make_from_lengths([300, 77], seed=10)
+    q = inp.q_bits.reshape(2, 16, 576).copy()
+    q[:, :, :512] = 0
+    inp.q_bits = q
+    kv = inp.kv_bits.copy()
+    kv[:, 512:] = kv[0, 512:]
+    inp.kv_bits = kv
+    dev = DeviceCase(inp)
+    gpu, err, _, _ = dev.run(sms=4)
+    assert err == 0
+    codes = dev.kv_codes.cpu().numpy().astype(np.uint8)
+    scale = float(dev.kv_scale.item())
+    for b, (j0, j1) in enumerate([(0, 300), (300, 377)]):
+        mean_v = (e4m3fn_decode(codes[j0:j1, :512]) * scale).mean(axis=0)
+        np.testing.assert_allclose(gpu[b], np.broadcast_to(mean_v, (16, 512)), rtol=1e-2, atol=1e-3)
+
+
+def test_permuted_cache_matches_contiguous():
+    inp = make_from_lengths([900, 33, 1500], seed=11)
+    a, err_a, _, _ = DeviceCase(inp).run(sms=7)
+    perm = np.random.default_rng(3).permutation(inp.kv_bits.shape[0])
+    paged = make_from_lengths([900, 33, 1500], seed=11)
+    paged.kv_bits = np.empty_like(inp.kv_bits)
+    paged.kv_bits[perm] = inp.kv_bits          # token j now lives in cache row perm[j]
+    paged.kv_indices = perm.astype(np.int32)
+    b, err_b, _, _ = DeviceCase(paged).run(sms=7)
+    assert err_a == 0 and err_b == 0
+    np.testing.assert_allclose(a, b, rtol=1e-2, atol=2e-3)
+
+
+def test_split_count_invariance():
+    inp = make_from_lengths([3000, 1024, 17], seed=12, paged=True)
+    dev = DeviceCase(inp)
+    ref = OracleCase(inp).reference()
+    for sms in (1, 2, 3, 9, 40, 152):
+        gpu, err, _, _ = dev.run(sms=sms)
+        assert err == 0
+        assert_close(gpu, ref)
+
+
+# ------------------------------------------------------------------ codec
+def test_fp8_quantize_bit_exact():
+    inp = make_from_lengths([3000, 1], seed=13)
+    dev, ora = DeviceCase(inp), OracleCase(inp)
+    assert np.float32(dev.kv_scale.item()) == ora.scale
+    assert np.array_equal(dev.kv_codes.cpu().numpy(), ora.codes())
+
+
+def test_fp8_quantize_every_bf16_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    exp = (bits >> 7) & 0xFF
+    bits = bits[exp != 0xFF]                   # finite values only
+    src = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    codes = torch.empty(bits.size, dtype=torch.uint8, device="cuda")
+    scale = torch.empty(1, dtype=torch.float32, device="cuda")
+    binding.mla_fp8_quantize_per_tensor(src, codes, scale, torch.empty(16, dtype=torch.uint8, device="cuda"))
+    from mla_decode_attention_08_gb300.inputs import bf16_bits_to_f32
+    from oracle.quant import quantize_per_tensor
+    want_codes, want_scale = quantize_per_tensor(bf16_bits_to_f32(bits))
+    assert np.float32(scale.item()) == want_scale
+    assert np.array_equal(codes.cpu().numpy(), want_codes)
+
+
+# ------------------------------------------------------------------ host-made input errors
+def test_bad_query_row_is_flagged_and_skipped():
+    inp = make_from_lengths([200, 300, 100], seed=14)
+    dev = DeviceCase(inp)
+    dev.qo_indptr = torch.tensor([0, 2, 2, 3], dtype=torch.int32, device="cuda")
+    dev.out.fill_(7.0)
+    gpu, err, _, _ = dev.run(sms=2)
+    assert err & 1
+    ref = OracleCase(make_from_lengths([200, 300, 100], seed=14)).reference()
+    assert_close(gpu[2:3], ref[2:3])
+
+
+def test_decreasing_kv_indptr_gives_zeros_and_flag():
+    inp = make_from_lengths([200, 300], seed=15)
+    dev = DeviceCase(inp)
+    dev.kv_indptr = torch.tensor([0, 300, 200], dtype=torch.int32, device="cuda")
+    gpu, err, _, _ = dev.run()
+    assert err & 2 and np.all(gpu == 0)
+
+
+def test_out_of_range_page_index_is_flagged():
+    inp = make_from_lengths([50, 60], seed=16, paged=True)
+    dev = DeviceCase(inp)
+    bad = dev.kv_indices.clone()
+    bad[5] = 10 ** 6
+    dev.kv_indices = bad
+    _, err, _, _ = dev.run()
+    assert err & 4
+
+
+# ------------------------------------------------------------------ the benchmark workloads
+def _sample_rows(inp, plan, k=6):
+    """First, last, and rows split across workers (both kinds of output path)."""
+    sch = oracle_schedule(inp.kv_indptr, plan.grid)
+    split = [b for b, ws in sch["covers"].items() if len(ws) > 1]
+    whole = [b for b, ws in sch["covers"].items() if len(ws) == 1]
+    rows = {0, inp.batch - 1}
+    rows.update(split[:k // 2])
+    rows.update(whole[:k // 2])
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workload_parity(name):
+    inp = make_inputs(name)
+    dev = DeviceCase(inp)
+    gpu, err, plan, ws = dev.run()
+    assert err == 0
+    assert np.isfinite(gpu).all()
+    ora = OracleCase(inp)
+    full = inp.batch * inp.max_kv_len <= 32 * 1024
+    rows = None if full else _sample_rows(inp, plan)
+    ref = ora.reference(rows)
+    st = assert_close(gpu, ref, rows)
+    print(name, "grid", plan.grid, st)
+    # the cache codes the kernel read, bit-exact on the sampled cache rows
+    check = np.arange(min(4096, inp.kv_bits.shape[0]))
+    assert np.float32(dev.kv_scale.item()) == ora.scale
+    assert np.array_equal(dev.kv_codes[: check.size].cpu().numpy(), ora.codes(check))
+    views = binding.workspace_views(plan, ws)
+    assert np.array_equal(views["workers"].cpu().numpy(), worker_table(inp.kv_indptr, plan.grid))
+    assert plan.grid == plan_grid(inp.batch, inp.max_kv_len, num_sms())
