@@ -11,8 +11,8 @@ constexpr int kNumVSlots = 10;      // 16 KB slots: tokens x 128 latent dims (sw
 constexpr int kNumRSlots = 3;       // 8 KB slots: tokens x 64 rope dims (swizzle 64B)
 constexpr int kVPanelBytes = 128 * 128;
 constexpr int kRPanelBytes = 128 * 64;
-constexpr int kStage1Threads = 192; // warps 0-3 softmax/epilogue, 4 TMA producer, 5 MMA issuer
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
+constexpr int kStage1Threads = 224; // warps 0-3 softmax/epilogue, 4 TMA producer, 5 MMA issuer, 6 TMA watcher
+constexpr long long kWaitLimitCycles = 2000000000LL;  // ~1 s per pipeline wait at 2 GHz
 
 struct Stage1Params {
   const uint16_t* q;          // bf16 bits [B, 16, 576]

@@ -17,6 +17,8 @@
 // Both operands of each product are FP8 e4m3 (kind::f8f6f4).  Q and P keep
 // bf16-level precision by a two-term split x ~= hi + lo / 16 with both terms
 // e4m3: the 16 "hi" heads and 16 "lo" heads form N = 32.
+#include <cstddef>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -45,15 +47,20 @@ struct Misc {
   uint64_t v_empty[kNumVSlots];
   uint64_t r_full[kNumRSlots];
   uint64_t r_empty[kNumRSlots];
-  uint64_t s_full[2];
-  uint64_t p_full;
-  uint64_t pv_done;
-  uint64_t q_full;
-  uint64_t q_empty;
-  uint64_t o_empty;
+  uint64_t s_full[2];   // QK of tile i landed in S[i & 1]
+  uint64_t pv_done[2];  // PV of tile i completed (P[i & 1] free again)
+  uint64_t q_empty;     // the segment's last QK completed (Q operand free)
   uint64_t mma_done;
-  float red_max[2][4][16];
-  float red_sum[4][16];
+  // Monotonic counters the MMA issuer polls (st.release / ld.acquire).  It never
+  // polls the TMA barriers themselves: testing a barrier whose copy is still in
+  // flight stalls the testing thread for about a panel's transfer time.
+  uint32_t data_ready;  // tiles whose five panels have landed (set by the watcher warp)
+  uint32_t q_ready;     // segments whose Q operand is written
+  uint32_t s_read;      // tiles whose S has been read out by every softmax warp
+  uint32_t p_ready;     // tiles whose P is published (and O rescaled)
+  uint32_t o_free;      // segments whose epilogue has read O out of TMEM
+  alignas(16) float red_max[2][4][16];  // read and written as float4
+  alignas(16) float red_sum[4][16];
   uint32_t red_u32[8];
   int32_t scan[8];
   uint32_t tmem_base;
@@ -63,6 +70,10 @@ struct Misc {
   int32_t first_row, first_prefix, last_row;
   int32_t bad;
 };
+
+static_assert(offsetof(Misc, red_max) % 16 == 0 && offsetof(Misc, red_sum) % 16 == 0,
+              "vector accesses to the reduction scratch need 16-byte alignment");
+static_assert(kOffMisc % 16 == 0, "the barrier block must start 16-byte aligned");
 
 constexpr int kSmemUsed = kOffMisc + static_cast<int>(sizeof(Misc));
 constexpr int kSmemAlloc = kSmemUsed + 1024;  // room to align the base to 1024 B
@@ -75,7 +86,8 @@ constexpr uint32_t kColO = 64;
 
 constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kMmaWarp = 5;  // the single tcgen05.mma issuer; owns the TMEM allocation
+constexpr int kWatchWarp = 6;  // waits on the TMA barriers, publishes data_ready
 constexpr uint32_t kBarSoftmax = 1;  // named barrier id of warps 0-3
 
 // Operand descriptors (layout codes: 2 = 128B swizzle, 4 = 64B, 6 = 32B).
@@ -94,16 +106,18 @@ __device__ __forceinline__ int32_t ldg_i32(const int32_t* p) { return __ldg(p); 
 __device__ __forceinline__ void set_error(int32_t* err, int32_t bits) { atomicOr(err, bits); }
 
 // Bounded wait on an mbarrier phase.  Returns false when the call is being
-// abandoned (this or another role timed out); never spins without limit.
+// abandoned (this or another role timed out); never spins without limit.  The
+// limit is counted in SM cycles (clock64 is cheap to read, unlike the global
+// timer): kWaitLimitCycles is about one second at the maximum SM clock.
 __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, Misc* ms, int32_t* err) {
   if (ms->abort_flag) return false;
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t start = global_timer_ns();
+  const long long start = clock64();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 31) == 0) {
+    if ((n & 15) == 0) {
       if (ms->abort_flag) return false;
-      if (global_timer_ns() - start > kWaitLimitNs) {
+      if (clock64() - start > kWaitLimitCycles) {
         ms->abort_flag = 1;
         set_error(err, MLA_DERR_TIMEOUT);
         return false;
@@ -167,12 +181,12 @@ __device__ bool cursor_next_tile(Cursor& c, const Misc* ms, const int32_t* kv_in
   return c.live;
 }
 
-// Bounded wait used only while draining after an abandoned call.
+// Bounded wait used only while draining at the end of a call.
 __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity) {
-  const uint64_t start = global_timer_ns();
+  const long long start = clock64();
   for (uint32_t n = 0;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 31) == 31 && global_timer_ns() - start > kWaitLimitNs) return false;
+    if ((n & 15) == 15 && clock64() - start > kWaitLimitCycles) return false;
   }
 }
 
@@ -391,83 +405,78 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, uint32_t
   }
 }
 
+// MMA issuer (warp 5, lane 0): the only thread that issues tcgen05.mma.
+// QK of tile i needs its five panels landed, the segment's Q operand (first
+// tile of a segment) and S[i & 1] read out by the softmax of tile i - 2.  PV of
+// tile i needs P[i & 1] published and, on the first tile of a later segment, O
+// read out by the previous segment's epilogue.  All five conditions are
+// monotonic counters in shared memory; both products are polled so that
+// neither waits behind the other.
 __device__ void run_mma(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
   Cursor qc, pc;
   cursor_start(qc, ms, p.kv_indptr, p.batch);
   cursor_start(pc, ms, p.kv_indptr, p.batch);
   uint32_t qk_n = 0, pv_n = 0;  // tiles whose QK / PV have been issued
-  uint32_t qk_stage = 0;        // preconditions of the next QK already observed
-  uint64_t last_progress = global_timer_ns();
+  long long last_progress = clock64();
 
   while (pc.live) {
     bool progressed = false;
-    // QK of tile qk_n: its rope + 4 latent panels landed, its Q operand is
-    // written (first tile of a segment), and the S buffer it overwrites has
-    // been read (PV of tile qk_n - 2 issued implies that softmax finished it).
-    if (qc.live && qk_n <= pv_n + 1) {
-      while (qk_stage < 6) {
-        uint32_t bar, parity;
-        if (qk_stage == 0) {
-          bar = smem_u32(&ms->r_full[qk_n % kNumRSlots]);
-          parity = (qk_n / kNumRSlots) & 1;
-        } else if (qk_stage <= 4) {
-          const uint32_t g = qk_n * 4 + (qk_stage - 1);
-          bar = smem_u32(&ms->v_full[g % kNumVSlots]);
-          parity = (g / kNumVSlots) & 1;
-        } else {
-          if (qc.j != qc.j0) {
-            qk_stage = 6;
-            break;
-          }
-          bar = smem_u32(&ms->q_full);
-          parity = qc.seg & 1;
-        }
-        if (!mbar_test_wait(bar, parity)) break;
-        ++qk_stage;
-      }
-      if (qk_stage == 6) {
-        tc_fence_after();
-        issue_qk(tmem, sbase, qk_n);
-        umma_commit(smem_u32(&ms->s_full[qk_n & 1]));
-        umma_commit(smem_u32(&ms->r_empty[qk_n % kNumRSlots]));
-        if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
-        ++qk_n;
-        qk_stage = 0;
-        progressed = true;
-        cursor_next_tile(qc, ms, p.kv_indptr, p.batch);
-      }
+    if (qc.live && ld_acquire_u32(&ms->data_ready) > qk_n &&
+        (qc.j != qc.j0 || ld_acquire_u32(&ms->q_ready) > static_cast<uint32_t>(qc.seg)) &&
+        (qk_n < 2 || ld_acquire_u32(&ms->s_read) + 1 >= qk_n)) {
+      tc_fence_after();
+      issue_qk(tmem, sbase, qk_n);
+      umma_commit(smem_u32(&ms->s_full[qk_n & 1]));
+      umma_commit(smem_u32(&ms->r_empty[qk_n % kNumRSlots]));
+      if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
+      ++qk_n;
+      progressed = true;
+      cursor_next_tile(qc, ms, p.kv_indptr, p.batch);
     }
-    // PV of tile pv_n: its P is published, and (first tile of a later segment)
-    // the previous segment's epilogue has read O out of TMEM.
     if (pv_n < qk_n) {
       const bool first = pc.j == pc.j0;
-      bool ready = mbar_test_wait(smem_u32(&ms->p_full), pv_n & 1);
-      if (ready && first && pc.seg > 0)
-        ready = mbar_test_wait(smem_u32(&ms->o_empty), (pc.seg - 1) & 1);
-      if (ready) {
+      if (ld_acquire_u32(&ms->p_ready) > pv_n &&
+          (!first || pc.seg == 0 || ld_acquire_u32(&ms->o_free) >= static_cast<uint32_t>(pc.seg))) {
         tc_fence_after();
         issue_pv(tmem, sbase, pv_n, first, ms);
-        umma_commit(smem_u32(&ms->pv_done));
+        umma_commit(smem_u32(&ms->pv_done[pv_n & 1]));
         ++pv_n;
         progressed = true;
         cursor_next_tile(pc, ms, p.kv_indptr, p.batch);
       }
     }
     if (progressed) {
-      last_progress = global_timer_ns();
+      last_progress = clock64();
     } else {
       if (ms->abort_flag) break;
-      if (global_timer_ns() - last_progress > kWaitLimitNs) {
+      if (clock64() - last_progress > kWaitLimitCycles) {
         ms->abort_flag = 1;
         set_error(p.err, MLA_DERR_TIMEOUT);
         break;
       }
-      __nanosleep(20);
     }
   }
   // Every MMA issued by this thread completes before TMEM is released.
   umma_commit(smem_u32(&ms->mma_done));
   drain_phase(smem_u32(&ms->mma_done), 0);
+}
+
+// Watcher (warp 6, lane 0): waits for each tile's rope and latent panels to
+// land, in tile order, and publishes the count.
+__device__ void run_watcher(const Stage1Params& p, Misc* ms) {
+  Cursor cur;
+  cursor_start(cur, ms, p.kv_indptr, p.batch);
+  uint32_t tile = 0;
+  while (cur.live) {
+    bool ok = wait_phase(smem_u32(&ms->r_full[tile % kNumRSlots]), (tile / kNumRSlots) & 1, ms, p.err);
+    for (int c = 0; c < 4 && ok; ++c) {
+      const uint32_t g = tile * 4 + c;
+      ok = wait_phase(smem_u32(&ms->v_full[g % kNumVSlots]), (g / kNumVSlots) & 1, ms, p.err);
+    }
+    if (!ok) break;
+    st_release_u32(&ms->data_ready, ++tile);
+    cursor_next_tile(cur, ms, p.kv_indptr, p.batch);
+  }
 }
 
 // ------------------------------------------------------------ softmax warps (0-3)
@@ -595,8 +604,45 @@ __device__ float prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t
   }
   fence_proxy_async_smem();
   named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-  if (t == 0) mbar_arrive(smem_u32(&ms->q_full));
   return down * kv_scale * kSmScaleLog2;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Named-barrier arrival of the softmax warpgroup that also ORs a predicate.
+__device__ __forceinline__ bool softmax_bar_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; bar.red.or.pred po, %2, %3, pi;"
+      " selp.u32 %0, 1, 0, po; }"
+      : "=r"(r) : "r"(static_cast<uint32_t>(v)), "r"(kBarSoftmax), "r"(kSoftmaxThreads) : "memory");
+  return r != 0;
+}
+
+// Two-term e4m3 split of 16 probabilities (0 <= p <= 256) via packed half2:
+// hi = e4m3(p), lo = e4m3(16 (p - hi)).
+__device__ __forceinline__ void split_p_16(const float (&x)[16], uint32_t (&hi)[4],
+                                           uint32_t (&lo)[4]) {
+  const __half2 sixteen = __float2half2_rn(16.0f);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const __half2 p2 = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
+    const uint16_t h8 = cvt_f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&p2));
+    const uint32_t hb = cvt_e4m3x2_to_f16x2(h8);
+    const __half2 r = __hmul2(__hsub2(p2, *reinterpret_cast<const __half2*>(&hb)), sixteen);
+    const uint16_t l8 = cvt_f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&r));
+    if (k & 1) {
+      hi[k >> 1] |= static_cast<uint32_t>(h8) << 16;
+      lo[k >> 1] |= static_cast<uint32_t>(l8) << 16;
+    } else {
+      hi[k >> 1] = h8;
+      lo[k >> 1] = l8;
+    }
+  }
 }
 
 __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem,
@@ -608,13 +654,15 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
 
   Cursor cur;
   cursor_start(cur, ms, p.kv_indptr, p.batch);
-  uint32_t tile = 0;     // tiles processed by this CTA
-  uint32_t pv_seen = 0;  // pv_done phases consumed
+  uint32_t tile = 0;                 // tiles processed by this CTA
+  uint32_t pv_seen[2] = {0, 0};      // pv_done[b] phases consumed
 
-  auto wait_pv_through = [&](uint32_t k) {
-    while (pv_seen <= k) {
-      wait_phase(smem_u32(&ms->pv_done), pv_seen & 1, ms, p.err);
-      ++pv_seen;
+  // Wait until the PV of tile k has completed (phases are consumed in order).
+  auto wait_pv = [&](uint32_t k) {
+    const uint32_t b = k & 1;
+    while (pv_seen[b] <= (k >> 1)) {
+      wait_phase(smem_u32(&ms->pv_done[b]), pv_seen[b] & 1, ms, p.err);
+      ++pv_seen[b];
     }
   };
 
@@ -626,6 +674,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     if (!row_ok && t == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
     if (cur.seg > 0) wait_phase(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
     const float qk_scale = prepare_q(p, ms, sbase + kOffQ, row_ok ? tq : -1, kv_scale);
+    const float qk_scale_lo = qk_scale * 0.0625f;
+    if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 1));
 
     float m_ref[16], l[16];
 #pragma unroll
@@ -644,48 +694,57 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       uint32_t r[32];
       tmem_ld32(tmem + lane_base + kColS + 32 * sb, r);
       tmem_wait_ld();
+      tc_fence_before();
 
       const bool tok_ok = token < valid;
       float s[16];
+      bool exceed = false;
 #pragma unroll
-      for (int h = 0; h < 16; ++h)
-        s[h] = tok_ok ? (u2f(r[h]) + u2f(r[16 + h]) * 0.0625f) * qk_scale : -INFINITY;
-
-      // Row maximum of this tile, per head, over the 128 tokens.
-      float mx[16];
-#pragma unroll
-      for (int h = 0; h < 16; ++h) mx[h] = warp_max(s[h]);
-      if (lane == 0) {
-        float4* dst = reinterpret_cast<float4*>(&ms->red_max[sb][warp][0]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          dst[k] = make_float4(mx[4 * k], mx[4 * k + 1], mx[4 * k + 2], mx[4 * k + 3]);
-      }
-      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float4 m4 = reinterpret_cast<const float4*>(&ms->red_max[sb][0][0])[k];
-#pragma unroll
-        for (int w = 1; w < 4; ++w) {
-          const float4 o4 = reinterpret_cast<const float4*>(&ms->red_max[sb][w][0])[k];
-          m4.x = fmaxf(m4.x, o4.x); m4.y = fmaxf(m4.y, o4.y);
-          m4.z = fmaxf(m4.z, o4.z); m4.w = fmaxf(m4.w, o4.w);
-        }
-        mx[4 * k] = m4.x; mx[4 * k + 1] = m4.y; mx[4 * k + 2] = m4.z; mx[4 * k + 3] = m4.w;
+      for (int h = 0; h < 16; ++h) {
+        s[h] = tok_ok ? fmaf(u2f(r[16 + h]), qk_scale_lo, u2f(r[h]) * qk_scale) : -INFINITY;
+        exceed |= s[h] > m_ref[h] + kRescaleThreshold;
       }
 
-      // Lazy reference maximum: move it only when the tile maximum exceeds it by
-      // more than the threshold (always on a segment's first tile).
+      // The reference maximum moves only when some score exceeds it by more
+      // than the threshold (always on a segment's first tile); then the tile
+      // maximum per head is reduced over the 128 tokens.
       float alpha[16];
       bool moved = false;
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        alpha[h] = 1.0f;
-        if (mx[h] > m_ref[h] + kRescaleThreshold) {
-          alpha[h] = exp2f(m_ref[h] - mx[h]);
-          m_ref[h] = mx[h];
-          l[h] *= alpha[h];
-          moved = true;
+      for (int h = 0; h < 16; ++h) alpha[h] = 1.0f;
+      const bool any_exceed = softmax_bar_or(exceed);
+      // Every softmax warp has read S[sb] (its tcgen05.ld completed before the barrier).
+      if (t == 0) st_release_u32(&ms->s_read, tile + 1);
+      if (any_exceed) {
+        float mx[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) mx[h] = warp_max(s[h]);
+        if (lane == 0) {
+          float4* dst = reinterpret_cast<float4*>(&ms->red_max[sb][warp][0]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            dst[k] = make_float4(mx[4 * k], mx[4 * k + 1], mx[4 * k + 2], mx[4 * k + 3]);
+        }
+        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float4 m4 = reinterpret_cast<const float4*>(&ms->red_max[sb][0][0])[k];
+#pragma unroll
+          for (int w = 1; w < 4; ++w) {
+            const float4 o4 = reinterpret_cast<const float4*>(&ms->red_max[sb][w][0])[k];
+            m4.x = fmaxf(m4.x, o4.x); m4.y = fmaxf(m4.y, o4.y);
+            m4.z = fmaxf(m4.z, o4.z); m4.w = fmaxf(m4.w, o4.w);
+          }
+          mx[4 * k] = m4.x; mx[4 * k + 1] = m4.y; mx[4 * k + 2] = m4.z; mx[4 * k + 3] = m4.w;
+        }
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          if (mx[h] > m_ref[h] + kRescaleThreshold) {
+            alpha[h] = fast_exp2(m_ref[h] - mx[h]);  // 0 on a segment's first tile
+            m_ref[h] = mx[h];
+            l[h] *= alpha[h];
+            moved = true;
+          }
         }
       }
       const bool rescale_o = moved && tile != seg_first_tile;
@@ -693,11 +752,14 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       float pr[16];
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
-        pr[h] = tok_ok ? exp2f(s[h] - m_ref[h]) : 0.0f;
+        pr[h] = tok_ok ? fast_exp2(s[h] - m_ref[h]) : 0.0f;
         l[h] += pr[h];
       }
       uint32_t phi[4], plo[4];
-      split_e4m3_16(pr, phi, plo);
+      split_p_16(pr, phi, plo);
+
+      // P[sb] was last read by the PV of tile - 2.
+      if (tile >= 2) wait_pv(tile - 2);
       {
         const uint32_t pa = sbase + kOffP + sb * kPBytes + token * 32;
         const uint32_t sw = (token >> 2) & 1;
@@ -705,11 +767,9 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         st_shared_v4(pa + ((1 ^ sw) << 4), plo[0], plo[1], plo[2], plo[3]);
       }
       fence_proxy_async_smem();
-
-      // PV of the previous tile must be complete before this tile's P is
-      // published (and before O is rescaled).
-      if (tile > 0) wait_pv_through(tile - 1);
       if (rescale_o) {
+        // O must hold every earlier tile before it is rescaled.
+        wait_pv(tile - 1);
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
@@ -725,7 +785,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       }
       tc_fence_before();
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-      if (t == 0) mbar_arrive(smem_u32(&ms->p_full));
+      if (t == 0) st_release_u32(&ms->p_ready, tile + 1);
       ++tile;
       if (cur.j + 1 == cur.j1) break;
       ++cur.j;
@@ -744,7 +804,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       for (int h = 0; h < 16; ++h)
         l_tot[h] = (ms->red_sum[0][h] + ms->red_sum[1][h]) + (ms->red_sum[2][h] + ms->red_sum[3][h]);
     }
-    wait_pv_through(tile - 1);
+    wait_pv(tile - 1);  // PV of the segment's last tile (and so of all before it)
     tc_fence_after();
     const bool write = row_ok && !ms->abort_flag;
     const int32_t slot = cur.whole ? -1 : partial_slot(c, ms->t0, cur.row_a);
@@ -779,7 +839,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     }
     tc_fence_before();
     named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-    if (t == 0) mbar_arrive(smem_u32(&ms->o_empty));
+    if (t == 0) st_release_u32(&ms->o_free, static_cast<uint32_t>(cur.seg + 1));
     cursor_next_tile(cur, ms, p.kv_indptr, p.batch);
   }
 }
@@ -806,13 +866,12 @@ __global__ void __launch_bounds__(kStage1Threads, 1)
       mbar_init(smem_u32(&ms->r_full[s]), 1);
       mbar_init(smem_u32(&ms->r_empty[s]), 1);
     }
-    mbar_init(smem_u32(&ms->s_full[0]), 1);
-    mbar_init(smem_u32(&ms->s_full[1]), 1);
-    mbar_init(smem_u32(&ms->p_full), 1);
-    mbar_init(smem_u32(&ms->pv_done), 1);
-    mbar_init(smem_u32(&ms->q_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ms->s_full[i]), 1);
+      mbar_init(smem_u32(&ms->pv_done[i]), 1);
+    }
     mbar_init(smem_u32(&ms->q_empty), 1);
-    mbar_init(smem_u32(&ms->o_empty), 1);
+    ms->data_ready = ms->q_ready = ms->s_read = ms->p_ready = ms->o_free = 0;
     mbar_init(smem_u32(&ms->mma_done), 1);
     ms->abort_flag = 0;
     fence_mbar_init();
@@ -832,8 +891,10 @@ __global__ void __launch_bounds__(kStage1Threads, 1)
     run_softmax(p, ms, sbase, tmem, __ldg(p.kv_scale));
   } else if (warp == kProducerWarp) {
     run_producer<kGather>(p, &map_v, &map_r, ms, sbase);
-  } else if (lane == 0) {
+  } else if (warp == kMmaWarp && lane == 0) {
     run_mma(p, ms, sbase, tmem);
+  } else if (warp == kWatchWarp && lane == 0) {
+    run_watcher(p, ms);
   }
   __syncwarp();
   tc_fence_before();
