@@ -113,6 +113,34 @@ mla_status_t mla_decode_fwd(const void* q_bf16, const void* kv_fp8, const float*
                             const int32_t* kv_indices, int64_t kv_indices_len, int64_t kv_rows,
                             void* workspace, size_t workspace_bytes);
 
+/*
+ * mla_decode_fwd_static_scratch — mla_decode_fwd without a caller workspace.
+ * The pages have no counterpart: this entry exists for callers that must not
+ * allocate device memory, such as a plugin inside a host application that owns
+ * every device allocation and passes the plugin only its inputs and outputs, or
+ * a serving loop where an allocation (which can synchronise the device) is not
+ * allowed.  The scratch is a static array of MLA_STATIC_SCRATCH_BYTES that the
+ * library reserves on every GPU it is loaded on and keeps until the process
+ * exits; nothing is allocated per call.
+ *   Arguments as mla_decode_fwd, minus workspace / workspace_bytes.
+ *   Returns MLA_ERR_WORKSPACE_TOO_SMALL when plan->ws_bytes exceeds
+ *   MLA_STATIC_SCRATCH_BYTES (on a 152-SM GB300 every batch of up to ~600,000
+ *   rows fits).
+ *   The first call on a device looks up that device's copy of the array; make
+ *   that first call before any stream capture.
+ *   All calls share the one array: calls that may overlap on the GPU (different
+ *   streams, or different host threads on the same device) race and must be
+ *   ordered by the caller.  Device-side input errors (MLA_DERR_*) are not
+ *   reported through this entry point; use mla_decode_fwd to diagnose inputs.
+ */
+#define MLA_STATIC_SCRATCH_BYTES (12u * 1024u * 1024u)
+mla_status_t mla_decode_fwd_static_scratch(const void* q_bf16, const void* kv_fp8,
+                                           const float* kv_scale, const int32_t* qo_indptr,
+                                           const int32_t* kv_indptr, void* out_bf16,
+                                           cudaStream_t stream, const mla_plan_t* plan,
+                                           const int32_t* kv_indices, int64_t kv_indices_len,
+                                           int64_t kv_rows);
+
 /* The two stages of mla_decode_fwd launched separately (same arguments); the
  * pair is equivalent to one mla_decode_fwd call.  Used to time stage 1 alone. */
 mla_status_t mla_decode_stage1(const void* q_bf16, const void* kv_fp8, const float* kv_scale,

@@ -43,6 +43,7 @@ SIGNATURES = {
     "mla_decode_plan": (ctypes.c_int, [_I32, _I32, _I32, _PLANP]),
     "mla_decode_fwd": (ctypes.c_int, _FWD_ARGS),
     "mla_decode_stage1": (ctypes.c_int, _FWD_ARGS),
+    "mla_decode_fwd_static_scratch": (ctypes.c_int, _FWD_ARGS[:-2]),
     "mla_decode_stage2": (ctypes.c_int, [_VP, _VP, _VP, _PLANP, _VP, _SZ]),
     "mla_fp8_quantize_per_tensor": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP, _SZ, _VP]),
     "mla_decode_workspace_init": (ctypes.c_int, [_VP, _SZ, _VP]),
@@ -123,6 +124,21 @@ def mla_decode_fwd(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream=None, 
     _check("mla_decode_fwd", load_library().mla_decode_fwd(
         *_fwd_args(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream, plan, kv_indices,
                    workspace)))
+    return out
+
+
+def mla_decode_fwd_static_scratch(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream=None, *,
+                                  plan, kv_indices=None) -> torch.Tensor:
+    """Decode step with the library's own static scratch instead of a workspace,
+    for callers that may not allocate device memory (see the C header)."""
+    if kv_fp8.dim() == 3:
+        kv_fp8 = kv_fp8.reshape(kv_fp8.shape[0], -1)
+    _check("mla_decode_fwd_static_scratch", load_library().mla_decode_fwd_static_scratch(
+        _dev_ptr(q, "q", torch.bfloat16), _dev_ptr(kv_fp8, "kv_fp8"),
+        _dev_ptr(kv_scale, "kv_scale", torch.float32), _dev_ptr(qo_indptr, "qo_indptr", torch.int32),
+        _dev_ptr(kv_indptr, "kv_indptr", torch.int32), _dev_ptr(out, "out", torch.bfloat16),
+        _stream(stream), ctypes.byref(plan), _dev_ptr(kv_indices, "kv_indices", torch.int32),
+        0 if kv_indices is None else int(kv_indices.numel()), int(kv_fp8.shape[0])))
     return out
 
 
