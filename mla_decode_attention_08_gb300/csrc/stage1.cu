@@ -421,18 +421,7 @@ __device__ void run_mma(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_
 
   while (pc.live) {
     bool progressed = false;
-    if (qc.live && ld_acquire_u32(&ms->data_ready) > qk_n &&
-        (qc.j != qc.j0 || ld_acquire_u32(&ms->q_ready) > static_cast<uint32_t>(qc.seg)) &&
-        (qk_n < 2 || ld_acquire_u32(&ms->s_read) + 1 >= qk_n)) {
-      tc_fence_after();
-      issue_qk(tmem, sbase, qk_n);
-      umma_commit(smem_u32(&ms->s_full[qk_n & 1]));
-      umma_commit(smem_u32(&ms->r_empty[qk_n % kNumRSlots]));
-      if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
-      ++qk_n;
-      progressed = true;
-      cursor_next_tile(qc, ms, p.kv_indptr, p.batch);
-    }
+    // PV first: it releases the tile's latent slots for the next loads.
     if (pv_n < qk_n) {
       const bool first = pc.j == pc.j0;
       if (ld_acquire_u32(&ms->p_ready) > pv_n &&
@@ -444,6 +433,18 @@ __device__ void run_mma(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_
         progressed = true;
         cursor_next_tile(pc, ms, p.kv_indptr, p.batch);
       }
+    }
+    if (qc.live && ld_acquire_u32(&ms->data_ready) > qk_n &&
+        (qc.j != qc.j0 || ld_acquire_u32(&ms->q_ready) > static_cast<uint32_t>(qc.seg)) &&
+        (qk_n < 2 || ld_acquire_u32(&ms->s_read) + 1 >= qk_n)) {
+      tc_fence_after();
+      issue_qk(tmem, sbase, qk_n);
+      umma_commit(smem_u32(&ms->s_full[qk_n & 1]));
+      umma_commit(smem_u32(&ms->r_empty[qk_n % kNumRSlots]));
+      if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
+      ++qk_n;
+      progressed = true;
+      cursor_next_tile(qc, ms, p.kv_indptr, p.batch);
     }
     if (progressed) {
       last_progress = clock64();
