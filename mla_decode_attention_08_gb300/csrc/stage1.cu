@@ -51,7 +51,8 @@ struct Misc {
   uint64_t pv_done[2];  // PV of tile i completed (P[i & 1] free again)
   uint64_t q_empty;     // the segment's last QK completed (Q operand free)
   uint64_t mma_done;
-  // Monotonic counters the MMA issuer polls (st.release / ld.acquire).  It never
+  // Monotonic counters the MMA issuer polls (st.release, then relaxed loads
+  // followed by fence.acq_rel once a condition holds).  It never
   // polls the TMA barriers themselves: testing a barrier whose copy is still in
   // flight stalls the testing thread for about a panel's transfer time.
   uint32_t data_ready;  // tiles whose five panels have landed (set by the watcher warp)
@@ -109,7 +110,7 @@ __device__ __forceinline__ void set_error(int32_t* err, int32_t bits) { atomicOr
 // abandoned (this or another role timed out); never spins without limit.  The
 // limit is counted in SM cycles (clock64 is cheap to read, unlike the global
 // timer): kWaitLimitCycles is about one second at the maximum SM clock.
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, Misc* ms, int32_t* err) {
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, Misc* ms, int32_t* err) {
   if (ms->abort_flag) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
@@ -124,6 +125,11 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, Misc* ms,
       }
     }
   }
+}
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Misc* ms, int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;  // the common case: already complete
+  return wait_phase_slow(bar, parity, ms, err);
 }
 
 // ------------------------------------------------------------ segment cursor
@@ -278,20 +284,18 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
 
 // ------------------------------------------------------------ producer (warp 4)
 // Streams each tile once: the rope panel (64 dims) then four latent panels.
+// Contiguous rows: lane 0 alone issues one tiled box per panel.  Page table:
+// every lane gathers four rows (tile::gather4) for each panel.
 template <bool kGather>
 __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
                              const CUtensorMap* map_r, Misc* ms, uint32_t sbase) {
   const int lane = threadIdx.x & 31;
-  int32_t last_r[kNumRSlots], last_v[kNumVSlots];  // last fill issued per slot (-1: none)
-#pragma unroll
-  for (int s = 0; s < kNumRSlots; ++s) last_r[s] = -1;
-#pragma unroll
-  for (int s = 0; s < kNumVSlots; ++s) last_v[s] = -1;
-
+  if (!kGather && lane != 0) return;
   Cursor cur;
   cursor_start(cur, ms, p.kv_indptr, p.batch);
-  uint32_t tile = 0;
-  while (cur.live) {
+  uint32_t tile = 0;  // tiles whose panels have all been issued
+  bool ok = true;
+  while (cur.live && ok) {
     const int32_t tok0 = cur.kb + cur.j * kTileTokens;
     const int32_t valid = min(kTileTokens, cur.len - cur.j * kTileTokens);
     int32_t rows[4] = {0, 0, 0, 0};
@@ -308,55 +312,66 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
         rows[k] = idx;
       }
     }
-    // rope panel
-    {
-      const uint32_t slot = tile % kNumRSlots, use = tile / kNumRSlots;
-      int ok = 1;
-      if (lane == 0 && use > 0)
-        ok = wait_phase(smem_u32(&ms->r_empty[slot]), (use - 1) & 1, ms, p.err);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (ok) {
-        const uint32_t dst = sbase + kOffR + slot * kRPanelBytes;
-        const uint32_t bar = smem_u32(&ms->r_full[slot]);
-        if (lane == 0) mbar_arrive_expect_tx(bar, kRPanelBytes);
-        __syncwarp();
-        if (kGather)
-          tma_gather4(dst + lane * 4 * 64, map_r, kVDim, rows[0], rows[1], rows[2], rows[3], bar);
-        else if (lane == 0)
-          tma_load_2d(dst, map_r, kVDim, tok0, bar);
-        last_r[slot] = static_cast<int32_t>(use);
-      }
-    }
-    // latent panels
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t g = tile * 4 + c;
-      const uint32_t slot = g % kNumVSlots, use = g / kNumVSlots;
-      int ok = 1;
-      if (lane == 0 && use > 0)
-        ok = wait_phase(smem_u32(&ms->v_empty[slot]), (use - 1) & 1, ms, p.err);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (ok) {
-        const uint32_t dst = sbase + kOffV + slot * kVPanelBytes;
-        const uint32_t bar = smem_u32(&ms->v_full[slot]);
-        if (lane == 0) mbar_arrive_expect_tx(bar, kVPanelBytes);
+    for (int c = -1; c < 4 && ok; ++c) {  // c = -1: rope panel, 0..3: latent panels
+      uint32_t slot, use, bytes, dst, full, empty;
+      int32_t x;
+      const CUtensorMap* map;
+      if (c < 0) {
+        slot = tile % kNumRSlots;
+        use = tile / kNumRSlots;
+        bytes = kRPanelBytes;
+        dst = sbase + kOffR + slot * kRPanelBytes;
+        full = smem_u32(&ms->r_full[slot]);
+        empty = smem_u32(&ms->r_empty[slot]);
+        x = kVDim;
+        map = map_r;
+      } else {
+        const uint32_t g = tile * 4 + c;
+        slot = g % kNumVSlots;
+        use = g / kNumVSlots;
+        bytes = kVPanelBytes;
+        dst = sbase + kOffV + slot * kVPanelBytes;
+        full = smem_u32(&ms->v_full[slot]);
+        empty = smem_u32(&ms->v_empty[slot]);
+        x = 128 * c;
+        map = map_v;
+      }
+      if (kGather) {
+        int w = 1;
+        if (lane == 0 && use > 0) w = wait_phase(empty, (use - 1) & 1, ms, p.err);
+        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(full, bytes);
         __syncwarp();
-        if (kGather)
-          tma_gather4(dst + lane * 4 * 128, map_v, 128 * c, rows[0], rows[1], rows[2], rows[3], bar);
-        else if (lane == 0)
-          tma_load_2d(dst, map_v, 128 * c, tok0, bar);
-        last_v[slot] = static_cast<int32_t>(use);
+        tma_gather4(dst + lane * 4 * (bytes / kTileTokens), map, x, rows[0], rows[1], rows[2],
+                    rows[3], full);
+      } else {
+        if (use > 0) ok = wait_phase(empty, (use - 1) & 1, ms, p.err);
+        if (!ok) break;
+        mbar_arrive_expect_tx(full, bytes);
+        tma_load_2d(dst, map, x, tok0, full);
       }
     }
+    if (!ok) break;
     ++tile;
     if (!cursor_next_tile(cur, ms, p.kv_indptr, p.batch)) break;
   }
-  // An abandoned call must not leave copies landing in shared memory after exit.
+  // An abandoned call must not leave copies landing in shared memory after
+  // exit: wait (bounded) for the last fill issued into every slot.  A tile cut
+  // short by the abandonment may have issued some of its panels; waiting on
+  // those too is harmless (bounded), waiting on complete ones returns at once.
   if (ms->abort_flag && lane == 0) {
-    for (int s = 0; s < kNumRSlots; ++s)
-      if (last_r[s] >= 0) drain_phase(smem_u32(&ms->r_full[s]), last_r[s] & 1);
-    for (int s = 0; s < kNumVSlots; ++s)
-      if (last_v[s] >= 0) drain_phase(smem_u32(&ms->v_full[s]), last_v[s] & 1);
+    const uint32_t tiles_started = tile + 1;
+    for (uint32_t s = 0; s < kNumRSlots && s < tiles_started; ++s) {
+      const uint32_t last = (tiles_started - 1 - s) / kNumRSlots;
+      drain_phase(smem_u32(&ms->r_full[s]), last & 1);
+    }
+    const uint32_t panels = tiles_started * 4;
+    for (uint32_t s = 0; s < kNumVSlots && s < panels; ++s) {
+      const uint32_t last = (panels - 1 - s) / kNumVSlots;
+      drain_phase(smem_u32(&ms->v_full[s]), last & 1);
+    }
   }
 }
 
@@ -424,8 +439,9 @@ __device__ void run_mma(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_
     // PV first: it releases the tile's latent slots for the next loads.
     if (pv_n < qk_n) {
       const bool first = pc.j == pc.j0;
-      if (ld_acquire_u32(&ms->p_ready) > pv_n &&
-          (!first || pc.seg == 0 || ld_acquire_u32(&ms->o_free) >= static_cast<uint32_t>(pc.seg))) {
+      if (ld_relaxed_u32(&ms->p_ready) > pv_n &&
+          (!first || pc.seg == 0 || ld_relaxed_u32(&ms->o_free) >= static_cast<uint32_t>(pc.seg))) {
+        fence_acquire_cta();
         tc_fence_after();
         issue_pv(tmem, sbase, pv_n, first, ms);
         umma_commit(smem_u32(&ms->pv_done[pv_n & 1]));
@@ -434,9 +450,10 @@ __device__ void run_mma(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_
         cursor_next_tile(pc, ms, p.kv_indptr, p.batch);
       }
     }
-    if (qc.live && ld_acquire_u32(&ms->data_ready) > qk_n &&
-        (qc.j != qc.j0 || ld_acquire_u32(&ms->q_ready) > static_cast<uint32_t>(qc.seg)) &&
-        (qk_n < 2 || ld_acquire_u32(&ms->s_read) + 1 >= qk_n)) {
+    if (qc.live && ld_relaxed_u32(&ms->data_ready) > qk_n &&
+        (qc.j != qc.j0 || ld_relaxed_u32(&ms->q_ready) > static_cast<uint32_t>(qc.seg)) &&
+        (qk_n < 2 || ld_relaxed_u32(&ms->s_read) + 1 >= qk_n)) {
+      fence_acquire_cta();
       tc_fence_after();
       issue_qk(tmem, sbase, qk_n);
       umma_commit(smem_u32(&ms->s_full[qk_n & 1]));
