@@ -7,8 +7,8 @@
 namespace mla {
 
 // Stage 1 ring / layout constants.
-constexpr int kNumVSlots = 10;      // 16 KB slots: tokens x 128 latent dims (swizzle 128B)
-constexpr int kNumRSlots = 3;       // 8 KB slots: tokens x 64 rope dims (swizzle 64B)
+constexpr int kNumVSlots = 11;      // 16 KB slots: tokens x 128 latent dims (swizzle 128B)
+constexpr int kNumRSlots = 2;       // 8 KB slots: tokens x 64 rope dims (swizzle 64B)
 constexpr int kVPanelBytes = 128 * 128;
 constexpr int kRPanelBytes = 128 * 64;
 constexpr int kStage1Threads = 224; // warps 0-3 softmax/epilogue, 4 TMA producer, 5 MMA issuer, 6 TMA watcher
