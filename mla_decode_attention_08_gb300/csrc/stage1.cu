@@ -46,7 +46,6 @@ struct Misc {
   uint64_t v_full[kNumVSlots];
   uint64_t v_empty[kNumVSlots];
   uint64_t r_full[kNumRSlots];
-  uint64_t r_empty[kNumRSlots];
   uint64_t s_full[2];   // QK of tile i landed in S[i & 1]
   uint64_t pv_done[2];  // PV of tile i completed (P[i & 1] free again)
   uint64_t q_empty;     // the segment's last QK completed (Q operand free)
@@ -75,6 +74,8 @@ struct Misc {
 static_assert(offsetof(Misc, red_max) % 16 == 0 && offsetof(Misc, red_sum) % 16 == 0,
               "vector accesses to the reduction scratch need 16-byte alignment");
 static_assert(kOffMisc % 16 == 0, "the barrier block must start 16-byte aligned");
+
+static_assert(kNumRSlots == 2, "rope slots are released through s_full, which has two phases in flight");
 
 constexpr int kSmemUsed = kOffMisc + static_cast<int>(sizeof(Misc));
 constexpr int kSmemAlloc = kSmemUsed + 1024;  // room to align the base to 1024 B
@@ -323,7 +324,10 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
         bytes = kRPanelBytes;
         dst = sbase + kOffR + slot * kRPanelBytes;
         full = smem_u32(&ms->r_full[slot]);
-        empty = smem_u32(&ms->r_empty[slot]);
+        // With two rope slots and two S buffers, rope slot (tile & 1) is free
+        // exactly when the QK of the tile before last has completed, which is
+        // the phase of s_full[tile & 1] for that tile.
+        empty = smem_u32(&ms->s_full[slot]);
         x = kVDim;
         map = map_r;
       } else {
@@ -456,8 +460,7 @@ __device__ void run_mma(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_
       fence_acquire_cta();
       tc_fence_after();
       issue_qk(tmem, sbase, qk_n);
-      umma_commit(smem_u32(&ms->s_full[qk_n & 1]));
-      umma_commit(smem_u32(&ms->r_empty[qk_n % kNumRSlots]));
+      umma_commit(smem_u32(&ms->s_full[qk_n & 1]));  // also frees rope slot qk_n & 1
       if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
       ++qk_n;
       progressed = true;
@@ -880,10 +883,7 @@ __global__ void __launch_bounds__(kStage1Threads, 1)
       mbar_init(smem_u32(&ms->v_full[s]), 1);
       mbar_init(smem_u32(&ms->v_empty[s]), 1);
     }
-    for (int s = 0; s < kNumRSlots; ++s) {
-      mbar_init(smem_u32(&ms->r_full[s]), 1);
-      mbar_init(smem_u32(&ms->r_empty[s]), 1);
-    }
+    for (int s = 0; s < kNumRSlots; ++s) mbar_init(smem_u32(&ms->r_full[s]), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ms->s_full[i]), 1);
       mbar_init(smem_u32(&ms->pv_done[i]), 1);
