@@ -4,7 +4,7 @@
 // range.  Per 128-token tile of the FP8 latent cache:
 //   * warp 4 streams the tile once through TMA into a ring of swizzled panels
 //     (four 128-dim latent panels + one 64-dim rope panel; page-table rows are
-//     fetched with tile::gather4),
+//     fetched with tile::gather4, the panels alternating between warps 4 and 7),
 //   * warp 5 issues tcgen05 MMAs: S^T[128 tok x 32] = K_tile . [Q_hi;Q_lo]^T
 //     and O^T[512 x 32] += V_tile^T . [P_hi;P_lo]^T, accumulators in TMEM,
 //   * warps 0-3 run the exp2 online softmax on S read from TMEM, write P, and
@@ -69,6 +69,7 @@ struct Misc {
   int32_t t0, t1;
   int32_t first_row, first_prefix, last_row;
   int32_t bad;
+  uint32_t next_panel[2];  // per producer warp: one past its last issued panel
 };
 
 static_assert(offsetof(Misc, red_max) % 16 == 0 && offsetof(Misc, red_sum) % 16 == 0,
@@ -90,7 +91,9 @@ constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;  // the single tcgen05.mma issuer; owns the TMEM allocation
 constexpr int kWatchWarp = 6;  // waits on the TMA barriers, publishes data_ready
+constexpr int kProducer2Warp = 7;  // second page-table producer
 constexpr uint32_t kBarSoftmax = 1;  // named barrier id of warps 0-3
+constexpr uint32_t kBarProducers = 2;  // named barrier id of warps 4 and 7 (page-table mode)
 
 // Operand descriptors (layout codes: 2 = 128B swizzle, 4 = 64B, 6 = 32B).
 constexpr uint32_t kLayoutSw128 = 2, kLayoutSw64 = 4, kLayoutSw32 = 6;
@@ -283,18 +286,29 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
   }
 }
 
-// ------------------------------------------------------------ producer (warp 4)
-// Streams each tile once: the rope panel (64 dims) then four latent panels.
-// Contiguous rows: lane 0 alone issues one tiled box per panel.  Page table:
-// every lane gathers four rows (tile::gather4) for each panel.
+// ------------------------------------------------------------ producers (warps 4 and 7)
+// Stream each tile once: the rope panel (64 dims) then four latent panels,
+// panel k = 5 * tile + 1 + c in one sequence over the worker's tiles.
+// Contiguous rows: lane 0 of warp 4 alone issues one tiled box per panel.
+// Page table: every lane gathers four rows (tile::gather4) per panel, and the
+// panels alternate between warps 4 and 7 (k even / odd): a warp issues its
+// gathers one lane after another, so two issuing warps double the rate at
+// which row fetches enter the copy engine.
+//
+// Every fill of a slot is issued only after the previous fill of that slot has
+// been consumed, so a producer can never be more than one phase ahead on a
+// barrier: its own previous panel already waited for the consumption that the
+// phase before would need.
 template <bool kGather>
 __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
-                             const CUtensorMap* map_r, Misc* ms, uint32_t sbase) {
+                             const CUtensorMap* map_r, Misc* ms, uint32_t sbase, uint32_t who) {
+  constexpr uint32_t kProducers = kGather ? 2 : 1;
   const int lane = threadIdx.x & 31;
   if (!kGather && lane != 0) return;
   Cursor cur;
   cursor_start(cur, ms, p.kv_indptr, p.batch);
-  uint32_t tile = 0;  // tiles whose panels have all been issued
+  uint32_t tile = 0;
+  uint32_t next_k = 0;  // one past the last panel this warp issued
   bool ok = true;
   while (cur.live && ok) {
     const int32_t tok0 = cur.kb + cur.j * kTileTokens;
@@ -315,6 +329,8 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
     }
 #pragma unroll 1
     for (int c = -1; c < 4 && ok; ++c) {  // c = -1: rope panel, 0..3: latent panels
+      const uint32_t k = tile * 5 + 1 + c;
+      if (kProducers > 1 && k % kProducers != who) continue;
       uint32_t slot, use, bytes, dst, full, empty;
       int32_t x;
       const CUtensorMap* map;
@@ -356,25 +372,39 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
         mbar_arrive_expect_tx(full, bytes);
         tma_load_2d(dst, map, x, tok0, full);
       }
+      next_k = k + 1;
     }
     if (!ok) break;
     ++tile;
     if (!cursor_next_tile(cur, ms, p.kv_indptr, p.batch)) break;
   }
   // An abandoned call must not leave copies landing in shared memory after
-  // exit: wait (bounded) for the last fill issued into every slot.  A tile cut
-  // short by the abandonment may have issued some of its panels; waiting on
-  // those too is harmless (bounded), waiting on complete ones returns at once.
-  if (ms->abort_flag && lane == 0) {
-    const uint32_t tiles_started = tile + 1;
-    for (uint32_t s = 0; s < kNumRSlots && s < tiles_started; ++s) {
-      const uint32_t last = (tiles_started - 1 - s) / kNumRSlots;
-      drain_phase(smem_u32(&ms->r_full[s]), last & 1);
-    }
-    const uint32_t panels = tiles_started * 4;
-    for (uint32_t s = 0; s < kNumVSlots && s < panels; ++s) {
-      const uint32_t last = (panels - 1 - s) / kNumVSlots;
-      drain_phase(smem_u32(&ms->v_full[s]), last & 1);
+  // exit: wait (bounded) for the last fill issued into every slot; every
+  // earlier fill of a slot was consumed before the next one was issued.
+  if (lane == 0) ms->next_panel[who] = next_k;
+  if (kGather) named_bar_sync(kBarProducers, 64);
+  if (who != 0 || lane != 0 || !ms->abort_flag) return;
+  uint32_t issued[2] = {ms->next_panel[0], kProducers > 1 ? ms->next_panel[1] : 0};
+  const uint32_t kmax = max(issued[0], issued[1]);
+  uint32_t need_v = (1u << kNumVSlots) - 1, need_r = (1u << kNumRSlots) - 1;
+  // Holes in the issued set lie within the last ring's worth of panels.
+  for (uint32_t n = 0; n < 64 && n < kmax && (need_v | need_r); ++n) {
+    const uint32_t k = kmax - 1 - n;
+    if (k >= issued[k % kProducers]) continue;  // never issued
+    const uint32_t t = k / 5;
+    const int c = static_cast<int>(k % 5) - 1;
+    if (c < 0) {
+      const uint32_t slot = t % kNumRSlots;
+      if (need_r & (1u << slot)) {
+        drain_phase(smem_u32(&ms->r_full[slot]), (t / kNumRSlots) & 1);
+        need_r &= ~(1u << slot);
+      }
+    } else {
+      const uint32_t g = t * 4 + c, slot = g % kNumVSlots;
+      if (need_v & (1u << slot)) {
+        drain_phase(smem_u32(&ms->v_full[slot]), (g / kNumVSlots) & 1);
+        need_v &= ~(1u << slot);
+      }
     }
   }
 }
@@ -908,7 +938,9 @@ __global__ void __launch_bounds__(kStage1Threads, 1)
   if (warp < 4) {
     run_softmax(p, ms, sbase, tmem, __ldg(p.kv_scale));
   } else if (warp == kProducerWarp) {
-    run_producer<kGather>(p, &map_v, &map_r, ms, sbase);
+    run_producer<kGather>(p, &map_v, &map_r, ms, sbase, 0);
+  } else if (kGather && warp == kProducer2Warp) {
+    run_producer<kGather>(p, &map_v, &map_r, ms, sbase, 1);
   } else if (warp == kMmaWarp && lane == 0) {
     run_mma(p, ms, sbase, tmem);
   } else if (warp == kWatchWarp && lane == 0) {
