@@ -11,7 +11,7 @@ constexpr int kNumVSlots = 11;      // 16 KB slots: tokens x 128 latent dims (sw
 constexpr int kNumRSlots = 2;       // 8 KB slots: tokens x 64 rope dims (swizzle 64B)
 constexpr int kVPanelBytes = 128 * 128;
 constexpr int kRPanelBytes = 128 * 64;
-// warps 0-3 softmax/epilogue, 4 TMA producer, 5 MMA issuer, 6 TMA watcher,
+// warps 0-3 softmax/epilogue, 4 TMA producer, 5 PV MMA issuer, 6 QK MMA issuer,
 // 7 second TMA producer (page-table mode only)
 constexpr int kStage1Threads = 256;
 constexpr long long kWaitLimitCycles = 2000000000LL;  // ~1 s per pipeline wait at 2 GHz

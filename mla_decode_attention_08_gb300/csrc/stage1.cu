@@ -5,8 +5,9 @@
 //   * warp 4 streams the tile once through TMA into a ring of swizzled panels
 //     (four 128-dim latent panels + one 64-dim rope panel; page-table rows are
 //     fetched with tile::gather4, the panels alternating between warps 4 and 7),
-//   * warp 5 issues tcgen05 MMAs: S^T[128 tok x 32] = K_tile . [Q_hi;Q_lo]^T
-//     and O^T[512 x 32] += V_tile^T . [P_hi;P_lo]^T, accumulators in TMEM,
+//   * warp 6 issues the tcgen05 MMAs S^T[128 tok x 32] = K_tile . [Q_hi;Q_lo]^T
+//     and warp 5 the MMAs O^T[512 x 32] += V_tile^T . [P_hi;P_lo]^T,
+//     accumulators in TMEM,
 //   * warps 0-3 run the exp2 online softmax on S read from TMEM, write P, and
 //     at the end of a segment write either the bf16 output (row fully inside
 //     this worker) or a normalised partial plus its base-2 log-sum-exp.
@@ -50,11 +51,8 @@ struct Misc {
   uint64_t pv_done[2];  // PV of tile i completed (P[i & 1] free again)
   uint64_t q_empty;     // the segment's last QK completed (Q operand free)
   uint64_t mma_done;
-  // Monotonic counters the MMA issuer polls (st.release, then relaxed loads
-  // followed by fence.acq_rel once a condition holds).  It never
-  // polls the TMA barriers themselves: testing a barrier whose copy is still in
-  // flight stalls the testing thread for about a panel's transfer time.
-  uint32_t data_ready;  // tiles whose five panels have landed (set by the watcher warp)
+  // Monotonic counters the MMA issuers poll (st.release, then relaxed loads
+  // followed by fence.acq_rel once a condition holds).
   uint32_t q_ready;     // segments whose Q operand is written
   uint32_t s_read;      // tiles whose S has been read out by every softmax warp
   uint32_t p_ready;     // tiles whose P is published (and O rescaled)
@@ -89,8 +87,8 @@ constexpr uint32_t kColO = 64;
 
 constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;  // the single tcgen05.mma issuer; owns the TMEM allocation
-constexpr int kWatchWarp = 6;  // waits on the TMA barriers, publishes data_ready
+constexpr int kMmaWarp = 5;    // PV issuer; owns the TMEM allocation
+constexpr int kMmaQkWarp = 6;  // QK issuer
 constexpr int kProducer2Warp = 7;  // second page-table producer
 constexpr uint32_t kBarSoftmax = 1;  // named barrier id of warps 0-3
 constexpr uint32_t kBarProducers = 2;  // named barrier id of warps 4 and 7 (page-table mode)
@@ -454,80 +452,84 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, uint32_t
   }
 }
 
-// MMA issuer (warp 5, lane 0): the only thread that issues tcgen05.mma.
-// QK of tile i needs its five panels landed, the segment's Q operand (first
-// tile of a segment) and S[i & 1] read out by the softmax of tile i - 2.  PV of
-// tile i needs P[i & 1] published and, on the first tile of a later segment, O
-// read out by the previous segment's epilogue.  All five conditions are
-// monotonic counters in shared memory; both products are polled so that
-// neither waits behind the other.
-__device__ void run_mma(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
-  Cursor qc, pc;
-  cursor_start(qc, ms, p.kv_indptr, p.batch);
-  cursor_start(pc, ms, p.kv_indptr, p.batch);
-  uint32_t qk_n = 0, pv_n = 0;  // tiles whose QK / PV have been issued
-  long long last_progress = clock64();
-
-  while (pc.live) {
-    bool progressed = false;
-    // PV first: it releases the tile's latent slots for the next loads.
-    if (pv_n < qk_n) {
-      const bool first = pc.j == pc.j0;
-      if (ld_relaxed_u32(&ms->p_ready) > pv_n &&
-          (!first || pc.seg == 0 || ld_relaxed_u32(&ms->o_free) >= static_cast<uint32_t>(pc.seg))) {
-        fence_acquire_cta();
-        tc_fence_after();
-        issue_pv(tmem, sbase, pv_n, first, ms);
-        umma_commit(smem_u32(&ms->pv_done[pv_n & 1]));
-        ++pv_n;
-        progressed = true;
-        cursor_next_tile(pc, ms, p.kv_indptr, p.batch);
-      }
-    }
-    if (qc.live && ld_relaxed_u32(&ms->data_ready) > qk_n &&
-        (qc.j != qc.j0 || ld_relaxed_u32(&ms->q_ready) > static_cast<uint32_t>(qc.seg)) &&
-        (qk_n < 2 || ld_relaxed_u32(&ms->s_read) + 1 >= qk_n)) {
-      fence_acquire_cta();
-      tc_fence_after();
-      issue_qk(tmem, sbase, qk_n);
-      umma_commit(smem_u32(&ms->s_full[qk_n & 1]));  // also frees rope slot qk_n & 1
-      if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
-      ++qk_n;
-      progressed = true;
-      cursor_next_tile(qc, ms, p.kv_indptr, p.batch);
-    }
-    if (progressed) {
-      last_progress = clock64();
-    } else {
-      if (ms->abort_flag) break;
-      if (clock64() - last_progress > kWaitLimitCycles) {
+// Bounded spin until a monotonic shared counter reaches `target`; false when
+// the call is being abandoned.  The caller follows a true return with
+// fence_acquire_cta, which orders what the counter's writer published.
+__device__ __noinline__ bool spin_counter_slow(const uint32_t* ctr, uint32_t target, Misc* ms,
+                                               int32_t* err) {
+  const long long start = clock64();
+  for (uint32_t n = 1;; ++n) {
+    if (ld_relaxed_u32(ctr) >= target) return true;
+    if ((n & 15) == 0) {
+      if (ms->abort_flag) return false;
+      if (clock64() - start > kWaitLimitCycles) {
         ms->abort_flag = 1;
-        set_error(p.err, MLA_DERR_TIMEOUT);
-        break;
+        set_error(err, MLA_DERR_TIMEOUT);
+        return false;
       }
     }
+  }
+}
+
+__device__ __forceinline__ bool spin_counter(const uint32_t* ctr, uint32_t target, Misc* ms,
+                                             int32_t* err) {
+  if (ld_relaxed_u32(ctr) >= target) return true;
+  return spin_counter_slow(ctr, target, ms, err);
+}
+
+// Two threads issue tcgen05.mma, each for one product, so that neither
+// product's issue waits behind the other's (issuing one product blocks the
+// issuing thread for about its execution time, ~1200 cycles).
+//
+// QK issuer (warp 6, lane 0): QK of tile i needs its five panels landed (it
+// waits on the TMA barriers itself), the segment's Q operand (first tile of a
+// segment) and S[i & 1] read out by the softmax of tile i - 2.
+__device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
+  Cursor qc;
+  cursor_start(qc, ms, p.kv_indptr, p.batch);
+  uint32_t qk_n = 0;  // tiles whose QK has been issued
+  while (qc.live) {
+    bool ok = wait_phase(smem_u32(&ms->r_full[qk_n % kNumRSlots]), (qk_n / kNumRSlots) & 1, ms,
+                         p.err);
+    for (int c = 0; c < 4 && ok; ++c) {
+      const uint32_t g = qk_n * 4 + c;
+      ok = wait_phase(smem_u32(&ms->v_full[g % kNumVSlots]), (g / kNumVSlots) & 1, ms, p.err);
+    }
+    if (ok && qc.j == qc.j0) ok = spin_counter(&ms->q_ready, static_cast<uint32_t>(qc.seg) + 1, ms, p.err);
+    if (ok && qk_n >= 2) ok = spin_counter(&ms->s_read, qk_n - 1, ms, p.err);
+    if (!ok) break;
+    fence_acquire_cta();
+    tc_fence_after();
+    issue_qk(tmem, sbase, qk_n);
+    umma_commit(smem_u32(&ms->s_full[qk_n & 1]));  // also frees rope slot qk_n & 1
+    if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
+    ++qk_n;
+    cursor_next_tile(qc, ms, p.kv_indptr, p.batch);
   }
   // Every MMA issued by this thread completes before TMEM is released.
   umma_commit(smem_u32(&ms->mma_done));
-  drain_phase(smem_u32(&ms->mma_done), 0);
 }
 
-// Watcher (warp 6, lane 0): waits for each tile's rope and latent panels to
-// land, in tile order, and publishes the count.
-__device__ void run_watcher(const Stage1Params& p, Misc* ms) {
-  Cursor cur;
-  cursor_start(cur, ms, p.kv_indptr, p.batch);
-  uint32_t tile = 0;
-  while (cur.live) {
-    bool ok = wait_phase(smem_u32(&ms->r_full[tile % kNumRSlots]), (tile / kNumRSlots) & 1, ms, p.err);
-    for (int c = 0; c < 4 && ok; ++c) {
-      const uint32_t g = tile * 4 + c;
-      ok = wait_phase(smem_u32(&ms->v_full[g % kNumVSlots]), (g / kNumVSlots) & 1, ms, p.err);
-    }
+// PV issuer (warp 5, lane 0): PV of tile i needs P[i & 1] published and, on
+// the first tile of a later segment, O read out by the previous segment's
+// epilogue.
+__device__ void run_mma_pv(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
+  Cursor pc;
+  cursor_start(pc, ms, p.kv_indptr, p.batch);
+  uint32_t pv_n = 0;  // tiles whose PV has been issued
+  while (pc.live) {
+    const bool first = pc.j == pc.j0;
+    bool ok = spin_counter(&ms->p_ready, pv_n + 1, ms, p.err);
+    if (ok && first && pc.seg > 0) ok = spin_counter(&ms->o_free, static_cast<uint32_t>(pc.seg), ms, p.err);
     if (!ok) break;
-    st_release_u32(&ms->data_ready, ++tile);
-    cursor_next_tile(cur, ms, p.kv_indptr, p.batch);
+    fence_acquire_cta();
+    tc_fence_after();
+    issue_pv(tmem, sbase, pv_n, first, ms);
+    umma_commit(smem_u32(&ms->pv_done[pv_n & 1]));
+    ++pv_n;
+    cursor_next_tile(pc, ms, p.kv_indptr, p.batch);
   }
+  umma_commit(smem_u32(&ms->mma_done));
 }
 
 // ------------------------------------------------------------ softmax warps (0-3)
@@ -919,8 +921,8 @@ __global__ void __launch_bounds__(kStage1Threads, 1)
       mbar_init(smem_u32(&ms->pv_done[i]), 1);
     }
     mbar_init(smem_u32(&ms->q_empty), 1);
-    ms->data_ready = ms->q_ready = ms->s_read = ms->p_ready = ms->o_free = 0;
-    mbar_init(smem_u32(&ms->mma_done), 1);
+    ms->q_ready = ms->s_read = ms->p_ready = ms->o_free = 0;
+    mbar_init(smem_u32(&ms->mma_done), 2);  // one commit from each MMA issuer
     ms->abort_flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&map_v);
@@ -942,14 +944,16 @@ __global__ void __launch_bounds__(kStage1Threads, 1)
   } else if (kGather && warp == kProducer2Warp) {
     run_producer<kGather>(p, &map_v, &map_r, ms, sbase, 1);
   } else if (warp == kMmaWarp && lane == 0) {
-    run_mma(p, ms, sbase, tmem);
-  } else if (warp == kWatchWarp && lane == 0) {
-    run_watcher(p, ms);
+    run_mma_pv(p, ms, sbase, tmem);
+  } else if (warp == kMmaQkWarp && lane == 0) {
+    run_mma_qk(p, ms, sbase, tmem);
   }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
+    if (lane == 0) drain_phase(smem_u32(&ms->mma_done), 0);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
