@@ -36,7 +36,7 @@ extern "C" {
 #define MLA_QK_HEAD_DIM 576
 #define MLA_V_HEAD_DIM 512
 #define MLA_TILE_TOKENS 128
-#define MLA_ABI_VERSION 1
+#define MLA_ABI_VERSION 2
 
 typedef enum {
   MLA_OK = 0,
@@ -69,9 +69,13 @@ typedef struct {
   int32_t abi_version; /* MLA_ABI_VERSION                                          */
   uint64_t ws_bytes;   /* workspace bytes mla_decode_fwd needs                      */
   uint64_t ws_prefix_offset;  /* int32[B+1]   tile prefix over rows                 */
-  uint64_t ws_workers_offset; /* int32[grid*4] (t0, t1, first_row, last_row) / worker */
+  uint64_t ws_workers_offset; /* int32[grid*8] per worker: (t0, t1, first_row, last_row)
+                               * then the combine job of the split row whose first
+                               * worker boundary is t0: (output row or -1, first
+                               * worker, last worker, first worker's partial slot) */
   uint64_t ws_lse_offset;     /* float[2*grid*16] base-2 log-sum-exp of partials    */
-  uint64_t ws_partial_offset; /* float[2*grid*16*512] normalised split partials     */
+  uint64_t ws_partial_offset; /* float[2*grid*16*512] normalised split partials,
+                               * stored [slot][dim/128][head/4][dim%128][head%4]   */
 } mla_plan_t;
 
 /*

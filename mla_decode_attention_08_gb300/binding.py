@@ -206,7 +206,9 @@ def workspace_views(plan: mla_plan_t, ws: torch.Tensor) -> dict:
 
     return {"err": view(0, 1, torch.int32),
             "prefix": view(plan.ws_prefix_offset, b + 1, torch.int32),
-            "workers": view(plan.ws_workers_offset, 4 * g, torch.int32).view(g, 4),
+            "workers": view(plan.ws_workers_offset, 8 * g, torch.int32).view(g, 8)[:, :4],
+            "jobs": view(plan.ws_workers_offset, 8 * g, torch.int32).view(g, 8)[:, 4:],
             "lse": view(plan.ws_lse_offset, 2 * g * 16, torch.float32).view(2 * g, 16),
-            "partial": view(plan.ws_partial_offset, 2 * g * 16 * 512,
-                            torch.float32).view(2 * g, 16, 512)}
+            # stored [slot][dim / 128][head / 4][dim % 128][head % 4]; viewed as [slot][head][dim]
+            "partial": view(plan.ws_partial_offset, 2 * g * 16 * 512, torch.float32)
+                       .view(2 * g, 4, 4, 128, 4).permute(0, 2, 4, 1, 3).reshape(2 * g, 16, 512)}

@@ -127,6 +127,7 @@ mla::Stage2Params stage2_params(const int32_t* qo_indptr, void* out, const mla_p
   s.out = static_cast<uint16_t*>(out);
   s.err = reinterpret_cast<int32_t*>(ws);
   s.prefix = reinterpret_cast<const int32_t*>(ws + plan->ws_prefix_offset);
+  s.workers = reinterpret_cast<const int32_t*>(ws + plan->ws_workers_offset);
   s.lse = reinterpret_cast<const float*>(ws + plan->ws_lse_offset);
   s.partial = reinterpret_cast<const float*>(ws + plan->ws_partial_offset);
   s.batch = plan->batch;
@@ -217,7 +218,7 @@ mla_status_t mla_decode_plan(int32_t batch, int32_t max_kv_len, int32_t num_sms,
   p.ws_prefix_offset = off;
   off += round_up((static_cast<uint64_t>(batch) + 1) * sizeof(int32_t));
   p.ws_workers_offset = off;
-  off += round_up(g * 4 * sizeof(int32_t));
+  off += round_up(g * 8 * sizeof(int32_t));
   p.ws_lse_offset = off;
   off += round_up(2 * g * kNumHeads * sizeof(float));
   p.ws_partial_offset = off;

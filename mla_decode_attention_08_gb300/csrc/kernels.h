@@ -25,7 +25,7 @@ struct Stage1Params {
   uint16_t* out;              // bf16 bits [B, 16, 512]
   int32_t* err;               // workspace error word
   int32_t* prefix;            // [B+1]
-  int32_t* workers;           // [grid*4]
+  int32_t* workers;           // [grid*8]: worker record + combine job
   float* lse;                 // [2*grid*16]
   float* partial;             // [2*grid*16*512]
   int64_t kv_rows;
@@ -39,6 +39,8 @@ struct Stage2Params {
   uint16_t* out;
   int32_t* err;
   const int32_t* prefix;
+  const int32_t* workers;  // [grid*8] (t0, t1, first_row, last_row, job tq, job first
+                           // worker, job last worker, job first slot), written by stage 1
   const float* lse;
   const float* partial;
   int32_t batch;

@@ -65,9 +65,10 @@ struct Misc {
   volatile int32_t abort_flag;
   int32_t total_tiles;
   int32_t t0, t1;
-  int32_t first_row, first_prefix, last_row;
+  int32_t first_row, first_prefix, first_tiles, last_row;
   int32_t bad;
   uint32_t next_panel[2];  // per producer warp: one past its last issued panel
+  alignas(16) float lse_stage[16];  // a split piece's base-2 LSE on its way out (bulk store)
 };
 
 static_assert(offsetof(Misc, red_max) % 16 == 0 && offsetof(Misc, red_sum) % 16 == 0,
@@ -202,6 +203,15 @@ __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity) {
 // All threads.  Tile counts of every row, their prefix, this worker's range
 // [t0, t1) and the rows holding its first and last tile.  Worker 0 also stores
 // the prefix for stage 2; every worker stores its (t0, t1, first, last) record.
+// Zero output for row b (a row without cached tokens, or every row when
+// kv_indptr is invalid), written by the one prologue thread that finds it.
+__device__ __noinline__ void zero_row(const Stage1Params& p, int32_t b) {
+  const int32_t tq = ldg_i32(p.qo_indptr + b);
+  if (ldg_i32(p.qo_indptr + b + 1) - tq != 1 || tq < 0 || tq >= p.batch) return;
+  uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(tq) * kNumHeads * kVDim);
+  for (int i = 0; i < kNumHeads * kVDim * 2 / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+}
+
 __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, nwarps = nthreads >> 5;
@@ -262,10 +272,12 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
       const int32_t next = ldg_i32(p.kv_indptr + b + 1);
       const int32_t nt = bad ? 0 : tiles_of_length(static_cast<int64_t>(next) - prev);
       if (c == 0) p.prefix[b] = a;
+      if (nt == 0 && b % p.grid == c) zero_row(p, b);  // no cached token: zero output
       if (nt > 0 && t1 > t0) {
         if (a <= t0 && t0 < a + nt) {
           ms->first_row = b;
           ms->first_prefix = a;
+          ms->first_tiles = nt;
         }
         if (a <= t1 - 1 && t1 - 1 < a + nt) ms->last_row = b;
       }
@@ -276,11 +288,25 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
   if (c == 0 && tid == 0) p.prefix[batch] = total;
   __syncthreads();
   if (tid == 0) {
-    int32_t* w = p.workers + 4 * c;
-    w[0] = t0;
-    w[1] = t1;
-    w[2] = ms->first_row;
-    w[3] = ms->last_row;
+    // The worker record, then the combine job of the split row (if any) whose
+    // first worker boundary is this worker's start: output row, first and last
+    // worker of the row, partial slot of the first worker (the others use 2c).
+    int32_t job[4] = {-1, 0, 0, 0};
+    const int32_t b = ms->first_row, a0 = ms->first_prefix;
+    if (t1 > t0 && b >= 0 && a0 < t0) {
+      const int32_t c_first = worker_of_tile(a0, total, p.grid);
+      if (worker_of_tile(t0 - 1, total, p.grid) == c_first) {
+        const int32_t tq = ldg_i32(p.qo_indptr + b);
+        const bool row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == 1 && tq >= 0 && tq < batch;
+        job[0] = row_ok ? tq : -1;
+        job[1] = c_first;
+        job[2] = worker_of_tile(a0 + ms->first_tiles - 1, total, p.grid);
+        job[3] = partial_slot(c_first, worker_begin(c_first, total, p.grid), a0);
+      }
+    }
+    int4* w = reinterpret_cast<int4*>(p.workers) + 2 * c;
+    w[0] = make_int4(t0, t1, ms->first_row, ms->last_row);
+    w[1] = make_int4(job[0], job[1], job[2], job[3]);
   }
 }
 
@@ -569,6 +595,13 @@ __device__ __forceinline__ uint32_t q_chunk_addr(uint32_t sq, int row, int ch) {
   return sq + 4 * kQPanelBytes + row * 64 + ((cc ^ ((row >> 1) & 3)) << 4);
 }
 
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -602,6 +635,9 @@ __device__ __forceinline__ void split_e4m3_16(const float (&x)[16], uint32_t (&h
 __device__ float prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq,
                            float kv_scale) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  // The previous segment's output may still be leaving the Q and P regions
+  // through bulk stores; the barrier below orders every write after this wait.
+  if (t == 0) bulk_wait_read<0>();
   uint4 raw[5][2];
   uint32_t amax = 0;
 #pragma unroll
@@ -845,6 +881,11 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     }
 
     // ------------------------------------------------ segment epilogue
+    // The output leaves through the TMA engine: O is staged in shared memory
+    // (the Q and P regions are free once the segment's last PV has completed)
+    // and one thread issues bulk stores, so the warps do not wait for their
+    // global stores to drain before the next segment.
+    if (t == 0) ms->red_u32[4] = static_cast<uint32_t>(ms->abort_flag);
     float l_tot[16];
     {
       float v[16];
@@ -857,44 +898,87 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       for (int h = 0; h < 16; ++h)
         l_tot[h] = (ms->red_sum[0][h] + ms->red_sum[1][h]) + (ms->red_sum[2][h] + ms->red_sum[3][h]);
     }
-    wait_pv(tile - 1);  // PV of the segment's last tile (and so of all before it)
-    tc_fence_after();
-    const bool write = row_ok && !ms->abort_flag;
-    const int32_t slot = cur.whole ? -1 : partial_slot(c, ms->t0, cur.row_a);
+    const bool write = row_ok && ms->red_u32[4] == 0;  // the same for every softmax thread
     float inv[16];
 #pragma unroll
     for (int h = 0; h < 16; ++h) inv[h] = kv_scale / l_tot[h];
+    wait_pv(tile - 1);  // PV of the segment's last tile (and so of all before it)
+    tc_fence_after();
+    const uint32_t stage_q = sbase + kOffQ;
+    if (cur.whole) {
+      // bf16 row [16 heads][512 dims], 16 KB, staged in the Q region.
 #pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
-      uint32_t o[32];
-      tmem_ld32(tmem + lane_base + kColO + 32 * cc, o);
-      tmem_wait_ld();
-      const int dim = 128 * cc + token;
-      if (write) {
-        if (cur.whole) {
-          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                               static_cast<size_t>(tq) * kNumHeads * kVDim + dim;
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_base + kColO + 32 * cc, o);
+        tmem_wait_ld();
+        const int dim = 128 * cc + token;
+        if (write) {
 #pragma unroll
           for (int h = 0; h < 16; ++h)
-            dst[h * kVDim] = __float2bfloat16_rn((u2f(o[h]) + u2f(o[16 + h]) * 0.0625f) * inv[h]);
-        } else {
-          float* dst = p.partial + static_cast<size_t>(slot) * kNumHeads * kVDim + dim;
+            st_shared_u16(stage_q + (h * kVDim + dim) * 2,
+                          bf16_bits((u2f(o[h]) + u2f(o[16 + h]) * 0.0625f) * inv[h]));
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+      if (t == 0 && write) {
+        bulk_store(p.out + static_cast<size_t>(tq) * kNumHeads * kVDim, stage_q, kNumHeads * kVDim * 2);
+        bulk_commit();
+      }
+    } else {
+      // fp32 partial, stored [slot][dim / 128][head / 4][dim % 128][head % 4]:
+      // each 128-dim chunk is 8 KB of contiguous memory, staged in one of three
+      // 8 KB buffers (two in the Q region, one over the P buffers).  The
+      // base-2 log-sum-exp follows the last chunk in the same bulk group.
+      const int32_t slot = partial_slot(c, ms->t0, cur.row_a);
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_base + kColO + 32 * cc, o);
+        tmem_wait_ld();
+        const uint32_t buf = cc == 1 ? stage_q + 8192 : (cc == 2 ? sbase + kOffP : stage_q);
+        if (cc == 3) {  // reuses chunk 0's buffer
+          if (t == 0) bulk_wait_read<2>();
+          named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+        }
+        if (write) {
+          float v[16];
 #pragma unroll
-          for (int h = 0; h < 16; ++h)
-            dst[h * kVDim] = (u2f(o[h]) + u2f(o[16 + h]) * 0.0625f) * inv[h];
+          for (int h = 0; h < 16; ++h) v[h] = (u2f(o[h]) + u2f(o[16 + h]) * 0.0625f) * inv[h];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            st_shared_v4(buf + (j * 128 + token) * 16, __float_as_uint(v[4 * j]),
+                         __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                         __float_as_uint(v[4 * j + 3]));
+          if (cc == 3 && t < 16) {
+            float x = m_ref[0] + log2f(l_tot[0]);
+#pragma unroll
+            for (int h = 1; h < 16; ++h) x = t == h ? m_ref[h] + log2f(l_tot[h]) : x;
+            ms->lse_stage[t] = x;
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+        if (t == 0 && write) {
+          bulk_store(p.partial + (static_cast<size_t>(slot) * 4 + cc) * (kNumHeads * 128), buf,
+                     kNumHeads * 128 * 4);
+          if (cc == 3) bulk_store(p.lse + slot * kNumHeads, smem_u32(ms->lse_stage), 64);
+          bulk_commit();
         }
       }
     }
-    if (write && !cur.whole) {
-#pragma unroll
-      for (int h = 0; h < 16; ++h)
-        if (t == h) p.lse[slot * kNumHeads + h] = m_ref[h] + log2f(l_tot[h]);
-    }
+    // O has been read out (tcgen05.wait::ld above): the next segment's PV may
+    // overwrite it.  Nothing else is published, so the flag is stored relaxed
+    // and does not wait for the output stores to drain.
     tc_fence_before();
     named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-    if (t == 0) st_release_u32(&ms->o_free, static_cast<uint32_t>(cur.seg + 1));
+    if (t == 0) st_relaxed_u32(&ms->o_free, static_cast<uint32_t>(cur.seg + 1));
     cursor_next_tile(cur, ms, p.kv_indptr, p.batch);
   }
+  // The bulk stores have read their staging and written global memory before
+  // the CTA exits.
+  if (t == 0) bulk_wait_all();
 }
 
 // ------------------------------------------------------------ kernel
@@ -928,6 +1012,11 @@ __global__ void __launch_bounds__(kStage1Threads, 1)
     prefetch_tensormap(&map_v);
     prefetch_tensormap(&map_r);
   }
+  // Launched as a programmatic dependent, this grid may start while the
+  // previous kernel of the stream is finishing: everything above touches only
+  // this CTA's own resources, everything below may read that kernel's results
+  // or write what it reads.  (Without the launch attribute the wait is a no-op.)
+  pdl_wait_primary();
   // Stage 2 may start launching now; it waits for this grid's completion
   // before it reads anything this grid writes.
   pdl_launch_dependents();
@@ -974,12 +1063,21 @@ cudaError_t stage1_prepare(int device) {
 
 cudaError_t launch_stage1(const Stage1Params& p, const CUtensorMap& map_v,
                           const CUtensorMap& map_r, bool gather, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>(p.grid)), block(kStage1Threads);
-  if (gather)
-    mla_decode_stage1_kernel<true><<<grid, block, kSmemAlloc, stream>>>(map_v, map_r, p);
-  else
-    mla_decode_stage1_kernel<false><<<grid, block, kSmemAlloc, stream>>>(map_v, map_r, p);
-  return cudaGetLastError();
+  // A programmatic dependent of the previous kernel in the stream: its CTAs
+  // may be scheduled while that kernel finishes, and wait for it (griddepcontrol
+  // .wait) before touching global memory.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+  cfg.blockDim = dim3(kStage1Threads);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return gather ? cudaLaunchKernelEx(&cfg, mla_decode_stage1_kernel<true>, map_v, map_r, p)
+                : cudaLaunchKernelEx(&cfg, mla_decode_stage1_kernel<false>, map_v, map_r, p);
 }
 
 }  // namespace mla

@@ -1,12 +1,18 @@
 // Stage 2 of the decode step: log-sum-exp combine of the rows that stage 1
 // split across workers (kernelbot-amd-mixed-mla submission 722089, `_mla_reduce`:
 // M = max_s lse_s, w_s = 2^(lse_s - M), out = sum_s w_s partial_s / sum_s w_s),
-// done here in one online pass.  Rows held whole by one worker were written by
-// stage 1 and are skipped; rows without cached tokens are written as zeros.
+// done here in one online pass.
 //
-// Grid (B, 4) x 256 threads: block (b, g) covers heads 4g..4g+3 of row b, each
-// thread 8 consecutive dims, loaded as two float4 per partial and stored as one
-// 128-bit bf16 vector.
+// A split row contains at least one worker boundary, so the grid is sized by
+// the workers, not the rows: stage 1 records in worker c's entry the combine
+// job of the split row whose first boundary is worker c's start (output row,
+// first and last worker, first worker's partial slot; the others use slot 2c),
+// and block (c, 4 * cc + j) combines dims 128cc..128cc+127 of heads 4j..4j+3
+// of that row, one dim per thread.  Rows held whole by one worker, and rows
+// without cached tokens, are written by stage 1.  Partials are stored as
+// [slot][dim / 128][head / 4][dim % 128][head % 4] (stage 1's epilogue), so a
+// warp's float4 loads cover 512 contiguous bytes; the partials of a row are
+// visited four at a time, their loads in flight together.
 #include <cuda_bf16.h>
 
 #include "../../include/mla_decode.h"
@@ -17,70 +23,82 @@
 namespace mla {
 namespace {
 
-__global__ void __launch_bounds__(256) mla_decode_stage2_kernel(const Stage2Params p) {
+constexpr int kStage2Threads = 128;  // one thread per dim of a 128-dim chunk
+constexpr int kStage2Unroll = 4;     // partials loaded together
+
+__global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const Stage2Params p) {
+  __shared__ __align__(16) uint16_t blk[4 * kStage2Threads];  // bf16 [4 heads][128 dims]
+  // The next kernel of the stream may start launching; it waits for this
+  // grid's completion before it touches global memory.
+  pdl_launch_dependents();
   // Everything read below is written by stage 1.
   pdl_wait_primary();
 
-  const int32_t b = blockIdx.x;
-  const int head = blockIdx.y * 4 + (threadIdx.x >> 6);
-  const int d0 = (threadIdx.x & 63) * 8;
-  const int32_t tq = __ldg(p.qo_indptr + b);
-  if (__ldg(p.qo_indptr + b + 1) - tq != 1 || tq < 0 || tq >= p.batch) return;
+  const int32_t c = blockIdx.x;
+  const int cc = blockIdx.y >> 2, j = blockIdx.y & 3, dd = threadIdx.x;
+  const int4* rec = reinterpret_cast<const int4*>(p.workers);
+  const int4 job = rec[2 * c + 1];  // (output row, first worker, last worker, first slot)
+  const int32_t tq = job.x;
+  if (tq < 0) return;
 
-  const int32_t a_begin = p.prefix[b];
-  const int32_t a_end = p.prefix[b + 1];
-  const int32_t total = p.prefix[p.batch];
-  uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(tq) * kNumHeads + head) * kVDim + d0);
-
-  if (a_end <= a_begin) {  // no cached token: zero output
-    *dst = make_uint4(0, 0, 0, 0);
-    return;
-  }
-  const int32_t c_first = worker_of_tile(a_begin, total, p.grid);
-  const int32_t c_last = worker_of_tile(a_end - 1, total, p.grid);
-  if (c_first == c_last) return;  // written whole by stage 1
-
-  float m = -INFINITY, wsum = 0.0f;
-  float acc[8];
+  const float4* lse4 = reinterpret_cast<const float4*>(p.lse);
+  const float4* part4 = reinterpret_cast<const float4*>(p.partial);
+  // One online pass: m_h is the running maximum of lse_s,h, and the weights of
+  // the partials seen so far are rescaled when it grows.
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  float wsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int32_t w0 = job.y; w0 <= job.z; w0 += kStage2Unroll) {
+    // Issue every load of the group first; a worker with no tiles (possible
+    // only when the grid exceeds the tile count) wrote no partial, and its
+    // values are dropped.
+    int4 wr[kStage2Unroll];
+    float4 x[kStage2Unroll], v[kStage2Unroll];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int32_t c = c_first; c <= c_last; ++c) {
-    const int32_t t0 = worker_begin(c, total, p.grid);
-    if (worker_begin(c + 1, total, p.grid) == t0) continue;  // empty worker
-    const int32_t slot = partial_slot(c, t0, a_begin);
-    const float lse = p.lse[slot * kNumHeads + head];
-    const float4* src = reinterpret_cast<const float4*>(
-        p.partial + (static_cast<size_t>(slot) * kNumHeads + head) * kVDim + d0);
-    const float4 v0 = src[0], v1 = src[1];
-    if (lse > m) {
-      const float f = exp2f(m - lse);
-      wsum *= f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] *= f;
-      m = lse;
+    for (int u = 0; u < kStage2Unroll; ++u) {
+      const int32_t cu = w0 + u;
+      if (cu <= job.z) {
+        const int32_t slot = cu == job.y ? job.w : 2 * cu;
+        wr[u] = rec[2 * cu];
+        x[u] = lse4[slot * 4 + j];
+        v[u] = part4[((static_cast<size_t>(slot) * 4 + cc) * 4 + j) * kStage2Threads + dd];
+      }
     }
-    const float w = exp2f(lse - m);
-    wsum += w;
-    acc[0] += w * v0.x; acc[1] += w * v0.y; acc[2] += w * v0.z; acc[3] += w * v0.w;
-    acc[4] += w * v1.x; acc[5] += w * v1.y; acc[6] += w * v1.z; acc[7] += w * v1.w;
-  }
-  const float inv = 1.0f / wsum;
-  uint4 o;
-  uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-    ow[i] = *reinterpret_cast<const uint32_t*>(&h2);
+    for (int u = 0; u < kStage2Unroll; ++u) {
+      if (w0 + u > job.z || wr[u].y <= wr[u].x) continue;
+      const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+      const float vs[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float mn = fmaxf(m[h], xs[h]);
+        const float f = exp2f(m[h] - mn), w = exp2f(xs[h] - mn);
+        wsum[h] = wsum[h] * f + w;
+        acc[h] = acc[h] * f + w * vs[h];
+        m[h] = mn;
+      }
+    }
   }
-  *dst = o;
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const __nv_bfloat16 y = __float2bfloat16_rn(acc[h] / wsum[h]);
+    blk[h * kStage2Threads + dd] = *reinterpret_cast<const uint16_t*>(&y);
+  }
+  __syncthreads();
+  // 4 heads x 16 vectors of 8 dims.
+  if (dd < 64) {
+    const int h = dd >> 4, part = dd & 15;
+    uint16_t* dst = p.out + (static_cast<size_t>(tq) * kNumHeads + 4 * j + h) * kVDim + 128 * cc + part * 8;
+    *reinterpret_cast<uint4*>(dst) = reinterpret_cast<const uint4*>(blk)[dd];
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_stage2(const Stage2Params& p, bool programmatic, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.batch), 4);
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid), 16);
+  cfg.blockDim = dim3(kStage2Threads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -34,7 +34,7 @@ def test_every_declared_function_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.mla_decode_abi_version() == 1
+    assert lib.mla_decode_abi_version() == 2
     for s in range(5):
         assert lib.mla_status_string(s)
 
@@ -49,7 +49,7 @@ def test_plan_matches_oracle_grid(lib, batch, max_len, sms):
     g = plan.grid
     assert plan.ws_prefix_offset >= 4 and plan.ws_prefix_offset % 256 == 0
     assert plan.ws_workers_offset >= plan.ws_prefix_offset + 4 * (batch + 1)
-    assert plan.ws_lse_offset >= plan.ws_workers_offset + 16 * g
+    assert plan.ws_lse_offset >= plan.ws_workers_offset + 32 * g
     assert plan.ws_partial_offset >= plan.ws_lse_offset + 4 * 32 * g
     assert plan.ws_bytes >= plan.ws_partial_offset + 4 * 2 * g * 16 * 512
     assert all(o % 256 == 0 for o in (plan.ws_workers_offset, plan.ws_lse_offset,

@@ -43,6 +43,21 @@ def test_small_shapes(name, lengths, paged, sms):
     views = binding.workspace_views(plan, ws)
     assert np.array_equal(views["workers"].cpu().numpy(), worker_table(inp.kv_indptr, plan.grid))
     assert views["prefix"].cpu().numpy().tolist() == oracle_schedule(inp.kv_indptr, plan.grid)["prefix"]
+    assert np.array_equal(views["jobs"].cpu().numpy(), expected_jobs(inp, plan.grid))
+
+
+def expected_jobs(inp, grid):
+    """Combine job per worker from the oracle's schedule: a split row is
+    combined by the entry of its second worker (the first worker boundary inside
+    it), holding (query row, first worker, last worker, first worker's slot)."""
+    sch = oracle_schedule(inp.kv_indptr, grid)
+    jobs = np.zeros((grid, 4), dtype=np.int64)
+    jobs[:, 0] = -1
+    first_slot = {(sg["worker"], sg["row"]): sg["slot"] for sg in sch["segments"]}
+    for b, ws in sch["covers"].items():
+        if len(ws) > 1:
+            jobs[ws[1]] = (int(inp.qo_indptr[b]), ws[0], ws[-1], first_slot[(ws[0], b)])
+    return jobs
 
 
 def test_grid_larger_than_tile_count():
@@ -207,3 +222,78 @@ def test_workload_parity(name):
     views = binding.workspace_views(plan, ws)
     assert np.array_equal(views["workers"].cpu().numpy(), worker_table(inp.kv_indptr, plan.grid))
     assert plan.grid == plan_grid(inp.batch, inp.max_kv_len, num_sms())
+
+
+# ------------------------------------------------------------------ split partials
+def test_split_partials_and_lse_match_oracle():
+    """Stage 1's normalised partial and base-2 log-sum-exp of every split segment
+    against the oracle's split_partial over the same token range (the combine
+    inputs, checked before the combine can hide an error in one of them)."""
+    from oracle.attention import _row_tokens, dequant_rows, split_partial
+
+    from .gpu_util import ATOL, RTOL
+
+    inp = make_from_lengths([300, 1000, 17, 4500, 129, 0, 2000], seed=4242, paged=True)
+    dev = DeviceCase(inp)
+    plan = binding.mla_decode_plan(inp.batch, inp.max_kv_len, 7)
+    ws = binding.new_workspace(plan)
+    # The two-kernel form writes every piece's partial (the fused call lets the
+    # worker that completes a row skip its own).
+    binding.mla_decode_stage1(dev.q, dev.kv_codes, dev.kv_scale, dev.qo_indptr, dev.kv_indptr,
+                              dev.out, plan=plan, workspace=ws, kv_indices=dev.kv_indices)
+    binding.mla_decode_stage2(dev.qo_indptr, dev.out, plan=plan, workspace=ws)
+    torch.cuda.synchronize()
+    assert binding.mla_decode_read_error(ws) == 0
+    gpu = dev.out.float().cpu().numpy()
+    views = binding.workspace_views(plan, ws)
+    part = views["partial"].cpu().numpy()  # [slot][head][dim]
+    lse = views["lse"].cpu().numpy()       # [slot][head]
+    orc = OracleCase(inp)
+    codes = orc.codes()
+    checked = 0
+    for s in oracle_schedule(inp.kv_indptr, plan.grid)["segments"]:
+        if not s["split"]:
+            continue
+        b = s["row"]
+        length = int(inp.kv_indptr[b + 1] - inp.kv_indptr[b])
+        j0, j1 = s["tile_begin"] * 128, min(length, s["tile_end"] * 128)
+        slots = _row_tokens(b, inp.kv_indptr, inp.kv_indices)[j0:j1]
+        o, l = split_partial(orc.q[int(inp.qo_indptr[b])], dequant_rows(codes, orc.scale, slots))
+        got = part[s["slot"]].astype(np.float64)
+        assert np.all(np.abs(got - o) <= ATOL + RTOL * np.abs(o)), (s, np.abs(got - o).max())
+        assert np.all(np.abs(lse[s["slot"]] - l) <= 2e-2), (s, lse[s["slot"]], l)
+        checked += 1
+    assert checked >= 6
+    assert_close(gpu, orc.reference())
+
+
+# ------------------------------------------------------------------ combine edge cases
+COMBINE_CASES = [
+    ("split_paged", [300, 1000, 17, 4500, 129, 0, 2000], True, 7),
+    ("many_pieces", [4000, 1, 4000], False, 40),  # rows split over up to ~30 workers
+    ("empty_workers", [130, 1, 0, 120], False, 8),  # grid larger than the tile count
+    ("all_empty", [0, 0, 0], False, 5),
+    ("zero_rows_between_splits", [0, 900, 0, 0, 700, 0], True, 11),
+]
+
+
+@pytest.mark.parametrize("name,lengths,paged,sms", COMBINE_CASES, ids=[c[0] for c in COMBINE_CASES])
+def test_combine_edge_cases_and_separate_stages(name, lengths, paged, sms):
+    """Rows split over many workers, workers with no tiles, rows without cached
+    tokens: mla_decode_fwd matches the oracle, and launching its two kernels
+    through mla_decode_stage1 / mla_decode_stage2 gives the same bits."""
+    inp = make_from_lengths(lengths, seed=99 + len(lengths), paged=paged, max_kv_len=max(max(lengths), 1))
+    dev = DeviceCase(inp)
+    plan = binding.mla_decode_plan(inp.batch, inp.max_kv_len, sms)
+    ws = binding.new_workspace(plan)
+    dev.out.fill_(float("nan"))
+    gpu, err, _, _ = dev.run(plan=plan, workspace=ws)
+    assert err == 0
+    assert_close(gpu, OracleCase(inp).reference())
+    out2 = torch.full_like(dev.out, float("nan"))
+    binding.mla_decode_stage1(dev.q, dev.kv_codes, dev.kv_scale, dev.qo_indptr, dev.kv_indptr,
+                              out2, plan=plan, workspace=ws, kv_indices=dev.kv_indices)
+    binding.mla_decode_stage2(dev.qo_indptr, out2, plan=plan, workspace=ws)
+    torch.cuda.synchronize()
+    assert binding.mla_decode_read_error(ws) == 0
+    assert np.array_equal(out2.float().cpu().numpy(), gpu)
