@@ -149,7 +149,7 @@ struct Cursor {
 };
 
 // Advance to the next row holding tiles of [t0, t1).
-__device__ bool cursor_next_segment(Cursor& c, const int32_t* kv_indptr, int32_t batch,
+__device__ __forceinline__ bool cursor_next_segment(Cursor& c, const int32_t* kv_indptr, int32_t batch,
                                     int32_t t0, int32_t t1) {
   while (c.next_a < t1) {
     const int32_t b = ++c.b;
@@ -174,7 +174,7 @@ __device__ bool cursor_next_segment(Cursor& c, const int32_t* kv_indptr, int32_t
   return false;
 }
 
-__device__ void cursor_start(Cursor& c, const Misc* ms, const int32_t* kv_indptr, int32_t batch) {
+__device__ __forceinline__ void cursor_start(Cursor& c, const Misc* ms, const int32_t* kv_indptr, int32_t batch) {
   c.b = ms->first_row - 1;
   c.next_a = ms->first_prefix;
   c.seg = -1;
@@ -183,7 +183,7 @@ __device__ void cursor_start(Cursor& c, const Misc* ms, const int32_t* kv_indptr
 }
 
 // Step to the next tile; returns false when the worker's range is exhausted.
-__device__ bool cursor_next_tile(Cursor& c, const Misc* ms, const int32_t* kv_indptr,
+__device__ __forceinline__ bool cursor_next_tile(Cursor& c, const Misc* ms, const int32_t* kv_indptr,
                                  int32_t batch) {
   if (++c.j < c.j1) return true;
   c.live = cursor_next_segment(c, kv_indptr, batch, ms->t0, ms->t1);
@@ -205,7 +205,7 @@ __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity) {
 // the prefix for stage 2; every worker stores its (t0, t1, first, last) record.
 // Zero output for row b (a row without cached tokens, or every row when
 // kv_indptr is invalid), written by the one prologue thread that finds it.
-__device__ __noinline__ void zero_row(const Stage1Params& p, int32_t b) {
+__device__ __forceinline__ void zero_row(const Stage1Params& p, int32_t b) {
   const int32_t tq = ldg_i32(p.qo_indptr + b);
   if (ldg_i32(p.qo_indptr + b + 1) - tq != 1 || tq < 0 || tq >= p.batch) return;
   uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(tq) * kNumHeads * kVDim);
@@ -635,11 +635,7 @@ __device__ __forceinline__ void split_e4m3_16(const float (&x)[16], uint32_t (&h
 __device__ float prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq,
                            float kv_scale) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  // The previous segment's output may still be leaving the Q and P regions
-  // through bulk stores; the barrier below orders every write after this wait.
-  if (t == 0) bulk_wait_read<0>();
   uint4 raw[5][2];
-  uint32_t amax = 0;
 #pragma unroll
   for (int r = 0; r < 5; ++r) {
     const int job = t + 128 * r;
@@ -651,11 +647,21 @@ __device__ float prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t
       raw[r][0] = __ldg(src);
       raw[r][1] = __ldg(src + 1);
     }
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(&raw[r][0]);
+  }
+  // The previous segment's output may still be leaving the Q and P regions
+  // through bulk stores (the loads above are already in flight); the barrier
+  // below orders every write to them after this wait.
+  if (t == 0) bulk_wait_read<0>();
+  uint32_t amax = 0;
+  auto fold = [&](uint32_t w) { amax = max(amax, max(w & 0x7FFFu, (w >> 16) & 0x7FFFu)); };
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      amax = max(amax, w[i] & 0x7FFFu);
-      amax = max(amax, (w[i] >> 16) & 0x7FFFu);
+  for (int r = 0; r < 5; ++r) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      fold(raw[r][k].x);
+      fold(raw[r][k].y);
+      fold(raw[r][k].z);
+      fold(raw[r][k].w);
     }
   }
   amax = __reduce_max_sync(0xffffffffu, amax);
@@ -885,6 +891,15 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     // (the Q and P regions are free once the segment's last PV has completed)
     // and one thread issues bulk stores, so the warps do not wait for their
     // global stores to drain before the next segment.
+    if (cur.next_a < ms->t1 && b + 1 < p.batch) {
+      // More segments follow: bring the next row's query (18 KB) into L2 now,
+      // so that its Q preparation after this epilogue reads it from there.
+      const int32_t tq_next = ldg_i32(p.qo_indptr + b + 1);
+      if (tq_next >= 0 && tq_next < p.batch) {
+        const char* qn = reinterpret_cast<const char*>(p.q + static_cast<size_t>(tq_next) * kNumHeads * kQkDim);
+        for (int i = t; i < kNumHeads * kQkDim * 2 / 128; i += kSoftmaxThreads) prefetch_l2(qn + 128 * i);
+      }
+    }
     if (t == 0) ms->red_u32[4] = static_cast<uint32_t>(ms->abort_flag);
     float l_tot[16];
     {
@@ -899,9 +914,9 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         l_tot[h] = (ms->red_sum[0][h] + ms->red_sum[1][h]) + (ms->red_sum[2][h] + ms->red_sum[3][h]);
     }
     const bool write = row_ok && ms->red_u32[4] == 0;  // the same for every softmax thread
-    float inv[16];
+    float inv[16];  // l >= 1 (the reference maximum contributes 1): a fast divide suffices
 #pragma unroll
-    for (int h = 0; h < 16; ++h) inv[h] = kv_scale / l_tot[h];
+    for (int h = 0; h < 16; ++h) inv[h] = __fdividef(kv_scale, l_tot[h]);
     wait_pv(tile - 1);  // PV of the segment's last tile (and so of all before it)
     tc_fence_after();
     const uint32_t stage_q = sbase + kOffQ;
