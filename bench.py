@@ -53,7 +53,8 @@ def algorithmic_bytes(inp) -> int:
     page-table entry), the bf16 query and output rows, and both indptr arrays."""
     tokens = int(inp.kv_indptr[-1])
     per_token = 576 + (4 if inp.kv_indices is not None else 0)
-    return tokens * per_token + inp.batch * 16 * (576 + 512) * 2 + 2 * (inp.batch + 1) * 4
+    queries = inp.batch * getattr(inp, "qo_len", 1)
+    return tokens * per_token + queries * 16 * (576 + 512) * 2 + 2 * (inp.batch + 1) * 4
 
 
 def measured_peak():
@@ -170,8 +171,8 @@ class DeviceWorkload:
         self.qo_indptr = torch.from_numpy(inp.qo_indptr).to(dev)
         self.kv_indptr = torch.from_numpy(inp.kv_indptr).to(dev)
         self.kv_indices = None if inp.kv_indices is None else torch.from_numpy(inp.kv_indices).to(dev)
-        self.out = torch.empty((inp.batch, 16, 512), dtype=torch.bfloat16, device=dev)
-        self.plan = binding.mla_decode_plan(inp.batch, inp.max_kv_len, sms)
+        self.out = torch.empty((inp.batch * inp.qo_len, 16, 512), dtype=torch.bfloat16, device=dev)
+        self.plan = binding.mla_decode_plan(inp.batch, inp.max_kv_len, sms, qo_len=inp.qo_len)
         self.ws = binding.new_workspace(self.plan)
         self.bytes = algorithmic_bytes(inp)
         self.binding = binding
@@ -274,8 +275,10 @@ class OracleSample:
         """Seconds of one oracle call restricted to row b."""
         from oracle.attention import mla_decode_ref
         codes, length = prepared
+        n = self.inp.qo_len
+        t0 = int(self.inp.qo_indptr[b])
         t = time.perf_counter()
-        mla_decode_ref(self.q[b:b + 1], codes, self.scale, np.array([0, 1]), np.array([0, length]))
+        mla_decode_ref(self.q[t0:t0 + n], codes, self.scale, np.array([0, n]), np.array([0, length]))
         return time.perf_counter() - t
 
 
@@ -360,7 +363,7 @@ def workload_config(name: str, world: int) -> dict:
             "kv_len_dist": "uniform 1..kv_len" if w.ragged else "fixed",
             "page_table": "random permutation, page size 1" if w.paged else "identity",
             "heads": 16, "qk_head_dim": 576, "v_head_dim": 512,
-            "kv_cache": "e4m3fn, per-tensor scale", "qseqlen": 1,
+            "kv_cache": "e4m3fn, per-tensor scale", "qseqlen": w.qo_len,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": "cache larger than L2, no flush between steps"}
 
@@ -384,6 +387,7 @@ def workload_bytes(name: str) -> int:
 
     class _Shape:
         batch = wl.batch
+        qo_len = wl.qo_len
         kv_indptr = np.concatenate([[0], np.cumsum(lengths)])
         kv_indices = np.zeros(1) if wl.paged else None
     return algorithmic_bytes(_Shape)

@@ -36,7 +36,7 @@ extern "C" {
 #define MLA_QK_HEAD_DIM 576
 #define MLA_V_HEAD_DIM 512
 #define MLA_TILE_TOKENS 128
-#define MLA_ABI_VERSION 2
+#define MLA_ABI_VERSION 3
 
 typedef enum {
   MLA_OK = 0,
@@ -67,15 +67,17 @@ typedef struct {
   int32_t grid;        /* persistent stage-1 workers: max(1, min(num_sms, B*ceil(max_kv_len/128))) */
   int32_t tile_tokens; /* 128                                                      */
   int32_t abi_version; /* MLA_ABI_VERSION                                          */
+  int32_t qo_len;      /* query tokens per row: 1 (decode) or 2 (two-token decode) */
+  int32_t reserved;    /* 0                                                        */
   uint64_t ws_bytes;   /* workspace bytes mla_decode_fwd needs                      */
   uint64_t ws_prefix_offset;  /* int32[B+1]   tile prefix over rows                 */
   uint64_t ws_workers_offset; /* int32[grid*8] per worker: (t0, t1, first_row, last_row)
                                * then the combine job of the split row whose first
                                * worker boundary is t0: (output row or -1, first
                                * worker, last worker, first worker's partial slot) */
-  uint64_t ws_lse_offset;     /* float[2*grid*16] base-2 log-sum-exp of partials    */
-  uint64_t ws_partial_offset; /* float[2*grid*16*512] normalised split partials,
-                               * stored [slot][dim/128][head/4][dim%128][head%4]   */
+  uint64_t ws_lse_offset;     /* float[2*grid*qo_len*16] base-2 log-sum-exp of partials */
+  uint64_t ws_partial_offset; /* float[2*grid*qo_len*16*512] normalised split partials,
+                               * stored [slot][token][dim/128][head/4][dim%128][head%4] */
 } mla_plan_t;
 
 /*
@@ -85,6 +87,20 @@ typedef struct {
  *   Fills *plan.  Returns MLA_ERR_INVALID_ARG for bad sizes / null plan.
  */
 mla_status_t mla_decode_plan(int32_t batch, int32_t max_kv_len, int32_t num_sms, mla_plan_t* plan);
+
+/*
+ * mla_decode_plan_mtp — as mla_decode_plan, for rows of qo_len query tokens
+ * (multi-token decode, e.g. one speculative / multi-token-prediction draft
+ * token: qo_len = 2).  qo_indptr[b+1] - qo_indptr[b] must then be qo_len for
+ * every row; q is [B*qo_len, 16, 576] and out [B*qo_len, 16, 512].  Query token
+ * i of a row with L cached tokens attends to the row's first L - qo_len + 1 + i
+ * tokens (its own entry and those before it: the row's last qo_len cached
+ * tokens are the query tokens'); a token that sees none outputs zeros.  The
+ * KV tile is loaded once for all qo_len x 16 heads.  qo_len must be 1 or 2.
+ */
+mla_status_t mla_decode_plan_mtp(int32_t batch, int32_t qo_len, int32_t max_kv_len, int32_t num_sms,
+                                 mla_plan_t* plan);
+
 
 /*
  * mla_decode_fwd — the decode step: stage 1 (split attention) then stage 2

@@ -31,6 +31,7 @@ class mla_plan_t(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("max_kv_len", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("tile_tokens", ctypes.c_int32), ("abi_version", ctypes.c_int32),
+                ("qo_len", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("ws_bytes", ctypes.c_uint64), ("ws_prefix_offset", ctypes.c_uint64),
                 ("ws_workers_offset", ctypes.c_uint64), ("ws_lse_offset", ctypes.c_uint64),
                 ("ws_partial_offset", ctypes.c_uint64)]
@@ -41,6 +42,7 @@ _PLANP = ctypes.POINTER(mla_plan_t)
 _FWD_ARGS = [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _PLANP, _VP, _I64, _I64, _VP, _SZ]
 SIGNATURES = {
     "mla_decode_plan": (ctypes.c_int, [_I32, _I32, _I32, _PLANP]),
+    "mla_decode_plan_mtp": (ctypes.c_int, [_I32, _I32, _I32, _I32, _PLANP]),
     "mla_decode_fwd": (ctypes.c_int, _FWD_ARGS),
     "mla_decode_stage1": (ctypes.c_int, _FWD_ARGS),
     "mla_decode_fwd_static_scratch": (ctypes.c_int, _FWD_ARGS[:-2]),
@@ -96,10 +98,11 @@ def _stream(stream) -> Optional[int]:
     return int(stream)
 
 
-def mla_decode_plan(batch: int, max_kv_len: int, num_sms: int = 0) -> mla_plan_t:
+def mla_decode_plan(batch: int, max_kv_len: int, num_sms: int = 0, qo_len: int = 1) -> mla_plan_t:
+    """Plan for ``batch`` rows of ``qo_len`` query tokens (1, or 2 for two-token decode)."""
     plan = mla_plan_t()
-    _check("mla_decode_plan", load_library().mla_decode_plan(batch, max_kv_len, num_sms,
-                                                            ctypes.byref(plan)))
+    _check("mla_decode_plan_mtp", load_library().mla_decode_plan_mtp(batch, qo_len, max_kv_len,
+                                                                    num_sms, ctypes.byref(plan)))
     return plan
 
 
@@ -198,7 +201,7 @@ def new_workspace(plan: mla_plan_t, device=None) -> torch.Tensor:
 
 def workspace_views(plan: mla_plan_t, ws: torch.Tensor) -> dict:
     """Typed views of the workspace regions (for tests and tools)."""
-    g, b = int(plan.grid), int(plan.batch)
+    g, b, nq = int(plan.grid), int(plan.batch), int(plan.qo_len)
 
     def view(off, n, dtype):
         size = torch.tensor([], dtype=dtype).element_size()
@@ -208,7 +211,9 @@ def workspace_views(plan: mla_plan_t, ws: torch.Tensor) -> dict:
             "prefix": view(plan.ws_prefix_offset, b + 1, torch.int32),
             "workers": view(plan.ws_workers_offset, 8 * g, torch.int32).view(g, 8)[:, :4],
             "jobs": view(plan.ws_workers_offset, 8 * g, torch.int32).view(g, 8)[:, 4:],
-            "lse": view(plan.ws_lse_offset, 2 * g * 16, torch.float32).view(2 * g, 16),
-            # stored [slot][dim / 128][head / 4][dim % 128][head % 4]; viewed as [slot][head][dim]
-            "partial": view(plan.ws_partial_offset, 2 * g * 16 * 512, torch.float32)
-                       .view(2 * g, 4, 4, 128, 4).permute(0, 2, 4, 1, 3).reshape(2 * g, 16, 512)}
+            "lse": view(plan.ws_lse_offset, 2 * g * nq * 16, torch.float32).view(2 * g, nq, 16),
+            # stored [slot][token][dim / 128][head / 4][dim % 128][head % 4];
+            # viewed as [slot][token][head][dim]
+            "partial": view(plan.ws_partial_offset, 2 * g * nq * 16 * 512, torch.float32)
+                       .view(2 * g, nq, 4, 4, 128, 4).permute(0, 1, 3, 5, 2, 4)
+                       .reshape(2 * g, nq, 16, 512)}

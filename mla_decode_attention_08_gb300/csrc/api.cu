@@ -108,7 +108,8 @@ mla_status_t prepare_device(int* device_out) {
 
 mla_status_t check_plan(const mla_plan_t* plan) {
   if (plan == nullptr || plan->abi_version != MLA_ABI_VERSION || plan->batch < 1 ||
-      plan->grid < 1 || plan->tile_tokens != kTileTokens || plan->max_kv_len < 0)
+      plan->grid < 1 || plan->tile_tokens != kTileTokens || plan->max_kv_len < 0 ||
+      (plan->qo_len != 1 && plan->qo_len != 2))
     return MLA_ERR_INVALID_ARG;
   return MLA_OK;
 }
@@ -132,6 +133,7 @@ mla::Stage2Params stage2_params(const int32_t* qo_indptr, void* out, const mla_p
   s.partial = reinterpret_cast<const float*>(ws + plan->ws_partial_offset);
   s.batch = plan->batch;
   s.grid = plan->grid;
+  s.qo_len = plan->qo_len;
   return s;
 }
 
@@ -176,6 +178,7 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
   p.kv_indices_len = gather ? kv_indices_len : 0;
   p.batch = plan->batch;
   p.grid = plan->grid;
+  p.qo_len = plan->qo_len;
   return mla::launch_stage1(p, map_v, map_r, gather, stream) == cudaSuccess ? MLA_OK
                                                                            : MLA_ERR_CUDA;
 }
@@ -198,7 +201,14 @@ const char* mla_status_string(mla_status_t status) {
 int32_t mla_decode_abi_version(void) { return MLA_ABI_VERSION; }
 
 mla_status_t mla_decode_plan(int32_t batch, int32_t max_kv_len, int32_t num_sms, mla_plan_t* plan) {
-  if (plan == nullptr || batch < 1 || max_kv_len < 0) return MLA_ERR_INVALID_ARG;
+  return mla_decode_plan_mtp(batch, 1, max_kv_len, num_sms, plan);
+}
+
+mla_status_t mla_decode_plan_mtp(int32_t batch, int32_t qo_len, int32_t max_kv_len, int32_t num_sms,
+                                 mla_plan_t* plan) {
+  if (plan == nullptr || batch < 1 || max_kv_len < 0 || (qo_len != 1 && qo_len != 2))
+    return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(batch) * qo_len > INT32_MAX) return MLA_ERR_INVALID_ARG;
   if (num_sms <= 0) {
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess ||
@@ -213,16 +223,18 @@ mla_status_t mla_decode_plan(int32_t batch, int32_t max_kv_len, int32_t num_sms,
   p.grid = mla::plan_grid(batch, max_kv_len, num_sms);
   p.tile_tokens = kTileTokens;
   p.abi_version = MLA_ABI_VERSION;
+  p.qo_len = qo_len;
   const uint64_t g = static_cast<uint64_t>(p.grid);
+  const uint64_t nq = static_cast<uint64_t>(qo_len);
   uint64_t off = kAlign;  // error word + reserved header
   p.ws_prefix_offset = off;
   off += round_up((static_cast<uint64_t>(batch) + 1) * sizeof(int32_t));
   p.ws_workers_offset = off;
   off += round_up(g * 8 * sizeof(int32_t));
   p.ws_lse_offset = off;
-  off += round_up(2 * g * kNumHeads * sizeof(float));
+  off += round_up(2 * g * nq * kNumHeads * sizeof(float));
   p.ws_partial_offset = off;
-  off += round_up(2 * g * kNumHeads * kVDim * sizeof(float));
+  off += round_up(2 * g * nq * kNumHeads * kVDim * sizeof(float));
   p.ws_bytes = off;
   *plan = p;
   return MLA_OK;

@@ -7,9 +7,8 @@
 namespace mla {
 
 // Stage 1 ring / layout constants.
-constexpr int kNumVSlots = 11;      // 16 KB slots: tokens x 128 latent dims (swizzle 128B)
 constexpr int kNumRSlots = 2;       // 8 KB slots: tokens x 64 rope dims (swizzle 64B)
-constexpr int kVPanelBytes = 128 * 128;
+constexpr int kVPanelBytes = 128 * 128;  // latent ring slot: 128 tokens x 128 dims (swizzle 128B)
 constexpr int kRPanelBytes = 128 * 64;
 // warps 0-3 softmax/epilogue, 4 TMA producer, 5 PV MMA issuer, 6 QK MMA issuer,
 // 7 second TMA producer (page-table mode only)
@@ -26,12 +25,13 @@ struct Stage1Params {
   int32_t* err;               // workspace error word
   int32_t* prefix;            // [B+1]
   int32_t* workers;           // [grid*8]: worker record + combine job
-  float* lse;                 // [2*grid*16]
-  float* partial;             // [2*grid*16*512]
+  float* lse;                 // [2*grid*qo_len*16]
+  float* partial;             // [2*grid*qo_len*16*512]
   int64_t kv_rows;
   int64_t kv_indices_len;
   int32_t batch;
   int32_t grid;
+  int32_t qo_len;             // query tokens per row (1 or 2)
 };
 
 struct Stage2Params {
@@ -45,6 +45,7 @@ struct Stage2Params {
   const float* partial;
   int32_t batch;
   int32_t grid;
+  int32_t qo_len;
 };
 
 size_t stage1_smem_bytes();

@@ -32,20 +32,52 @@ namespace mla {
 namespace {
 
 // ------------------------------------------------------------ layout
-constexpr int kQPanelBytes = 32 * 128;   // 32 operand rows x 128 dims (swizzle 128B)
-constexpr int kQRopeBytes = 32 * 64;     // 32 operand rows x 64 dims (swizzle 64B)
-constexpr int kPBytes = 128 * 32;        // 128 tokens x 32 operand columns (swizzle 32B)
+// Operand descriptors (layout codes: 2 = 128B swizzle, 4 = 64B, 6 = 32B).
+constexpr uint32_t kLayoutSw128 = 2, kLayoutSw64 = 4, kLayoutSw32 = 6;
 
-constexpr int kOffV = 0;
-constexpr int kOffR = kOffV + kNumVSlots * kVPanelBytes;
-constexpr int kOffQ = kOffR + kNumRSlots * kRPanelBytes;
-constexpr int kOffQRope = kOffQ + 4 * kQPanelBytes;
-constexpr int kOffP = kOffQRope + kQRopeBytes;
-constexpr int kOffMisc = kOffP + 2 * kPBytes;
+constexpr int kMaxQ = 2;          // query tokens per row handled by one CTA tile
+constexpr int kMaxVSlots = 11;    // latent ring slots (kQ = 1)
+
+// Everything that depends on the number kQ of query tokens per row.  The MMA
+// N dimension holds, for each query token, the 16 "hi" then the 16 "lo" heads:
+// column n = 32 qi + 16 lo + head.
+template <int kQ>
+struct Geo {
+  static_assert(kQ == 1 || kQ == 2, "one or two query tokens per row");
+  static constexpr int kN = 32 * kQ;               // MMA N / operand rows of Q and P
+  static constexpr int kNumV = kQ == 1 ? 11 : 9;   // latent ring slots (16 KB each)
+  static constexpr int kQPanelBytes = kN * 128;    // Q: kN rows x 128 dims (swizzle 128B)
+  static constexpr int kQRopeBytes = kN * 64;      // Q: kN rows x 64 rope dims (swizzle 64B)
+  static constexpr int kPBytes = 128 * kN;         // P: 128 tokens x kN columns
+  static constexpr uint32_t kPLayout = kQ == 1 ? kLayoutSw32 : kLayoutSw64;  // one atom = one P row
+
+  static constexpr int kOffV = 0;
+  static constexpr int kOffR = kOffV + kNumV * kVPanelBytes;
+  static constexpr int kOffQ = kOffR + kNumRSlots * kRPanelBytes;
+  static constexpr int kOffQRope = kOffQ + 4 * kQPanelBytes;
+  static constexpr int kOffP = kOffQRope + kQRopeBytes;
+  static constexpr int kOffMisc = kOffP + 2 * kPBytes;
+
+  // TMEM columns: two S buffers (kN each) then O (4 chunks x kN).
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColO = 2 * kN;
+  static constexpr uint32_t kTmemCols = kQ == 1 ? 256 : 512;
+  static_assert(kColO + 4 * kN <= kTmemCols, "TMEM columns");
+
+  static constexpr uint32_t kIdescQK = idesc_e4m3(128, kN, false, false);  // K-major A and B
+  static constexpr uint32_t kIdescPV = idesc_e4m3(128, kN, true, true);    // MN-major A and B
+
+  // 8 KB staging buffers of the epilogue: the Q operand region (4 kQ panels of
+  // 4 KB) then the two P buffers.
+  static constexpr int kNumStage = 2 * kQ + 2 * kPBytes / 8192;
+  static __device__ __forceinline__ uint32_t stage_buf(uint32_t sbase, int k) {
+    return k < 2 * kQ ? sbase + kOffQ + 8192 * k : sbase + kOffP + 8192 * (k - 2 * kQ);
+  }
+};
 
 struct Misc {
-  uint64_t v_full[kNumVSlots];
-  uint64_t v_empty[kNumVSlots];
+  uint64_t v_full[kMaxVSlots];
+  uint64_t v_empty[kMaxVSlots];
   uint64_t r_full[kNumRSlots];
   uint64_t s_full[2];   // QK of tile i landed in S[i & 1]
   uint64_t pv_done[2];  // PV of tile i completed (P[i & 1] free again)
@@ -57,8 +89,8 @@ struct Misc {
   uint32_t s_read;      // tiles whose S has been read out by every softmax warp
   uint32_t p_ready;     // tiles whose P is published (and O rescaled)
   uint32_t o_free;      // segments whose epilogue has read O out of TMEM
-  alignas(16) float red_max[2][4][16];  // read and written as float4
-  alignas(16) float red_sum[4][16];
+  alignas(16) float red_max[2][4][16 * kMaxQ];  // read and written as float4
+  alignas(16) float red_sum[4][16 * kMaxQ];
   uint32_t red_u32[8];
   int32_t scan[8];
   uint32_t tmem_base;
@@ -68,23 +100,23 @@ struct Misc {
   int32_t first_row, first_prefix, first_tiles, last_row;
   int32_t bad;
   uint32_t next_panel[2];  // per producer warp: one past its last issued panel
-  alignas(16) float lse_stage[16];  // a split piece's base-2 LSE on its way out (bulk store)
+  alignas(16) float lse_stage[16 * kMaxQ];  // a split piece's base-2 LSE on its way out (bulk store)
 };
 
 static_assert(offsetof(Misc, red_max) % 16 == 0 && offsetof(Misc, red_sum) % 16 == 0,
               "vector accesses to the reduction scratch need 16-byte alignment");
-static_assert(kOffMisc % 16 == 0, "the barrier block must start 16-byte aligned");
-
 static_assert(kNumRSlots == 2, "rope slots are released through s_full, which has two phases in flight");
 
-constexpr int kSmemUsed = kOffMisc + static_cast<int>(sizeof(Misc));
-constexpr int kSmemAlloc = kSmemUsed + 1024;  // room to align the base to 1024 B
-static_assert(kSmemAlloc <= 232448, "stage-1 shared memory exceeds the per-CTA limit");
-
-// TMEM columns: two S buffers (32 each) then O (4 chunks x 32).
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 64;
+template <int kQ>
+constexpr int smem_alloc() {
+  // + 1024: room to align the base to 1024 B
+  return Geo<kQ>::kOffMisc + static_cast<int>(sizeof(Misc)) + 1024;
+}
+static_assert(Geo<1>::kOffMisc % 16 == 0 && Geo<2>::kOffMisc % 16 == 0,
+              "the barrier block must start 16-byte aligned");
+static_assert(smem_alloc<1>() <= 232448 && smem_alloc<2>() <= 232448,
+              "stage-1 shared memory exceeds the per-CTA limit");
+static_assert(Geo<1>::kNumV <= kMaxVSlots && Geo<2>::kNumV <= kMaxVSlots, "ring slots");
 
 constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4;
@@ -93,11 +125,6 @@ constexpr int kMmaQkWarp = 6;  // QK issuer
 constexpr int kProducer2Warp = 7;  // second page-table producer
 constexpr uint32_t kBarSoftmax = 1;  // named barrier id of warps 0-3
 constexpr uint32_t kBarProducers = 2;  // named barrier id of warps 4 and 7 (page-table mode)
-
-// Operand descriptors (layout codes: 2 = 128B swizzle, 4 = 64B, 6 = 32B).
-constexpr uint32_t kLayoutSw128 = 2, kLayoutSw64 = 4, kLayoutSw32 = 6;
-constexpr uint32_t kIdescQK = idesc_e4m3(128, 32, false, false);  // K-major A and B
-constexpr uint32_t kIdescPV = idesc_e4m3(128, 32, true, true);    // MN-major A and B
 
 // log2(e) / sqrt(576): converts a dot product to base-2 softmax exponent units.
 constexpr float kSmScaleLog2 = 1.4426950408889634f / 24.0f;
@@ -205,13 +232,15 @@ __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity) {
 // the prefix for stage 2; every worker stores its (t0, t1, first, last) record.
 // Zero output for row b (a row without cached tokens, or every row when
 // kv_indptr is invalid), written by the one prologue thread that finds it.
+template <int kQ>
 __device__ __forceinline__ void zero_row(const Stage1Params& p, int32_t b) {
   const int32_t tq = ldg_i32(p.qo_indptr + b);
-  if (ldg_i32(p.qo_indptr + b + 1) - tq != 1 || tq < 0 || tq >= p.batch) return;
+  if (ldg_i32(p.qo_indptr + b + 1) - tq != kQ || tq < 0 || tq > p.batch * kQ - kQ) return;
   uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(tq) * kNumHeads * kVDim);
-  for (int i = 0; i < kNumHeads * kVDim * 2 / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+  for (int i = 0; i < kQ * kNumHeads * kVDim * 2 / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
 }
 
+template <int kQ>
 __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, nwarps = nthreads >> 5;
@@ -272,7 +301,7 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
       const int32_t next = ldg_i32(p.kv_indptr + b + 1);
       const int32_t nt = bad ? 0 : tiles_of_length(static_cast<int64_t>(next) - prev);
       if (c == 0) p.prefix[b] = a;
-      if (nt == 0 && b % p.grid == c) zero_row(p, b);  // no cached token: zero output
+      if (nt == 0 && b % p.grid == c) zero_row<kQ>(p, b);  // no cached token: zero output
       if (nt > 0 && t1 > t0) {
         if (a <= t0 && t0 < a + nt) {
           ms->first_row = b;
@@ -297,7 +326,7 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
       const int32_t c_first = worker_of_tile(a0, total, p.grid);
       if (worker_of_tile(t0 - 1, total, p.grid) == c_first) {
         const int32_t tq = ldg_i32(p.qo_indptr + b);
-        const bool row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == 1 && tq >= 0 && tq < batch;
+        const bool row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == kQ && tq >= 0 && tq <= batch * kQ - kQ;
         job[0] = row_ok ? tq : -1;
         job[1] = c_first;
         job[2] = worker_of_tile(a0 + ms->first_tiles - 1, total, p.grid);
@@ -323,9 +352,10 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
 // been consumed, so a producer can never be more than one phase ahead on a
 // barrier: its own previous panel already waited for the consumption that the
 // phase before would need.
-template <bool kGather>
+template <bool kGather, int kQ>
 __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
                              const CUtensorMap* map_r, Misc* ms, uint32_t sbase, uint32_t who) {
+  using G = Geo<kQ>;
   constexpr uint32_t kProducers = kGather ? 2 : 1;
   const int lane = threadIdx.x & 31;
   if (!kGather && lane != 0) return;
@@ -362,7 +392,7 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
         slot = tile % kNumRSlots;
         use = tile / kNumRSlots;
         bytes = kRPanelBytes;
-        dst = sbase + kOffR + slot * kRPanelBytes;
+        dst = sbase + G::kOffR + slot * kRPanelBytes;
         full = smem_u32(&ms->r_full[slot]);
         // With two rope slots and two S buffers, rope slot (tile & 1) is free
         // exactly when the QK of the tile before last has completed, which is
@@ -372,10 +402,10 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
         map = map_r;
       } else {
         const uint32_t g = tile * 4 + c;
-        slot = g % kNumVSlots;
-        use = g / kNumVSlots;
+        slot = g % G::kNumV;
+        use = g / G::kNumV;
         bytes = kVPanelBytes;
-        dst = sbase + kOffV + slot * kVPanelBytes;
+        dst = sbase + G::kOffV + slot * kVPanelBytes;
         full = smem_u32(&ms->v_full[slot]);
         empty = smem_u32(&ms->v_empty[slot]);
         x = 128 * c;
@@ -410,7 +440,7 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
   if (who != 0 || lane != 0 || !ms->abort_flag) return;
   uint32_t issued[2] = {ms->next_panel[0], kProducers > 1 ? ms->next_panel[1] : 0};
   const uint32_t kmax = max(issued[0], issued[1]);
-  uint32_t need_v = (1u << kNumVSlots) - 1, need_r = (1u << kNumRSlots) - 1;
+  uint32_t need_v = (1u << G::kNumV) - 1, need_r = (1u << kNumRSlots) - 1;
   // Holes in the issued set lie within the last ring's worth of panels.
   for (uint32_t n = 0; n < 64 && n < kmax && (need_v | need_r); ++n) {
     const uint32_t k = kmax - 1 - n;
@@ -424,9 +454,9 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
         need_r &= ~(1u << slot);
       }
     } else {
-      const uint32_t g = t * 4 + c, slot = g % kNumVSlots;
+      const uint32_t g = t * 4 + c, slot = g % G::kNumV;
       if (need_v & (1u << slot)) {
-        drain_phase(smem_u32(&ms->v_full[slot]), (g / kNumVSlots) & 1);
+        drain_phase(smem_u32(&ms->v_full[slot]), (g / G::kNumV) & 1);
         need_v &= ~(1u << slot);
       }
     }
@@ -434,45 +464,52 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
 }
 
 // ------------------------------------------------------------ MMA issuer (warp 5, lane 0)
-// S^T[tile & 1] = K_tile . [Q_hi; Q_lo]^T : 4 latent panels x 4 k-steps of 32
-// dims (128-byte swizzle) plus the rope panel's 2 k-steps (64-byte swizzle).
+// S^T[tile & 1] = K_tile . Q_op^T (Q_op: kN rows, per query token the hi then
+// lo heads): 4 latent panels x 4 k-steps of 32 dims (128-byte swizzle) plus the
+// rope panel's 2 k-steps (64-byte swizzle).
+template <int kQ>
 __device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t sbase, uint32_t tile) {
-  const uint32_t d = tmem + kColS + 32 * (tile & 1);
-  const uint32_t qb = sbase + kOffQ;
+  using G = Geo<kQ>;
+  const uint32_t d = tmem + G::kColS + G::kN * (tile & 1);
+  const uint32_t qb = sbase + G::kOffQ;
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
     const uint32_t g = tile * 4 + p;
-    const uint32_t vs = sbase + kOffV + (g % kNumVSlots) * kVPanelBytes;
+    const uint32_t vs = sbase + G::kOffV + (g % G::kNumV) * kVPanelBytes;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       umma_f8(d, smem_desc(vs + 32 * kk, 1024, 1024, kLayoutSw128),
-              smem_desc(qb + p * kQPanelBytes + 32 * kk, 1024, 1024, kLayoutSw128), kIdescQK,
+              smem_desc(qb + p * G::kQPanelBytes + 32 * kk, 1024, 1024, kLayoutSw128), G::kIdescQK,
               (p | kk) != 0);
     }
   }
-  const uint32_t rs = sbase + kOffR + (tile % kNumRSlots) * kRPanelBytes;
+  const uint32_t rs = sbase + G::kOffR + (tile % kNumRSlots) * kRPanelBytes;
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk) {
     umma_f8(d, smem_desc(rs + 32 * kk, 512, 512, kLayoutSw64),
-            smem_desc(sbase + kOffQRope + 32 * kk, 512, 512, kLayoutSw64), kIdescQK, 1);
+            smem_desc(sbase + G::kOffQRope + 32 * kk, 512, 512, kLayoutSw64), G::kIdescQK, 1);
   }
 }
 
-// O^T[chunk c] (+)= V_c^T . [P_hi; P_lo]^T over the tile's 128 tokens: V panel c
-// read MN-major (dims contiguous), P read MN-major (operand columns contiguous).
-// Each latent panel is released as soon as its four MMAs complete.
+// O^T[chunk c] (+)= V_c^T . P^T over the tile's 128 tokens: V panel c read
+// MN-major (dims contiguous), P read MN-major (a token's kN operand columns
+// contiguous, one swizzle atom: 32 or 64 bytes).  Each latent panel is
+// released as soon as its four MMAs complete.
+template <int kQ>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, uint32_t tile, bool first,
                                          Misc* ms) {
-  const uint32_t pb = sbase + kOffP + (tile & 1) * kPBytes;
+  using G = Geo<kQ>;
+  const uint32_t pb = sbase + G::kOffP + (tile & 1) * G::kPBytes;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint32_t g = tile * 4 + c;
-    const uint32_t slot = g % kNumVSlots;
-    const uint32_t vs = sbase + kOffV + slot * kVPanelBytes;
+    const uint32_t slot = g % G::kNumV;
+    const uint32_t vs = sbase + G::kOffV + slot * kVPanelBytes;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      umma_f8(tmem + kColO + 32 * c, smem_desc(vs + kk * 4096, 1024, 1024, kLayoutSw128),
-              smem_desc(pb + kk * 1024, 256, 256, kLayoutSw32), kIdescPV, !(first && kk == 0));
+      umma_f8(tmem + G::kColO + G::kN * c, smem_desc(vs + kk * 4096, 1024, 1024, kLayoutSw128),
+              smem_desc(pb + kk * 32 * G::kN, 8 * G::kN, 8 * G::kN, G::kPLayout), G::kIdescPV,
+              !(first && kk == 0));
     }
     umma_commit(smem_u32(&ms->v_empty[slot]));
   }
@@ -510,7 +547,9 @@ __device__ __forceinline__ bool spin_counter(const uint32_t* ctr, uint32_t targe
 // QK issuer (warp 6, lane 0): QK of tile i needs its five panels landed (it
 // waits on the TMA barriers itself), the segment's Q operand (first tile of a
 // segment) and S[i & 1] read out by the softmax of tile i - 2.
+template <int kQ>
 __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
+  using G = Geo<kQ>;
   Cursor qc;
   cursor_start(qc, ms, p.kv_indptr, p.batch);
   uint32_t qk_n = 0;  // tiles whose QK has been issued
@@ -519,14 +558,14 @@ __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
                          p.err);
     for (int c = 0; c < 4 && ok; ++c) {
       const uint32_t g = qk_n * 4 + c;
-      ok = wait_phase(smem_u32(&ms->v_full[g % kNumVSlots]), (g / kNumVSlots) & 1, ms, p.err);
+      ok = wait_phase(smem_u32(&ms->v_full[g % G::kNumV]), (g / G::kNumV) & 1, ms, p.err);
     }
     if (ok && qc.j == qc.j0) ok = spin_counter(&ms->q_ready, static_cast<uint32_t>(qc.seg) + 1, ms, p.err);
     if (ok && qk_n >= 2) ok = spin_counter(&ms->s_read, qk_n - 1, ms, p.err);
     if (!ok) break;
     fence_acquire_cta();
     tc_fence_after();
-    issue_qk(tmem, sbase, qk_n);
+    issue_qk<kQ>(tmem, sbase, qk_n);
     umma_commit(smem_u32(&ms->s_full[qk_n & 1]));  // also frees rope slot qk_n & 1
     if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
     ++qk_n;
@@ -539,6 +578,7 @@ __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
 // PV issuer (warp 5, lane 0): PV of tile i needs P[i & 1] published and, on
 // the first tile of a later segment, O read out by the previous segment's
 // epilogue.
+template <int kQ>
 __device__ void run_mma_pv(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
   Cursor pc;
   cursor_start(pc, ms, p.kv_indptr, p.batch);
@@ -550,7 +590,7 @@ __device__ void run_mma_pv(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
     if (!ok) break;
     fence_acquire_cta();
     tc_fence_after();
-    issue_pv(tmem, sbase, pv_n, first, ms);
+    issue_pv<kQ>(tmem, sbase, pv_n, first, ms);
     umma_commit(smem_u32(&ms->pv_done[pv_n & 1]));
     ++pv_n;
     cursor_next_tile(pc, ms, p.kv_indptr, p.batch);
@@ -584,15 +624,17 @@ __device__ __forceinline__ float warp_transpose_sum16(float (&v)[16]) {
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-// Byte address of 16-byte chunk `cc` of operand row `row` in the Q operand:
+// Byte address of 16-byte chunk `ch` of operand row `row` in the Q operand:
 // latent dims in four 128-byte-swizzled panels, rope dims in one 64-byte panel.
+template <int kQ>
 __device__ __forceinline__ uint32_t q_chunk_addr(uint32_t sq, int row, int ch) {
+  using G = Geo<kQ>;
   if (ch < 32) {
     const int panel = ch >> 3, cc = ch & 7;
-    return sq + panel * kQPanelBytes + row * 128 + ((cc ^ (row & 7)) << 4);
+    return sq + panel * G::kQPanelBytes + row * 128 + ((cc ^ (row & 7)) << 4);
   }
   const int cc = ch - 32;
-  return sq + 4 * kQPanelBytes + row * 64 + ((cc ^ ((row >> 1) & 3)) << 4);
+  return sq + 4 * G::kQPanelBytes + row * 64 + ((cc ^ ((row >> 1) & 3)) << 4);
 }
 
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
@@ -628,78 +670,91 @@ __device__ __forceinline__ void split_e4m3_16(const float (&x)[16], uint32_t (&h
   }
 }
 
-// Loads query token tq (16 heads x 576 bf16), scales it by a power of two so the
-// largest magnitude lands in (224, 448], and writes the hi / lo e4m3 operand rows
-// (rows 0-15 hi, 16-31 lo).  Returns the factor turning the QK accumulator into
-// base-2 softmax exponent units.  tq < 0 writes a zero query.
-__device__ float prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq,
-                           float kv_scale) {
+// Loads the row's query tokens tq .. tq + kQ - 1 (16 heads x 576 bf16 each),
+// scales each by a power of two so its largest magnitude lands in (224, 448],
+// and writes the hi / lo e4m3 operand rows of token qi (rows 32 qi + head for
+// hi, 32 qi + 16 + head for lo).  Sets qk_scale[qi], the factor turning the QK
+// accumulator of token qi into base-2 softmax exponent units.  tq < 0 writes a
+// zero query.
+template <int kQ>
+__device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq,
+                          float kv_scale, float (&qk_scale)[kQ]) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  uint4 raw[5][2];
+  uint4 raw[kQ][5][2];
 #pragma unroll
-  for (int r = 0; r < 5; ++r) {
-    const int job = t + 128 * r;
-    raw[r][0] = raw[r][1] = make_uint4(0, 0, 0, 0);
-    if (job < 576 && tq >= 0) {
-      const int head = job / 36, ch = job % 36;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + (static_cast<size_t>(tq) * kNumHeads + head) * kQkDim + ch * 16);
-      raw[r][0] = __ldg(src);
-      raw[r][1] = __ldg(src + 1);
+  for (int qi = 0; qi < kQ; ++qi) {
+#pragma unroll
+    for (int r = 0; r < 5; ++r) {
+      const int job = t + 128 * r;
+      raw[qi][r][0] = raw[qi][r][1] = make_uint4(0, 0, 0, 0);
+      if (job < 576 && tq >= 0) {
+        const int head = job / 36, ch = job % 36;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + (static_cast<size_t>(tq + qi) * kNumHeads + head) * kQkDim + ch * 16);
+        raw[qi][r][0] = __ldg(src);
+        raw[qi][r][1] = __ldg(src + 1);
+      }
     }
   }
   // The previous segment's output may still be leaving the Q and P regions
   // through bulk stores (the loads above are already in flight); the barrier
   // below orders every write to them after this wait.
   if (t == 0) bulk_wait_read<0>();
-  uint32_t amax = 0;
-  auto fold = [&](uint32_t w) { amax = max(amax, max(w & 0x7FFFu, (w >> 16) & 0x7FFFu)); };
 #pragma unroll
-  for (int r = 0; r < 5; ++r) {
+  for (int qi = 0; qi < kQ; ++qi) {
+    uint32_t amax = 0;
+    auto fold = [&](uint32_t w) { amax = max(amax, max(w & 0x7FFFu, (w >> 16) & 0x7FFFu)); };
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      fold(raw[r][k].x);
-      fold(raw[r][k].y);
-      fold(raw[r][k].z);
-      fold(raw[r][k].w);
-    }
-  }
-  amax = __reduce_max_sync(0xffffffffu, amax);
-  if (lane == 0) ms->red_u32[warp] = amax;
-  named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-  amax = max(max(ms->red_u32[0], ms->red_u32[1]), max(ms->red_u32[2], ms->red_u32[3]));
-  const float a = __uint_as_float(amax << 16);
-  int k2 = 0;
-  if (a > 0.0f) {
-    int e;
-    const float f = frexpf(a, &e);  // a = f * 2^e, f in [0.5, 1)
-    k2 = (f <= 0.875f) ? 9 - e : 8 - e;
-    k2 = min(max(k2, -126), 126);
-  }
-  const float up = __int_as_float((k2 + 127) << 23);
-  const float down = __int_as_float((127 - k2) << 23);
-
+    for (int r = 0; r < 5; ++r) {
 #pragma unroll
-  for (int r = 0; r < 5; ++r) {
-    const int job = t + 128 * r;
-    if (job < 576) {
-      const int head = job / 36, ch = job % 36;
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(&raw[r][0]);
-      float x[16];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        x[2 * i] = u2f(w[i] << 16) * up;
-        x[2 * i + 1] = u2f(w[i] & 0xFFFF0000u) * up;
+      for (int k = 0; k < 2; ++k) {
+        fold(raw[qi][r][k].x);
+        fold(raw[qi][r][k].y);
+        fold(raw[qi][r][k].z);
+        fold(raw[qi][r][k].w);
       }
-      uint32_t hi[4], lo[4];
-      split_e4m3_16(x, hi, lo);
-      st_shared_v4(q_chunk_addr(sq, head, ch), hi[0], hi[1], hi[2], hi[3]);
-      st_shared_v4(q_chunk_addr(sq, 16 + head, ch), lo[0], lo[1], lo[2], lo[3]);
+    }
+    amax = __reduce_max_sync(0xffffffffu, amax);
+    if (lane == 0) ms->red_u32[4 * qi + warp] = amax;
+  }
+  named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+#pragma unroll
+  for (int qi = 0; qi < kQ; ++qi) {
+    const uint32_t amax = max(max(ms->red_u32[4 * qi], ms->red_u32[4 * qi + 1]),
+                              max(ms->red_u32[4 * qi + 2], ms->red_u32[4 * qi + 3]));
+    const float a = __uint_as_float(amax << 16);
+    int k2 = 0;
+    if (a > 0.0f) {
+      int e;
+      const float f = frexpf(a, &e);  // a = f * 2^e, f in [0.5, 1)
+      k2 = (f <= 0.875f) ? 9 - e : 8 - e;
+      k2 = min(max(k2, -126), 126);
+    }
+    const float up = __int_as_float((k2 + 127) << 23);
+    qk_scale[qi] = __int_as_float((127 - k2) << 23) * kv_scale * kSmScaleLog2;
+#pragma unroll
+    for (int r = 0; r < 5; ++r) {
+      const int job = t + 128 * r;
+      if (job < 576) {
+        const int head = job / 36, ch = job % 36;
+        float x[16];
+        auto unpack = [&](uint32_t w, int i) {
+          x[2 * i] = u2f(w << 16) * up;
+          x[2 * i + 1] = u2f(w & 0xFFFF0000u) * up;
+        };
+        unpack(raw[qi][r][0].x, 0); unpack(raw[qi][r][0].y, 1);
+        unpack(raw[qi][r][0].z, 2); unpack(raw[qi][r][0].w, 3);
+        unpack(raw[qi][r][1].x, 4); unpack(raw[qi][r][1].y, 5);
+        unpack(raw[qi][r][1].z, 6); unpack(raw[qi][r][1].w, 7);
+        uint32_t hi[4], lo[4];
+        split_e4m3_16(x, hi, lo);
+        st_shared_v4(q_chunk_addr<kQ>(sq, 32 * qi + head, ch), hi[0], hi[1], hi[2], hi[3]);
+        st_shared_v4(q_chunk_addr<kQ>(sq, 32 * qi + 16 + head, ch), lo[0], lo[1], lo[2], lo[3]);
+      }
     }
   }
   fence_proxy_async_smem();
   named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-  return down * kv_scale * kSmScaleLog2;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -740,12 +795,15 @@ __device__ __forceinline__ void split_p_16(const float (&x)[16], uint32_t (&hi)[
   }
 }
 
+template <int kQ>
 __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem,
                             float kv_scale) {
+  using G = Geo<kQ>;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;  // TMEM lane quarter
   const int token = warp * 32 + lane;  // S row (token) / O row (dim within a chunk) of this thread
   const int32_t c = static_cast<int32_t>(blockIdx.x);
+  const int32_t num_q = p.batch * kQ;  // query tokens in q and out
 
   Cursor cur;
   cursor_start(cur, ms, p.kv_indptr, p.batch);
@@ -764,102 +822,133 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
   while (cur.live) {
     // ------------------------------------------------ segment start
     const int32_t b = cur.b;
-    const int32_t tq = ldg_i32(p.qo_indptr + b);
-    const bool row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == 1 && tq >= 0 && tq < p.batch;
+    const int32_t tq = ldg_i32(p.qo_indptr + b);  // the row's first query token
+    const bool row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == kQ && tq >= 0 && tq <= num_q - kQ;
     if (!row_ok && t == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
     if (cur.seg > 0) wait_phase(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
-    const float qk_scale = prepare_q(p, ms, sbase + kOffQ, row_ok ? tq : -1, kv_scale);
-    const float qk_scale_lo = qk_scale * 0.0625f;
+    float qk_scale[kQ];
+    prepare_q<kQ>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, kv_scale, qk_scale);
     if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 1));
 
-    float m_ref[16], l[16];
+    float m_ref[kQ][16], l[kQ][16];
 #pragma unroll
-    for (int h = 0; h < 16; ++h) {
-      m_ref[h] = -INFINITY;
-      l[h] = 0.0f;
+    for (int qi = 0; qi < kQ; ++qi) {
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        m_ref[qi][h] = -INFINITY;
+        l[qi][h] = 0.0f;
+      }
     }
     const uint32_t seg_first_tile = tile;
 
     // ------------------------------------------------ tiles
     for (;;) {
-      const int32_t valid = min(kTileTokens, cur.len - cur.j * kTileTokens);
       const uint32_t sb = tile & 1;
       wait_phase(smem_u32(&ms->s_full[sb]), (tile >> 1) & 1, ms, p.err);
       tc_fence_after();
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_base + kColS + 32 * sb, r);
-      tmem_wait_ld();
-      tc_fence_before();
-
-      const bool tok_ok = token < valid;
-      float s[16];
+      // Query token qi sees the row's first len - kQ + 1 + qi tokens (causal,
+      // aligned to the end of the row; for kQ = 1 the whole row).
+      const int32_t pos = cur.j * kTileTokens + token;  // row-local token of this thread
+      bool tok_ok[kQ];
+      float s[kQ][16];
       bool exceed = false;
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        s[h] = tok_ok ? fmaf(u2f(r[16 + h]), qk_scale_lo, u2f(r[h]) * qk_scale) : -INFINITY;
-        exceed |= s[h] > m_ref[h] + kRescaleThreshold;
+      for (int qi = 0; qi < kQ; ++qi) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + G::kColS + G::kN * sb + 32 * qi, r);
+        tmem_wait_ld();
+        tok_ok[qi] = pos < cur.len - kQ + 1 + qi;
+        const float sc = qk_scale[qi], sc_lo = sc * 0.0625f;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          s[qi][h] = tok_ok[qi] ? fmaf(u2f(r[16 + h]), sc_lo, u2f(r[h]) * sc) : -INFINITY;
+          exceed |= s[qi][h] > m_ref[qi][h] + kRescaleThreshold;
+        }
       }
+      tc_fence_before();
 
       // The reference maximum moves only when some score exceeds it by more
       // than the threshold (always on a segment's first tile); then the tile
-      // maximum per head is reduced over the 128 tokens.
-      float alpha[16];
+      // maximum per column is reduced over the 128 tokens.
+      float alpha[kQ][16];
       bool moved = false;
 #pragma unroll
-      for (int h = 0; h < 16; ++h) alpha[h] = 1.0f;
+      for (int qi = 0; qi < kQ; ++qi) {
+#pragma unroll
+        for (int h = 0; h < 16; ++h) alpha[qi][h] = 1.0f;
+      }
       const bool any_exceed = softmax_bar_or(exceed);
       // Every softmax warp has read S[sb] (its tcgen05.ld completed before the barrier).
       if (t == 0) st_release_u32(&ms->s_read, tile + 1);
       if (any_exceed) {
-        float mx[16];
+        float mx[kQ][16];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) mx[h] = warp_max(s[h]);
+        for (int qi = 0; qi < kQ; ++qi) {
+#pragma unroll
+          for (int h = 0; h < 16; ++h) mx[qi][h] = warp_max(s[qi][h]);
+        }
         if (lane == 0) {
           float4* dst = reinterpret_cast<float4*>(&ms->red_max[sb][warp][0]);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dst[k] = make_float4(mx[4 * k], mx[4 * k + 1], mx[4 * k + 2], mx[4 * k + 3]);
+          for (int qi = 0; qi < kQ; ++qi) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              dst[4 * qi + k] = make_float4(mx[qi][4 * k], mx[qi][4 * k + 1], mx[qi][4 * k + 2],
+                                            mx[qi][4 * k + 3]);
+          }
         }
         named_bar_sync(kBarSoftmax, kSoftmaxThreads);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float4 m4 = reinterpret_cast<const float4*>(&ms->red_max[sb][0][0])[k];
+        for (int qi = 0; qi < kQ; ++qi) {
 #pragma unroll
-          for (int w = 1; w < 4; ++w) {
-            const float4 o4 = reinterpret_cast<const float4*>(&ms->red_max[sb][w][0])[k];
-            m4.x = fmaxf(m4.x, o4.x); m4.y = fmaxf(m4.y, o4.y);
-            m4.z = fmaxf(m4.z, o4.z); m4.w = fmaxf(m4.w, o4.w);
+          for (int k = 0; k < 4; ++k) {
+            float4 m4 = reinterpret_cast<const float4*>(&ms->red_max[sb][0][0])[4 * qi + k];
+#pragma unroll
+            for (int w = 1; w < 4; ++w) {
+              const float4 o4 = reinterpret_cast<const float4*>(&ms->red_max[sb][w][0])[4 * qi + k];
+              m4.x = fmaxf(m4.x, o4.x); m4.y = fmaxf(m4.y, o4.y);
+              m4.z = fmaxf(m4.z, o4.z); m4.w = fmaxf(m4.w, o4.w);
+            }
+            mx[qi][4 * k] = m4.x; mx[qi][4 * k + 1] = m4.y;
+            mx[qi][4 * k + 2] = m4.z; mx[qi][4 * k + 3] = m4.w;
           }
-          mx[4 * k] = m4.x; mx[4 * k + 1] = m4.y; mx[4 * k + 2] = m4.z; mx[4 * k + 3] = m4.w;
-        }
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          if (mx[h] > m_ref[h] + kRescaleThreshold) {
-            alpha[h] = fast_exp2(m_ref[h] - mx[h]);  // 0 on a segment's first tile
-            m_ref[h] = mx[h];
-            l[h] *= alpha[h];
-            moved = true;
+          for (int h = 0; h < 16; ++h) {
+            if (mx[qi][h] > m_ref[qi][h] + kRescaleThreshold) {
+              alpha[qi][h] = fast_exp2(m_ref[qi][h] - mx[qi][h]);  // 0 on a segment's first tile
+              m_ref[qi][h] = mx[qi][h];
+              l[qi][h] *= alpha[qi][h];
+              moved = true;
+            }
           }
         }
       }
       const bool rescale_o = moved && tile != seg_first_tile;
 
-      float pr[16];
+      uint32_t phi[kQ][4], plo[kQ][4];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        pr[h] = tok_ok ? fast_exp2(s[h] - m_ref[h]) : 0.0f;
-        l[h] += pr[h];
+      for (int qi = 0; qi < kQ; ++qi) {
+        float pr[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          pr[h] = tok_ok[qi] ? fast_exp2(s[qi][h] - m_ref[qi][h]) : 0.0f;
+          l[qi][h] += pr[h];
+        }
+        split_p_16(pr, phi[qi], plo[qi]);
       }
-      uint32_t phi[4], plo[4];
-      split_p_16(pr, phi, plo);
 
       // P[sb] was last read by the PV of tile - 2.
       if (tile >= 2) wait_pv(tile - 2);
       {
-        const uint32_t pa = sbase + kOffP + sb * kPBytes + token * 32;
-        const uint32_t sw = (token >> 2) & 1;
-        st_shared_v4(pa + ((0 ^ sw) << 4), phi[0], phi[1], phi[2], phi[3]);
-        st_shared_v4(pa + ((1 ^ sw) << 4), plo[0], plo[1], plo[2], plo[3]);
+        // One P row per token: kN bytes, 16-byte chunks (hi then lo of each
+        // query token) swizzled as the 32- or 64-byte atom requires.
+        const uint32_t pa = sbase + G::kOffP + sb * G::kPBytes + token * G::kN;
+        const uint32_t sw = kQ == 1 ? (token >> 2) & 1 : (token >> 1) & 3;
+#pragma unroll
+        for (int qi = 0; qi < kQ; ++qi) {
+          st_shared_v4(pa + (((2 * qi) ^ sw) << 4), phi[qi][0], phi[qi][1], phi[qi][2], phi[qi][3]);
+          st_shared_v4(pa + (((2 * qi + 1) ^ sw) << 4), plo[qi][0], plo[qi][1], plo[qi][2], plo[qi][3]);
+        }
       }
       fence_proxy_async_smem();
       if (rescale_o) {
@@ -868,13 +957,16 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
-          uint32_t o[32];
-          const uint32_t addr = tmem + lane_base + kColO + 32 * cc;
-          tmem_ld32(addr, o);
-          tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(u2f(o[j]) * alpha[j & 15]);
-          tmem_st32(addr, o);
+          for (int qi = 0; qi < kQ; ++qi) {
+            uint32_t o[32];
+            const uint32_t addr = tmem + lane_base + G::kColO + G::kN * cc + 32 * qi;
+            tmem_ld32(addr, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(u2f(o[j]) * alpha[qi][j & 15]);
+            tmem_st32(addr, o);
+          }
         }
         tmem_wait_st();
       }
@@ -892,93 +984,113 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     // and one thread issues bulk stores, so the warps do not wait for their
     // global stores to drain before the next segment.
     if (cur.next_a < ms->t1 && b + 1 < p.batch) {
-      // More segments follow: bring the next row's query (18 KB) into L2 now,
-      // so that its Q preparation after this epilogue reads it from there.
+      // More segments follow: bring the next row's query into L2 now, so that
+      // its Q preparation after this epilogue reads it from there.
       const int32_t tq_next = ldg_i32(p.qo_indptr + b + 1);
-      if (tq_next >= 0 && tq_next < p.batch) {
+      if (tq_next >= 0 && tq_next <= num_q - kQ) {
         const char* qn = reinterpret_cast<const char*>(p.q + static_cast<size_t>(tq_next) * kNumHeads * kQkDim);
-        for (int i = t; i < kNumHeads * kQkDim * 2 / 128; i += kSoftmaxThreads) prefetch_l2(qn + 128 * i);
+        for (int i = t; i < kQ * kNumHeads * kQkDim * 2 / 128; i += kSoftmaxThreads) prefetch_l2(qn + 128 * i);
       }
     }
     if (t == 0) ms->red_u32[4] = static_cast<uint32_t>(ms->abort_flag);
-    float l_tot[16];
-    {
+    float l_tot[kQ][16];
+#pragma unroll
+    for (int qi = 0; qi < kQ; ++qi) {
       float v[16];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) v[h] = l[h];
+      for (int h = 0; h < 16; ++h) v[h] = l[qi][h];
       const float ws = warp_transpose_sum16(v);
-      if ((lane & 1) == 0) ms->red_sum[warp][lane >> 1] = ws;
-      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+      if ((lane & 1) == 0) ms->red_sum[warp][16 * qi + (lane >> 1)] = ws;
+    }
+    named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+#pragma unroll
+    for (int qi = 0; qi < kQ; ++qi) {
 #pragma unroll
       for (int h = 0; h < 16; ++h)
-        l_tot[h] = (ms->red_sum[0][h] + ms->red_sum[1][h]) + (ms->red_sum[2][h] + ms->red_sum[3][h]);
+        l_tot[qi][h] = (ms->red_sum[0][16 * qi + h] + ms->red_sum[1][16 * qi + h]) +
+                       (ms->red_sum[2][16 * qi + h] + ms->red_sum[3][16 * qi + h]);
     }
     const bool write = row_ok && ms->red_u32[4] == 0;  // the same for every softmax thread
-    float inv[16];  // l >= 1 (the reference maximum contributes 1): a fast divide suffices
+    // l >= 1 when the token saw a cached token here (its reference maximum
+    // contributes 1): a fast divide suffices; l = 0 (nothing visible) gives 0.
+    float inv[kQ][16];
 #pragma unroll
-    for (int h = 0; h < 16; ++h) inv[h] = __fdividef(kv_scale, l_tot[h]);
+    for (int qi = 0; qi < kQ; ++qi) {
+#pragma unroll
+      for (int h = 0; h < 16; ++h) inv[qi][h] = l_tot[qi][h] > 0.0f ? __fdividef(kv_scale, l_tot[qi][h]) : 0.0f;
+    }
     wait_pv(tile - 1);  // PV of the segment's last tile (and so of all before it)
     tc_fence_after();
-    const uint32_t stage_q = sbase + kOffQ;
+    const uint32_t stage_q = sbase + G::kOffQ;
     if (cur.whole) {
-      // bf16 row [16 heads][512 dims], 16 KB, staged in the Q region.
+      // bf16 rows [kQ tokens][16 heads][512 dims] (16 KB each), staged in the Q region.
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_base + kColO + 32 * cc, o);
-        tmem_wait_ld();
-        const int dim = 128 * cc + token;
-        if (write) {
 #pragma unroll
-          for (int h = 0; h < 16; ++h)
-            st_shared_u16(stage_q + (h * kVDim + dim) * 2,
-                          bf16_bits((u2f(o[h]) + u2f(o[16 + h]) * 0.0625f) * inv[h]));
+        for (int qi = 0; qi < kQ; ++qi) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_base + G::kColO + G::kN * cc + 32 * qi, o);
+          tmem_wait_ld();
+          const int dim = 128 * cc + token;
+          if (write) {
+#pragma unroll
+            for (int h = 0; h < 16; ++h)
+              st_shared_u16(stage_q + ((16 * qi + h) * kVDim + dim) * 2,
+                            bf16_bits((u2f(o[h]) + u2f(o[16 + h]) * 0.0625f) * inv[qi][h]));
+          }
         }
       }
       fence_proxy_async_smem();
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);
       if (t == 0 && write) {
-        bulk_store(p.out + static_cast<size_t>(tq) * kNumHeads * kVDim, stage_q, kNumHeads * kVDim * 2);
+        bulk_store(p.out + static_cast<size_t>(tq) * kNumHeads * kVDim, stage_q,
+                   kQ * kNumHeads * kVDim * 2);
         bulk_commit();
       }
     } else {
-      // fp32 partial, stored [slot][dim / 128][head / 4][dim % 128][head % 4]:
-      // each 128-dim chunk is 8 KB of contiguous memory, staged in one of three
-      // 8 KB buffers (two in the Q region, one over the P buffers).  The
-      // base-2 log-sum-exp follows the last chunk in the same bulk group.
+      // fp32 partial of query token qi, stored
+      // [slot][qi][dim / 128][head / 4][dim % 128][head % 4]: each 128-dim chunk
+      // is 8 KB of contiguous memory, staged in the 8 KB buffers of Geo (the Q
+      // region, then the P buffers), reused once their bulk store has read them.
+      // The base-2 log-sum-exps follow the last chunk in the same bulk group.
       const int32_t slot = partial_slot(c, ms->t0, cur.row_a);
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int k = 0; k < 4 * kQ; ++k) {
+        const int qi = k >> 2, cc = k & 3;
         uint32_t o[32];
-        tmem_ld32(tmem + lane_base + kColO + 32 * cc, o);
+        tmem_ld32(tmem + lane_base + G::kColO + G::kN * cc + 32 * qi, o);
         tmem_wait_ld();
-        const uint32_t buf = cc == 1 ? stage_q + 8192 : (cc == 2 ? sbase + kOffP : stage_q);
-        if (cc == 3) {  // reuses chunk 0's buffer
-          if (t == 0) bulk_wait_read<2>();
+        const uint32_t buf = G::stage_buf(sbase, k % G::kNumStage);
+        if (k >= G::kNumStage) {  // reuses the buffer of chunk k - kNumStage
+          if (t == 0) bulk_wait_read<G::kNumStage - 1>();
           named_bar_sync(kBarSoftmax, kSoftmaxThreads);
         }
         if (write) {
           float v[16];
 #pragma unroll
-          for (int h = 0; h < 16; ++h) v[h] = (u2f(o[h]) + u2f(o[16 + h]) * 0.0625f) * inv[h];
+          for (int h = 0; h < 16; ++h) v[h] = (u2f(o[h]) + u2f(o[16 + h]) * 0.0625f) * inv[qi][h];
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             st_shared_v4(buf + (j * 128 + token) * 16, __float_as_uint(v[4 * j]),
                          __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
                          __float_as_uint(v[4 * j + 3]));
-          if (cc == 3 && t < 16) {
-            float x = m_ref[0] + log2f(l_tot[0]);
+          if (k == 4 * kQ - 1 && t < 16 * kQ) {
+            // thread t stages the LSE of (token t / 16, head t % 16); -inf when it saw nothing
+            float x = m_ref[0][0] + log2f(l_tot[0][0]);
 #pragma unroll
-            for (int h = 1; h < 16; ++h) x = t == h ? m_ref[h] + log2f(l_tot[h]) : x;
+            for (int e = 1; e < 16 * kQ; ++e)
+              x = t == e ? m_ref[e >> 4][e & 15] + log2f(l_tot[e >> 4][e & 15]) : x;
             ms->lse_stage[t] = x;
           }
         }
         fence_proxy_async_smem();
         named_bar_sync(kBarSoftmax, kSoftmaxThreads);
         if (t == 0 && write) {
-          bulk_store(p.partial + (static_cast<size_t>(slot) * 4 + cc) * (kNumHeads * 128), buf,
-                     kNumHeads * 128 * 4);
-          if (cc == 3) bulk_store(p.lse + slot * kNumHeads, smem_u32(ms->lse_stage), 64);
+          bulk_store(p.partial + ((static_cast<size_t>(slot) * kQ + qi) * 4 + cc) * (kNumHeads * 128),
+                     buf, kNumHeads * 128 * 4);
+          if (k == 4 * kQ - 1)
+            bulk_store(p.lse + static_cast<size_t>(slot) * kQ * kNumHeads, smem_u32(ms->lse_stage),
+                       kQ * kNumHeads * 4);
           bulk_commit();
         }
       }
@@ -997,20 +1109,21 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
 }
 
 // ------------------------------------------------------------ kernel
-template <bool kGather>
+template <bool kGather, int kQ>
 __global__ void __launch_bounds__(kStage1Threads, 1)
     mla_decode_stage1_kernel(const __grid_constant__ CUtensorMap map_v,
                              const __grid_constant__ CUtensorMap map_r, const Stage1Params p) {
+  using G = Geo<kQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Misc* ms = reinterpret_cast<Misc*>(smem + kOffMisc);
+  Misc* ms = reinterpret_cast<Misc*>(smem + G::kOffMisc);
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  if (warp == kMmaWarp) tmem_alloc(smem_u32(&ms->tmem_base), kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(&ms->tmem_base), G::kTmemCols);
   if (tid == kProducerWarp * 32) {
-    for (int s = 0; s < kNumVSlots; ++s) {
+    for (int s = 0; s < G::kNumV; ++s) {
       mbar_init(smem_u32(&ms->v_full[s]), 1);
       mbar_init(smem_u32(&ms->v_empty[s]), 1);
     }
@@ -1035,22 +1148,22 @@ __global__ void __launch_bounds__(kStage1Threads, 1)
   // Stage 2 may start launching now; it waits for this grid's completion
   // before it reads anything this grid writes.
   pdl_launch_dependents();
-  schedule_prologue(p, ms);
+  schedule_prologue<kQ>(p, ms);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ms->tmem_base;
 
   if (warp < 4) {
-    run_softmax(p, ms, sbase, tmem, __ldg(p.kv_scale));
+    run_softmax<kQ>(p, ms, sbase, tmem, __ldg(p.kv_scale));
   } else if (warp == kProducerWarp) {
-    run_producer<kGather>(p, &map_v, &map_r, ms, sbase, 0);
+    run_producer<kGather, kQ>(p, &map_v, &map_r, ms, sbase, 0);
   } else if (kGather && warp == kProducer2Warp) {
-    run_producer<kGather>(p, &map_v, &map_r, ms, sbase, 1);
+    run_producer<kGather, kQ>(p, &map_v, &map_r, ms, sbase, 1);
   } else if (warp == kMmaWarp && lane == 0) {
-    run_mma_pv(p, ms, sbase, tmem);
+    run_mma_pv<kQ>(p, ms, sbase, tmem);
   } else if (warp == kMmaQkWarp && lane == 0) {
-    run_mma_qk(p, ms, sbase, tmem);
+    run_mma_qk<kQ>(p, ms, sbase, tmem);
   }
   __syncwarp();
   tc_fence_before();
@@ -1059,40 +1172,55 @@ __global__ void __launch_bounds__(kStage1Threads, 1)
     if (lane == 0) drain_phase(smem_u32(&ms->mma_done), 0);
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, G::kTmemCols);
   }
 }
 
-}  // namespace
-
-size_t stage1_smem_bytes() { return static_cast<size_t>(kSmemAlloc); }
-
-cudaError_t stage1_prepare(int device) {
-  (void)device;
-  cudaError_t e = cudaFuncSetAttribute(mla_decode_stage1_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(mla_decode_stage1_kernel<true>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+template <bool kGather, int kQ>
+cudaError_t set_smem_limit() {
+  return cudaFuncSetAttribute(mla_decode_stage1_kernel<kGather, kQ>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem_alloc<kQ>());
 }
 
-cudaError_t launch_stage1(const Stage1Params& p, const CUtensorMap& map_v,
-                          const CUtensorMap& map_r, bool gather, cudaStream_t stream) {
+template <bool kGather, int kQ>
+cudaError_t launch(const Stage1Params& p, const CUtensorMap& map_v, const CUtensorMap& map_r,
+                   cudaStream_t stream) {
   // A programmatic dependent of the previous kernel in the stream: its CTAs
   // may be scheduled while that kernel finishes, and wait for it (griddepcontrol
   // .wait) before touching global memory.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
   cfg.blockDim = dim3(kStage1Threads);
-  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.dynamicSmemBytes = smem_alloc<kQ>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return gather ? cudaLaunchKernelEx(&cfg, mla_decode_stage1_kernel<true>, map_v, map_r, p)
-                : cudaLaunchKernelEx(&cfg, mla_decode_stage1_kernel<false>, map_v, map_r, p);
+  return cudaLaunchKernelEx(&cfg, mla_decode_stage1_kernel<kGather, kQ>, map_v, map_r, p);
+}
+
+}  // namespace
+
+size_t stage1_smem_bytes() {
+  return static_cast<size_t>(smem_alloc<1>() > smem_alloc<2>() ? smem_alloc<1>() : smem_alloc<2>());
+}
+
+cudaError_t stage1_prepare(int device) {
+  (void)device;
+  cudaError_t e = set_smem_limit<false, 1>();
+  if (e == cudaSuccess) e = set_smem_limit<true, 1>();
+  if (e == cudaSuccess) e = set_smem_limit<false, 2>();
+  if (e == cudaSuccess) e = set_smem_limit<true, 2>();
+  return e;
+}
+
+cudaError_t launch_stage1(const Stage1Params& p, const CUtensorMap& map_v,
+                          const CUtensorMap& map_r, bool gather, cudaStream_t stream) {
+  if (p.qo_len == 2)
+    return gather ? launch<true, 2>(p, map_v, map_r, stream) : launch<false, 2>(p, map_v, map_r, stream);
+  return gather ? launch<true, 1>(p, map_v, map_r, stream) : launch<false, 1>(p, map_v, map_r, stream);
 }
 
 }  // namespace mla

@@ -7,10 +7,10 @@
 // the workers, not the rows: stage 1 records in worker c's entry the combine
 // job of the split row whose first boundary is worker c's start (output row,
 // first and last worker, first worker's partial slot; the others use slot 2c),
-// and block (c, 4 * cc + j) combines dims 128cc..128cc+127 of heads 4j..4j+3
-// of that row, one dim per thread.  Rows held whole by one worker, and rows
+// and block (c, 16 qi + 4 cc + j) combines dims 128cc..128cc+127 of heads
+// 4j..4j+3 of query token qi of that row, one dim per thread.  Rows held whole by one worker, and rows
 // without cached tokens, are written by stage 1.  Partials are stored as
-// [slot][dim / 128][head / 4][dim % 128][head % 4] (stage 1's epilogue), so a
+// [slot][token][dim / 128][head / 4][dim % 128][head % 4] (stage 1's epilogue), so a
 // warp's float4 loads cover 512 contiguous bytes; the partials of a row are
 // visited four at a time, their loads in flight together.
 #include <cuda_bf16.h>
@@ -35,11 +35,12 @@ __global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const
   pdl_wait_primary();
 
   const int32_t c = blockIdx.x;
-  const int cc = blockIdx.y >> 2, j = blockIdx.y & 3, dd = threadIdx.x;
+  const int qi = blockIdx.y >> 4, cc = (blockIdx.y >> 2) & 3, j = blockIdx.y & 3, dd = threadIdx.x;
+  const int32_t nq = p.qo_len;
   const int4* rec = reinterpret_cast<const int4*>(p.workers);
   const int4 job = rec[2 * c + 1];  // (output row, first worker, last worker, first slot)
-  const int32_t tq = job.x;
-  if (tq < 0) return;
+  if (job.x < 0) return;
+  const int32_t tq = job.x + qi;  // output row: query token qi of the row
 
   const float4* lse4 = reinterpret_cast<const float4*>(p.lse);
   const float4* part4 = reinterpret_cast<const float4*>(p.partial);
@@ -58,10 +59,10 @@ __global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const
     for (int u = 0; u < kStage2Unroll; ++u) {
       const int32_t cu = w0 + u;
       if (cu <= job.z) {
-        const int32_t slot = cu == job.y ? job.w : 2 * cu;
+        const int32_t piece = (cu == job.y ? job.w : 2 * cu) * nq + qi;  // (slot, token)
         wr[u] = rec[2 * cu];
-        x[u] = lse4[slot * 4 + j];
-        v[u] = part4[((static_cast<size_t>(slot) * 4 + cc) * 4 + j) * kStage2Threads + dd];
+        x[u] = lse4[piece * 4 + j];
+        v[u] = part4[((static_cast<size_t>(piece) * 4 + cc) * 4 + j) * kStage2Threads + dd];
       }
     }
 #pragma unroll
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const
       const float vs[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
+        if (xs[h] == -INFINITY) continue;  // the token saw no cached token in this piece
         const float mn = fmaxf(m[h], xs[h]);
         const float f = exp2f(m[h] - mn), w = exp2f(xs[h] - mn);
         wsum[h] = wsum[h] * f + w;
@@ -81,7 +83,7 @@ __global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const
   }
 #pragma unroll
   for (int h = 0; h < 4; ++h) {
-    const __nv_bfloat16 y = __float2bfloat16_rn(acc[h] / wsum[h]);
+    const __nv_bfloat16 y = __float2bfloat16_rn(wsum[h] > 0.0f ? acc[h] / wsum[h] : 0.0f);
     blk[h * kStage2Threads + dd] = *reinterpret_cast<const uint16_t*>(&y);
   }
   __syncthreads();
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const
 
 cudaError_t launch_stage2(const Stage2Params& p, bool programmatic, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.grid), 16);
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid), 16 * p.qo_len);
   cfg.blockDim = dim3(kStage2Threads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

@@ -45,7 +45,7 @@ KV_CHUNK_ROWS = 16384
 
 @dataclass(frozen=True)
 class Workload:
-    """One benchmark shape: ``batch`` rows of one query token each."""
+    """One benchmark shape: ``batch`` rows of ``qo_len`` query tokens each."""
 
     name: str
     batch: int
@@ -53,6 +53,7 @@ class Workload:
     ragged: bool = False       # lengths ~ U{1..kv_len}
     paged: bool = False        # cache rows addressed through a permuted page table
     seed: int = BASE_SEED
+    qo_len: int = 1            # query tokens per row (2: two-token decode)
 
     @property
     def max_kv_len(self) -> int:
@@ -68,6 +69,8 @@ WORKLOADS = {
         Workload("bs256_kv8192", 256, 8192, seed=BASE_SEED + 3),
         Workload("ragged_bs128_kv8192_paged", 128, 8192, ragged=True, paged=True,
                  seed=BASE_SEED + 4),
+        # Two query tokens per row (speculative / multi-token-prediction decode).
+        Workload("bs64_q2_kv8192", 64, 8192, seed=BASE_SEED + 5, qo_len=2),
     )
 }
 
@@ -79,7 +82,7 @@ HEADLINE = "bs256_kv8192"
 class Inputs:
     """Host arrays for one decode call; bf16 values are kept as raw uint16 bits."""
 
-    q_bits: np.ndarray              # uint16 [B, 16, 576]
+    q_bits: np.ndarray              # uint16 [B * qo_len, 16, 576]
     kv_bits: np.ndarray             # uint16 [N, 576]   (bf16 source of the latent cache)
     qo_indptr: np.ndarray           # int32 [B + 1]
     kv_indptr: np.ndarray           # int32 [B + 1]
@@ -90,6 +93,10 @@ class Inputs:
     @property
     def batch(self) -> int:
         return int(self.qo_indptr.shape[0] - 1)
+
+    @property
+    def qo_len(self) -> int:
+        return int(self.meta.get("qo_len", 1))
 
     @property
     def lengths(self) -> np.ndarray:
@@ -151,11 +158,12 @@ def normal_bf16_rows(seed: int, rows: int, cols: int = QK_HEAD_DIM,
 
 
 def make_from_lengths(lengths, seed: int, *, paged: bool = False,
-                      max_kv_len: Optional[int] = None) -> Inputs:
-    """Inputs for arbitrary per-row cache lengths (zero allowed)."""
+                      max_kv_len: Optional[int] = None, qo_len: int = 1) -> Inputs:
+    """Inputs for arbitrary per-row cache lengths (zero allowed) and
+    ``qo_len`` query tokens per row (``qo_indptr = qo_len * arange``)."""
     lengths = np.asarray(lengths, dtype=np.int64)
     batch = int(lengths.shape[0])
-    q = np.empty((batch, NUM_HEADS, QK_HEAD_DIM), dtype=np.float32)
+    q = np.empty((batch * qo_len, NUM_HEADS, QK_HEAD_DIM), dtype=np.float32)
     _rng(seed, 0).standard_normal(out=q, dtype=np.float32)
     kv_indptr = np.zeros(batch + 1, dtype=np.int64)
     np.cumsum(lengths, out=kv_indptr[1:])
@@ -169,11 +177,11 @@ def make_from_lengths(lengths, seed: int, *, paged: bool = False,
     return Inputs(
         q_bits=f32_to_bf16_bits(q),
         kv_bits=kv_bits,
-        qo_indptr=np.arange(batch + 1, dtype=np.int32),
+        qo_indptr=(qo_len * np.arange(batch + 1)).astype(np.int32),
         kv_indptr=kv_indptr.astype(np.int32),
         kv_indices=kv_indices,
         max_kv_len=int(max_kv_len if max_kv_len is not None else max(1, int(lengths.max(initial=0)))),
-        meta={"seed": seed, "paged": paged},
+        meta={"seed": seed, "paged": paged, "qo_len": qo_len},
     )
 
 
@@ -187,6 +195,7 @@ def make_inputs(w) -> Inputs:
     """Inputs of a named workload (see ``WORKLOADS``)."""
     if isinstance(w, str):
         w = WORKLOADS[w]
-    inp = make_from_lengths(workload_lengths(w), w.seed, paged=w.paged, max_kv_len=w.max_kv_len)
+    inp = make_from_lengths(workload_lengths(w), w.seed, paged=w.paged, max_kv_len=w.max_kv_len,
+                            qo_len=w.qo_len)
     inp.meta["workload"] = w.name
     return inp

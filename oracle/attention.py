@@ -16,7 +16,13 @@ is the exact bf16 value handed in.
 
 Readings taken where the pages are silent:
   * a row with no cached tokens (``kv_len == 0``) yields all-zero output;
-  * ``qo_indptr`` must give each row exactly one query token (decode, qseqlen 1).
+  * a row may hold n >= 1 query tokens (``qo_indptr[b+1] - qo_indptr[b] = n``;
+    the pages pass ``max_seqlen_qo`` / ``uni_seqlen_qo`` but only ever run
+    n = 1).  Multi-token decode (speculative / multi-token prediction) appends
+    the n query tokens' own entries as the row's last n cached tokens, so query
+    token i (0-based) attends to the first ``L - n + 1 + i`` cached tokens
+    (causal, aligned to the end of the row); a token that sees no cached token
+    yields zeros.  For n = 1 this is the plain decode step.
 """
 from __future__ import annotations
 
@@ -48,11 +54,24 @@ def _row_tokens(b: int, kv_indptr, kv_indices) -> np.ndarray:
     return np.asarray(kv_indices[j0:j1], dtype=np.int64)
 
 
-def _query_row(b: int, qo_indptr) -> int:
+def _query_rows(b: int, qo_indptr) -> tuple[int, int]:
+    """(first query token, query token count n >= 1) of row b."""
     t0, t1 = int(qo_indptr[b]), int(qo_indptr[b + 1])
-    if t1 - t0 != 1:
-        raise ValueError(f"row {b} has {t1 - t0} query tokens; decode takes exactly one")
+    if t1 - t0 < 1:
+        raise ValueError(f"row {b} has {t1 - t0} query tokens")
+    return t0, t1 - t0
+
+
+def _query_row(b: int, qo_indptr) -> int:
+    t0, n = _query_rows(b, qo_indptr)
+    if n != 1:
+        raise ValueError(f"row {b} has {n} query tokens; this function takes one")
     return t0
+
+
+def visible_tokens(length: int, n: int, i: int) -> int:
+    """Cached tokens query token i of an n-token row sees (causal, end-aligned)."""
+    return max(0, length - n + 1 + i)
 
 
 def dequant_rows(kv_codes: np.ndarray, kv_scale, slots: np.ndarray) -> np.ndarray:
@@ -77,19 +96,24 @@ def mla_decode_ref(q, kv_codes, kv_scale, qo_indptr, kv_indptr,
     ``q`` is float64-convertible ``[T, 16, 576]`` (exact bf16 values);
     ``kv_codes`` uint8 ``[N, 576]`` (or ``[N, 1, 576]``); ``kv_scale`` the float32
     per-tensor scale; ``kv_indices`` maps flattened token j to cache slot
-    ``kv_indices[j]`` (identity when None).  ``rows`` restricts the work to a
-    subset of batch rows; the other output rows are left as NaN.
+    ``kv_indices[j]`` (identity when None).  Query token ``qo_indptr[b] + i`` of
+    an n-token row sees the row's first ``visible_tokens(L, n, i)`` cached tokens.
+    ``rows`` restricts the work to a subset of batch rows; the other output rows
+    are left as NaN.
     """
     q = np.asarray(q, dtype=np.float64)
     batch = len(qo_indptr) - 1
     out = np.full((q.shape[0], NUM_HEADS, V_HEAD_DIM), np.nan)
     for b in (range(batch) if rows is None else rows):
-        t = _query_row(b, qo_indptr)
+        t0, n = _query_rows(b, qo_indptr)
         slots = _row_tokens(b, kv_indptr, kv_indices)
-        if slots.size == 0:
-            out[t] = 0.0
-            continue
-        _, out[t] = row_attention(q[t], dequant_rows(kv_codes, kv_scale, slots))
+        k_rows = dequant_rows(kv_codes, kv_scale, slots)
+        for i in range(n):
+            vis = visible_tokens(slots.size, n, i)
+            if vis == 0:
+                out[t0 + i] = 0.0
+                continue
+            _, out[t0 + i] = row_attention(q[t0 + i], k_rows[:vis])
     return out
 
 
@@ -143,19 +167,23 @@ def mla_decode_split_ref(q, kv_codes, kv_scale, qo_indptr, kv_indptr, segments,
 
     ``segments`` maps batch row b to a list of token ranges ``(j0, j1)`` (row-local
     token offsets) that partition ``[0, L_b)``; any partition gives the same
-    result as ``mla_decode_ref`` up to rounding.
+    result as ``mla_decode_ref`` up to rounding.  With n query tokens per row,
+    each split is cut to the tokens the query token sees (an empty cut gives a
+    zero partial with lse -inf).
     """
     q = np.asarray(q, dtype=np.float64)
     batch = len(qo_indptr) - 1
     out = np.zeros((q.shape[0], NUM_HEADS, V_HEAD_DIM))
     for b in range(batch):
-        t = _query_row(b, qo_indptr)
+        t0, n = _query_rows(b, qo_indptr)
         slots = _row_tokens(b, kv_indptr, kv_indices)
         k_rows = dequant_rows(kv_codes, kv_scale, slots)
-        parts, lses = [], []
-        for (j0, j1) in segments.get(b, [(0, slots.size)]):
-            o, lse = split_partial(q[t], k_rows[j0:j1])
-            parts.append(o)
-            lses.append(lse)
-        out[t] = combine_partials(parts, lses) if parts else 0.0
+        for i in range(n):
+            vis = visible_tokens(slots.size, n, i)
+            parts, lses = [], []
+            for (j0, j1) in segments.get(b, [(0, slots.size)]):
+                o, lse = split_partial(q[t0 + i], k_rows[j0:min(j1, vis)] if j0 < vis else k_rows[:0])
+                parts.append(o)
+                lses.append(lse)
+            out[t0 + i] = combine_partials(parts, lses) if parts else 0.0
     return out

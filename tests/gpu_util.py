@@ -45,11 +45,12 @@ class DeviceCase:
         self.kv_indptr = torch.from_numpy(inp.kv_indptr).to(device)
         self.kv_indices = (None if inp.kv_indices is None
                            else torch.from_numpy(inp.kv_indices).to(device))
-        self.out = torch.empty((inp.batch, 16, 512), dtype=torch.bfloat16, device=device)
+        self.out = torch.empty((inp.batch * inp.qo_len, 16, 512), dtype=torch.bfloat16,
+                               device=device)
 
     def run(self, sms: int | None = None, workspace=None, plan=None):
         plan = plan or binding.mla_decode_plan(self.inp.batch, self.inp.max_kv_len,
-                                               sms or num_sms())
+                                               sms or num_sms(), qo_len=self.inp.qo_len)
         ws = workspace if workspace is not None else binding.new_workspace(plan)
         binding.mla_decode_fwd(self.q, self.kv_codes, self.kv_scale, self.qo_indptr,
                                self.kv_indptr, self.out, plan=plan, workspace=ws,
@@ -80,16 +81,18 @@ class OracleCase:
             return mla_decode_ref(self.q, self.codes(), self.scale, inp.qo_indptr, inp.kv_indptr,
                                   inp.kv_indices)
         # Encode only the cache rows the sampled batch rows read.
-        out = np.full((inp.batch, 16, 512), np.nan)
+        n = inp.qo_len
+        out = np.full((inp.batch * n, 16, 512), np.nan)
         for b in rows:
             j0, j1 = int(inp.kv_indptr[b]), int(inp.kv_indptr[b + 1])
             slots = (np.arange(j0, j1) if inp.kv_indices is None
                      else inp.kv_indices[j0:j1].astype(np.int64))
             codes = encode_with_scale(self.kv_f32[slots], self.scale) if slots.size else \
                 np.zeros((0, 576), np.uint8)
-            sub = mla_decode_ref(self.q[b:b + 1], codes, self.scale, np.array([0, 1]),
+            t0 = int(inp.qo_indptr[b])
+            sub = mla_decode_ref(self.q[t0:t0 + n], codes, self.scale, np.array([0, n]),
                                  np.array([0, slots.size]))
-            out[b] = sub[0]
+            out[t0:t0 + n] = sub
         return out
 
 

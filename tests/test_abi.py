@@ -34,7 +34,7 @@ def test_every_declared_function_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.mla_decode_abi_version() == 2
+    assert lib.mla_decode_abi_version() == 3
     for s in range(5):
         assert lib.mla_status_string(s)
 
@@ -107,3 +107,18 @@ def test_binding_refuses_cpu_tensors(lib):
     q = torch.zeros(1, 16, 576, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         binding.mla_decode_fwd(q, q, q, q, q, q, plan=plan, workspace=q)
+
+
+@pytest.mark.parametrize("qo_len", [1, 2])
+def test_plan_mtp_sizes_the_partials_by_query_tokens(lib, qo_len):
+    plan = binding.mla_decode_plan(64, 8192, 152, qo_len=qo_len)
+    assert plan.qo_len == qo_len and plan.grid == plan_grid(64, 8192, 152)
+    g = plan.grid
+    assert plan.ws_partial_offset >= plan.ws_lse_offset + 4 * 2 * g * qo_len * 16
+    assert plan.ws_bytes >= plan.ws_partial_offset + 4 * 2 * g * qo_len * 16 * 512
+
+
+def test_plan_mtp_rejects_unsupported_token_counts(lib):
+    plan = binding.mla_plan_t()
+    for n in (0, 3, 4, -1):
+        assert lib.mla_decode_plan_mtp(8, n, 1024, 152, ctypes.byref(plan)) == 1

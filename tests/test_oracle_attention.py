@@ -138,6 +138,103 @@ def test_combine_with_empty_split_and_single_split():
     assert np.all(combine_partials([z], [zl]) == 0)
 
 
-def test_rejects_multi_token_queries():
+def test_rejects_rows_without_query_tokens():
     with pytest.raises(ValueError):
-        mla_decode_ref(np.zeros((2, 16, 576)), np.zeros((4, 576), np.uint8), 1.0, [0, 2], [0, 4])
+        mla_decode_ref(np.zeros((2, 16, 576)), np.zeros((4, 576), np.uint8), 1.0, [0, 2, 2], [0, 4, 4])
+
+
+# ------------------------------------------------------------------ multi-token rows
+def multi_token_case(rng, lengths, n, paged=False):
+    """Rows of n query tokens each (qo_indptr = n * arange), small query values."""
+    q, codes, scale, _, kv_indptr, idx = random_case(rng, lengths, paged)
+    batch = len(lengths)
+    q = bf16_bits_to_f64(f32_to_bf16_bits(
+        (0.05 * rng.standard_normal((batch * n, 16, 576))).astype(np.float32)))
+    qo_indptr = (n * np.arange(batch + 1)).astype(np.int32)
+    return q, codes, scale, qo_indptr, kv_indptr, idx
+
+
+def brute_force_positions(q, codes, scale, qo_indptr, kv_indptr, idx):
+    """Multi-token decode with scalar loops, phrased by sequence positions: a
+    row's cache holds positions 0..L-1, its n query tokens are the last n of
+    them (positions L-n..L-1), and a query at position p sees positions <= p."""
+    out = np.zeros((q.shape[0], 16, 512))
+    for b in range(len(qo_indptr) - 1):
+        n = int(qo_indptr[b + 1] - qo_indptr[b])
+        length = int(kv_indptr[b + 1] - kv_indptr[b])
+        for i in range(n):
+            t = int(qo_indptr[b]) + i
+            pos = length - n + i
+            slots = []
+            for j in range(length):
+                if j <= pos:
+                    g = int(kv_indptr[b]) + j
+                    slots.append(int(idx[g]) if idx is not None else g)
+            for h in range(16):
+                weights = []
+                for sl in slots:
+                    k = [float(v) * float(scale) for v in e4m3fn_decode(codes[sl])]
+                    weights.append(math.exp(sum(q[t, h, d] * k[d] for d in range(576)) / 24.0))
+                total = sum(weights)
+                for w, sl in zip(weights, slots):
+                    out[t, h] += (w / total) * (e4m3fn_decode(codes[sl][:512]) * float(scale))
+    return out
+
+
+@pytest.mark.parametrize("lengths,n,paged", [([3, 5], 2, False), ([4, 1, 6], 2, True), ([5], 3, False),
+                                             ([2], 4, False)])
+def test_multi_token_brute_force(lengths, n, paged):
+    rng = np.random.default_rng(1000 + 7 * n + sum(lengths))
+    case = multi_token_case(rng, lengths, n, paged)
+    ref = mla_decode_ref(*case[:5], kv_indices=case[5])
+    np.testing.assert_allclose(ref, brute_force_positions(*case), rtol=1e-10, atol=1e-12)
+
+
+def test_multi_token_full_row_is_causal_attention():
+    """With as many query tokens as cached tokens the step is plain causal
+    attention over the row: a lower-triangular mask on the score matrix."""
+    rng = np.random.default_rng(77)
+    length = 9
+    q, codes, scale, qo, kvp, idx = multi_token_case(rng, [length], length)
+    ref = mla_decode_ref(q, codes, scale, qo, kvp)
+    k = e4m3fn_decode(codes[:length]) * float(scale)
+    for h in range(16):
+        z = (q[:, h, :] @ k.T) / 24.0
+        z[np.triu(np.ones((length, length), dtype=bool), 1)] = -np.inf
+        w = np.exp(z - z.max(axis=1, keepdims=True))
+        w /= w.sum(axis=1, keepdims=True)
+        np.testing.assert_allclose(ref[:, h, :], w @ k[:, :512], rtol=1e-12, atol=1e-14)
+
+
+def test_multi_token_last_token_is_plain_decode_and_early_tokens_see_less():
+    rng = np.random.default_rng(78)
+    lengths, n = [7, 3, 12], 3
+    q, codes, scale, qo, kvp, idx = multi_token_case(rng, lengths, n, paged=True)
+    ref = mla_decode_ref(q, codes, scale, qo, kvp, kv_indices=idx)
+    for b, length in enumerate(lengths):
+        for i in range(n):
+            # token i alone, as a one-token row over the first L - n + 1 + i tokens
+            vis = length - n + 1 + i
+            one = mla_decode_ref(q[[n * b + i]], codes, scale, [0, 1], [0, vis],
+                                 kv_indices=idx[kvp[b]:kvp[b] + vis])
+            np.testing.assert_array_equal(ref[n * b + i], one[0])
+
+
+def test_multi_token_tokens_that_see_nothing_are_zero():
+    rng = np.random.default_rng(79)
+    q, codes, scale, qo, kvp, idx = multi_token_case(rng, [1, 2], 3)
+    ref = mla_decode_ref(q, codes, scale, qo, kvp)
+    # row 0 (L=1): tokens 0 and 1 see nothing, token 2 sees one; row 1 (L=2): token 0 sees nothing
+    assert np.all(ref[[0, 1, 3]] == 0) and all(np.any(ref[t] != 0) for t in (2, 4, 5))
+    np.testing.assert_array_equal(ref[2], e4m3fn_decode(codes[0, :512])[None, :].repeat(16, 0) * float(scale))
+
+
+def test_multi_token_split_equals_unsplit():
+    rng = np.random.default_rng(80)
+    lengths, n = [300, 129, 5], 2
+    case = multi_token_case(rng, lengths, n, paged=True)
+    ref = mla_decode_ref(*case[:5], kv_indices=case[5])
+    for grid in (1, 3, 7):
+        segs = token_segments(case[4], grid)
+        got = mla_decode_split_ref(*case[:5], segs, kv_indices=case[5])
+        np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
