@@ -10,9 +10,11 @@ namespace mla {
 constexpr int kNumRSlots = 2;       // 8 KB slots: tokens x 64 rope dims (swizzle 64B)
 constexpr int kVPanelBytes = 128 * 128;  // latent ring slot: 128 tokens x 128 dims (swizzle 128B)
 constexpr int kRPanelBytes = 128 * 64;
-// warps 0-3 softmax/epilogue, 4 TMA producer, 5 PV MMA issuer, 6 QK MMA issuer,
-// 7 second TMA producer (page-table mode only)
+// warps 0-3 softmax/epilogue, 4 TMA producer, 5 PV MMA issuer, 6 QK MMA issuer;
+// page-table mode adds TMA producers in warps 7, 8 and 9 (12 warps, registers
+// rebalanced with setmaxnreg).
 constexpr int kStage1Threads = 256;
+constexpr int kStage1ThreadsGather = 384;
 constexpr long long kWaitLimitCycles = 2000000000LL;  // ~1 s per pipeline wait at 2 GHz
 
 struct Stage1Params {

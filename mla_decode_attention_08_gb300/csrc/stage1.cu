@@ -4,7 +4,7 @@
 // range.  Per 128-token tile of the FP8 latent cache:
 //   * warp 4 streams the tile once through TMA into a ring of swizzled panels
 //     (four 128-dim latent panels + one 64-dim rope panel; page-table rows are
-//     fetched with tile::gather4, the panels alternating between warps 4 and 7),
+//     fetched with tile::gather4, the panels spread over four producer warps),
 //   * warp 6 issues the tcgen05 MMAs S^T[128 tok x 32] = K_tile . [Q_hi;Q_lo]^T
 //     and warp 5 the MMAs O^T[512 x 32] += V_tile^T . [P_hi;P_lo]^T,
 //     accumulators in TMEM,
@@ -99,7 +99,7 @@ struct Misc {
   int32_t t0, t1;
   int32_t first_row, first_prefix, first_tiles, last_row;
   int32_t bad;
-  uint32_t next_panel[2];  // per producer warp: one past its last issued panel
+  uint32_t next_panel[4];  // per producer warp: one past its last issued panel
   alignas(16) float lse_stage[16 * kMaxQ];  // a split piece's base-2 LSE on its way out (bulk store)
 };
 
@@ -122,9 +122,27 @@ constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;    // PV issuer; owns the TMEM allocation
 constexpr int kMmaQkWarp = 6;  // QK issuer
-constexpr int kProducer2Warp = 7;  // second page-table producer
 constexpr uint32_t kBarSoftmax = 1;  // named barrier id of warps 0-3
-constexpr uint32_t kBarProducers = 2;  // named barrier id of warps 4 and 7 (page-table mode)
+constexpr uint32_t kBarProducers = 2;  // named barrier id of the page-table producers
+// Page-table mode with one query token: 12 warps, four producer warps (4, 7,
+// 8, 9) taking panels round-robin; the softmax warpgroup gets 240 registers and
+// the other two 128 (launched with 168 each: 128 x 240 + 256 x 128 <= 384 x 168).
+// With two query tokens the softmax needs more than 240 registers, so that
+// kernel keeps 8 warps and two producers (warps 4 and 7).
+template <bool kGather, int kQ>
+__host__ __device__ constexpr bool wide_gather() { return kGather && kQ == 1; }
+template <bool kGather, int kQ>
+__host__ __device__ constexpr int stage1_threads() { return wide_gather<kGather, kQ>() ? kStage1ThreadsGather : kStage1Threads; }
+template <bool kGather, int kQ>
+__host__ __device__ constexpr uint32_t num_producers() { return !kGather ? 1 : (kQ == 1 ? 4 : 2); }
+// Producer index of a warp in page-table mode (warps 4, 7, 8, 9), or -1.
+__device__ __forceinline__ int gather_producer_of_warp(int warp, uint32_t producers) {
+  const int who = warp == 4 ? 0 : (warp >= 7 ? warp - 6 : -1);
+  return who < static_cast<int>(producers) ? who : -1;
+}
+constexpr int kSoftmaxRegs = 240, kOtherRegs = 128;
+static_assert(128 * kSoftmaxRegs + 256 * kOtherRegs <= kStage1ThreadsGather * 168,
+              "register split exceeds the launch allocation");
 
 // log2(e) / sqrt(576): converts a dot product to base-2 softmax exponent units.
 constexpr float kSmScaleLog2 = 1.4426950408889634f / 24.0f;
@@ -160,6 +178,29 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, Misc
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Misc* ms, int32_t* err) {
   if (mbar_try_wait(bar, parity)) return true;  // the common case: already complete
   return wait_phase_slow(bar, parity, ms, err);
+}
+
+// The same wait with its slow path inlined, for the softmax warpgroup: a call
+// out of a region whose register count setmaxnreg raised does not compile.
+__device__ __forceinline__ bool wait_phase_inl(uint32_t bar, uint32_t parity, Misc* ms, int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long start = clock64();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15) == 0) {
+      if (ms->abort_flag) return false;
+      if (clock64() - start > kWaitLimitCycles) {
+        ms->abort_flag = 1;
+        set_error(err, MLA_DERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+template <bool kInline>
+__device__ __forceinline__ bool softmax_wait(uint32_t bar, uint32_t parity, Misc* ms, int32_t* err) {
+  return kInline ? wait_phase_inl(bar, parity, ms, err) : wait_phase(bar, parity, ms, err);
 }
 
 // ------------------------------------------------------------ segment cursor
@@ -344,9 +385,10 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
 // panel k = 5 * tile + 1 + c in one sequence over the worker's tiles.
 // Contiguous rows: lane 0 of warp 4 alone issues one tiled box per panel.
 // Page table: every lane gathers four rows (tile::gather4) per panel, and the
-// panels alternate between warps 4 and 7 (k even / odd): a warp issues its
-// gathers one lane after another, so two issuing warps double the rate at
-// which row fetches enter the copy engine.
+// panels go round-robin to four producer warps (panel k to producer k % 4): a
+// warp issues its gathers one lane after another, so more issuing warps raise
+// the rate at which row fetches enter the copy engine (measured pure-load
+// rates 1.78, 3.52 and 4.54 TB/s with one, two and four warps).
 //
 // Every fill of a slot is issued only after the previous fill of that slot has
 // been consumed, so a producer can never be more than one phase ahead on a
@@ -356,7 +398,7 @@ template <bool kGather, int kQ>
 __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
                              const CUtensorMap* map_r, Misc* ms, uint32_t sbase, uint32_t who) {
   using G = Geo<kQ>;
-  constexpr uint32_t kProducers = kGather ? 2 : 1;
+  constexpr uint32_t kProducers = num_producers<kGather, kQ>();
   const int lane = threadIdx.x & 31;
   if (!kGather && lane != 0) return;
   Cursor cur;
@@ -436,15 +478,23 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
   // exit: wait (bounded) for the last fill issued into every slot; every
   // earlier fill of a slot was consumed before the next one was issued.
   if (lane == 0) ms->next_panel[who] = next_k;
-  if (kGather) named_bar_sync(kBarProducers, 64);
+  if (kGather) named_bar_sync(kBarProducers, 32 * kProducers);
   if (who != 0 || lane != 0 || !ms->abort_flag) return;
-  uint32_t issued[2] = {ms->next_panel[0], kProducers > 1 ? ms->next_panel[1] : 0};
-  const uint32_t kmax = max(issued[0], issued[1]);
+  uint32_t issued[kProducers];
+  uint32_t kmax = 0;
+#pragma unroll
+  for (uint32_t w = 0; w < kProducers; ++w) {
+    issued[w] = ms->next_panel[w];
+    kmax = max(kmax, issued[w]);
+  }
   uint32_t need_v = (1u << G::kNumV) - 1, need_r = (1u << kNumRSlots) - 1;
   // Holes in the issued set lie within the last ring's worth of panels.
   for (uint32_t n = 0; n < 64 && n < kmax && (need_v | need_r); ++n) {
     const uint32_t k = kmax - 1 - n;
-    if (k >= issued[k % kProducers]) continue;  // never issued
+    uint32_t upto = issued[0];
+#pragma unroll
+    for (uint32_t w = 1; w < kProducers; ++w) upto = k % kProducers == w ? issued[w] : upto;
+    if (k >= upto) continue;  // never issued
     const uint32_t t = k / 5;
     const int c = static_cast<int>(k % 5) - 1;
     if (c < 0) {
@@ -795,7 +845,9 @@ __device__ __forceinline__ void split_p_16(const float (&x)[16], uint32_t (&hi)[
   }
 }
 
-template <int kQ>
+// kInlineWaits: the waits' slow paths inlined (required where setmaxnreg raised
+// the register count: a call out of such a region does not compile).
+template <int kQ, bool kInlineWaits>
 __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem,
                             float kv_scale) {
   using G = Geo<kQ>;
@@ -814,7 +866,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
   auto wait_pv = [&](uint32_t k) {
     const uint32_t b = k & 1;
     while (pv_seen[b] <= (k >> 1)) {
-      wait_phase(smem_u32(&ms->pv_done[b]), pv_seen[b] & 1, ms, p.err);
+      softmax_wait<kInlineWaits>(smem_u32(&ms->pv_done[b]), pv_seen[b] & 1, ms, p.err);
       ++pv_seen[b];
     }
   };
@@ -825,7 +877,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     const int32_t tq = ldg_i32(p.qo_indptr + b);  // the row's first query token
     const bool row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == kQ && tq >= 0 && tq <= num_q - kQ;
     if (!row_ok && t == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
-    if (cur.seg > 0) wait_phase(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
+    if (cur.seg > 0) softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
     float qk_scale[kQ];
     prepare_q<kQ>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, kv_scale, qk_scale);
     if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 1));
@@ -844,7 +896,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     // ------------------------------------------------ tiles
     for (;;) {
       const uint32_t sb = tile & 1;
-      wait_phase(smem_u32(&ms->s_full[sb]), (tile >> 1) & 1, ms, p.err);
+      softmax_wait<kInlineWaits>(smem_u32(&ms->s_full[sb]), (tile >> 1) & 1, ms, p.err);
       tc_fence_after();
       // Query token qi sees the row's first len - kQ + 1 + qi tokens (causal,
       // aligned to the end of the row; for kQ = 1 the whole row).
@@ -1110,7 +1162,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
 
 // ------------------------------------------------------------ kernel
 template <bool kGather, int kQ>
-__global__ void __launch_bounds__(kStage1Threads, 1)
+__global__ void __launch_bounds__((stage1_threads<kGather, kQ>()), 1)
     mla_decode_stage1_kernel(const __grid_constant__ CUtensorMap map_v,
                              const __grid_constant__ CUtensorMap map_r, const Stage1Params p) {
   using G = Geo<kQ>;
@@ -1154,16 +1206,24 @@ __global__ void __launch_bounds__(kStage1Threads, 1)
   tc_fence_after();
   const uint32_t tmem = ms->tmem_base;
 
+  // Page-table mode runs 12 warps: registers move from the producers and MMA
+  // issuers to the softmax warpgroup, inside the role branches so that each
+  // role's code is compiled under its own count.
+  constexpr bool kWide = wide_gather<kGather, kQ>();
   if (warp < 4) {
-    run_softmax<kQ>(p, ms, sbase, tmem, __ldg(p.kv_scale));
-  } else if (warp == kProducerWarp) {
-    run_producer<kGather, kQ>(p, &map_v, &map_r, ms, sbase, 0);
-  } else if (kGather && warp == kProducer2Warp) {
-    run_producer<kGather, kQ>(p, &map_v, &map_r, ms, sbase, 1);
-  } else if (warp == kMmaWarp && lane == 0) {
-    run_mma_pv<kQ>(p, ms, sbase, tmem);
-  } else if (warp == kMmaQkWarp && lane == 0) {
-    run_mma_qk<kQ>(p, ms, sbase, tmem);
+    if constexpr (kWide) setmaxnreg_inc<kSoftmaxRegs>();
+    run_softmax<kQ, kWide || kQ == 2>(p, ms, sbase, tmem, __ldg(p.kv_scale));
+  } else {
+    if constexpr (kWide) setmaxnreg_dec<kOtherRegs>();
+    const int who = kGather ? gather_producer_of_warp(warp, num_producers<kGather, kQ>())
+                            : (warp == kProducerWarp ? 0 : -1);
+    if (who >= 0) {
+      run_producer<kGather, kQ>(p, &map_v, &map_r, ms, sbase, static_cast<uint32_t>(who));
+    } else if (warp == kMmaWarp && lane == 0) {
+      run_mma_pv<kQ>(p, ms, sbase, tmem);
+    } else if (warp == kMmaQkWarp && lane == 0) {
+      run_mma_qk<kQ>(p, ms, sbase, tmem);
+    }
   }
   __syncwarp();
   tc_fence_before();
@@ -1190,7 +1250,7 @@ cudaError_t launch(const Stage1Params& p, const CUtensorMap& map_v, const CUtens
   // .wait) before touching global memory.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
-  cfg.blockDim = dim3(kStage1Threads);
+  cfg.blockDim = dim3(stage1_threads<kGather, kQ>());
   cfg.dynamicSmemBytes = smem_alloc<kQ>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
