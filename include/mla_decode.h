@@ -47,7 +47,7 @@ typedef enum {
 } mla_status_t;
 
 /* Bits of the device-side error word (sticky until cleared). */
-#define MLA_DERR_QO_INDPTR 1  /* a row does not hold exactly one query token in [0, batch) */
+#define MLA_DERR_QO_INDPTR 1  /* a row does not hold exactly plan->qo_len query tokens in range */
 #define MLA_DERR_KV_INDPTR 2  /* kv_indptr decreases, or its end exceeds kv_rows / kv_indices_len */
 #define MLA_DERR_KV_INDEX 4   /* a page-table entry lies outside [0, kv_rows)                */
 #define MLA_DERR_TIMEOUT 8    /* a pipeline wait ran past its time limit; the call gave up  */
@@ -170,6 +170,22 @@ mla_status_t mla_decode_stage1(const void* q_bf16, const void* kv_fp8, const flo
                                void* workspace, size_t workspace_bytes);
 mla_status_t mla_decode_stage2(const int32_t* qo_indptr, void* out_bf16, cudaStream_t stream,
                                const mla_plan_t* plan, void* workspace, size_t workspace_bytes);
+
+/*
+ * mla_decode_fwd_stall_stream — test hook for the bounded waits (no
+ * counterpart on the pages).  Same arguments and launches as mla_decode_fwd,
+ * but stage 1's producers issue no cache loads, so the waits on them run out
+ * after their time limit (about one second of SM cycles); the kernel then sets
+ * MLA_DERR_TIMEOUT in the workspace error word, stops issuing work, drains
+ * what it issued and returns.  Nothing faults and the context stays usable.
+ * The output is not written meaningfully.  Returns MLA_OK after launching.
+ */
+mla_status_t mla_decode_fwd_stall_stream(const void* q_bf16, const void* kv_fp8,
+                                         const float* kv_scale, const int32_t* qo_indptr,
+                                         const int32_t* kv_indptr, void* out_bf16,
+                                         cudaStream_t stream, const mla_plan_t* plan,
+                                         const int32_t* kv_indices, int64_t kv_indices_len,
+                                         int64_t kv_rows, void* workspace, size_t workspace_bytes);
 
 /*
  * mla_fp8_quantize_per_tensor — per-tensor absmax quantisation of a bf16 tensor

@@ -44,6 +44,7 @@ SIGNATURES = {
     "mla_decode_plan": (ctypes.c_int, [_I32, _I32, _I32, _PLANP]),
     "mla_decode_plan_mtp": (ctypes.c_int, [_I32, _I32, _I32, _I32, _PLANP]),
     "mla_decode_fwd": (ctypes.c_int, _FWD_ARGS),
+    "mla_decode_fwd_stall_stream": (ctypes.c_int, _FWD_ARGS),
     "mla_decode_stage1": (ctypes.c_int, _FWD_ARGS),
     "mla_decode_fwd_static_scratch": (ctypes.c_int, _FWD_ARGS[:-2]),
     "mla_decode_stage2": (ctypes.c_int, [_VP, _VP, _VP, _PLANP, _VP, _SZ]),
@@ -128,6 +129,15 @@ def mla_decode_fwd(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream=None, 
         *_fwd_args(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream, plan, kv_indices,
                    workspace)))
     return out
+
+
+def mla_decode_fwd_stall_stream(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream=None, *,
+                                plan, workspace, kv_indices=None) -> None:
+    """Test hook: the decode launches with a cache stream that never arrives,
+    so the bounded waits run out and the call reports MLA_DERR_TIMEOUT."""
+    _check("mla_decode_fwd_stall_stream", load_library().mla_decode_fwd_stall_stream(
+        *_fwd_args(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream, plan, kv_indices,
+                   workspace)))
 
 
 def mla_decode_fwd_static_scratch(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream=None, *,

@@ -141,7 +141,7 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
                         const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
                         cudaStream_t stream, const mla_plan_t* plan, const int32_t* kv_indices,
                         int64_t kv_indices_len, int64_t kv_rows, void* workspace,
-                        size_t workspace_bytes) {
+                        size_t workspace_bytes, bool stall_stream = false) {
   mla_status_t st = check_plan(plan);
   if (st != MLA_OK) return st;
   if (q == nullptr || kv == nullptr || kv_scale == nullptr || qo_indptr == nullptr ||
@@ -179,6 +179,7 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
   p.batch = plan->batch;
   p.grid = plan->grid;
   p.qo_len = plan->qo_len;
+  p.stall_stream = stall_stream ? 1 : 0;
   return mla::launch_stage1(p, map_v, map_r, gather, stream) == cudaSuccess ? MLA_OK
                                                                            : MLA_ERR_CUDA;
 }
@@ -271,6 +272,22 @@ mla_status_t mla_decode_fwd(const void* q_bf16, const void* kv_fp8, const float*
   mla_status_t st = run_stage1(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream,
                                plan, kv_indices, kv_indices_len, kv_rows, workspace,
                                workspace_bytes);
+  if (st != MLA_OK) return st;
+  return mla::launch_stage2(stage2_params(qo_indptr, out_bf16, plan, workspace), true, stream) ==
+                 cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+mla_status_t mla_decode_fwd_stall_stream(const void* q_bf16, const void* kv_fp8,
+                                         const float* kv_scale, const int32_t* qo_indptr,
+                                         const int32_t* kv_indptr, void* out_bf16,
+                                         cudaStream_t stream, const mla_plan_t* plan,
+                                         const int32_t* kv_indices, int64_t kv_indices_len,
+                                         int64_t kv_rows, void* workspace, size_t workspace_bytes) {
+  mla_status_t st = run_stage1(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream,
+                               plan, kv_indices, kv_indices_len, kv_rows, workspace,
+                               workspace_bytes, true);
   if (st != MLA_OK) return st;
   return mla::launch_stage2(stage2_params(qo_indptr, out_bf16, plan, workspace), true, stream) ==
                  cudaSuccess

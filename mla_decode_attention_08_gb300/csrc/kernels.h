@@ -34,6 +34,8 @@ struct Stage1Params {
   int32_t batch;
   int32_t grid;
   int32_t qo_len;             // query tokens per row (1 or 2)
+  int32_t stall_stream;       // test hook: the producers issue no cache loads, so the
+                              // pipeline waits run out (bounded) and the call gives up
 };
 
 struct Stage2Params {

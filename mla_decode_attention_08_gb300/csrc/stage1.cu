@@ -403,6 +403,7 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
   if (!kGather && lane != 0) return;
   Cursor cur;
   cursor_start(cur, ms, p.kv_indptr, p.batch);
+  if (p.stall_stream) cur.live = false;  // test hook: nothing is ever loaded
   uint32_t tile = 0;
   uint32_t next_k = 0;  // one past the last panel this warp issued
   bool ok = true;

@@ -1,0 +1,48 @@
+"""The bounded waits, made to run out on the GPU without a fault.
+
+mla_decode_fwd_stall_stream launches the decode with producers that never
+load the cache, so the waits on those loads (a flag nothing sets) reach their
+time limit.  The kernel must report MLA_DERR_TIMEOUT in the workspace error
+word, return, and leave the context usable: the next call on the same
+workspace gives the right answer.  Both the contiguous and the page-table
+kernels, with one and two query tokens, are covered.
+"""
+import time
+
+import pytest
+import torch
+
+from mla_decode_attention_08_gb300 import binding
+from mla_decode_attention_08_gb300.inputs import make_from_lengths
+
+from .gpu_util import DeviceCase, OracleCase, assert_close
+
+pytestmark = pytest.mark.gpu
+
+MLA_DERR_TIMEOUT = 8
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(built_library):
+    binding.load_library(built_library)
+
+
+@pytest.mark.parametrize("paged,qo_len", [(False, 1), (True, 1), (False, 2), (True, 2)])
+def test_stalled_stream_times_out_and_the_context_survives(paged, qo_len):
+    inp = make_from_lengths([700, 300, 2000, 5], seed=31, paged=paged, qo_len=qo_len)
+    dev = DeviceCase(inp)
+    plan = binding.mla_decode_plan(inp.batch, inp.max_kv_len, 6, qo_len=qo_len)
+    ws = binding.new_workspace(plan)
+    t0 = time.time()
+    binding.mla_decode_fwd_stall_stream(dev.q, dev.kv_codes, dev.kv_scale, dev.qo_indptr,
+                                        dev.kv_indptr, dev.out, plan=plan, workspace=ws,
+                                        kv_indices=dev.kv_indices)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    err = binding.mla_decode_read_error(ws)  # reads and clears
+    assert err == MLA_DERR_TIMEOUT, err
+    assert elapsed < 30.0
+    # the same workspace and context, a normal call
+    gpu, err, _, _ = dev.run(plan=plan, workspace=ws)
+    assert err == 0
+    assert_close(gpu, OracleCase(inp).reference())
