@@ -4,20 +4,22 @@
 // range.  Per 128-token tile of the FP8 latent cache:
 //   * warp 4 streams the tile once through TMA into a ring of swizzled panels
 //     (four 128-dim latent panels + one 64-dim rope panel; page-table rows are
-//     fetched with tile::gather4, the panels spread over four producer warps),
-//   * warp 6 issues the tcgen05 MMAs S^T[128 tok x 32] = K_tile . [Q_hi;Q_lo]^T
-//     and warp 5 the MMAs O^T[512 x 32] += V_tile^T . [P_hi;P_lo]^T,
-//     accumulators in TMEM,
+//     fetched with tile::gather4, the panels spread over several producer
+//     warps),
+//   * warp 6 issues the tcgen05 MMAs S^T[128 tok x N] = K_tile . Q_op^T and
+//     warp 5 the MMAs O^T[512 x N] += V_tile^T . P^T, accumulators in TMEM,
 //   * warps 0-3 run the exp2 online softmax on S read from TMEM, write P, and
 //     at the end of a segment write either the bf16 output (row fully inside
 //     this worker) or a normalised partial plus its base-2 log-sum-exp.
-// The same shared-memory tile feeds both products and all 16 heads, which is
-// the pages' multi-head KV reuse (kernelbot-amd-mixed-mla submission 722089,
-// module docstring and `_mla_multihead_stage1`).
+// The same shared-memory tile feeds both products and all 16 heads (of every
+// query token of the row), which is the pages' multi-head KV reuse
+// (kernelbot-amd-mixed-mla submission 722089, module docstring and
+// `_mla_multihead_stage1`).
 //
 // Both operands of each product are FP8 e4m3 (kind::f8f6f4).  Q and P keep
 // bf16-level precision by a two-term split x ~= hi + lo / 16 with both terms
-// e4m3: the 16 "hi" heads and 16 "lo" heads form N = 32.
+// e4m3: per query token the 16 "hi" and 16 "lo" heads, so N = 32 per token of
+// the row (one or two tokens, Geo<kQ>).
 #include <cstddef>
 
 #include <cuda_bf16.h>
@@ -380,15 +382,16 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
   }
 }
 
-// ------------------------------------------------------------ producers (warps 4 and 7)
+// ------------------------------------------------------------ producers (warp 4; page-table mode also 7, 8, 9)
 // Stream each tile once: the rope panel (64 dims) then four latent panels,
 // panel k = 5 * tile + 1 + c in one sequence over the worker's tiles.
 // Contiguous rows: lane 0 of warp 4 alone issues one tiled box per panel.
 // Page table: every lane gathers four rows (tile::gather4) per panel, and the
-// panels go round-robin to four producer warps (panel k to producer k % 4): a
-// warp issues its gathers one lane after another, so more issuing warps raise
-// the rate at which row fetches enter the copy engine (measured pure-load
-// rates 1.78, 3.52 and 4.54 TB/s with one, two and four warps).
+// panels go round-robin to the producer warps (panel k to producer k % n; n = 4
+// with one query token, 2 with two): a warp issues its gathers one lane after
+// another, so more issuing warps raise the rate at which row fetches enter the
+// copy engine (measured pure-load rates 1.78, 3.52 and 4.54 TB/s with one, two
+// and four warps).
 //
 // Every fill of a slot is issued only after the previous fill of that slot has
 // been consumed, so a producer can never be more than one phase ahead on a
@@ -514,7 +517,7 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
   }
 }
 
-// ------------------------------------------------------------ MMA issuer (warp 5, lane 0)
+// ------------------------------------------------------------ MMA issuers (warp 6: QK, warp 5: PV; lane 0)
 // S^T[tile & 1] = K_tile . Q_op^T (Q_op: kN rows, per query token the hi then
 // lo heads): 4 latent panels x 4 k-steps of 32 dims (128-byte swizzle) plus the
 // rope panel's 2 k-steps (64-byte swizzle).
