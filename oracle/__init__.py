@@ -10,8 +10,9 @@ arithmetic.
 Modules
   fp8        e4m3fn decode / encode written from the format's definition.
   quant      per-tensor absmax FP8 quantisation of the bf16 latent cache.
-  attention  exact softmax attention over the dequantised cache (float64),
-             and the split-KV partial / log-sum-exp combine restated.
+  attention  exact softmax attention over the dequantised e4m3 cache or the
+             bf16 cache (float64), and the split-KV partial / log-sum-exp
+             combine restated.
   schedule   the token-balanced split schedule restated with plain loops.
 
 Every function names the page passage it follows.  The pages are the three

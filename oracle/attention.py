@@ -12,7 +12,12 @@ query heads, page size 1, and no logit soft-capping (``logit_cap=0.0``).
 
 Cache rows hold e4m3fn codes with one float32 per-tensor scale; a row's value
 is ``code * scale`` (submission 738050, ``_quantize_fp8`` docstring).  The query
-is the exact bf16 value handed in.
+is the exact bf16 value handed in.  The harness also hands over the bf16 copy
+of the same cache (submission 738050, ``custom_kernel`` docstring), which
+submission 722089 reads, with the unquantised bf16 query, whenever the batch
+holds at most 131072 cached tokens (its AITER PATH section, ``_aiter_path``):
+``mla_decode_ref_bf16kv`` is that variant, the cache rows' values being the
+exact bf16 values.
 
 Readings taken where the pages are silent:
   * a row with no cached tokens (``kv_len == 0``) yields all-zero output;
@@ -80,6 +85,12 @@ def dequant_rows(kv_codes: np.ndarray, kv_scale, slots: np.ndarray) -> np.ndarra
     return e4m3fn_decode(codes[slots]) * float(np.float32(kv_scale))
 
 
+def bf16_rows(kv_bits: np.ndarray, slots: np.ndarray) -> np.ndarray:
+    """float64 values of the selected rows of a bf16 cache given as raw bits, ``[L, 576]``."""
+    bits = np.asarray(kv_bits, dtype=np.uint16).reshape(-1, QK_HEAD_DIM)
+    return bf16_bits_to_f64(bits[slots])
+
+
 def row_attention(q_row: np.ndarray, k_rows: np.ndarray):
     """Softmax weights ``[16, L]`` and output ``[16, 512]`` for one row, float64."""
     z = (q_row @ k_rows.T) * SM_SCALE
@@ -101,13 +112,30 @@ def mla_decode_ref(q, kv_codes, kv_scale, qo_indptr, kv_indptr,
     ``rows`` restricts the work to a subset of batch rows; the other output rows
     are left as NaN.
     """
+    return _decode(q, qo_indptr, kv_indptr, kv_indices, rows,
+                   lambda slots: dequant_rows(kv_codes, kv_scale, slots))
+
+
+def mla_decode_ref_bf16kv(q, kv_bits, qo_indptr, kv_indptr,
+                          kv_indices: Optional[np.ndarray] = None, rows=None) -> np.ndarray:
+    """float64 output ``[T, 16, 512]`` of the decode step over a bf16 cache.
+
+    As ``mla_decode_ref`` with ``kv_bits`` the uint16 bit patterns ``[N, 576]``
+    (or ``[N, 1, 576]``) of the bf16 cache; K and V are their exact values.
+    """
+    return _decode(q, qo_indptr, kv_indptr, kv_indices, rows,
+                   lambda slots: bf16_rows(kv_bits, slots))
+
+
+def _decode(q, qo_indptr, kv_indptr, kv_indices, rows, row_values) -> np.ndarray:
+    """The decode step given ``row_values(slots)``: float64 ``[L, 576]`` cache rows."""
     q = np.asarray(q, dtype=np.float64)
     batch = len(qo_indptr) - 1
     out = np.full((q.shape[0], NUM_HEADS, V_HEAD_DIM), np.nan)
     for b in (range(batch) if rows is None else rows):
         t0, n = _query_rows(b, qo_indptr)
         slots = _row_tokens(b, kv_indptr, kv_indices)
-        k_rows = dequant_rows(kv_codes, kv_scale, slots)
+        k_rows = row_values(slots)
         for i in range(n):
             vis = visible_tokens(slots.size, n, i)
             if vis == 0:

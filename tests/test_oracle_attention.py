@@ -238,3 +238,79 @@ def test_multi_token_split_equals_unsplit():
         segs = token_segments(case[4], grid)
         got = mla_decode_split_ref(*case[:5], segs, kv_indices=case[5])
         np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------------ bf16 cache
+def bf16_value(bits: int) -> float:
+    """A bf16 bit pattern is the upper half of a float32 (decoded through struct)."""
+    import struct
+    return struct.unpack("<f", struct.pack("<I", (int(bits) & 0xFFFF) << 16))[0]
+
+
+def brute_force_bf16(q, kv_bits, qo_indptr, kv_indptr, idx):
+    """The bf16-cache step with scalar loops over positions (multi-token aware)."""
+    out = np.zeros((q.shape[0], 16, 512))
+    for b in range(len(qo_indptr) - 1):
+        n = int(qo_indptr[b + 1] - qo_indptr[b])
+        length = int(kv_indptr[b + 1] - kv_indptr[b])
+        for i in range(n):
+            t = int(qo_indptr[b]) + i
+            slots = []
+            for j in range(length - n + i + 1):
+                g = int(kv_indptr[b]) + j
+                slots.append(int(idx[g]) if idx is not None else g)
+            rows = {s: [bf16_value(v) for v in kv_bits[s]] for s in slots}
+            for h in range(16):
+                weights = [math.exp(sum(q[t, h, d] * rows[s][d] for d in range(576)) / 24.0)
+                           for s in slots]
+                total = sum(weights)
+                for w, s in zip(weights, slots):
+                    out[t, h] += (w / total) * np.array(rows[s][:512])
+    return out
+
+
+def bf16_case(rng, lengths, n=1, paged=False):
+    batch = len(lengths)
+    q = bf16_bits_to_f64(f32_to_bf16_bits(
+        (0.05 * rng.standard_normal((batch * n, 16, 576))).astype(np.float32)))
+    total = int(sum(lengths))
+    kv_bits = f32_to_bf16_bits(rng.standard_normal((total + 3, 576)).astype(np.float32))
+    kv_indptr = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    qo_indptr = (n * np.arange(batch + 1)).astype(np.int32)
+    idx = rng.permutation(total + 3)[:total].astype(np.int32) if paged else None
+    return q, kv_bits, qo_indptr, kv_indptr, idx
+
+
+@pytest.mark.parametrize("lengths,n,paged", [([1, 3, 7], 1, False), ([5, 2], 1, True),
+                                             ([4, 1, 6], 2, True), ([3], 3, False)])
+def test_bf16_cache_brute_force_tiny(lengths, n, paged):
+    from oracle.attention import mla_decode_ref_bf16kv
+    rng = np.random.default_rng(2000 + 11 * n + sum(lengths) + paged)
+    q, kv_bits, qo, kvp, idx = bf16_case(rng, lengths, n, paged)
+    ref = mla_decode_ref_bf16kv(q, kv_bits, qo, kvp, kv_indices=idx)
+    np.testing.assert_allclose(ref, brute_force_bf16(q, kv_bits, qo, kvp, idx), rtol=1e-10, atol=1e-12)
+
+
+def test_bf16_cache_of_fp8_values_equals_the_fp8_step():
+    """A bf16 cache holding exactly the e4m3 values times a power-of-two scale
+    (three mantissa bits fit in bf16's seven) gives the fp8 step bit for bit."""
+    from oracle.attention import mla_decode_ref_bf16kv
+    rng = np.random.default_rng(2100)
+    q, codes, _, qo, kvp, idx = random_case(rng, [40, 0, 3, 129], paged=True)
+    scale = np.float32(2.0 ** -5)
+    vals = e4m3fn_decode(codes) * float(scale)
+    bits = f32_to_bf16_bits(vals.astype(np.float32))
+    assert np.array_equal(bf16_bits_to_f64(bits), vals)
+    a = mla_decode_ref(q, codes, scale, qo, kvp, kv_indices=idx)
+    b = mla_decode_ref_bf16kv(q, bits, qo, kvp, kv_indices=idx)
+    assert np.array_equal(a, b)
+
+
+def test_bf16_cache_one_token_returns_its_v():
+    from oracle.attention import mla_decode_ref_bf16kv
+    rng = np.random.default_rng(2200)
+    q, kv_bits, qo, kvp, idx = bf16_case(rng, [1, 1], paged=True)
+    out = mla_decode_ref_bf16kv(q, kv_bits, qo, kvp, kv_indices=idx)
+    for b in range(2):
+        want = [bf16_value(v) for v in kv_bits[idx[b], :512]]
+        assert np.array_equal(out[b], np.broadcast_to(want, (16, 512)))
