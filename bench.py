@@ -48,11 +48,12 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 
 
-def algorithmic_bytes(inp) -> int:
-    """Bytes one call must move: every cached token's 576-byte row (+4 for its
-    page-table entry), the bf16 query and output rows, and both indptr arrays."""
+def algorithmic_bytes(inp, bf16_cache: bool = False) -> int:
+    """Bytes one call must move: every cached token's row (576 bytes of e4m3
+    codes, or 1152 of bf16; +4 for its page-table entry), the bf16 query and
+    output rows, and both indptr arrays."""
     tokens = int(inp.kv_indptr[-1])
-    per_token = 576 + (4 if inp.kv_indices is not None else 0)
+    per_token = 576 * (2 if bf16_cache else 1) + (4 if inp.kv_indices is not None else 0)
     queries = inp.batch * getattr(inp, "qo_len", 1)
     return tokens * per_token + queries * 16 * (576 + 512) * 2 + 2 * (inp.batch + 1) * 4
 
@@ -167,7 +168,7 @@ class DeviceWorkload:
         self.kv_scale = torch.empty(1, dtype=torch.float32, device=dev)
         binding.mla_fp8_quantize_per_tensor(kv, self.kv, self.kv_scale,
                                             torch.empty(16, dtype=torch.uint8, device=dev))
-        del kv
+        self.kv_bf16 = kv  # the bf16 cache the e4m3 codes came from (the bf16-cache step's input)
         self.qo_indptr = torch.from_numpy(inp.qo_indptr).to(dev)
         self.kv_indptr = torch.from_numpy(inp.kv_indptr).to(dev)
         self.kv_indices = None if inp.kv_indices is None else torch.from_numpy(inp.kv_indices).to(dev)
@@ -175,6 +176,7 @@ class DeviceWorkload:
         self.plan = binding.mla_decode_plan(inp.batch, inp.max_kv_len, sms, qo_len=inp.qo_len)
         self.ws = binding.new_workspace(self.plan)
         self.bytes = algorithmic_bytes(inp)
+        self.bytes_bf16 = algorithmic_bytes(inp, bf16_cache=True)
         self.binding = binding
         torch.cuda.synchronize()
         self.inp.kv_bits = None  # release the host copy of the cache source
@@ -183,6 +185,11 @@ class DeviceWorkload:
         self.binding.mla_decode_fwd(self.q, self.kv, self.kv_scale, self.qo_indptr, self.kv_indptr,
                                     self.out, stream, plan=self.plan, workspace=self.ws,
                                     kv_indices=self.kv_indices)
+
+    def call_bf16kv(self, stream=None):
+        self.binding.mla_decode_fwd_bf16kv(self.q, self.kv_bf16, self.qo_indptr, self.kv_indptr,
+                                           self.out, stream, plan=self.plan, workspace=self.ws,
+                                           kv_indices=self.kv_indices)
 
     def stage1(self, stream=None):
         self.binding.mla_decode_stage1(self.q, self.kv, self.kv_scale, self.qo_indptr,
@@ -202,14 +209,14 @@ def time_loop(torch, fn, steps: int, stream) -> float:
     return start.elapsed_time(end)
 
 
-def per_call_cold(torch, w: DeviceWorkload, reps: int, stream, flush) -> list:
-    """Per-call device times (µs) with L2 flushed before each call."""
+def per_call_cold(torch, call, reps: int, stream, flush) -> list:
+    """Per-call device times (µs) of ``call(stream)`` with L2 flushed before each call."""
     times = []
     for _ in range(reps):
         flush.add_(1)
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
-        w.call(stream)
+        call(stream)
         e.record(stream)
         torch.cuda.synchronize()
         times.append(s.elapsed_time(e) * 1e3)
@@ -443,25 +450,33 @@ def ours_main(args) -> None:
     per_config = []
     if not args.no_per_config and rank == 0:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+        def cold(call, nbytes):
+            for _ in range(5):
+                call(stream)
+            times = per_call_cold(torch, call, args.cold_reps, stream, flush)
+            med = statistics.median(times)
+            return {"us_median": round(med, 2),
+                    "us_p10": round(float(np.percentile(times, 10)), 2),
+                    "us_p90": round(float(np.percentile(times, 90)), 2),
+                    "effective_tbps": round(nbytes / (med * 1e-6) / 1e12, 3),
+                    "frac_of_peak": round(nbytes / (med * 1e-6) / 1e9 / peak, 3),
+                    "algorithmic_bytes": nbytes}
+
         for name in WORKLOADS:
             ww = w if name == args.workload else DeviceWorkload(name, torch, binding, sms)
-            for _ in range(5):
-                ww.call(stream)
-            times = per_call_cold(torch, ww, args.cold_reps, stream, flush)
-            med = statistics.median(times)
-            per_config.append({
-                "workload": name, "us_median": round(med, 2),
-                "us_p10": round(float(np.percentile(times, 10)), 2),
-                "us_p90": round(float(np.percentile(times, 90)), 2),
-                "effective_tbps": round(ww.bytes / (med * 1e-6) / 1e12, 3),
-                "frac_of_peak": round(ww.bytes / (med * 1e-6) / 1e9 / peak, 3),
-                "algorithmic_bytes": ww.bytes, "grid": int(ww.plan.grid),
-                "l2": "flushed before each call"})
+            entry = {"workload": name, **cold(ww.call, ww.bytes), "grid": int(ww.plan.grid),
+                     "l2": "flushed before each call"}
+            # the same step over the bf16 cache (mla_decode_fwd_bf16kv; contiguous caches only)
+            entry["bf16_cache"] = (cold(ww.call_bf16kv, ww.bytes_bf16) if ww.kv_indices is None
+                                   else {"unsupported": "page table (bf16 caches are read contiguously)"})
+            per_config.append(entry)
             if ww is not w:
                 del ww
                 torch.cuda.empty_cache()
         del flush
 
+    w.kv_bf16 = None
+    torch.cuda.empty_cache()
     e2e = e2e_timing(torch, w, args.e2e_steps, stream)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

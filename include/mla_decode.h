@@ -11,7 +11,8 @@
  * cached tokens j of that row.  q has 16 heads of 576 dims (512 latent + 64
  * rope); the one shared KV head stores 576 e4m3fn codes per token with a single
  * float32 scale (value = code * scale); K is all 576 dims of a cache row and V
- * its first 512.  The output is bf16 [T, 16, 512].
+ * its first 512.  The output is bf16 [T, 16, 512].  The *_bf16kv entry points
+ * compute the same step over a bf16 cache (the values themselves, no scale).
  *
  * All pointers named "device" are CUDA device pointers; every buffer is owned
  * and allocated by the caller.  The library never allocates, frees or
@@ -36,7 +37,7 @@ extern "C" {
 #define MLA_QK_HEAD_DIM 576
 #define MLA_V_HEAD_DIM 512
 #define MLA_TILE_TOKENS 128
-#define MLA_ABI_VERSION 3
+#define MLA_ABI_VERSION 4
 
 typedef enum {
   MLA_OK = 0,
@@ -161,13 +162,40 @@ mla_status_t mla_decode_fwd_static_scratch(const void* q_bf16, const void* kv_fp
                                            const int32_t* kv_indices, int64_t kv_indices_len,
                                            int64_t kv_rows);
 
+/*
+ * mla_decode_fwd_bf16kv — the decode step over a bf16 latent cache, as the
+ * pages do for batches of at most 131072 cached tokens (submission 722089,
+ * AITER PATH section: `_aiter_path` passes the bf16 copy of the cache and the
+ * unquantised bf16 query; submission 738050's `custom_kernel` docstring lists
+ * that copy among the harness's inputs).  K and V are the cache's bf16 values;
+ * q . K and P . V run on bf16 tensor-core operands with float32 accumulation
+ * (P rounded to bf16), so each cached token moves 1152 bytes instead of 576.
+ *   kv_bf16  device, bf16 [kv_rows, 576] (= [kv_rows, 1, 576]), 16-byte aligned.
+ *   kv_indices must be NULL (the cache rows of the batch contiguous, as in the
+ *   pages' benchmark); a page table returns MLA_ERR_UNSUPPORTED.
+ *   Every other argument, the plan (either qo_len), the workspace, the error
+ *   word and the status codes are those of mla_decode_fwd; there is no scale.
+ */
+mla_status_t mla_decode_fwd_bf16kv(const void* q_bf16, const void* kv_bf16,
+                                   const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                   void* out_bf16, cudaStream_t stream, const mla_plan_t* plan,
+                                   const int32_t* kv_indices, int64_t kv_indices_len,
+                                   int64_t kv_rows, void* workspace, size_t workspace_bytes);
+
 /* The two stages of mla_decode_fwd launched separately (same arguments); the
- * pair is equivalent to one mla_decode_fwd call.  Used to time stage 1 alone. */
+ * pair is equivalent to one mla_decode_fwd call.  Used to time stage 1 alone.
+ * mla_decode_stage1_bf16kv is stage 1 of mla_decode_fwd_bf16kv; stage 2 is
+ * shared by both caches. */
 mla_status_t mla_decode_stage1(const void* q_bf16, const void* kv_fp8, const float* kv_scale,
                                const int32_t* qo_indptr, const int32_t* kv_indptr, void* out_bf16,
                                cudaStream_t stream, const mla_plan_t* plan,
                                const int32_t* kv_indices, int64_t kv_indices_len, int64_t kv_rows,
                                void* workspace, size_t workspace_bytes);
+mla_status_t mla_decode_stage1_bf16kv(const void* q_bf16, const void* kv_bf16,
+                                      const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                      void* out_bf16, cudaStream_t stream, const mla_plan_t* plan,
+                                      const int32_t* kv_indices, int64_t kv_indices_len,
+                                      int64_t kv_rows, void* workspace, size_t workspace_bytes);
 mla_status_t mla_decode_stage2(const int32_t* qo_indptr, void* out_bf16, cudaStream_t stream,
                                const mla_plan_t* plan, void* workspace, size_t workspace_bytes);
 

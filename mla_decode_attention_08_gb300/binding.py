@@ -40,12 +40,15 @@ class mla_plan_t(ctypes.Structure):
 _VP, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
 _PLANP = ctypes.POINTER(mla_plan_t)
 _FWD_ARGS = [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _PLANP, _VP, _I64, _I64, _VP, _SZ]
+_FWD_BF16KV_ARGS = _FWD_ARGS[:2] + _FWD_ARGS[3:]  # no kv_scale
 SIGNATURES = {
     "mla_decode_plan": (ctypes.c_int, [_I32, _I32, _I32, _PLANP]),
     "mla_decode_plan_mtp": (ctypes.c_int, [_I32, _I32, _I32, _I32, _PLANP]),
     "mla_decode_fwd": (ctypes.c_int, _FWD_ARGS),
     "mla_decode_fwd_stall_stream": (ctypes.c_int, _FWD_ARGS),
     "mla_decode_stage1": (ctypes.c_int, _FWD_ARGS),
+    "mla_decode_fwd_bf16kv": (ctypes.c_int, _FWD_BF16KV_ARGS),
+    "mla_decode_stage1_bf16kv": (ctypes.c_int, _FWD_BF16KV_ARGS),
     "mla_decode_fwd_static_scratch": (ctypes.c_int, _FWD_ARGS[:-2]),
     "mla_decode_stage2": (ctypes.c_int, [_VP, _VP, _VP, _PLANP, _VP, _SZ]),
     "mla_fp8_quantize_per_tensor": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP, _SZ, _VP]),
@@ -120,6 +123,34 @@ def _fwd_args(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream, plan, kv_i
             _dev_ptr(kv_indices, "kv_indices", torch.int32),
             0 if kv_indices is None else int(kv_indices.numel()), kv_rows,
             _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size())
+
+
+def _fwd_bf16kv_args(q, kv_bf16, qo_indptr, kv_indptr, out, stream, plan, kv_indices, workspace):
+    if kv_bf16.dim() == 3:
+        kv_bf16 = kv_bf16.reshape(kv_bf16.shape[0], -1)
+    return (_dev_ptr(q, "q", torch.bfloat16), _dev_ptr(kv_bf16, "kv_bf16", torch.bfloat16),
+            _dev_ptr(qo_indptr, "qo_indptr", torch.int32),
+            _dev_ptr(kv_indptr, "kv_indptr", torch.int32), _dev_ptr(out, "out", torch.bfloat16),
+            _stream(stream), ctypes.byref(plan),
+            _dev_ptr(kv_indices, "kv_indices", torch.int32),
+            0 if kv_indices is None else int(kv_indices.numel()), int(kv_bf16.shape[0]),
+            _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size())
+
+
+def mla_decode_fwd_bf16kv(q, kv_bf16, qo_indptr, kv_indptr, out, stream=None, *, plan,
+                          workspace, kv_indices=None) -> torch.Tensor:
+    """Decode step over a bf16 cache ``[N, 576]`` (no scale); writes and returns ``out``."""
+    _check("mla_decode_fwd_bf16kv", load_library().mla_decode_fwd_bf16kv(
+        *_fwd_bf16kv_args(q, kv_bf16, qo_indptr, kv_indptr, out, stream, plan, kv_indices,
+                          workspace)))
+    return out
+
+
+def mla_decode_stage1_bf16kv(q, kv_bf16, qo_indptr, kv_indptr, out, stream=None, *, plan,
+                             workspace, kv_indices=None) -> None:
+    _check("mla_decode_stage1_bf16kv", load_library().mla_decode_stage1_bf16kv(
+        *_fwd_bf16kv_args(q, kv_bf16, qo_indptr, kv_indptr, out, stream, plan, kv_indices,
+                          workspace)))
 
 
 def mla_decode_fwd(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream=None, *, plan,

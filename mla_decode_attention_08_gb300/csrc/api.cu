@@ -35,13 +35,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Rows of the [kv_rows, 576] uint8 cache: box_w bytes wide, box_h rows high.
-bool encode_kv_map(CUtensorMap* map, const void* kv, int64_t rows, uint32_t box_w, uint32_t box_h,
-                   CUtensorMapSwizzle swizzle) {
+// The cache addressed as bytes: [kv_rows, 576 * elem] uint8 (elem = 1 for
+// e4m3 codes, 2 for bf16, whose boxes are plain copies), box_w bytes wide and
+// box_h rows high.
+bool encode_kv_map(CUtensorMap* map, const void* kv, int64_t rows, bool bf16, uint32_t box_w,
+                   uint32_t box_h, CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kQkDim), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kQkDim)};
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(kQkDim) * (bf16 ? 2 : 1);
+  const cuuint64_t gdim[2] = {row_bytes, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t gstride[1] = {row_bytes};
   const cuuint32_t box[2] = {box_w, box_h};
   const cuuint32_t estride[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), gdim, gstride, box,
@@ -55,16 +58,21 @@ struct MapEntry {
   const void* kv = nullptr;
   int64_t rows = 0;
   bool gather = false;
+  bool bf16 = false;
   int device = -1;
   CUtensorMap v, r;
 };
 
-bool kv_maps(const void* kv, int64_t rows, bool gather, int device, CUtensorMap* v, CUtensorMap* r) {
+// Latent and rope boxes (tiles of 128 rows, or single rows for tile::gather4):
+// e4m3 128 and 64 bytes wide; bf16 128 bytes (64 dims) for both.
+bool kv_maps(const void* kv, int64_t rows, bool gather, bool bf16, int device, CUtensorMap* v,
+             CUtensorMap* r) {
   constexpr int kEntries = 8;
   thread_local MapEntry cache[kEntries];
   thread_local int next = 0;
   for (auto& e : cache) {
-    if (e.kv == kv && e.rows == rows && e.gather == gather && e.device == device) {
+    if (e.kv == kv && e.rows == rows && e.gather == gather && e.bf16 == bf16 &&
+        e.device == device) {
       *v = e.v;
       *r = e.r;
       return true;
@@ -74,10 +82,13 @@ bool kv_maps(const void* kv, int64_t rows, bool gather, int device, CUtensorMap*
   e.kv = kv;
   e.rows = rows;
   e.gather = gather;
+  e.bf16 = bf16;
   e.device = device;
   const uint32_t h = gather ? 1u : static_cast<uint32_t>(kTileTokens);
-  if (!encode_kv_map(&e.v, kv, rows, 128, h, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
-  if (!encode_kv_map(&e.r, kv, rows, 64, h, CU_TENSOR_MAP_SWIZZLE_64B)) return false;
+  if (!encode_kv_map(&e.v, kv, rows, bf16, 128, h, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
+  if (!encode_kv_map(&e.r, kv, rows, bf16, bf16 ? 128 : 64, h,
+                     bf16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+    return false;
   cache[next] = e;
   next = (next + 1) % kEntries;
   *v = e.v;
@@ -137,20 +148,22 @@ mla::Stage2Params stage2_params(const int32_t* qo_indptr, void* out, const mla_p
   return s;
 }
 
+// kv_scale is required for an e4m3 cache and ignored for a bf16 one.
 mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
                         const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
                         cudaStream_t stream, const mla_plan_t* plan, const int32_t* kv_indices,
                         int64_t kv_indices_len, int64_t kv_rows, void* workspace,
-                        size_t workspace_bytes, bool stall_stream = false) {
+                        size_t workspace_bytes, bool bf16_cache, bool stall_stream = false) {
   mla_status_t st = check_plan(plan);
   if (st != MLA_OK) return st;
-  if (q == nullptr || kv == nullptr || kv_scale == nullptr || qo_indptr == nullptr ||
-      kv_indptr == nullptr || out == nullptr)
+  if (q == nullptr || kv == nullptr || (kv_scale == nullptr && !bf16_cache) ||
+      qo_indptr == nullptr || kv_indptr == nullptr || out == nullptr)
     return MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16)) return MLA_ERR_INVALID_ARG;
   if (kv_rows < 1 || kv_rows > INT32_MAX) return MLA_ERR_INVALID_ARG;
   if (kv_indices != nullptr && (kv_indices_len < 0 || kv_indices_len > INT32_MAX))
     return MLA_ERR_INVALID_ARG;
+  if (bf16_cache && kv_indices != nullptr) return MLA_ERR_UNSUPPORTED;
   st = check_workspace(plan, workspace, workspace_bytes);
   if (st != MLA_OK) return st;
   int device = 0;
@@ -159,12 +172,12 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
 
   const bool gather = kv_indices != nullptr;
   CUtensorMap map_v, map_r;
-  if (!kv_maps(kv, kv_rows, gather, device, &map_v, &map_r)) return MLA_ERR_CUDA;
+  if (!kv_maps(kv, kv_rows, gather, bf16_cache, device, &map_v, &map_r)) return MLA_ERR_CUDA;
 
   auto* ws = static_cast<uint8_t*>(workspace);
   mla::Stage1Params p;
   p.q = static_cast<const uint16_t*>(q);
-  p.kv_scale = kv_scale;
+  p.kv_scale = bf16_cache ? nullptr : kv_scale;
   p.qo_indptr = qo_indptr;
   p.kv_indptr = kv_indptr;
   p.kv_indices = kv_indices;
@@ -180,8 +193,17 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
   p.grid = plan->grid;
   p.qo_len = plan->qo_len;
   p.stall_stream = stall_stream ? 1 : 0;
-  return mla::launch_stage1(p, map_v, map_r, gather, stream) == cudaSuccess ? MLA_OK
-                                                                           : MLA_ERR_CUDA;
+  return mla::launch_stage1(p, map_v, map_r, gather, bf16_cache, stream) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+mla_status_t run_stage2(const int32_t* qo_indptr, void* out, cudaStream_t stream,
+                        const mla_plan_t* plan, void* workspace, bool programmatic) {
+  return mla::launch_stage2(stage2_params(qo_indptr, out, plan, workspace), programmatic,
+                            stream) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 }  // namespace
@@ -247,7 +269,16 @@ mla_status_t mla_decode_stage1(const void* q_bf16, const void* kv_fp8, const flo
                                const int32_t* kv_indices, int64_t kv_indices_len, int64_t kv_rows,
                                void* workspace, size_t workspace_bytes) {
   return run_stage1(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream, plan,
-                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes);
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, false);
+}
+
+mla_status_t mla_decode_stage1_bf16kv(const void* q_bf16, const void* kv_bf16,
+                                      const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                      void* out_bf16, cudaStream_t stream, const mla_plan_t* plan,
+                                      const int32_t* kv_indices, int64_t kv_indices_len,
+                                      int64_t kv_rows, void* workspace, size_t workspace_bytes) {
+  return run_stage1(q_bf16, kv_bf16, nullptr, qo_indptr, kv_indptr, out_bf16, stream, plan,
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, true);
 }
 
 mla_status_t mla_decode_stage2(const int32_t* qo_indptr, void* out_bf16, cudaStream_t stream,
@@ -258,10 +289,7 @@ mla_status_t mla_decode_stage2(const int32_t* qo_indptr, void* out_bf16, cudaStr
     return MLA_ERR_INVALID_ARG;
   st = check_workspace(plan, workspace, workspace_bytes);
   if (st != MLA_OK) return st;
-  return mla::launch_stage2(stage2_params(qo_indptr, out_bf16, plan, workspace), false, stream) ==
-                 cudaSuccess
-             ? MLA_OK
-             : MLA_ERR_CUDA;
+  return run_stage2(qo_indptr, out_bf16, stream, plan, workspace, false);
 }
 
 mla_status_t mla_decode_fwd(const void* q_bf16, const void* kv_fp8, const float* kv_scale,
@@ -271,12 +299,21 @@ mla_status_t mla_decode_fwd(const void* q_bf16, const void* kv_fp8, const float*
                             void* workspace, size_t workspace_bytes) {
   mla_status_t st = run_stage1(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream,
                                plan, kv_indices, kv_indices_len, kv_rows, workspace,
-                               workspace_bytes);
+                               workspace_bytes, false);
   if (st != MLA_OK) return st;
-  return mla::launch_stage2(stage2_params(qo_indptr, out_bf16, plan, workspace), true, stream) ==
-                 cudaSuccess
-             ? MLA_OK
-             : MLA_ERR_CUDA;
+  return run_stage2(qo_indptr, out_bf16, stream, plan, workspace, true);
+}
+
+mla_status_t mla_decode_fwd_bf16kv(const void* q_bf16, const void* kv_bf16,
+                                   const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                   void* out_bf16, cudaStream_t stream, const mla_plan_t* plan,
+                                   const int32_t* kv_indices, int64_t kv_indices_len,
+                                   int64_t kv_rows, void* workspace, size_t workspace_bytes) {
+  mla_status_t st = run_stage1(q_bf16, kv_bf16, nullptr, qo_indptr, kv_indptr, out_bf16, stream,
+                               plan, kv_indices, kv_indices_len, kv_rows, workspace,
+                               workspace_bytes, true);
+  if (st != MLA_OK) return st;
+  return run_stage2(qo_indptr, out_bf16, stream, plan, workspace, true);
 }
 
 mla_status_t mla_decode_fwd_stall_stream(const void* q_bf16, const void* kv_fp8,
@@ -287,12 +324,9 @@ mla_status_t mla_decode_fwd_stall_stream(const void* q_bf16, const void* kv_fp8,
                                          int64_t kv_rows, void* workspace, size_t workspace_bytes) {
   mla_status_t st = run_stage1(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream,
                                plan, kv_indices, kv_indices_len, kv_rows, workspace,
-                               workspace_bytes, true);
+                               workspace_bytes, false, true);
   if (st != MLA_OK) return st;
-  return mla::launch_stage2(stage2_params(qo_indptr, out_bf16, plan, workspace), true, stream) ==
-                 cudaSuccess
-             ? MLA_OK
-             : MLA_ERR_CUDA;
+  return run_stage2(qo_indptr, out_bf16, stream, plan, workspace, true);
 }
 
 mla_status_t mla_fp8_quantize_per_tensor(const void* src_bf16, int64_t n, void* dst_fp8,

@@ -6,10 +6,9 @@
 
 namespace mla {
 
-// Stage 1 ring / layout constants.
-constexpr int kNumRSlots = 2;       // 8 KB slots: tokens x 64 rope dims (swizzle 64B)
-constexpr int kVPanelBytes = 128 * 128;  // latent ring slot: 128 tokens x 128 dims (swizzle 128B)
-constexpr int kRPanelBytes = 128 * 64;
+// Stage 1 ring: two rope slots (128 tokens x 64 dims); the latent slots and
+// every size depend on the cache format (stage1.cu, Geo).
+constexpr int kNumRSlots = 2;
 // warps 0-3 softmax/epilogue, 4 TMA producer, 5 PV MMA issuer, 6 QK MMA issuer;
 // page-table mode adds TMA producers in warps 7, 8 and 9 (12 warps, registers
 // rebalanced with setmaxnreg).
@@ -19,7 +18,7 @@ constexpr long long kWaitLimitCycles = 2000000000LL;  // ~1 s per pipeline wait 
 
 struct Stage1Params {
   const uint16_t* q;          // bf16 bits [B, 16, 576]
-  const float* kv_scale;      // [1]
+  const float* kv_scale;      // [1] (e4m3 cache; unused for a bf16 cache)
   const int32_t* qo_indptr;   // [B+1]
   const int32_t* kv_indptr;   // [B+1]
   const int32_t* kv_indices;  // [kv_indices_len] or null
@@ -54,8 +53,11 @@ struct Stage2Params {
 
 size_t stage1_smem_bytes();
 cudaError_t stage1_prepare(int device);  // sets the dynamic shared memory limit once
+// map_v / map_r: the cache's latent and rope boxes (e4m3: 128- and 64-byte
+// wide; bf16: both 64 dims); bf16_cache selects the bf16-cache kernels.
 cudaError_t launch_stage1(const Stage1Params& p, const CUtensorMap& map_v,
-                          const CUtensorMap& map_r, bool gather, cudaStream_t stream);
+                          const CUtensorMap& map_r, bool gather, bool bf16_cache,
+                          cudaStream_t stream);
 cudaError_t launch_stage2(const Stage2Params& p, bool programmatic, cudaStream_t stream);
 cudaError_t launch_fp8_quantize(const uint16_t* src, int64_t n, uint8_t* dst, float* scale_out,
                                 uint32_t* amax_bits, cudaStream_t stream);

@@ -16,10 +16,14 @@
 // (kernelbot-amd-mixed-mla submission 722089, module docstring and
 // `_mla_multihead_stage1`).
 //
-// Both operands of each product are FP8 e4m3 (kind::f8f6f4).  Q and P keep
+// Two cache formats (Kv).  An e4m3 cache (codes with one per-tensor scale):
+// both operands of each product are FP8 e4m3 (kind::f8f6f4), and Q and P keep
 // bf16-level precision by a two-term split x ~= hi + lo / 16 with both terms
 // e4m3: per query token the 16 "hi" and 16 "lo" heads, so N = 32 per token of
-// the row (one or two tokens, Geo<kQ>).
+// the row.  A bf16 cache (the pages' choice for small batches, submission
+// 722089 `_aiter_path`): bf16 Q and P operands (kind::f16), N = 16 per token,
+// and every tile moves twice the bytes.  One or two query tokens per row
+// (Geo<kQ, kFmt>).
 #include <cstddef>
 
 #include <cuda_bf16.h>
@@ -38,36 +42,59 @@ namespace {
 constexpr uint32_t kLayoutSw128 = 2, kLayoutSw64 = 4, kLayoutSw32 = 6;
 
 constexpr int kMaxQ = 2;          // query tokens per row handled by one CTA tile
-constexpr int kMaxVSlots = 11;    // latent ring slots (kQ = 1)
+constexpr int kMaxVSlots = 11;    // latent ring slots (e4m3, kQ = 1)
 
-// Everything that depends on the number kQ of query tokens per row.  The MMA
-// N dimension holds, for each query token, the 16 "hi" then the 16 "lo" heads:
-// column n = 32 qi + 16 lo + head.
-template <int kQ>
+// Latent cache formats.
+enum class Kv { kE4m3, kBf16 };
+
+// Everything that depends on the cache format and on the number kQ of query
+// tokens per row.  The MMA N dimension holds, for each query token, the 16
+// "hi" then the 16 "lo" heads (e4m3: column n = 32 qi + 16 lo + head) or the 16
+// heads (bf16: column n = 16 qi + head).
+template <int kQ, Kv kFmt>
 struct Geo {
   static_assert(kQ == 1 || kQ == 2, "one or two query tokens per row");
-  static constexpr int kN = 32 * kQ;               // MMA N / operand rows of Q and P
-  static constexpr int kNumV = kQ == 1 ? 11 : 9;   // latent ring slots (16 KB each)
-  static constexpr int kQPanelBytes = kN * 128;    // Q: kN rows x 128 dims (swizzle 128B)
-  static constexpr int kQRopeBytes = kN * 64;      // Q: kN rows x 64 rope dims (swizzle 64B)
-  static constexpr int kPBytes = 128 * kN;         // P: 128 tokens x kN columns
-  static constexpr uint32_t kPLayout = kQ == 1 ? kLayoutSw32 : kLayoutSw64;  // one atom = one P row
+  static constexpr bool kSplit = kFmt == Kv::kE4m3;  // two-term Q and P operands
+  static constexpr int kElem = kSplit ? 1 : 2;         // bytes per cache / operand element
+  static constexpr int kTokCols = kSplit ? 32 : 16;    // operand columns per query token
+  static constexpr int kN = kTokCols * kQ;             // MMA N / operand rows of Q and P
+  // Ring slots: a latent slot holds 128 tokens x 128 dims (16 or 32 KB), a rope
+  // slot 128 tokens x 64 dims.  A 128-byte-wide swizzled panel holds 128 e4m3 or
+  // 64 bf16 dims, so a bf16 latent slot is two panels 16 KB apart.
+  static constexpr int kVSlotBytes = 128 * 128 * kElem;
+  static constexpr int kRSlotBytes = 128 * 64 * kElem;
+  static constexpr int kNumV = kSplit ? (kQ == 1 ? 11 : 9) : (kQ == 1 ? 5 : 4);
+  static constexpr int kPanelDims = 128 / kElem;
+  // Q operand: kN rows; the 512 latent dims in 128-byte-wide panels, the 64
+  // rope dims in one more (64 bytes wide, swizzle 64B, for e4m3; 128 for bf16).
+  static constexpr int kQPanelBytes = kN * 128;
+  static constexpr int kQLatentPanels = 512 / kPanelDims;
+  static constexpr int kQRopeBytes = kN * 64 * kElem;
+  static constexpr int kRopeWidth = 64 * kElem;        // bytes per row of a rope panel
+  static constexpr uint32_t kRopeLayout = kSplit ? kLayoutSw64 : kLayoutSw128;
+  static constexpr int kPRowBytes = kN * kElem;        // P: one row per token (32 kQ bytes)
+  static constexpr int kPBytes = 128 * kPRowBytes;
+  static constexpr uint32_t kPLayout = kPRowBytes == 32 ? kLayoutSw32 : kLayoutSw64;  // one atom = one P row
 
   static constexpr int kOffV = 0;
-  static constexpr int kOffR = kOffV + kNumV * kVPanelBytes;
-  static constexpr int kOffQ = kOffR + kNumRSlots * kRPanelBytes;
-  static constexpr int kOffQRope = kOffQ + 4 * kQPanelBytes;
+  static constexpr int kOffR = kOffV + kNumV * kVSlotBytes;
+  static constexpr int kOffQ = kOffR + kNumRSlots * kRSlotBytes;
+  static constexpr int kOffQRope = kOffQ + kQLatentPanels * kQPanelBytes;
   static constexpr int kOffP = kOffQRope + kQRopeBytes;
   static constexpr int kOffMisc = kOffP + 2 * kPBytes;
+  static_assert(kOffP - kOffQ >= kQ * kNumHeads * kVDim * 2, "the Q region stages a bf16 output row");
 
   // TMEM columns: two S buffers (kN each) then O (4 chunks x kN).
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColO = 2 * kN;
-  static constexpr uint32_t kTmemCols = kQ == 1 ? 256 : 512;
+  static constexpr uint32_t kTmemCols = 6 * kN <= 128 ? 128 : (6 * kN <= 256 ? 256 : 512);
   static_assert(kColO + 4 * kN <= kTmemCols, "TMEM columns");
 
-  static constexpr uint32_t kIdescQK = idesc_e4m3(128, kN, false, false);  // K-major A and B
-  static constexpr uint32_t kIdescPV = idesc_e4m3(128, kN, true, true);    // MN-major A and B
+  // K-major A and B for QK; MN-major A and B for PV.
+  static constexpr uint32_t kIdescQK = kSplit ? idesc_e4m3(128, kN, false, false)
+                                              : idesc_bf16(128, kN, false, false);
+  static constexpr uint32_t kIdescPV = kSplit ? idesc_e4m3(128, kN, true, true)
+                                              : idesc_bf16(128, kN, true, true);
 
   // 8 KB staging buffers of the epilogue: the Q operand region (4 kQ panels of
   // 4 KB) then the two P buffers.
@@ -109,16 +136,19 @@ static_assert(offsetof(Misc, red_max) % 16 == 0 && offsetof(Misc, red_sum) % 16 
               "vector accesses to the reduction scratch need 16-byte alignment");
 static_assert(kNumRSlots == 2, "rope slots are released through s_full, which has two phases in flight");
 
-template <int kQ>
+template <int kQ, Kv kFmt>
 constexpr int smem_alloc() {
   // + 1024: room to align the base to 1024 B
-  return Geo<kQ>::kOffMisc + static_cast<int>(sizeof(Misc)) + 1024;
+  return Geo<kQ, kFmt>::kOffMisc + static_cast<int>(sizeof(Misc)) + 1024;
 }
-static_assert(Geo<1>::kOffMisc % 16 == 0 && Geo<2>::kOffMisc % 16 == 0,
-              "the barrier block must start 16-byte aligned");
-static_assert(smem_alloc<1>() <= 232448 && smem_alloc<2>() <= 232448,
-              "stage-1 shared memory exceeds the per-CTA limit");
-static_assert(Geo<1>::kNumV <= kMaxVSlots && Geo<2>::kNumV <= kMaxVSlots, "ring slots");
+template <int kQ, Kv kFmt>
+constexpr bool geo_fits() {
+  using G = Geo<kQ, kFmt>;
+  return G::kOffMisc % 16 == 0 && smem_alloc<kQ, kFmt>() <= 232448 && G::kNumV <= kMaxVSlots;
+}
+static_assert(geo_fits<1, Kv::kE4m3>() && geo_fits<2, Kv::kE4m3>() && geo_fits<1, Kv::kBf16>() &&
+                  geo_fits<2, Kv::kBf16>(),
+              "stage-1 shared memory: per-CTA limit, 16-byte aligned barrier block, ring slots");
 
 constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4;
@@ -383,8 +413,9 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
 }
 
 // ------------------------------------------------------------ producers (warp 4; page-table mode also 7, 8, 9)
-// Stream each tile once: the rope panel (64 dims) then four latent panels,
-// panel k = 5 * tile + 1 + c in one sequence over the worker's tiles.
+// Stream each tile once: the rope slot (64 dims) then four latent slots (128
+// dims each), slot fill k = 5 * tile + 1 + c in one sequence over the worker's
+// tiles (called "panels" below; a bf16 latent slot takes two boxes of 64 dims).
 // Contiguous rows: lane 0 of warp 4 alone issues one tiled box per panel.
 // Page table: every lane gathers four rows (tile::gather4) per panel, and the
 // panels go round-robin to the producer warps (panel k to producer k % n; n = 4
@@ -397,10 +428,11 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
 // been consumed, so a producer can never be more than one phase ahead on a
 // barrier: its own previous panel already waited for the consumption that the
 // phase before would need.
-template <bool kGather, int kQ>
+template <bool kGather, int kQ, Kv kFmt>
 __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
                              const CUtensorMap* map_r, Misc* ms, uint32_t sbase, uint32_t who) {
-  using G = Geo<kQ>;
+  using G = Geo<kQ, kFmt>;
+  static_assert(!kGather || G::kSplit, "a bf16 cache is read through tiled boxes only");
   constexpr uint32_t kProducers = num_producers<kGather, kQ>();
   const int lane = threadIdx.x & 31;
   if (!kGather && lane != 0) return;
@@ -437,27 +469,28 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
       if (c < 0) {
         slot = tile % kNumRSlots;
         use = tile / kNumRSlots;
-        bytes = kRPanelBytes;
-        dst = sbase + G::kOffR + slot * kRPanelBytes;
+        bytes = G::kRSlotBytes;
+        dst = sbase + G::kOffR + slot * G::kRSlotBytes;
         full = smem_u32(&ms->r_full[slot]);
         // With two rope slots and two S buffers, rope slot (tile & 1) is free
         // exactly when the QK of the tile before last has completed, which is
         // the phase of s_full[tile & 1] for that tile.
         empty = smem_u32(&ms->s_full[slot]);
-        x = kVDim;
+        x = kVDim * G::kElem;
         map = map_r;
       } else {
         const uint32_t g = tile * 4 + c;
         slot = g % G::kNumV;
         use = g / G::kNumV;
-        bytes = kVPanelBytes;
-        dst = sbase + G::kOffV + slot * kVPanelBytes;
+        bytes = G::kVSlotBytes;
+        dst = sbase + G::kOffV + slot * G::kVSlotBytes;
         full = smem_u32(&ms->v_full[slot]);
         empty = smem_u32(&ms->v_empty[slot]);
-        x = 128 * c;
+        x = 128 * c * G::kElem;
         map = map_v;
       }
-      if (kGather) {
+      // The maps address the cache as bytes, so x is a byte offset into the row.
+      if (kGather) {  // e4m3 only: one 128- or 64-byte-wide panel per slot
         int w = 1;
         if (lane == 0 && use > 0) w = wait_phase(empty, (use - 1) & 1, ms, p.err);
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
@@ -467,10 +500,14 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
         tma_gather4(dst + lane * 4 * (bytes / kTileTokens), map, x, rows[0], rows[1], rows[2],
                     rows[3], full);
       } else {
+        // Boxes of one 128-byte-wide panel each: the whole slot for e4m3; for
+        // bf16 64 dims, two per latent slot, 16 KB apart.
+        const int boxes = G::kSplit || c < 0 ? 1 : 2;
         if (use > 0) ok = wait_phase(empty, (use - 1) & 1, ms, p.err);
         if (!ok) break;
         mbar_arrive_expect_tx(full, bytes);
-        tma_load_2d(dst, map, x, tok0, full);
+        for (int i = 0; i < boxes; ++i)
+          tma_load_2d(dst + i * kTileTokens * 128, map, x + 128 * i, tok0, full);
       }
       next_k = k + 1;
     }
@@ -518,52 +555,73 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
 }
 
 // ------------------------------------------------------------ MMA issuers (warp 6: QK, warp 5: PV; lane 0)
+template <Kv kFmt>
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                     uint32_t accumulate) {
+  if constexpr (kFmt == Kv::kE4m3)
+    umma_f8(d, a, b, idesc, accumulate);
+  else
+    umma_f16(d, a, b, idesc, accumulate);
+}
+
 // S^T[tile & 1] = K_tile . Q_op^T (Q_op: kN rows, per query token the hi then
-// lo heads): 4 latent panels x 4 k-steps of 32 dims (128-byte swizzle) plus the
-// rope panel's 2 k-steps (64-byte swizzle).
-template <int kQ>
+// lo heads, or the heads): k-steps of 32 bytes (32 e4m3 or 16 bf16 dims) over
+// the latent panels (128-byte swizzle) and the rope panel (64-byte swizzle for
+// e4m3, 128-byte for bf16).
+template <int kQ, Kv kFmt>
 __device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t sbase, uint32_t tile) {
-  using G = Geo<kQ>;
+  using G = Geo<kQ, kFmt>;
   const uint32_t d = tmem + G::kColS + G::kN * (tile & 1);
   const uint32_t qb = sbase + G::kOffQ;
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
     const uint32_t g = tile * 4 + p;
-    const uint32_t vs = sbase + G::kOffV + (g % G::kNumV) * kVPanelBytes;
+    const uint32_t vs = sbase + G::kOffV + (g % G::kNumV) * G::kVSlotBytes;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      umma_f8(d, smem_desc(vs + 32 * kk, 1024, 1024, kLayoutSw128),
-              smem_desc(qb + p * G::kQPanelBytes + 32 * kk, 1024, 1024, kLayoutSw128), G::kIdescQK,
-              (p | kk) != 0);
+    for (int h = 0; h < G::kElem; ++h) {  // 128-byte-wide panels of the slot
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        umma<kFmt>(d, smem_desc(vs + h * kTileTokens * 128 + 32 * kk, 1024, 1024, kLayoutSw128),
+                   smem_desc(qb + (p * G::kElem + h) * G::kQPanelBytes + 32 * kk, 1024, 1024,
+                             kLayoutSw128),
+                   G::kIdescQK, (p | h | kk) != 0);
+      }
     }
   }
-  const uint32_t rs = sbase + G::kOffR + (tile % kNumRSlots) * kRPanelBytes;
+  const uint32_t rs = sbase + G::kOffR + (tile % kNumRSlots) * G::kRSlotBytes;
+  constexpr uint32_t kRopeSbo = 8 * G::kRopeWidth;
 #pragma unroll
-  for (int kk = 0; kk < 2; ++kk) {
-    umma_f8(d, smem_desc(rs + 32 * kk, 512, 512, kLayoutSw64),
-            smem_desc(sbase + G::kOffQRope + 32 * kk, 512, 512, kLayoutSw64), G::kIdescQK, 1);
+  for (int kk = 0; kk < G::kRopeWidth / 32; ++kk) {
+    umma<kFmt>(d, smem_desc(rs + 32 * kk, kRopeSbo, kRopeSbo, G::kRopeLayout),
+               smem_desc(sbase + G::kOffQRope + 32 * kk, kRopeSbo, kRopeSbo, G::kRopeLayout),
+               G::kIdescQK, 1);
   }
 }
 
-// O^T[chunk c] (+)= V_c^T . P^T over the tile's 128 tokens: V panel c read
-// MN-major (dims contiguous), P read MN-major (a token's kN operand columns
-// contiguous, one swizzle atom: 32 or 64 bytes).  Each latent panel is
-// released as soon as its four MMAs complete.
-template <int kQ>
+// O^T[chunk c] (+)= V_c^T . P^T over the tile's 128 tokens: latent slot c read
+// MN-major (dims contiguous; M = 128 dims is one 128-byte atom of e4m3, or the
+// slot's two bf16 panels, 16 KB apart), P read MN-major (a token's P row
+// contiguous, one swizzle atom: 32 or 64 bytes), k-steps of 32 e4m3 or 16 bf16
+// tokens.  Each latent slot is released as soon as its MMAs complete.
+template <int kQ, Kv kFmt>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, uint32_t tile, bool first,
                                          Misc* ms) {
-  using G = Geo<kQ>;
+  using G = Geo<kQ, kFmt>;
+  constexpr int kStepTokens = 32 / G::kElem;
+  constexpr uint32_t kLbo = G::kSplit ? 1024 : kTileTokens * 128;
   const uint32_t pb = sbase + G::kOffP + (tile & 1) * G::kPBytes;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint32_t g = tile * 4 + c;
     const uint32_t slot = g % G::kNumV;
-    const uint32_t vs = sbase + G::kOffV + slot * kVPanelBytes;
+    const uint32_t vs = sbase + G::kOffV + slot * G::kVSlotBytes;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      umma_f8(tmem + G::kColO + G::kN * c, smem_desc(vs + kk * 4096, 1024, 1024, kLayoutSw128),
-              smem_desc(pb + kk * 32 * G::kN, 8 * G::kN, 8 * G::kN, G::kPLayout), G::kIdescPV,
-              !(first && kk == 0));
+    for (int kk = 0; kk < kTileTokens / kStepTokens; ++kk) {
+      umma<kFmt>(tmem + G::kColO + G::kN * c,
+                 smem_desc(vs + kk * kStepTokens * 128, kLbo, 1024, kLayoutSw128),
+                 smem_desc(pb + kk * kStepTokens * G::kPRowBytes, 8 * G::kPRowBytes,
+                           8 * G::kPRowBytes, G::kPLayout),
+                 G::kIdescPV, !(first && kk == 0));
     }
     umma_commit(smem_u32(&ms->v_empty[slot]));
   }
@@ -601,9 +659,9 @@ __device__ __forceinline__ bool spin_counter(const uint32_t* ctr, uint32_t targe
 // QK issuer (warp 6, lane 0): QK of tile i needs its five panels landed (it
 // waits on the TMA barriers itself), the segment's Q operand (first tile of a
 // segment) and S[i & 1] read out by the softmax of tile i - 2.
-template <int kQ>
+template <int kQ, Kv kFmt>
 __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
-  using G = Geo<kQ>;
+  using G = Geo<kQ, kFmt>;
   Cursor qc;
   cursor_start(qc, ms, p.kv_indptr, p.batch);
   uint32_t qk_n = 0;  // tiles whose QK has been issued
@@ -619,7 +677,7 @@ __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
     if (!ok) break;
     fence_acquire_cta();
     tc_fence_after();
-    issue_qk<kQ>(tmem, sbase, qk_n);
+    issue_qk<kQ, kFmt>(tmem, sbase, qk_n);
     umma_commit(smem_u32(&ms->s_full[qk_n & 1]));  // also frees rope slot qk_n & 1
     if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
     ++qk_n;
@@ -632,7 +690,7 @@ __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
 // PV issuer (warp 5, lane 0): PV of tile i needs P[i & 1] published and, on
 // the first tile of a later segment, O read out by the previous segment's
 // epilogue.
-template <int kQ>
+template <int kQ, Kv kFmt>
 __device__ void run_mma_pv(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
   Cursor pc;
   cursor_start(pc, ms, p.kv_indptr, p.batch);
@@ -644,7 +702,7 @@ __device__ void run_mma_pv(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
     if (!ok) break;
     fence_acquire_cta();
     tc_fence_after();
-    issue_pv<kQ>(tmem, sbase, pv_n, first, ms);
+    issue_pv<kQ, kFmt>(tmem, sbase, pv_n, first, ms);
     umma_commit(smem_u32(&ms->pv_done[pv_n & 1]));
     ++pv_n;
     cursor_next_tile(pc, ms, p.kv_indptr, p.batch);
@@ -679,11 +737,12 @@ __device__ __forceinline__ float warp_transpose_sum16(float (&v)[16]) {
 }
 
 // Byte address of 16-byte chunk `ch` of operand row `row` in the Q operand:
-// latent dims in four 128-byte-swizzled panels, rope dims in one 64-byte panel.
-template <int kQ>
+// latent dims in 128-byte-swizzled panels, rope dims in one more panel (64-byte
+// swizzle for e4m3; for bf16 it is the ninth 128-byte panel).
+template <int kQ, Kv kFmt>
 __device__ __forceinline__ uint32_t q_chunk_addr(uint32_t sq, int row, int ch) {
-  using G = Geo<kQ>;
-  if (ch < 32) {
+  using G = Geo<kQ, kFmt>;
+  if (!G::kSplit || ch < 32) {
     const int panel = ch >> 3, cc = ch & 7;
     return sq + panel * G::kQPanelBytes + row * 128 + ((cc ^ (row & 7)) << 4);
   }
@@ -724,36 +783,37 @@ __device__ __forceinline__ void split_e4m3_16(const float (&x)[16], uint32_t (&h
   }
 }
 
-// Loads the row's query tokens tq .. tq + kQ - 1 (16 heads x 576 bf16 each),
-// scales each by a power of two so its largest magnitude lands in (224, 448],
-// and writes the hi / lo e4m3 operand rows of token qi (rows 32 qi + head for
-// hi, 32 qi + 16 + head for lo).  Sets qk_scale[qi], the factor turning the QK
-// accumulator of token qi into base-2 softmax exponent units.  tq < 0 writes a
-// zero query.
+// Q operand rows of a bf16 cache: the bf16 values themselves, row 16 qi + head.
 template <int kQ>
-__device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq,
-                          float kv_scale, float (&qk_scale)[kQ]) {
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  uint4 raw[kQ][5][2];
+__device__ __forceinline__ void store_q_bf16(uint32_t sq, const uint4 (&raw)[kQ][5][2],
+                                             float (&qk_scale)[kQ]) {
+  const int t = threadIdx.x;
+  named_bar_sync(kBarSoftmax, kSoftmaxThreads);
 #pragma unroll
   for (int qi = 0; qi < kQ; ++qi) {
+    qk_scale[qi] = kSmScaleLog2;
 #pragma unroll
     for (int r = 0; r < 5; ++r) {
       const int job = t + 128 * r;
-      raw[qi][r][0] = raw[qi][r][1] = make_uint4(0, 0, 0, 0);
-      if (job < 576 && tq >= 0) {
-        const int head = job / 36, ch = job % 36;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            p.q + (static_cast<size_t>(tq + qi) * kNumHeads + head) * kQkDim + ch * 16);
-        raw[qi][r][0] = __ldg(src);
-        raw[qi][r][1] = __ldg(src + 1);
+      if (job < 576) {
+        const int head = job / 36, ch = job % 36;  // ch: 16 dims = two 16-byte chunks
+        const uint4 a = raw[qi][r][0], b = raw[qi][r][1];
+        st_shared_v4(q_chunk_addr<kQ, Kv::kBf16>(sq, 16 * qi + head, 2 * ch), a.x, a.y, a.z, a.w);
+        st_shared_v4(q_chunk_addr<kQ, Kv::kBf16>(sq, 16 * qi + head, 2 * ch + 1), b.x, b.y, b.z, b.w);
       }
     }
   }
-  // The previous segment's output may still be leaving the Q and P regions
-  // through bulk stores (the loads above are already in flight); the barrier
-  // below orders every write to them after this wait.
-  if (t == 0) bulk_wait_read<0>();
+  fence_proxy_async_smem();
+  named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+}
+
+// Q operand rows of an e4m3 cache: each query token scaled by a power of two so
+// its largest magnitude lands in (224, 448], then split into hi / lo e4m3 rows
+// (32 qi + head for hi, 32 qi + 16 + head for lo).
+template <int kQ>
+__device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 (&raw)[kQ][5][2],
+                                             float kv_scale, float (&qk_scale)[kQ]) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
 #pragma unroll
   for (int qi = 0; qi < kQ; ++qi) {
     uint32_t amax = 0;
@@ -802,13 +862,47 @@ __device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t 
         unpack(raw[qi][r][1].z, 6); unpack(raw[qi][r][1].w, 7);
         uint32_t hi[4], lo[4];
         split_e4m3_16(x, hi, lo);
-        st_shared_v4(q_chunk_addr<kQ>(sq, 32 * qi + head, ch), hi[0], hi[1], hi[2], hi[3]);
-        st_shared_v4(q_chunk_addr<kQ>(sq, 32 * qi + 16 + head, ch), lo[0], lo[1], lo[2], lo[3]);
+        st_shared_v4(q_chunk_addr<kQ, Kv::kE4m3>(sq, 32 * qi + head, ch), hi[0], hi[1], hi[2], hi[3]);
+        st_shared_v4(q_chunk_addr<kQ, Kv::kE4m3>(sq, 32 * qi + 16 + head, ch), lo[0], lo[1], lo[2], lo[3]);
       }
     }
   }
   fence_proxy_async_smem();
   named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+}
+
+// Loads the row's query tokens tq .. tq + kQ - 1 (16 heads x 576 bf16 each)
+// and writes the Q operand of the cache format.  Sets qk_scale[qi], the factor
+// turning the QK accumulator of token qi into base-2 softmax exponent units.
+// tq < 0 writes a zero query.
+template <int kQ, Kv kFmt>
+__device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq,
+                          float kv_scale, float (&qk_scale)[kQ]) {
+  const int t = threadIdx.x;
+  uint4 raw[kQ][5][2];
+#pragma unroll
+  for (int qi = 0; qi < kQ; ++qi) {
+#pragma unroll
+    for (int r = 0; r < 5; ++r) {
+      const int job = t + 128 * r;
+      raw[qi][r][0] = raw[qi][r][1] = make_uint4(0, 0, 0, 0);
+      if (job < 576 && tq >= 0) {
+        const int head = job / 36, ch = job % 36;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + (static_cast<size_t>(tq + qi) * kNumHeads + head) * kQkDim + ch * 16);
+        raw[qi][r][0] = __ldg(src);
+        raw[qi][r][1] = __ldg(src + 1);
+      }
+    }
+  }
+  // The previous segment's output may still be leaving the Q and P regions
+  // through bulk stores (the loads above are already in flight); the barrier
+  // below orders every write to them after this wait.
+  if (t == 0) bulk_wait_read<0>();
+  if constexpr (kFmt == Kv::kBf16)
+    store_q_bf16<kQ>(sq, raw, qk_scale);
+  else
+    store_q_e4m3<kQ>(ms, sq, raw, kv_scale, qk_scale);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -849,12 +943,37 @@ __device__ __forceinline__ void split_p_16(const float (&x)[16], uint32_t (&hi)[
   }
 }
 
+// The 16 heads' accumulator values of query token qi in TMEM columns `col`
+// onward: e4m3 operands give hi and lo columns, combined as hi + lo / 16; bf16
+// operands one column per head.
+template <Kv kFmt>
+__device__ __forceinline__ void tmem_ld_heads(uint32_t addr, float (&v)[16]) {
+  if constexpr (kFmt == Kv::kE4m3) {
+    uint32_t r[32];
+    tmem_ld32(addr, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int h = 0; h < 16; ++h) v[h] = fmaf(u2f(r[16 + h]), 0.0625f, u2f(r[h]));
+  } else {
+    uint32_t r[16];
+    tmem_ld16(addr, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int h = 0; h < 16; ++h) v[h] = u2f(r[h]);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 // kInlineWaits: the waits' slow paths inlined (required where setmaxnreg raised
 // the register count: a call out of such a region does not compile).
-template <int kQ, bool kInlineWaits>
+template <int kQ, Kv kFmt, bool kInlineWaits>
 __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem,
                             float kv_scale) {
-  using G = Geo<kQ>;
+  using G = Geo<kQ, kFmt>;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;  // TMEM lane quarter
   const int token = warp * 32 + lane;  // S row (token) / O row (dim within a chunk) of this thread
@@ -883,7 +1002,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     if (!row_ok && t == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
     if (cur.seg > 0) softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
     float qk_scale[kQ];
-    prepare_q<kQ>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, kv_scale, qk_scale);
+    prepare_q<kQ, kFmt>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, kv_scale, qk_scale);
     if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 1));
 
     float m_ref[kQ][16], l[kQ][16];
@@ -910,15 +1029,28 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       bool exceed = false;
 #pragma unroll
       for (int qi = 0; qi < kQ; ++qi) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + G::kColS + G::kN * sb + 32 * qi, r);
-        tmem_wait_ld();
+        const uint32_t addr = tmem + lane_base + G::kColS + G::kN * sb + G::kTokCols * qi;
         tok_ok[qi] = pos < cur.len - kQ + 1 + qi;
-        const float sc = qk_scale[qi], sc_lo = sc * 0.0625f;
+        const float sc = qk_scale[qi];
+        if constexpr (G::kSplit) {
+          uint32_t r[32];
+          tmem_ld32(addr, r);
+          tmem_wait_ld();
+          const float sc_lo = sc * 0.0625f;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          s[qi][h] = tok_ok[qi] ? fmaf(u2f(r[16 + h]), sc_lo, u2f(r[h]) * sc) : -INFINITY;
-          exceed |= s[qi][h] > m_ref[qi][h] + kRescaleThreshold;
+          for (int h = 0; h < 16; ++h) {
+            s[qi][h] = tok_ok[qi] ? fmaf(u2f(r[16 + h]), sc_lo, u2f(r[h]) * sc) : -INFINITY;
+            exceed |= s[qi][h] > m_ref[qi][h] + kRescaleThreshold;
+          }
+        } else {
+          uint32_t r[16];
+          tmem_ld16(addr, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            s[qi][h] = tok_ok[qi] ? u2f(r[h]) * sc : -INFINITY;
+            exceed |= s[qi][h] > m_ref[qi][h] + kRescaleThreshold;
+          }
         }
       }
       tc_fence_before();
@@ -981,6 +1113,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       }
       const bool rescale_o = moved && tile != seg_first_tile;
 
+      // P row chunks of query token qi: e4m3 hi then lo (16 bytes each), or the
+      // bf16 values of heads 0-7 then 8-15.
       uint32_t phi[kQ][4], plo[kQ][4];
 #pragma unroll
       for (int qi = 0; qi < kQ; ++qi) {
@@ -990,15 +1124,23 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
           pr[h] = tok_ok[qi] ? fast_exp2(s[qi][h] - m_ref[qi][h]) : 0.0f;
           l[qi][h] += pr[h];
         }
-        split_p_16(pr, phi[qi], plo[qi]);
+        if constexpr (G::kSplit) {
+          split_p_16(pr, phi[qi], plo[qi]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            phi[qi][k] = pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
+            plo[qi][k] = pack_bf16x2(pr[8 + 2 * k], pr[9 + 2 * k]);
+          }
+        }
       }
 
       // P[sb] was last read by the PV of tile - 2.
       if (tile >= 2) wait_pv(tile - 2);
       {
-        // One P row per token: kN bytes, 16-byte chunks (hi then lo of each
-        // query token) swizzled as the 32- or 64-byte atom requires.
-        const uint32_t pa = sbase + G::kOffP + sb * G::kPBytes + token * G::kN;
+        // One P row per token: 32 kQ bytes, two 16-byte chunks per query token
+        // swizzled as the 32- or 64-byte atom requires.
+        const uint32_t pa = sbase + G::kOffP + sb * G::kPBytes + token * G::kPRowBytes;
         const uint32_t sw = kQ == 1 ? (token >> 2) & 1 : (token >> 1) & 3;
 #pragma unroll
         for (int qi = 0; qi < kQ; ++qi) {
@@ -1015,13 +1157,22 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll
           for (int qi = 0; qi < kQ; ++qi) {
-            uint32_t o[32];
-            const uint32_t addr = tmem + lane_base + G::kColO + G::kN * cc + 32 * qi;
-            tmem_ld32(addr, o);
-            tmem_wait_ld();
+            const uint32_t addr = tmem + lane_base + G::kColO + G::kN * cc + G::kTokCols * qi;
+            if constexpr (G::kSplit) {
+              uint32_t o[32];
+              tmem_ld32(addr, o);
+              tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(u2f(o[j]) * alpha[qi][j & 15]);
-            tmem_st32(addr, o);
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(u2f(o[j]) * alpha[qi][j & 15]);
+              tmem_st32(addr, o);
+            } else {
+              uint32_t o[16];
+              tmem_ld16(addr, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(u2f(o[j]) * alpha[qi][j]);
+              tmem_st16(addr, o);
+            }
           }
         }
         tmem_wait_st();
@@ -1084,15 +1235,13 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll
         for (int qi = 0; qi < kQ; ++qi) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_base + G::kColO + G::kN * cc + 32 * qi, o);
-          tmem_wait_ld();
+          float o[16];
+          tmem_ld_heads<kFmt>(tmem + lane_base + G::kColO + G::kN * cc + G::kTokCols * qi, o);
           const int dim = 128 * cc + token;
           if (write) {
 #pragma unroll
             for (int h = 0; h < 16; ++h)
-              st_shared_u16(stage_q + ((16 * qi + h) * kVDim + dim) * 2,
-                            bf16_bits((u2f(o[h]) + u2f(o[16 + h]) * 0.0625f) * inv[qi][h]));
+              st_shared_u16(stage_q + ((16 * qi + h) * kVDim + dim) * 2, bf16_bits(o[h] * inv[qi][h]));
           }
         }
       }
@@ -1113,9 +1262,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
 #pragma unroll 1
       for (int k = 0; k < 4 * kQ; ++k) {
         const int qi = k >> 2, cc = k & 3;
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_base + G::kColO + G::kN * cc + 32 * qi, o);
-        tmem_wait_ld();
+        float o[16];
+        tmem_ld_heads<kFmt>(tmem + lane_base + G::kColO + G::kN * cc + G::kTokCols * qi, o);
         const uint32_t buf = G::stage_buf(sbase, k % G::kNumStage);
         if (k >= G::kNumStage) {  // reuses the buffer of chunk k - kNumStage
           if (t == 0) bulk_wait_read<G::kNumStage - 1>();
@@ -1124,7 +1272,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         if (write) {
           float v[16];
 #pragma unroll
-          for (int h = 0; h < 16; ++h) v[h] = (u2f(o[h]) + u2f(o[16 + h]) * 0.0625f) * inv[qi][h];
+          for (int h = 0; h < 16; ++h) v[h] = o[h] * inv[qi][h];
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             st_shared_v4(buf + (j * 128 + token) * 16, __float_as_uint(v[4 * j]),
@@ -1165,11 +1313,11 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
 }
 
 // ------------------------------------------------------------ kernel
-template <bool kGather, int kQ>
+template <bool kGather, int kQ, Kv kFmt>
 __global__ void __launch_bounds__((stage1_threads<kGather, kQ>()), 1)
     mla_decode_stage1_kernel(const __grid_constant__ CUtensorMap map_v,
                              const __grid_constant__ CUtensorMap map_r, const Stage1Params p) {
-  using G = Geo<kQ>;
+  using G = Geo<kQ, kFmt>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -1216,17 +1364,18 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ>()), 1)
   constexpr bool kWide = wide_gather<kGather, kQ>();
   if (warp < 4) {
     if constexpr (kWide) setmaxnreg_inc<kSoftmaxRegs>();
-    run_softmax<kQ, kWide || kQ == 2>(p, ms, sbase, tmem, __ldg(p.kv_scale));
+    run_softmax<kQ, kFmt, kWide || kQ == 2>(p, ms, sbase, tmem,
+                                            G::kSplit ? __ldg(p.kv_scale) : 1.0f);
   } else {
     if constexpr (kWide) setmaxnreg_dec<kOtherRegs>();
     const int who = kGather ? gather_producer_of_warp(warp, num_producers<kGather, kQ>())
                             : (warp == kProducerWarp ? 0 : -1);
     if (who >= 0) {
-      run_producer<kGather, kQ>(p, &map_v, &map_r, ms, sbase, static_cast<uint32_t>(who));
+      run_producer<kGather, kQ, kFmt>(p, &map_v, &map_r, ms, sbase, static_cast<uint32_t>(who));
     } else if (warp == kMmaWarp && lane == 0) {
-      run_mma_pv<kQ>(p, ms, sbase, tmem);
+      run_mma_pv<kQ, kFmt>(p, ms, sbase, tmem);
     } else if (warp == kMmaQkWarp && lane == 0) {
-      run_mma_qk<kQ>(p, ms, sbase, tmem);
+      run_mma_qk<kQ, kFmt>(p, ms, sbase, tmem);
     }
   }
   __syncwarp();
@@ -1240,13 +1389,23 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ>()), 1)
   }
 }
 
-template <bool kGather, int kQ>
+template <bool kGather, int kQ, Kv kFmt>
 cudaError_t set_smem_limit() {
-  return cudaFuncSetAttribute(mla_decode_stage1_kernel<kGather, kQ>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem_alloc<kQ>());
+  return cudaFuncSetAttribute(mla_decode_stage1_kernel<kGather, kQ, kFmt>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem_alloc<kQ, kFmt>());
 }
 
-template <bool kGather, int kQ>
+cudaError_t set_smem_limits() {
+  cudaError_t e = set_smem_limit<false, 1, Kv::kE4m3>();
+  if (e == cudaSuccess) e = set_smem_limit<true, 1, Kv::kE4m3>();
+  if (e == cudaSuccess) e = set_smem_limit<false, 2, Kv::kE4m3>();
+  if (e == cudaSuccess) e = set_smem_limit<true, 2, Kv::kE4m3>();
+  if (e == cudaSuccess) e = set_smem_limit<false, 1, Kv::kBf16>();
+  if (e == cudaSuccess) e = set_smem_limit<false, 2, Kv::kBf16>();
+  return e;
+}
+
+template <bool kGather, int kQ, Kv kFmt>
 cudaError_t launch(const Stage1Params& p, const CUtensorMap& map_v, const CUtensorMap& map_r,
                    cudaStream_t stream) {
   // A programmatic dependent of the previous kernel in the stream: its CTAs
@@ -1255,36 +1414,45 @@ cudaError_t launch(const Stage1Params& p, const CUtensorMap& map_v, const CUtens
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
   cfg.blockDim = dim3(stage1_threads<kGather, kQ>());
-  cfg.dynamicSmemBytes = smem_alloc<kQ>();
+  cfg.dynamicSmemBytes = smem_alloc<kQ, kFmt>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_decode_stage1_kernel<kGather, kQ>, map_v, map_r, p);
+  return cudaLaunchKernelEx(&cfg, mla_decode_stage1_kernel<kGather, kQ, kFmt>, map_v, map_r, p);
 }
+
+
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 }  // namespace
 
 size_t stage1_smem_bytes() {
-  return static_cast<size_t>(smem_alloc<1>() > smem_alloc<2>() ? smem_alloc<1>() : smem_alloc<2>());
+  return static_cast<size_t>(cmax(cmax(smem_alloc<1, Kv::kE4m3>(), smem_alloc<2, Kv::kE4m3>()),
+                                  cmax(smem_alloc<1, Kv::kBf16>(), smem_alloc<2, Kv::kBf16>())));
 }
 
 cudaError_t stage1_prepare(int device) {
   (void)device;
-  cudaError_t e = set_smem_limit<false, 1>();
-  if (e == cudaSuccess) e = set_smem_limit<true, 1>();
-  if (e == cudaSuccess) e = set_smem_limit<false, 2>();
-  if (e == cudaSuccess) e = set_smem_limit<true, 2>();
-  return e;
+  return set_smem_limits();
 }
 
 cudaError_t launch_stage1(const Stage1Params& p, const CUtensorMap& map_v,
-                          const CUtensorMap& map_r, bool gather, cudaStream_t stream) {
-  if (p.qo_len == 2)
-    return gather ? launch<true, 2>(p, map_v, map_r, stream) : launch<false, 2>(p, map_v, map_r, stream);
-  return gather ? launch<true, 1>(p, map_v, map_r, stream) : launch<false, 1>(p, map_v, map_r, stream);
+                          const CUtensorMap& map_r, bool gather, bool bf16_cache,
+                          cudaStream_t stream) {
+  const bool two = p.qo_len == 2;
+  if (bf16_cache) {
+    if (gather) return cudaErrorNotSupported;  // the host rejects this before launching
+    return two ? launch<false, 2, Kv::kBf16>(p, map_v, map_r, stream)
+               : launch<false, 1, Kv::kBf16>(p, map_v, map_r, stream);
+  }
+  if (two)
+    return gather ? launch<true, 2, Kv::kE4m3>(p, map_v, map_r, stream)
+                  : launch<false, 2, Kv::kE4m3>(p, map_v, map_r, stream);
+  return gather ? launch<true, 1, Kv::kE4m3>(p, map_v, map_r, stream)
+                : launch<false, 1, Kv::kE4m3>(p, map_v, map_r, stream);
 }
 
 }  // namespace mla

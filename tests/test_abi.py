@@ -34,7 +34,7 @@ def test_every_declared_function_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.mla_decode_abi_version() == 3
+    assert lib.mla_decode_abi_version() == 4
     for s in range(5):
         assert lib.mla_status_string(s)
 
@@ -99,6 +99,16 @@ def test_host_side_argument_errors(lib):
     assert lib.mla_decode_plan(0, 10, 152, ctypes.byref(binding.mla_plan_t())) == 1
     assert lib.mla_decode_plan(3, -1, 152, ctypes.byref(binding.mla_plan_t())) == 1
     assert lib.mla_decode_schedule_host(None, 3, 3, None, None) == 1
+    # the bf16-cache entry points take no scale and check the same arguments
+    assert lib.mla_decode_fwd_bf16kv(fake, fake, fake, fake, fake, None, p, None, 0, 4096,
+                                     fake, plan.ws_bytes - 1) == 3
+    assert lib.mla_decode_fwd_bf16kv(fake, None, fake, fake, fake, None, p, None, 0, 4096,
+                                     fake, plan.ws_bytes) == 1
+    assert lib.mla_decode_stage1_bf16kv(fake, fake, fake, fake, ctypes.c_void_p((1 << 20) + 8),
+                                        None, p, None, 0, 4096, fake, plan.ws_bytes) == 1
+    # a bf16 cache is read contiguously: a page table is unsupported
+    assert lib.mla_decode_fwd_bf16kv(fake, fake, fake, fake, fake, None, p, fake, 4096, 4096,
+                                     fake, plan.ws_bytes) == 2
 
 
 def test_binding_refuses_cpu_tensors(lib):
