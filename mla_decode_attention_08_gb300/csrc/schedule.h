@@ -33,13 +33,29 @@ MLA_HD int32_t plan_grid(int32_t batch, int32_t max_kv_len, int32_t num_sms) {
   return g < 1 ? 1 : static_cast<int32_t>(g);
 }
 
+// floor(c * total / grid) for 0 <= c <= grid and total >= 0, without a 64-bit
+// division (a slow call on the GPU): with total = q * grid + r it is
+// c * q + floor(c * r / grid), and c * r < grid^2 fits 32 bits whenever
+// grid < 65536.
 MLA_HD int32_t worker_begin(int32_t c, int32_t total, int32_t grid) {
-  return static_cast<int32_t>((static_cast<int64_t>(c) * total) / grid);
+  const uint32_t g = static_cast<uint32_t>(grid);
+  const uint32_t q = static_cast<uint32_t>(total) / g, r = static_cast<uint32_t>(total) % g;
+  const uint64_t cr = static_cast<uint64_t>(c) * r;
+  const uint32_t extra = cr <= 0xFFFFFFFFull ? static_cast<uint32_t>(cr) / g
+                                             : static_cast<uint32_t>(cr / g);
+  return static_cast<int32_t>(static_cast<uint32_t>(c) * q + extra);
 }
 
-// Worker holding global tile t (0 <= t < total).
+// Worker holding global tile t (0 <= t < total): the largest c with
+// worker_begin(c) <= t, i.e. floor(((t + 1) * grid - 1) / total).  A float
+// estimate is stepped to the exact answer with worker_begin.
 MLA_HD int32_t worker_of_tile(int32_t t, int32_t total, int32_t grid) {
-  return static_cast<int32_t>(((static_cast<int64_t>(t) + 1) * grid - 1) / total);
+  int32_t c = static_cast<int32_t>(static_cast<float>(t) * static_cast<float>(grid) /
+                                   static_cast<float>(total));
+  c = c < 0 ? 0 : (c > grid - 1 ? grid - 1 : c);
+  while (c > 0 && worker_begin(c, total, grid) > t) --c;
+  while (c + 1 < grid && worker_begin(c + 1, total, grid) <= t) ++c;
+  return c;
 }
 
 // Workspace slot of worker c's partial for a split row whose tiles start at

@@ -565,36 +565,40 @@ __device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_
 }
 
 // S^T[tile & 1] = K_tile . Q_op^T (Q_op: kN rows, per query token the hi then
-// lo heads, or the heads): k-steps of 32 bytes (32 e4m3 or 16 bf16 dims) over
-// the latent panels (128-byte swizzle) and the rope panel (64-byte swizzle for
-// e4m3, 128-byte for bf16).
+// lo heads, or the heads), issued slot by slot as the slots land: first the
+// rope slot (64-byte swizzle for e4m3, 128-byte for bf16; it starts the sum),
+// then latent slot p (128-byte-swizzled panels), in k-steps of 32 bytes
+// (32 e4m3 or 16 bf16 dims).
 template <int kQ, Kv kFmt>
-__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t sbase, uint32_t tile) {
+__device__ __forceinline__ void issue_qk_rope(uint32_t tmem, uint32_t sbase, uint32_t tile) {
   using G = Geo<kQ, kFmt>;
   const uint32_t d = tmem + G::kColS + G::kN * (tile & 1);
-  const uint32_t qb = sbase + G::kOffQ;
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const uint32_t g = tile * 4 + p;
-    const uint32_t vs = sbase + G::kOffV + (g % G::kNumV) * G::kVSlotBytes;
-#pragma unroll
-    for (int h = 0; h < G::kElem; ++h) {  // 128-byte-wide panels of the slot
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        umma<kFmt>(d, smem_desc(vs + h * kTileTokens * 128 + 32 * kk, 1024, 1024, kLayoutSw128),
-                   smem_desc(qb + (p * G::kElem + h) * G::kQPanelBytes + 32 * kk, 1024, 1024,
-                             kLayoutSw128),
-                   G::kIdescQK, (p | h | kk) != 0);
-      }
-    }
-  }
   const uint32_t rs = sbase + G::kOffR + (tile % kNumRSlots) * G::kRSlotBytes;
   constexpr uint32_t kRopeSbo = 8 * G::kRopeWidth;
 #pragma unroll
   for (int kk = 0; kk < G::kRopeWidth / 32; ++kk) {
     umma<kFmt>(d, smem_desc(rs + 32 * kk, kRopeSbo, kRopeSbo, G::kRopeLayout),
                smem_desc(sbase + G::kOffQRope + 32 * kk, kRopeSbo, kRopeSbo, G::kRopeLayout),
-               G::kIdescQK, 1);
+               G::kIdescQK, kk != 0);
+  }
+}
+
+template <int kQ, Kv kFmt>
+__device__ __forceinline__ void issue_qk_latent(uint32_t tmem, uint32_t sbase, uint32_t tile,
+                                                int p) {
+  using G = Geo<kQ, kFmt>;
+  const uint32_t d = tmem + G::kColS + G::kN * (tile & 1);
+  const uint32_t qb = sbase + G::kOffQ;
+  const uint32_t vs = sbase + G::kOffV + ((tile * 4 + p) % G::kNumV) * G::kVSlotBytes;
+#pragma unroll
+  for (int h = 0; h < G::kElem; ++h) {  // 128-byte-wide panels of the slot
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      umma<kFmt>(d, smem_desc(vs + h * kTileTokens * 128 + 32 * kk, 1024, 1024, kLayoutSw128),
+                 smem_desc(qb + (p * G::kElem + h) * G::kQPanelBytes + 32 * kk, 1024, 1024,
+                           kLayoutSw128),
+                 G::kIdescQK, 1);
+    }
   }
 }
 
@@ -656,9 +660,11 @@ __device__ __forceinline__ bool spin_counter(const uint32_t* ctr, uint32_t targe
 // product's issue waits behind the other's (issuing one product blocks the
 // issuing thread for about its execution time, ~1200 cycles).
 //
-// QK issuer (warp 6, lane 0): QK of tile i needs its five panels landed (it
-// waits on the TMA barriers itself), the segment's Q operand (first tile of a
-// segment) and S[i & 1] read out by the softmax of tile i - 2.
+// QK issuer (warp 6, lane 0): QK of tile i needs the segment's Q operand
+// (first tile of a segment) and S[i & 1] read out by the softmax of tile i - 2;
+// then each of its five slots is multiplied as soon as its copy has landed (the
+// issuer waits on the TMA barriers itself), so that the products overlap the
+// copies still in flight.
 template <int kQ, Kv kFmt>
 __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
   using G = Geo<kQ, kFmt>;
@@ -666,18 +672,23 @@ __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
   cursor_start(qc, ms, p.kv_indptr, p.batch);
   uint32_t qk_n = 0;  // tiles whose QK has been issued
   while (qc.live) {
-    bool ok = wait_phase(smem_u32(&ms->r_full[qk_n % kNumRSlots]), (qk_n / kNumRSlots) & 1, ms,
-                         p.err);
+    bool ok = true;
+    if (qc.j == qc.j0) ok = spin_counter(&ms->q_ready, static_cast<uint32_t>(qc.seg) + 1, ms, p.err);
+    if (ok && qk_n >= 2) ok = spin_counter(&ms->s_read, qk_n - 1, ms, p.err);
+    if (ok) fence_acquire_cta();
+    if (ok) ok = wait_phase(smem_u32(&ms->r_full[qk_n % kNumRSlots]), (qk_n / kNumRSlots) & 1, ms,
+                            p.err);
+    if (!ok) break;
+    tc_fence_after();
+    issue_qk_rope<kQ, kFmt>(tmem, sbase, qk_n);
     for (int c = 0; c < 4 && ok; ++c) {
       const uint32_t g = qk_n * 4 + c;
       ok = wait_phase(smem_u32(&ms->v_full[g % G::kNumV]), (g / G::kNumV) & 1, ms, p.err);
+      if (!ok) break;
+      tc_fence_after();
+      issue_qk_latent<kQ, kFmt>(tmem, sbase, qk_n, c);
     }
-    if (ok && qc.j == qc.j0) ok = spin_counter(&ms->q_ready, static_cast<uint32_t>(qc.seg) + 1, ms, p.err);
-    if (ok && qk_n >= 2) ok = spin_counter(&ms->s_read, qk_n - 1, ms, p.err);
     if (!ok) break;
-    fence_acquire_cta();
-    tc_fence_after();
-    issue_qk<kQ, kFmt>(tmem, sbase, qk_n);
     umma_commit(smem_u32(&ms->s_full[qk_n & 1]));  // also frees rope slot qk_n & 1
     if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
     ++qk_n;
@@ -1280,11 +1291,13 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
                          __float_as_uint(v[4 * j + 3]));
           if (k == 4 * kQ - 1 && t < 16 * kQ) {
             // thread t stages the LSE of (token t / 16, head t % 16); -inf when it saw nothing
-            float x = m_ref[0][0] + log2f(l_tot[0][0]);
+            float mm = m_ref[0][0], ll = l_tot[0][0];
 #pragma unroll
-            for (int e = 1; e < 16 * kQ; ++e)
-              x = t == e ? m_ref[e >> 4][e & 15] + log2f(l_tot[e >> 4][e & 15]) : x;
-            ms->lse_stage[t] = x;
+            for (int e = 1; e < 16 * kQ; ++e) {
+              mm = t == e ? m_ref[e >> 4][e & 15] : mm;
+              ll = t == e ? l_tot[e >> 4][e & 15] : ll;
+            }
+            ms->lse_stage[t] = mm + log2f(ll);
           }
         }
         fence_proxy_async_smem();
