@@ -128,7 +128,7 @@ struct Misc {
   int32_t t0, t1;
   int32_t first_row, first_prefix, first_tiles, last_row;
   int32_t bad;
-  uint32_t next_panel[4];  // per producer warp: one past its last issued panel
+  uint32_t next_panel[6];  // per producer warp: one past its last issued panel
   alignas(16) float lse_stage[16 * kMaxQ];  // a split piece's base-2 LSE on its way out (bulk store)
 };
 
@@ -156,9 +156,10 @@ constexpr int kMmaWarp = 5;    // PV issuer; owns the TMEM allocation
 constexpr int kMmaQkWarp = 6;  // QK issuer
 constexpr uint32_t kBarSoftmax = 1;  // named barrier id of warps 0-3
 constexpr uint32_t kBarProducers = 2;  // named barrier id of the page-table producers
-// Page-table mode with one query token: 12 warps, four producer warps (4, 7,
-// 8, 9) taking panels round-robin; the softmax warpgroup gets 240 registers and
-// the other two 128 (launched with 168 each: 128 x 240 + 256 x 128 <= 384 x 168).
+// Page-table mode with one query token: 12 warps, six producer warps (4, 7,
+// 8, 9, 10, 11) taking panels round-robin; the softmax warpgroup gets 240
+// registers and the other two 128 (launched with 168 each: 128 x 240 + 256 x 128
+// <= 384 x 168).
 // With two query tokens the softmax needs more than 240 registers, so that
 // kernel keeps 8 warps and two producers (warps 4 and 7).
 template <bool kGather, int kQ>
@@ -166,8 +167,8 @@ __host__ __device__ constexpr bool wide_gather() { return kGather && kQ == 1; }
 template <bool kGather, int kQ>
 __host__ __device__ constexpr int stage1_threads() { return wide_gather<kGather, kQ>() ? kStage1ThreadsGather : kStage1Threads; }
 template <bool kGather, int kQ>
-__host__ __device__ constexpr uint32_t num_producers() { return !kGather ? 1 : (kQ == 1 ? 4 : 2); }
-// Producer index of a warp in page-table mode (warps 4, 7, 8, 9), or -1.
+__host__ __device__ constexpr uint32_t num_producers() { return !kGather ? 1 : (kQ == 1 ? 6 : 2); }
+// Producer index of a warp in page-table mode (warps 4, 7, 8, ...), or -1.
 __device__ __forceinline__ int gather_producer_of_warp(int warp, uint32_t producers) {
   const int who = warp == 4 ? 0 : (warp >= 7 ? warp - 6 : -1);
   return who < static_cast<int>(producers) ? who : -1;
@@ -412,28 +413,29 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
   }
 }
 
-// ------------------------------------------------------------ producers (warp 4; page-table mode also 7, 8, 9)
+// ------------------------------------------------------------ producers (warp 4; page-table mode also 7-11)
 // Stream each tile once: the rope slot (64 dims) then four latent slots (128
 // dims each), slot fill k = 5 * tile + 1 + c in one sequence over the worker's
 // tiles (called "panels" below; a bf16 latent slot takes two boxes of 64 dims).
 // Contiguous rows: lane 0 of warp 4 alone issues one tiled box per panel.
 // Page table: every lane gathers four rows (tile::gather4) per panel, and the
-// panels go round-robin to the producer warps (panel k to producer k % n; n = 4
+// panels go round-robin to the producer warps (panel k to producer k % n; n = 6
 // with one query token, 2 with two): a warp issues its gathers one lane after
 // another, so more issuing warps raise the rate at which row fetches enter the
-// copy engine (measured pure-load rates 1.78, 3.52 and 4.54 TB/s with one, two
-// and four warps).
+// copy engine (measured pure-load rates 1.79, 3.53, 4.51, 4.93 and 5.02 TB/s
+// with one, two, four, six and eight warps).
 //
 // Every fill of a slot is issued only after the previous fill of that slot has
 // been consumed, so a producer can never be more than one phase ahead on a
-// barrier: its own previous panel already waited for the consumption that the
-// phase before would need.
+// barrier: of its two previous panels at least one is a latent slot, and the
+// consumption that panel waited for lies at most two ring laps back.
 template <bool kGather, int kQ, Kv kFmt>
 __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
                              const CUtensorMap* map_r, Misc* ms, uint32_t sbase, uint32_t who) {
   using G = Geo<kQ, kFmt>;
   static_assert(!kGather || G::kSplit, "a bf16 cache is read through tiled boxes only");
   constexpr uint32_t kProducers = num_producers<kGather, kQ>();
+  static_assert(kProducers <= sizeof(Misc::next_panel) / sizeof(uint32_t), "producer slots");
   const int lane = threadIdx.x & 31;
   if (!kGather && lane != 0) return;
   Cursor cur;
