@@ -77,8 +77,8 @@ typedef struct {
                                * worker boundary is t0: (output row or -1, first
                                * worker, last worker, first worker's partial slot) */
   uint64_t ws_lse_offset;     /* float[2*grid*qo_len*16] base-2 log-sum-exp of partials */
-  uint64_t ws_partial_offset; /* float[2*grid*qo_len*16*512] normalised split partials,
-                               * stored [slot][token][dim/128][head/4][dim%128][head%4] */
+  uint64_t ws_partial_offset; /* bf16[2*grid*qo_len*16*512] normalised split partials,
+                               * stored [slot][token][dim/128][head/8][dim%128][head%8] */
 } mla_plan_t;
 
 /*

@@ -253,8 +253,8 @@ def workspace_views(plan: mla_plan_t, ws: torch.Tensor) -> dict:
             "workers": view(plan.ws_workers_offset, 8 * g, torch.int32).view(g, 8)[:, :4],
             "jobs": view(plan.ws_workers_offset, 8 * g, torch.int32).view(g, 8)[:, 4:],
             "lse": view(plan.ws_lse_offset, 2 * g * nq * 16, torch.float32).view(2 * g, nq, 16),
-            # stored [slot][token][dim / 128][head / 4][dim % 128][head % 4];
+            # bf16, stored [slot][token][dim / 128][head / 8][dim % 128][head % 8];
             # viewed as [slot][token][head][dim]
-            "partial": view(plan.ws_partial_offset, 2 * g * nq * 16 * 512, torch.float32)
-                       .view(2 * g, nq, 4, 4, 128, 4).permute(0, 1, 3, 5, 2, 4)
+            "partial": view(plan.ws_partial_offset, 2 * g * nq * 16 * 512, torch.bfloat16)
+                       .view(2 * g, nq, 4, 2, 128, 8).permute(0, 1, 3, 5, 2, 4)
                        .reshape(2 * g, nq, 16, 512)}

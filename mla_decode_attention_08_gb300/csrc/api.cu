@@ -141,7 +141,7 @@ mla::Stage2Params stage2_params(const int32_t* qo_indptr, void* out, const mla_p
   s.prefix = reinterpret_cast<const int32_t*>(ws + plan->ws_prefix_offset);
   s.workers = reinterpret_cast<const int32_t*>(ws + plan->ws_workers_offset);
   s.lse = reinterpret_cast<const float*>(ws + plan->ws_lse_offset);
-  s.partial = reinterpret_cast<const float*>(ws + plan->ws_partial_offset);
+  s.partial = reinterpret_cast<const uint16_t*>(ws + plan->ws_partial_offset);
   s.batch = plan->batch;
   s.grid = plan->grid;
   s.qo_len = plan->qo_len;
@@ -186,7 +186,7 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
   p.prefix = reinterpret_cast<int32_t*>(ws + plan->ws_prefix_offset);
   p.workers = reinterpret_cast<int32_t*>(ws + plan->ws_workers_offset);
   p.lse = reinterpret_cast<float*>(ws + plan->ws_lse_offset);
-  p.partial = reinterpret_cast<float*>(ws + plan->ws_partial_offset);
+  p.partial = reinterpret_cast<uint16_t*>(ws + plan->ws_partial_offset);
   p.kv_rows = kv_rows;
   p.kv_indices_len = gather ? kv_indices_len : 0;
   p.batch = plan->batch;
@@ -257,7 +257,7 @@ mla_status_t mla_decode_plan_mtp(int32_t batch, int32_t qo_len, int32_t max_kv_l
   p.ws_lse_offset = off;
   off += round_up(2 * g * nq * kNumHeads * sizeof(float));
   p.ws_partial_offset = off;
-  off += round_up(2 * g * nq * kNumHeads * kVDim * sizeof(float));
+  off += round_up(2 * g * nq * kNumHeads * kVDim * sizeof(uint16_t));
   p.ws_bytes = off;
   *plan = p;
   return MLA_OK;

@@ -27,7 +27,7 @@ struct Stage1Params {
   int32_t* prefix;            // [B+1]
   int32_t* workers;           // [grid*8]: worker record + combine job
   float* lse;                 // [2*grid*qo_len*16]
-  float* partial;             // [2*grid*qo_len*16*512]
+  uint16_t* partial;          // bf16 bits [2*grid*qo_len*16*512]
   int64_t kv_rows;
   int64_t kv_indices_len;
   int32_t batch;
@@ -45,7 +45,7 @@ struct Stage2Params {
   const int32_t* workers;  // [grid*8] (t0, t1, first_row, last_row, job tq, job first
                            // worker, job last worker, job first slot), written by stage 1
   const float* lse;
-  const float* partial;
+  const uint16_t* partial;  // bf16 bits
   int32_t batch;
   int32_t grid;
   int32_t qo_len;

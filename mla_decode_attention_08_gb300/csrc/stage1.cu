@@ -127,6 +127,9 @@ struct Misc {
   int32_t total_tiles;
   int32_t t0, t1;
   int32_t first_row, first_prefix, first_tiles, last_row;
+  // The first row's cached tokens and query token, found by the prologue so
+  // that no role loads them again before its first tile.
+  int32_t first_kb, first_len, first_tq, first_row_ok;
   int32_t bad;
   uint32_t next_panel[6];  // per producer warp: one past its last issued panel
   alignas(16) float lse_stage[16 * kMaxQ];  // a split piece's base-2 LSE on its way out (bulk store)
@@ -275,12 +278,23 @@ __device__ __forceinline__ bool cursor_next_segment(Cursor& c, const int32_t* kv
   return false;
 }
 
-__device__ __forceinline__ void cursor_start(Cursor& c, const Misc* ms, const int32_t* kv_indptr, int32_t batch) {
-  c.b = ms->first_row - 1;
-  c.next_a = ms->first_prefix;
+// The first segment comes from the prologue's record of the first row (the
+// same values cursor_next_segment would load).
+__device__ __forceinline__ void cursor_start(Cursor& c, const Misc* ms) {
   c.seg = -1;
-  c.live = ms->t1 > ms->t0 && ms->first_row >= 0 &&
-           cursor_next_segment(c, kv_indptr, batch, ms->t0, ms->t1);
+  c.live = ms->t1 > ms->t0 && ms->first_row >= 0;
+  if (!c.live) return;
+  const int32_t a = ms->first_prefix, nt = ms->first_tiles, t0 = ms->t0, t1 = ms->t1;
+  c.b = ms->first_row;
+  c.next_a = a + nt;
+  c.row_a = a;
+  c.kb = ms->first_kb;
+  c.len = ms->first_len;
+  c.j0 = t0 - a;
+  c.j1 = (t1 < a + nt ? t1 : a + nt) - a;
+  c.j = c.j0;
+  c.whole = a >= t0 && a + nt <= t1;
+  c.seg = 0;
 }
 
 // Step to the next tile; returns false when the worker's range is exhausted.
@@ -324,6 +338,13 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
 
   int32_t local = 0;
   int bad = 0;
+  // A thread owning a single row also loads its query-token bounds here, in the
+  // same round trip (used if that row turns out to be the worker's first).
+  int32_t q_lo = 0, q_hi = 0;
+  if (r1 - r0 == 1) {
+    q_lo = ldg_i32(p.qo_indptr + r0);
+    q_hi = ldg_i32(p.qo_indptr + r0 + 1);
+  }
   if (r0 < r1) {
     int32_t prev = ldg_i32(p.kv_indptr + r0);
     for (int32_t b = r0; b < r1; ++b) {
@@ -381,6 +402,14 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
           ms->first_row = b;
           ms->first_prefix = a;
           ms->first_tiles = nt;
+          ms->first_kb = prev;
+          ms->first_len = next - prev;
+          if (r1 - r0 != 1) {
+            q_lo = ldg_i32(p.qo_indptr + b);
+            q_hi = ldg_i32(p.qo_indptr + b + 1);
+          }
+          ms->first_tq = q_lo;
+          ms->first_row_ok = q_hi - q_lo == kQ && q_lo >= 0 && q_lo <= batch * kQ - kQ;
         }
         if (a <= t1 - 1 && t1 - 1 < a + nt) ms->last_row = b;
       }
@@ -439,7 +468,7 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
   const int lane = threadIdx.x & 31;
   if (!kGather && lane != 0) return;
   Cursor cur;
-  cursor_start(cur, ms, p.kv_indptr, p.batch);
+  cursor_start(cur, ms);
   if (p.stall_stream) cur.live = false;  // test hook: nothing is ever loaded
   uint32_t tile = 0;
   uint32_t next_k = 0;  // one past the last panel this warp issued
@@ -671,7 +700,7 @@ template <int kQ, Kv kFmt>
 __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
   using G = Geo<kQ, kFmt>;
   Cursor qc;
-  cursor_start(qc, ms, p.kv_indptr, p.batch);
+  cursor_start(qc, ms);
   uint32_t qk_n = 0;  // tiles whose QK has been issued
   while (qc.live) {
     bool ok = true;
@@ -706,7 +735,7 @@ __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
 template <int kQ, Kv kFmt>
 __device__ void run_mma_pv(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
   Cursor pc;
-  cursor_start(pc, ms, p.kv_indptr, p.batch);
+  cursor_start(pc, ms);
   uint32_t pv_n = 0;  // tiles whose PV has been issued
   while (pc.live) {
     const bool first = pc.j == pc.j0;
@@ -994,7 +1023,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
   const int32_t num_q = p.batch * kQ;  // query tokens in q and out
 
   Cursor cur;
-  cursor_start(cur, ms, p.kv_indptr, p.batch);
+  cursor_start(cur, ms);
   uint32_t tile = 0;                 // tiles processed by this CTA
   uint32_t pv_seen[2] = {0, 0};      // pv_done[b] phases consumed
 
@@ -1010,8 +1039,15 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
   while (cur.live) {
     // ------------------------------------------------ segment start
     const int32_t b = cur.b;
-    const int32_t tq = ldg_i32(p.qo_indptr + b);  // the row's first query token
-    const bool row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == kQ && tq >= 0 && tq <= num_q - kQ;
+    int32_t tq;  // the row's first query token
+    bool row_ok;
+    if (cur.seg == 0) {
+      tq = ms->first_tq;
+      row_ok = ms->first_row_ok != 0;
+    } else {
+      tq = ldg_i32(p.qo_indptr + b);
+      row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == kQ && tq >= 0 && tq <= num_q - kQ;
+    }
     if (!row_ok && t == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
     if (cur.seg > 0) softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
     float qk_scale[kQ];
@@ -1266,11 +1302,12 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         bulk_commit();
       }
     } else {
-      // fp32 partial of query token qi, stored
-      // [slot][qi][dim / 128][head / 4][dim % 128][head % 4]: each 128-dim chunk
-      // is 8 KB of contiguous memory, staged in the 8 KB buffers of Geo (the Q
-      // region, then the P buffers), reused once their bulk store has read them.
-      // The base-2 log-sum-exps follow the last chunk in the same bulk group.
+      // bf16 partial of query token qi (as the pages keep their split
+      // outputs), stored [slot][qi][dim / 128][head / 8][dim % 128][head % 8]:
+      // each 128-dim chunk is 4 KB of contiguous memory, staged in the 8 KB
+      // buffers of Geo (the Q region, then the P buffers), reused once their
+      // bulk store has read them.  The float base-2 log-sum-exps follow the
+      // last chunk in the same bulk group.
       const int32_t slot = partial_slot(c, ms->t0, cur.row_a);
 #pragma unroll 1
       for (int k = 0; k < 4 * kQ; ++k) {
@@ -1287,10 +1324,11 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
 #pragma unroll
           for (int h = 0; h < 16; ++h) v[h] = o[h] * inv[qi][h];
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            st_shared_v4(buf + (j * 128 + token) * 16, __float_as_uint(v[4 * j]),
-                         __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
-                         __float_as_uint(v[4 * j + 3]));
+          for (int j = 0; j < 2; ++j)
+            st_shared_v4(buf + (j * 128 + token) * 16, pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                         pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                         pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                         pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
           if (k == 4 * kQ - 1 && t < 16 * kQ) {
             // thread t stages the LSE of (token t / 16, head t % 16); -inf when it saw nothing
             float mm = m_ref[0][0], ll = l_tot[0][0];
@@ -1306,7 +1344,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         named_bar_sync(kBarSoftmax, kSoftmaxThreads);
         if (t == 0 && write) {
           bulk_store(p.partial + ((static_cast<size_t>(slot) * kQ + qi) * 4 + cc) * (kNumHeads * 128),
-                     buf, kNumHeads * 128 * 4);
+                     buf, kNumHeads * 128 * 2);
           if (k == 4 * kQ - 1)
             bulk_store(p.lse + static_cast<size_t>(slot) * kQ * kNumHeads, smem_u32(ms->lse_stage),
                        kQ * kNumHeads * 4);

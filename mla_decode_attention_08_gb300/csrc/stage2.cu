@@ -8,11 +8,13 @@
 // job of the split row whose first boundary is worker c's start (output row,
 // first and last worker, first worker's partial slot; the others use slot 2c),
 // and block (c, 16 qi + 4 cc + j) combines dims 128cc..128cc+127 of heads
-// 4j..4j+3 of query token qi of that row, one dim per thread.  Rows held whole by one worker, and rows
-// without cached tokens, are written by stage 1.  Partials are stored as
-// [slot][token][dim / 128][head / 4][dim % 128][head % 4] (stage 1's epilogue), so a
-// warp's float4 loads cover 512 contiguous bytes; the partials of a row are
-// visited four at a time, their loads in flight together.
+// 4j..4j+3 of query token qi of that row, one dim per thread.  Rows held whole
+// by one worker, and rows without cached tokens, are written by stage 1.
+// Partials are bf16, stored [slot][token][dim / 128][head / 8][dim % 128][head % 8]
+// (stage 1's epilogue): a thread reads its four heads as one 8-byte load, and
+// the blocks of heads 8k..8k+3 and 8k+4..8k+7 read the two halves of the same
+// 512-byte spans.  The partials of a row are visited four at a time, their
+// loads in flight together.
 #include <cuda_bf16.h>
 
 #include "../../include/mla_decode.h"
@@ -43,7 +45,7 @@ __global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const
   const int32_t tq = job.x + qi;  // output row: query token qi of the row
 
   const float4* lse4 = reinterpret_cast<const float4*>(p.lse);
-  const float4* part4 = reinterpret_cast<const float4*>(p.partial);
+  const uint2* part8 = reinterpret_cast<const uint2*>(p.partial);
   // One online pass: m_h is the running maximum of lse_s,h, and the weights of
   // the partials seen so far are rescaled when it grows.
   float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -54,7 +56,8 @@ __global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const
     // only when the grid exceeds the tile count) wrote no partial, and its
     // values are dropped.
     int4 wr[kStage2Unroll];
-    float4 x[kStage2Unroll], v[kStage2Unroll];
+    float4 x[kStage2Unroll];
+    uint2 v[kStage2Unroll];
 #pragma unroll
     for (int u = 0; u < kStage2Unroll; ++u) {
       const int32_t cu = w0 + u;
@@ -62,14 +65,16 @@ __global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const
         const int32_t piece = (cu == job.y ? job.w : 2 * cu) * nq + qi;  // (slot, token)
         wr[u] = rec[2 * cu];
         x[u] = lse4[piece * 4 + j];
-        v[u] = part4[((static_cast<size_t>(piece) * 4 + cc) * 4 + j) * kStage2Threads + dd];
+        v[u] = part8[(((static_cast<size_t>(piece) * 4 + cc) * 2 + (j >> 1)) * kStage2Threads + dd) * 2 +
+                     (j & 1)];
       }
     }
 #pragma unroll
     for (int u = 0; u < kStage2Unroll; ++u) {
       if (w0 + u > job.z || wr[u].y <= wr[u].x) continue;
       const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-      const float vs[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      const float vs[4] = {__uint_as_float(v[u].x << 16), __uint_as_float(v[u].x & 0xFFFF0000u),
+                           __uint_as_float(v[u].y << 16), __uint_as_float(v[u].y & 0xFFFF0000u)};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         if (xs[h] == -INFINITY) continue;  // the token saw no cached token in this piece

@@ -51,7 +51,7 @@ def test_plan_matches_oracle_grid(lib, batch, max_len, sms):
     assert plan.ws_workers_offset >= plan.ws_prefix_offset + 4 * (batch + 1)
     assert plan.ws_lse_offset >= plan.ws_workers_offset + 32 * g
     assert plan.ws_partial_offset >= plan.ws_lse_offset + 4 * 32 * g
-    assert plan.ws_bytes >= plan.ws_partial_offset + 4 * 2 * g * 16 * 512
+    assert plan.ws_bytes >= plan.ws_partial_offset + 2 * 2 * g * 16 * 512
     assert all(o % 256 == 0 for o in (plan.ws_workers_offset, plan.ws_lse_offset,
                                       plan.ws_partial_offset, plan.ws_bytes))
 
@@ -125,7 +125,7 @@ def test_plan_mtp_sizes_the_partials_by_query_tokens(lib, qo_len):
     assert plan.qo_len == qo_len and plan.grid == plan_grid(64, 8192, 152)
     g = plan.grid
     assert plan.ws_partial_offset >= plan.ws_lse_offset + 4 * 2 * g * qo_len * 16
-    assert plan.ws_bytes >= plan.ws_partial_offset + 4 * 2 * g * qo_len * 16 * 512
+    assert plan.ws_bytes >= plan.ws_partial_offset + 2 * 2 * g * qo_len * 16 * 512
 
 
 def test_plan_mtp_rejects_unsupported_token_counts(lib):

@@ -248,7 +248,7 @@ def test_split_partials_and_lse_match_oracle():
     assert binding.mla_decode_read_error(ws) == 0
     gpu = dev.out.float().cpu().numpy()
     views = binding.workspace_views(plan, ws)
-    part = views["partial"].cpu().numpy()[:, 0]  # [slot][head][dim] (one query token)
+    part = views["partial"].float().cpu().numpy()[:, 0]  # [slot][head][dim] (one query token)
     lse = views["lse"].cpu().numpy()[:, 0]       # [slot][head]
     orc = OracleCase(inp)
     codes = orc.codes()
