@@ -157,6 +157,7 @@ constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;    // PV issuer; owns the TMEM allocation
 constexpr int kMmaQkWarp = 6;  // QK issuer
+constexpr int kIdleWarp = 7;   // contiguous rows: writes the worker record for stage 2
 constexpr uint32_t kBarSoftmax = 1;  // named barrier id of warps 0-3
 constexpr uint32_t kBarProducers = 2;  // named barrier id of the page-table producers
 // Page-table mode with one query token: 12 warps, six producer warps (4, 7,
@@ -317,9 +318,10 @@ __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity) {
 // ------------------------------------------------------------ schedule prologue
 // All threads.  Tile counts of every row, their prefix, this worker's range
 // [t0, t1) and the rows holding its first and last tile.  Worker 0 also stores
-// the prefix for stage 2; every worker stores its (t0, t1, first, last) record.
-// Zero output for row b (a row without cached tokens, or every row when
-// kv_indptr is invalid), written by the one prologue thread that finds it.
+// the prefix for stage 2 (every worker's record for stage 2 follows later, in
+// write_worker_record).  Zero output for row b (a row without cached tokens, or
+// every row when kv_indptr is invalid), written by the one prologue thread that
+// finds it.
 template <int kQ>
 __device__ __forceinline__ void zero_row(const Stage1Params& p, int32_t b) {
   const int32_t tq = ldg_i32(p.qo_indptr + b);
@@ -418,28 +420,37 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
     }
   }
   if (c == 0 && tid == 0) p.prefix[batch] = total;
-  __syncthreads();
-  if (tid == 0) {
-    // The worker record, then the combine job of the split row (if any) whose
-    // first worker boundary is this worker's start: output row, first and last
-    // worker of the row, partial slot of the first worker (the others use 2c).
-    int32_t job[4] = {-1, 0, 0, 0};
-    const int32_t b = ms->first_row, a0 = ms->first_prefix;
-    if (t1 > t0 && b >= 0 && a0 < t0) {
-      const int32_t c_first = worker_of_tile(a0, total, p.grid);
-      if (worker_of_tile(t0 - 1, total, p.grid) == c_first) {
-        const int32_t tq = ldg_i32(p.qo_indptr + b);
-        const bool row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == kQ && tq >= 0 && tq <= batch * kQ - kQ;
-        job[0] = row_ok ? tq : -1;
-        job[1] = c_first;
-        job[2] = worker_of_tile(a0 + ms->first_tiles - 1, total, p.grid);
-        job[3] = partial_slot(c_first, worker_begin(c_first, total, p.grid), a0);
-      }
+}
+
+template <int kQ>
+__device__ __forceinline__ void write_worker_record(const Stage1Params& p, const Misc* ms);
+
+// The worker record, then the combine job of the split row (if any) whose
+// first worker boundary is this worker's start: output row, first and last
+// worker of the row, partial slot of the first worker (the others use 2c).
+// Only stage 2 reads them: with contiguous rows the otherwise idle warp 7
+// writes them while the pipeline starts; the page-table kernels have no idle
+// warp, and the prologue's thread 0 writes them before the pipeline starts.
+template <int kQ>
+__device__ __forceinline__ void write_worker_record(const Stage1Params& p, const Misc* ms) {
+  const int32_t c = static_cast<int32_t>(blockIdx.x);
+  const int32_t total = ms->total_tiles, t0 = ms->t0, t1 = ms->t1;
+  int32_t job[4] = {-1, 0, 0, 0};
+  const int32_t b = ms->first_row, a0 = ms->first_prefix;
+  if (t1 > t0 && b >= 0 && a0 < t0) {
+    const int32_t c_first = worker_of_tile(a0, total, p.grid);
+    if (worker_of_tile(t0 - 1, total, p.grid) == c_first) {
+      const int32_t tq = ldg_i32(p.qo_indptr + b);
+      const bool row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == kQ && tq >= 0 && tq <= p.batch * kQ - kQ;
+      job[0] = row_ok ? tq : -1;
+      job[1] = c_first;
+      job[2] = worker_of_tile(a0 + ms->first_tiles - 1, total, p.grid);
+      job[3] = partial_slot(c_first, worker_begin(c_first, total, p.grid), a0);
     }
-    int4* w = reinterpret_cast<int4*>(p.workers) + 2 * c;
-    w[0] = make_int4(t0, t1, ms->first_row, ms->last_row);
-    w[1] = make_int4(job[0], job[1], job[2], job[3]);
   }
+  int4* w = reinterpret_cast<int4*>(p.workers) + 2 * c;
+  w[0] = make_int4(t0, t1, ms->first_row, ms->last_row);
+  w[1] = make_int4(job[0], job[1], job[2], job[3]);
 }
 
 // ------------------------------------------------------------ producers (warp 4; page-table mode also 7-11)
@@ -1406,6 +1417,10 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ>()), 1)
   // before it reads anything this grid writes.
   pdl_launch_dependents();
   schedule_prologue<kQ>(p, ms);
+  if constexpr (kGather) {
+    __syncthreads();
+    if (tid == 0) write_worker_record<kQ>(p, ms);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1429,6 +1444,8 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ>()), 1)
       run_mma_pv<kQ, kFmt>(p, ms, sbase, tmem);
     } else if (warp == kMmaQkWarp && lane == 0) {
       run_mma_qk<kQ, kFmt>(p, ms, sbase, tmem);
+    } else if (!kGather && warp == kIdleWarp && lane == 0) {
+      write_worker_record<kQ>(p, ms);
     }
   }
   __syncwarp();
