@@ -103,7 +103,7 @@ def _stream(stream) -> Optional[int]:
 
 
 def mla_decode_plan(batch: int, max_kv_len: int, num_sms: int = 0, qo_len: int = 1) -> mla_plan_t:
-    """Plan for ``batch`` rows of ``qo_len`` query tokens (1, or 2 for two-token decode)."""
+    """Plan for ``batch`` rows of ``qo_len`` query tokens (1 to 4; 2-4 for multi-token decode)."""
     plan = mla_plan_t()
     _check("mla_decode_plan_mtp", load_library().mla_decode_plan_mtp(batch, qo_len, max_kv_len,
                                                                     num_sms, ctypes.byref(plan)))
@@ -242,7 +242,8 @@ def new_workspace(plan: mla_plan_t, device=None) -> torch.Tensor:
 
 def workspace_views(plan: mla_plan_t, ws: torch.Tensor) -> dict:
     """Typed views of the workspace regions (for tests and tools)."""
-    g, b, nq = int(plan.grid), int(plan.batch), int(plan.qo_len)
+    # partials hold one launch's tokens: min(qo_len, 2)
+    g, b, nq = int(plan.grid), int(plan.batch), min(int(plan.qo_len), 2)
 
     def view(off, n, dtype):
         size = torch.tensor([], dtype=dtype).element_size()

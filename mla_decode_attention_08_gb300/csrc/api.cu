@@ -120,7 +120,7 @@ mla_status_t prepare_device(int* device_out) {
 mla_status_t check_plan(const mla_plan_t* plan) {
   if (plan == nullptr || plan->abi_version != MLA_ABI_VERSION || plan->batch < 1 ||
       plan->grid < 1 || plan->tile_tokens != kTileTokens || plan->max_kv_len < 0 ||
-      (plan->qo_len != 1 && plan->qo_len != 2))
+      plan->qo_len < 1 || plan->qo_len > 4)
     return MLA_ERR_INVALID_ARG;
   return MLA_OK;
 }
@@ -131,8 +131,16 @@ mla_status_t check_workspace(const mla_plan_t* plan, void* workspace, size_t wor
   return MLA_OK;
 }
 
+// Query tokens per row one stage-1 launch handles: up to two (TMEM holds the
+// accumulators of two tokens); rows of three or four take two launches.
+constexpr int32_t kMaxLaunchTokens = 2;
+int32_t launch_tokens(const mla_plan_t* plan, int32_t q_off) {
+  const int32_t left = plan->qo_len - q_off;
+  return left < kMaxLaunchTokens ? left : kMaxLaunchTokens;
+}
+
 mla::Stage2Params stage2_params(const int32_t* qo_indptr, void* out, const mla_plan_t* plan,
-                                void* workspace) {
+                                void* workspace, int32_t q_off) {
   auto* ws = static_cast<uint8_t*>(workspace);
   mla::Stage2Params s;
   s.qo_indptr = qo_indptr;
@@ -144,7 +152,7 @@ mla::Stage2Params stage2_params(const int32_t* qo_indptr, void* out, const mla_p
   s.partial = reinterpret_cast<const uint16_t*>(ws + plan->ws_partial_offset);
   s.batch = plan->batch;
   s.grid = plan->grid;
-  s.qo_len = plan->qo_len;
+  s.qo_len = launch_tokens(plan, q_off);
   return s;
 }
 
@@ -153,7 +161,8 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
                         const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
                         cudaStream_t stream, const mla_plan_t* plan, const int32_t* kv_indices,
                         int64_t kv_indices_len, int64_t kv_rows, void* workspace,
-                        size_t workspace_bytes, bool bf16_cache, bool stall_stream = false) {
+                        size_t workspace_bytes, bool bf16_cache, int32_t q_off,
+                        bool stall_stream = false) {
   mla_status_t st = check_plan(plan);
   if (st != MLA_OK) return st;
   if (q == nullptr || kv == nullptr || (kv_scale == nullptr && !bf16_cache) ||
@@ -191,7 +200,8 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
   p.kv_indices_len = gather ? kv_indices_len : 0;
   p.batch = plan->batch;
   p.grid = plan->grid;
-  p.qo_len = plan->qo_len;
+  p.row_tokens = plan->qo_len;
+  p.q_off = q_off;
   p.stall_stream = stall_stream ? 1 : 0;
   return mla::launch_stage1(p, map_v, map_r, gather, bf16_cache, stream) == cudaSuccess
              ? MLA_OK
@@ -199,12 +209,33 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
 }
 
 mla_status_t run_stage2(const int32_t* qo_indptr, void* out, cudaStream_t stream,
-                        const mla_plan_t* plan, void* workspace, bool programmatic) {
-  return mla::launch_stage2(stage2_params(qo_indptr, out, plan, workspace), programmatic,
+                        const mla_plan_t* plan, void* workspace, bool programmatic,
+                        int32_t q_off) {
+  return mla::launch_stage2(stage2_params(qo_indptr, out, plan, workspace, q_off), programmatic,
                             stream) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
 }
+
+// The whole step: per group of up to two of the row's query tokens, stage 1
+// then stage 2, all on `stream` (each a programmatic dependent of the last).
+mla_status_t run_decode(const void* q, const void* kv, const float* kv_scale,
+                        const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
+                        cudaStream_t stream, const mla_plan_t* plan, const int32_t* kv_indices,
+                        int64_t kv_indices_len, int64_t kv_rows, void* workspace,
+                        size_t workspace_bytes, bool bf16_cache, bool stall_stream = false) {
+  mla_status_t st = check_plan(plan);
+  for (int32_t q_off = 0; st == MLA_OK && q_off < plan->qo_len; q_off += kMaxLaunchTokens) {
+    st = run_stage1(q, kv, kv_scale, qo_indptr, kv_indptr, out, stream, plan, kv_indices,
+                    kv_indices_len, kv_rows, workspace, workspace_bytes, bf16_cache, q_off,
+                    stall_stream);
+    if (st == MLA_OK) st = run_stage2(qo_indptr, out, stream, plan, workspace, true, q_off);
+  }
+  return st;
+}
+
+// The separate-stage entry points exist for plans whose rows take one launch.
+bool one_launch(const mla_plan_t* plan) { return plan != nullptr && plan->qo_len <= kMaxLaunchTokens; }
 
 }  // namespace
 
@@ -229,7 +260,7 @@ mla_status_t mla_decode_plan(int32_t batch, int32_t max_kv_len, int32_t num_sms,
 
 mla_status_t mla_decode_plan_mtp(int32_t batch, int32_t qo_len, int32_t max_kv_len, int32_t num_sms,
                                  mla_plan_t* plan) {
-  if (plan == nullptr || batch < 1 || max_kv_len < 0 || (qo_len != 1 && qo_len != 2))
+  if (plan == nullptr || batch < 1 || max_kv_len < 0 || qo_len < 1 || qo_len > 4)
     return MLA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(batch) * qo_len > INT32_MAX) return MLA_ERR_INVALID_ARG;
   if (num_sms <= 0) {
@@ -248,7 +279,8 @@ mla_status_t mla_decode_plan_mtp(int32_t batch, int32_t qo_len, int32_t max_kv_l
   p.abi_version = MLA_ABI_VERSION;
   p.qo_len = qo_len;
   const uint64_t g = static_cast<uint64_t>(p.grid);
-  const uint64_t nq = static_cast<uint64_t>(qo_len);
+  // partials of one launch: up to two query tokens per row
+  const uint64_t nq = static_cast<uint64_t>(qo_len < kMaxLaunchTokens ? qo_len : kMaxLaunchTokens);
   uint64_t off = kAlign;  // error word + reserved header
   p.ws_prefix_offset = off;
   off += round_up((static_cast<uint64_t>(batch) + 1) * sizeof(int32_t));
@@ -268,8 +300,9 @@ mla_status_t mla_decode_stage1(const void* q_bf16, const void* kv_fp8, const flo
                                cudaStream_t stream, const mla_plan_t* plan,
                                const int32_t* kv_indices, int64_t kv_indices_len, int64_t kv_rows,
                                void* workspace, size_t workspace_bytes) {
+  if (!one_launch(plan)) return MLA_ERR_INVALID_ARG;
   return run_stage1(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream, plan,
-                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, false);
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, false, 0);
 }
 
 mla_status_t mla_decode_stage1_bf16kv(const void* q_bf16, const void* kv_bf16,
@@ -277,19 +310,20 @@ mla_status_t mla_decode_stage1_bf16kv(const void* q_bf16, const void* kv_bf16,
                                       void* out_bf16, cudaStream_t stream, const mla_plan_t* plan,
                                       const int32_t* kv_indices, int64_t kv_indices_len,
                                       int64_t kv_rows, void* workspace, size_t workspace_bytes) {
+  if (!one_launch(plan)) return MLA_ERR_INVALID_ARG;
   return run_stage1(q_bf16, kv_bf16, nullptr, qo_indptr, kv_indptr, out_bf16, stream, plan,
-                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, true);
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, true, 0);
 }
 
 mla_status_t mla_decode_stage2(const int32_t* qo_indptr, void* out_bf16, cudaStream_t stream,
                                const mla_plan_t* plan, void* workspace, size_t workspace_bytes) {
   mla_status_t st = check_plan(plan);
   if (st != MLA_OK) return st;
-  if (qo_indptr == nullptr || out_bf16 == nullptr || !aligned(out_bf16, 16))
+  if (!one_launch(plan) || qo_indptr == nullptr || out_bf16 == nullptr || !aligned(out_bf16, 16))
     return MLA_ERR_INVALID_ARG;
   st = check_workspace(plan, workspace, workspace_bytes);
   if (st != MLA_OK) return st;
-  return run_stage2(qo_indptr, out_bf16, stream, plan, workspace, false);
+  return run_stage2(qo_indptr, out_bf16, stream, plan, workspace, false, 0);
 }
 
 mla_status_t mla_decode_fwd(const void* q_bf16, const void* kv_fp8, const float* kv_scale,
@@ -297,11 +331,8 @@ mla_status_t mla_decode_fwd(const void* q_bf16, const void* kv_fp8, const float*
                             cudaStream_t stream, const mla_plan_t* plan,
                             const int32_t* kv_indices, int64_t kv_indices_len, int64_t kv_rows,
                             void* workspace, size_t workspace_bytes) {
-  mla_status_t st = run_stage1(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream,
-                               plan, kv_indices, kv_indices_len, kv_rows, workspace,
-                               workspace_bytes, false);
-  if (st != MLA_OK) return st;
-  return run_stage2(qo_indptr, out_bf16, stream, plan, workspace, true);
+  return run_decode(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream, plan,
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, false);
 }
 
 mla_status_t mla_decode_fwd_bf16kv(const void* q_bf16, const void* kv_bf16,
@@ -309,11 +340,8 @@ mla_status_t mla_decode_fwd_bf16kv(const void* q_bf16, const void* kv_bf16,
                                    void* out_bf16, cudaStream_t stream, const mla_plan_t* plan,
                                    const int32_t* kv_indices, int64_t kv_indices_len,
                                    int64_t kv_rows, void* workspace, size_t workspace_bytes) {
-  mla_status_t st = run_stage1(q_bf16, kv_bf16, nullptr, qo_indptr, kv_indptr, out_bf16, stream,
-                               plan, kv_indices, kv_indices_len, kv_rows, workspace,
-                               workspace_bytes, true);
-  if (st != MLA_OK) return st;
-  return run_stage2(qo_indptr, out_bf16, stream, plan, workspace, true);
+  return run_decode(q_bf16, kv_bf16, nullptr, qo_indptr, kv_indptr, out_bf16, stream, plan,
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, true);
 }
 
 mla_status_t mla_decode_fwd_stall_stream(const void* q_bf16, const void* kv_fp8,
@@ -322,11 +350,8 @@ mla_status_t mla_decode_fwd_stall_stream(const void* q_bf16, const void* kv_fp8,
                                          cudaStream_t stream, const mla_plan_t* plan,
                                          const int32_t* kv_indices, int64_t kv_indices_len,
                                          int64_t kv_rows, void* workspace, size_t workspace_bytes) {
-  mla_status_t st = run_stage1(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream,
-                               plan, kv_indices, kv_indices_len, kv_rows, workspace,
-                               workspace_bytes, false, true);
-  if (st != MLA_OK) return st;
-  return run_stage2(qo_indptr, out_bf16, stream, plan, workspace, true);
+  return run_decode(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream, plan,
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, false, true);
 }
 
 mla_status_t mla_fp8_quantize_per_tensor(const void* src_bf16, int64_t n, void* dst_fp8,

@@ -26,13 +26,15 @@ struct Stage1Params {
   int32_t* err;               // workspace error word
   int32_t* prefix;            // [B+1]
   int32_t* workers;           // [grid*8]: worker record + combine job
-  float* lse;                 // [2*grid*qo_len*16]
-  uint16_t* partial;          // bf16 bits [2*grid*qo_len*16*512]
+  float* lse;                 // [2*grid*kQ*16] (kQ: this launch's tokens per row)
+  uint16_t* partial;          // bf16 bits [2*grid*kQ*16*512]
   int64_t kv_rows;
   int64_t kv_indices_len;
   int32_t batch;
   int32_t grid;
-  int32_t qo_len;             // query tokens per row (1 or 2)
+  int32_t row_tokens;         // query tokens per row (1 to 4)
+  int32_t q_off;              // first of the row's tokens this launch handles (0 or 2);
+                              // it handles kQ = min(2, row_tokens - q_off) of them
   int32_t stall_stream;       // test hook: the producers issue no cache loads, so the
                               // pipeline waits run out (bounded) and the call gives up
 };
@@ -48,7 +50,7 @@ struct Stage2Params {
   const uint16_t* partial;  // bf16 bits
   int32_t batch;
   int32_t grid;
-  int32_t qo_len;
+  int32_t qo_len;  // tokens per row combined by this launch (1 or 2)
 };
 
 size_t stage1_smem_bytes();

@@ -127,12 +127,14 @@ struct Misc {
   int32_t total_tiles;
   int32_t t0, t1;
   int32_t first_row, first_prefix, first_tiles, last_row;
-  // The first row's cached tokens and query token, found by the prologue so
-  // that no role loads them again before its first tile.
-  int32_t first_kb, first_len, first_tq, first_row_ok;
+  // The first row's cached tokens and this launch's first query token of it
+  // (-1: malformed row), found by the prologue so that no role loads them
+  // again before its first tile.
+  int32_t first_kb, first_len, first_tq;
   int32_t bad;
   uint32_t next_panel[6];  // per producer warp: one past its last issued panel
   alignas(16) float lse_stage[16 * kMaxQ];  // a split piece's base-2 LSE on its way out (bulk store)
+  alignas(16) float alpha_stage[16 * kMaxQ];  // O rescale factors of the current tile (thread 0 writes)
 };
 
 static_assert(offsetof(Misc, red_max) % 16 == 0 && offsetof(Misc, red_sum) % 16 == 0,
@@ -316,6 +318,14 @@ __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity) {
 }
 
 // ------------------------------------------------------------ schedule prologue
+// This launch's first query token of a row whose query tokens span
+// [q_lo, q_hi), or -1 when that span is not the row_tokens tokens it must be.
+__device__ __forceinline__ int32_t launch_token(const Stage1Params& p, int32_t q_lo, int32_t q_hi) {
+  const int32_t n = p.row_tokens;
+  const bool ok = q_hi - q_lo == n && q_lo >= 0 && q_lo <= p.batch * n - n;
+  return ok ? q_lo + p.q_off : -1;
+}
+
 // All threads.  Tile counts of every row, their prefix, this worker's range
 // [t0, t1) and the rows holding its first and last tile.  Worker 0 also stores
 // the prefix for stage 2 (every worker's record for stage 2 follows later, in
@@ -324,8 +334,8 @@ __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity) {
 // finds it.
 template <int kQ>
 __device__ __forceinline__ void zero_row(const Stage1Params& p, int32_t b) {
-  const int32_t tq = ldg_i32(p.qo_indptr + b);
-  if (ldg_i32(p.qo_indptr + b + 1) - tq != kQ || tq < 0 || tq > p.batch * kQ - kQ) return;
+  const int32_t tq = launch_token(p, ldg_i32(p.qo_indptr + b), ldg_i32(p.qo_indptr + b + 1));
+  if (tq < 0) return;
   uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(tq) * kNumHeads * kVDim);
   for (int i = 0; i < kQ * kNumHeads * kVDim * 2 / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
 }
@@ -410,8 +420,7 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
             q_lo = ldg_i32(p.qo_indptr + b);
             q_hi = ldg_i32(p.qo_indptr + b + 1);
           }
-          ms->first_tq = q_lo;
-          ms->first_row_ok = q_hi - q_lo == kQ && q_lo >= 0 && q_lo <= batch * kQ - kQ;
+          ms->first_tq = launch_token(p, q_lo, q_hi);
         }
         if (a <= t1 - 1 && t1 - 1 < a + nt) ms->last_row = b;
       }
@@ -440,9 +449,7 @@ __device__ __forceinline__ void write_worker_record(const Stage1Params& p, const
   if (t1 > t0 && b >= 0 && a0 < t0) {
     const int32_t c_first = worker_of_tile(a0, total, p.grid);
     if (worker_of_tile(t0 - 1, total, p.grid) == c_first) {
-      const int32_t tq = ldg_i32(p.qo_indptr + b);
-      const bool row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == kQ && tq >= 0 && tq <= p.batch * kQ - kQ;
-      job[0] = row_ok ? tq : -1;
+      job[0] = launch_token(p, ldg_i32(p.qo_indptr + b), ldg_i32(p.qo_indptr + b + 1));
       job[1] = c_first;
       job[2] = worker_of_tile(a0 + ms->first_tiles - 1, total, p.grid);
       job[3] = partial_slot(c_first, worker_begin(c_first, total, p.grid), a0);
@@ -1031,7 +1038,6 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;  // TMEM lane quarter
   const int token = warp * 32 + lane;  // S row (token) / O row (dim within a chunk) of this thread
   const int32_t c = static_cast<int32_t>(blockIdx.x);
-  const int32_t num_q = p.batch * kQ;  // query tokens in q and out
 
   Cursor cur;
   cursor_start(cur, ms);
@@ -1050,15 +1056,10 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
   while (cur.live) {
     // ------------------------------------------------ segment start
     const int32_t b = cur.b;
-    int32_t tq;  // the row's first query token
-    bool row_ok;
-    if (cur.seg == 0) {
-      tq = ms->first_tq;
-      row_ok = ms->first_row_ok != 0;
-    } else {
-      tq = ldg_i32(p.qo_indptr + b);
-      row_ok = ldg_i32(p.qo_indptr + b + 1) - tq == kQ && tq >= 0 && tq <= num_q - kQ;
-    }
+    // This launch's first query token of the row.
+    const int32_t tq = cur.seg == 0 ? ms->first_tq
+                                    : launch_token(p, ldg_i32(p.qo_indptr + b), ldg_i32(p.qo_indptr + b + 1));
+    const bool row_ok = tq >= 0;
     if (!row_ok && t == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
     if (cur.seg > 0) softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
     float qk_scale[kQ];
@@ -1075,14 +1076,16 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       }
     }
     const uint32_t seg_first_tile = tile;
+    // Query token i of the row's n sees its first len - n + 1 + i tokens
+    // (causal, aligned to the end of the row; for n = 1 the whole row); this
+    // launch's token qi is token q_off + qi and sees vis0 + qi of them.
+    const int32_t vis0 = cur.len - p.row_tokens + 1 + p.q_off;
 
     // ------------------------------------------------ tiles
     for (;;) {
       const uint32_t sb = tile & 1;
       softmax_wait<kInlineWaits>(smem_u32(&ms->s_full[sb]), (tile >> 1) & 1, ms, p.err);
       tc_fence_after();
-      // Query token qi sees the row's first len - kQ + 1 + qi tokens (causal,
-      // aligned to the end of the row; for kQ = 1 the whole row).
       const int32_t pos = cur.j * kTileTokens + token;  // row-local token of this thread
       bool tok_ok[kQ];
       float s[kQ][16];
@@ -1090,7 +1093,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
 #pragma unroll
       for (int qi = 0; qi < kQ; ++qi) {
         const uint32_t addr = tmem + lane_base + G::kColS + G::kN * sb + G::kTokCols * qi;
-        tok_ok[qi] = pos < cur.len - kQ + 1 + qi;
+        tok_ok[qi] = pos < vis0 + qi;
         const float sc = qk_scale[qi];
         if constexpr (G::kSplit) {
           uint32_t r[32];
@@ -1118,13 +1121,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       // The reference maximum moves only when some score exceeds it by more
       // than the threshold (always on a segment's first tile); then the tile
       // maximum per column is reduced over the 128 tokens.
-      float alpha[kQ][16];
       bool moved = false;
-#pragma unroll
-      for (int qi = 0; qi < kQ; ++qi) {
-#pragma unroll
-        for (int h = 0; h < 16; ++h) alpha[qi][h] = 1.0f;
-      }
       const bool any_exceed = softmax_bar_or(exceed);
       // Every softmax warp has read S[sb] (its tcgen05.ld completed before the barrier).
       if (t == 0) st_release_u32(&ms->s_read, tile + 1);
@@ -1160,14 +1157,18 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
             mx[qi][4 * k] = m4.x; mx[qi][4 * k + 1] = m4.y;
             mx[qi][4 * k + 2] = m4.z; mx[qi][4 * k + 3] = m4.w;
           }
+          // The O rescale factors go to shared memory (every thread computes
+          // the same ones), so that they hold no registers across the P work.
 #pragma unroll
           for (int h = 0; h < 16; ++h) {
+            float alpha = 1.0f;
             if (mx[qi][h] > m_ref[qi][h] + kRescaleThreshold) {
-              alpha[qi][h] = fast_exp2(m_ref[qi][h] - mx[qi][h]);  // 0 on a segment's first tile
+              alpha = fast_exp2(m_ref[qi][h] - mx[qi][h]);  // 0 on a segment's first tile
               m_ref[qi][h] = mx[qi][h];
-              l[qi][h] *= alpha[qi][h];
+              l[qi][h] *= alpha;
               moved = true;
             }
+            if (t == 0) ms->alpha_stage[16 * qi + h] = alpha;
           }
         }
       }
@@ -1209,9 +1210,10 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         }
       }
       fence_proxy_async_smem();
-      if (rescale_o) {
+      if (rescale_o) {  // the same for every softmax thread
         // O must hold every earlier tile before it is rescaled.
         wait_pv(tile - 1);
+        named_bar_sync(kBarSoftmax, kSoftmaxThreads);  // thread 0's alpha_stage is written
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
@@ -1223,14 +1225,14 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
               tmem_ld32(addr, o);
               tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(u2f(o[j]) * alpha[qi][j & 15]);
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(u2f(o[j]) * ms->alpha_stage[16 * qi + (j & 15)]);
               tmem_st32(addr, o);
             } else {
               uint32_t o[16];
               tmem_ld16(addr, o);
               tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(u2f(o[j]) * alpha[qi][j]);
+              for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(u2f(o[j]) * ms->alpha_stage[16 * qi + j]);
               tmem_st16(addr, o);
             }
           }
@@ -1253,8 +1255,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     if (cur.next_a < ms->t1 && b + 1 < p.batch) {
       // More segments follow: bring the next row's query into L2 now, so that
       // its Q preparation after this epilogue reads it from there.
-      const int32_t tq_next = ldg_i32(p.qo_indptr + b + 1);
-      if (tq_next >= 0 && tq_next <= num_q - kQ) {
+      const int32_t tq_next = ldg_i32(p.qo_indptr + b + 1) + p.q_off;
+      if (tq_next >= 0 && tq_next <= p.batch * p.row_tokens - kQ) {
         const char* qn = reinterpret_cast<const char*>(p.q + static_cast<size_t>(tq_next) * kNumHeads * kQkDim);
         for (int i = t; i < kQ * kNumHeads * kQkDim * 2 / 128; i += kSoftmaxThreads) prefetch_l2(qn + 128 * i);
       }
@@ -1512,7 +1514,7 @@ cudaError_t stage1_prepare(int device) {
 cudaError_t launch_stage1(const Stage1Params& p, const CUtensorMap& map_v,
                           const CUtensorMap& map_r, bool gather, bool bf16_cache,
                           cudaStream_t stream) {
-  const bool two = p.qo_len == 2;
+  const bool two = p.row_tokens - p.q_off >= 2;
   if (bf16_cache) {
     if (gather) return cudaErrorNotSupported;  // the host rejects this before launching
     return two ? launch<false, 2, Kv::kBf16>(p, map_v, map_r, stream)

@@ -69,8 +69,9 @@ WORKLOADS = {
         Workload("bs256_kv8192", 256, 8192, seed=BASE_SEED + 3),
         Workload("ragged_bs128_kv8192_paged", 128, 8192, ragged=True, paged=True,
                  seed=BASE_SEED + 4),
-        # Two query tokens per row (speculative / multi-token-prediction decode).
+        # Two and four query tokens per row (speculative / multi-token-prediction decode).
         Workload("bs64_q2_kv8192", 64, 8192, seed=BASE_SEED + 5, qo_len=2),
+        Workload("bs64_q4_kv8192", 64, 8192, seed=BASE_SEED + 6, qo_len=4),
     )
 }
 

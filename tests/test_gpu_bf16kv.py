@@ -67,6 +67,8 @@ CASES = [
     ("two_token_tails", [2, 127, 128, 129, 130, 1000], 2),
     ("two_token_see_nothing", [1, 0, 2, 1], 2),
     ("two_token_mixed", [3, 129, 700, 64, 1, 2000], 2),
+    ("three_tokens", [3, 4, 129, 1000, 0, 2], 3),
+    ("four_tokens", [4, 5, 128, 131, 1000, 1], 4),
 ]
 
 
@@ -125,7 +127,7 @@ def test_bf16_cache_rejects_a_page_table():
 
 
 @pytest.mark.parametrize("name", ["bs4_kv1024", "bs32_kv1024", "bs64_kv8192", "bs256_kv8192",
-                                  "bs64_q2_kv8192"])
+                                  "bs64_q2_kv8192", "bs64_q4_kv8192"])
 def test_bf16_cache_workloads(name):
     """The contiguous benchmark shapes over their bf16 cache: every row of the
     small ones, sampled rows (first, last, a few in between) of the large ones."""

@@ -1,8 +1,9 @@
-"""Two-token decode (qo_len = 2) through the C ABI against the float64 oracle.
+"""Multi-token decode (qo_len = 2 to 4) through the C ABI against the float64 oracle.
 
-Each row holds two query tokens; token i sees the row's first L - 2 + 1 + i
+Each row holds n query tokens; token i sees the row's first L - n + 1 + i
 cached tokens (the oracle's causal, end-aligned reading).  One KV tile serves
-both tokens' 16 heads (MMA N = 64)."""
+two tokens' 16 heads (MMA N = 64); rows of three or four tokens take two
+launches (tokens 0-1, then 2-3)."""
 import numpy as np
 import pytest
 import torch
@@ -61,6 +62,35 @@ def test_rows_of_one_token_are_rejected_by_a_two_token_plan():
     inp = make_from_lengths([300, 200], seed=12, qo_len=2)
     dev = DeviceCase(inp)
     dev.qo_indptr.copy_(torch.tensor([0, 1, 2], dtype=torch.int32))
+    _, err, _, _ = dev.run(sms=3)
+    assert err & 1
+
+
+MANY = [
+    ("tails", [3, 4, 127, 128, 129, 131, 257, 1000]),
+    ("tokens_that_see_nothing", [1, 0, 2, 3, 4, 5]),
+    ("long_row", [5000]),
+]
+
+
+@pytest.mark.parametrize("qo_len", [3, 4])
+@pytest.mark.parametrize("name,lengths", MANY, ids=[c[0] for c in MANY])
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("sms", [1, 5, None])
+def test_three_and_four_token_decode_matches_oracle(qo_len, name, lengths, paged, sms):
+    inp = make_from_lengths(lengths, seed=600 + 10 * qo_len + len(lengths), paged=paged,
+                            qo_len=qo_len)
+    dev = DeviceCase(inp)
+    dev.out.fill_(float("nan"))
+    gpu, err, plan, _ = dev.run(sms=sms)
+    assert err == 0 and plan.qo_len == qo_len
+    assert_close(gpu, OracleCase(inp).reference())
+
+
+def test_four_token_rows_of_three_are_flagged():
+    inp = make_from_lengths([300, 200], seed=13, qo_len=4)
+    dev = DeviceCase(inp)
+    dev.qo_indptr.copy_(torch.tensor([0, 3, 8], dtype=torch.int32))
     _, err, _, _ = dev.run(sms=3)
     assert err & 1
 
