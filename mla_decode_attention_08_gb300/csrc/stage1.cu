@@ -121,7 +121,7 @@ struct Misc {
   alignas(16) float red_max[2][4][16 * kMaxQ];  // read and written as float4
   alignas(16) float red_sum[4][16 * kMaxQ];
   uint32_t red_u32[8];
-  int32_t scan[8];
+  int32_t scan[kStage1ThreadsGather / 32];  // per warp of the prologue's block scan
   uint32_t tmem_base;
   volatile int32_t abort_flag;
   int32_t total_tiles;

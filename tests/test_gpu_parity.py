@@ -299,3 +299,50 @@ def test_combine_edge_cases_and_separate_stages(name, lengths, paged, sms):
     torch.cuda.synchronize()
     assert binding.mla_decode_read_error(ws) == 0
     assert np.array_equal(out2.float().cpu().numpy(), gpu)
+
+
+# ------------------------------------------------------------------ larger and randomised shapes
+def test_more_rows_than_prologue_threads():
+    """1000 rows: each prologue thread scans several rows (the rows-per-thread
+    path of the block scan), with empty and one-token rows among them."""
+    rng = np.random.default_rng(71)
+    lengths = rng.integers(0, 300, size=1000)
+    lengths[rng.random(1000) < 0.05] = 0
+    lengths[rng.random(1000) < 0.05] = 1
+    for paged in (False, True):
+        inp = make_from_lengths(lengths, seed=72 + paged, paged=paged)
+        dev = DeviceCase(inp)
+        gpu, err, plan, ws = dev.run()
+        assert err == 0
+        assert_close(gpu, OracleCase(inp).reference())
+        views = binding.workspace_views(plan, ws)
+        assert np.array_equal(views["workers"].cpu().numpy(), worker_table(inp.kv_indptr, plan.grid))
+        assert np.array_equal(views["jobs"].cpu().numpy(), expected_jobs(inp, plan.grid))
+
+
+def test_one_very_long_row_among_short_ones():
+    """A 100,000-token row split over every worker next to short rows."""
+    inp = make_from_lengths([100_000, 3, 0, 129], seed=73)
+    dev = DeviceCase(inp)
+    gpu, err, plan, _ = dev.run()
+    assert err == 0 and plan.grid == num_sms()
+    assert_close(gpu, OracleCase(inp).reference())
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_randomised_shapes(seed):
+    """Random batch, lengths (with empty rows), page table, query tokens per
+    row (1 to 4) and grid, against the oracle."""
+    rng = np.random.default_rng(9000 + seed)
+    batch = int(rng.integers(1, 300))
+    lengths = rng.integers(0, int(rng.integers(2, 1500)), size=batch)
+    lengths[rng.random(batch) < 0.1] = 0
+    qo_len = int(rng.integers(1, 5))
+    paged = bool(rng.random() < 0.5)
+    sms = int(rng.integers(1, 153))
+    inp = make_from_lengths(lengths, seed=9100 + seed, paged=paged, qo_len=qo_len)
+    dev = DeviceCase(inp)
+    dev.out.fill_(float("nan"))
+    gpu, err, plan, _ = dev.run(sms=sms)
+    assert err == 0, (batch, qo_len, paged, sms)
+    assert_close(gpu, OracleCase(inp).reference())
