@@ -65,7 +65,8 @@ typedef struct {
   int32_t batch;       /* B, rows (one query token each)                          */
   int32_t max_kv_len;  /* upper bound on any row's cached tokens (sizes the grid)  */
   int32_t num_sms;     /* SMs the grid is sized for                               */
-  int32_t grid;        /* persistent stage-1 workers: max(1, min(num_sms, B*ceil(max_kv_len/128))) */
+  int32_t grid;        /* persistent stage-1 workers: max(1, min(S, B*ceil(max_kv_len/128))),
+                        * S = num_sms, or num_sms/2 for qo_len >= 3 (two CTAs per worker) */
   int32_t tile_tokens; /* 128                                                      */
   int32_t abi_version; /* MLA_ABI_VERSION                                          */
   int32_t qo_len;      /* query tokens per row: 1 (decode) to 4 (multi-token decode) */
@@ -76,9 +77,8 @@ typedef struct {
                                * then the combine job of the split row whose first
                                * worker boundary is t0: (output row or -1, first
                                * worker, last worker, first worker's partial slot) */
-  uint64_t ws_lse_offset;     /* float[2*grid*nq*16] base-2 log-sum-exp of partials,
-                               * nq = min(qo_len, 2) (the tokens of one launch) */
-  uint64_t ws_partial_offset; /* bf16[2*grid*nq*16*512] normalised split partials,
+  uint64_t ws_lse_offset;     /* float[2*grid*qo_len*16] base-2 log-sum-exp of partials */
+  uint64_t ws_partial_offset; /* bf16[2*grid*qo_len*16*512] normalised split partials,
                                * stored [slot][token][dim/128][head/8][dim%128][head%8] */
 } mla_plan_t;
 
@@ -97,10 +97,11 @@ mla_status_t mla_decode_plan(int32_t batch, int32_t max_kv_len, int32_t num_sms,
  * every row; q is [B*qo_len, 16, 576] and out [B*qo_len, 16, 512].  Query token
  * i of a row with L cached tokens attends to the row's first L - qo_len + 1 + i
  * tokens (its own entry and those before it: the row's last qo_len cached
- * tokens are the query tokens'); a token that sees none outputs zeros.  One
- * stage-1 launch loads each KV tile once for up to two query tokens x 16
- * heads; rows of three or four tokens are done as two such launches (tokens
- * 0-1, then 2-3), each reading the cache.  qo_len must be 1 to 4.
+ * tokens are the query tokens'); a token that sees none outputs zeros.  A
+ * stage-1 CTA loads each KV tile once for up to two query tokens x 16 heads;
+ * rows of three or four tokens are shared by two sibling CTAs per worker
+ * (tokens 0-1 and 2-3), which stream the same tiles at the same time, so the
+ * second one's copies mostly come from L2.  qo_len must be 1 to 4.
  */
 mla_status_t mla_decode_plan_mtp(int32_t batch, int32_t qo_len, int32_t max_kv_len, int32_t num_sms,
                                  mla_plan_t* plan);
@@ -188,8 +189,7 @@ mla_status_t mla_decode_fwd_bf16kv(const void* q_bf16, const void* kv_bf16,
 /* The two stages of mla_decode_fwd launched separately (same arguments); the
  * pair is equivalent to one mla_decode_fwd call.  Used to time stage 1 alone.
  * mla_decode_stage1_bf16kv is stage 1 of mla_decode_fwd_bf16kv; stage 2 is
- * shared by both caches.  Only for plans of one or two query tokens per row
- * (one launch each); others return MLA_ERR_INVALID_ARG. */
+ * shared by both caches. */
 mla_status_t mla_decode_stage1(const void* q_bf16, const void* kv_fp8, const float* kv_scale,
                                const int32_t* qo_indptr, const int32_t* kv_indptr, void* out_bf16,
                                cudaStream_t stream, const mla_plan_t* plan,

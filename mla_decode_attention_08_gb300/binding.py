@@ -242,8 +242,7 @@ def new_workspace(plan: mla_plan_t, device=None) -> torch.Tensor:
 
 def workspace_views(plan: mla_plan_t, ws: torch.Tensor) -> dict:
     """Typed views of the workspace regions (for tests and tools)."""
-    # partials hold one launch's tokens: min(qo_len, 2)
-    g, b, nq = int(plan.grid), int(plan.batch), min(int(plan.qo_len), 2)
+    g, b, nq = int(plan.grid), int(plan.batch), int(plan.qo_len)
 
     def view(off, n, dtype):
         size = torch.tensor([], dtype=dtype).element_size()

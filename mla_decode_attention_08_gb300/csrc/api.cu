@@ -131,16 +131,13 @@ mla_status_t check_workspace(const mla_plan_t* plan, void* workspace, size_t wor
   return MLA_OK;
 }
 
-// Query tokens per row one stage-1 launch handles: up to two (TMEM holds the
-// accumulators of two tokens); rows of three or four take two launches.
-constexpr int32_t kMaxLaunchTokens = 2;
-int32_t launch_tokens(const mla_plan_t* plan, int32_t q_off) {
-  const int32_t left = plan->qo_len - q_off;
-  return left < kMaxLaunchTokens ? left : kMaxLaunchTokens;
-}
+// One CTA holds the accumulators of up to two query tokens per row (TMEM);
+// rows of three or four are shared by two sibling CTAs per worker.
+constexpr int32_t kCtaTokens = 2;
+int32_t siblings_of(const mla_plan_t* plan) { return plan->qo_len > kCtaTokens ? 2 : 1; }
 
 mla::Stage2Params stage2_params(const int32_t* qo_indptr, void* out, const mla_plan_t* plan,
-                                void* workspace, int32_t q_off) {
+                                void* workspace) {
   auto* ws = static_cast<uint8_t*>(workspace);
   mla::Stage2Params s;
   s.qo_indptr = qo_indptr;
@@ -152,7 +149,7 @@ mla::Stage2Params stage2_params(const int32_t* qo_indptr, void* out, const mla_p
   s.partial = reinterpret_cast<const uint16_t*>(ws + plan->ws_partial_offset);
   s.batch = plan->batch;
   s.grid = plan->grid;
-  s.qo_len = launch_tokens(plan, q_off);
+  s.qo_len = plan->qo_len;
   return s;
 }
 
@@ -161,8 +158,7 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
                         const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
                         cudaStream_t stream, const mla_plan_t* plan, const int32_t* kv_indices,
                         int64_t kv_indices_len, int64_t kv_rows, void* workspace,
-                        size_t workspace_bytes, bool bf16_cache, int32_t q_off,
-                        bool stall_stream = false) {
+                        size_t workspace_bytes, bool bf16_cache, bool stall_stream = false) {
   mla_status_t st = check_plan(plan);
   if (st != MLA_OK) return st;
   if (q == nullptr || kv == nullptr || (kv_scale == nullptr && !bf16_cache) ||
@@ -201,7 +197,9 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
   p.batch = plan->batch;
   p.grid = plan->grid;
   p.row_tokens = plan->qo_len;
-  p.q_off = q_off;
+  p.q_off = 0;
+  p.siblings = siblings_of(plan);
+  p.slot_tokens = plan->qo_len;
   p.stall_stream = stall_stream ? 1 : 0;
   return mla::launch_stage1(p, map_v, map_r, gather, bf16_cache, stream) == cudaSuccess
              ? MLA_OK
@@ -209,33 +207,25 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
 }
 
 mla_status_t run_stage2(const int32_t* qo_indptr, void* out, cudaStream_t stream,
-                        const mla_plan_t* plan, void* workspace, bool programmatic,
-                        int32_t q_off) {
-  return mla::launch_stage2(stage2_params(qo_indptr, out, plan, workspace, q_off), programmatic,
+                        const mla_plan_t* plan, void* workspace, bool programmatic) {
+  return mla::launch_stage2(stage2_params(qo_indptr, out, plan, workspace), programmatic,
                             stream) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
 }
 
-// The whole step: per group of up to two of the row's query tokens, stage 1
-// then stage 2, all on `stream` (each a programmatic dependent of the last).
+// The whole step: stage 1 then stage 2 on `stream`, both programmatic dependents.
 mla_status_t run_decode(const void* q, const void* kv, const float* kv_scale,
                         const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
                         cudaStream_t stream, const mla_plan_t* plan, const int32_t* kv_indices,
                         int64_t kv_indices_len, int64_t kv_rows, void* workspace,
                         size_t workspace_bytes, bool bf16_cache, bool stall_stream = false) {
-  mla_status_t st = check_plan(plan);
-  for (int32_t q_off = 0; st == MLA_OK && q_off < plan->qo_len; q_off += kMaxLaunchTokens) {
-    st = run_stage1(q, kv, kv_scale, qo_indptr, kv_indptr, out, stream, plan, kv_indices,
-                    kv_indices_len, kv_rows, workspace, workspace_bytes, bf16_cache, q_off,
-                    stall_stream);
-    if (st == MLA_OK) st = run_stage2(qo_indptr, out, stream, plan, workspace, true, q_off);
-  }
+  mla_status_t st = run_stage1(q, kv, kv_scale, qo_indptr, kv_indptr, out, stream, plan,
+                               kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes,
+                               bf16_cache, stall_stream);
+  if (st == MLA_OK) st = run_stage2(qo_indptr, out, stream, plan, workspace, true);
   return st;
 }
-
-// The separate-stage entry points exist for plans whose rows take one launch.
-bool one_launch(const mla_plan_t* plan) { return plan != nullptr && plan->qo_len <= kMaxLaunchTokens; }
 
 }  // namespace
 
@@ -274,13 +264,15 @@ mla_status_t mla_decode_plan_mtp(int32_t batch, int32_t qo_len, int32_t max_kv_l
   p.batch = batch;
   p.max_kv_len = max_kv_len;
   p.num_sms = num_sms;
-  p.grid = mla::plan_grid(batch, max_kv_len, num_sms);
+  // Rows of three or four query tokens run two sibling CTAs per worker: one
+  // worker per pair of SMs.
+  p.grid = mla::plan_grid(batch, max_kv_len,
+                          qo_len > kCtaTokens ? (num_sms > 1 ? num_sms / 2 : 1) : num_sms);
   p.tile_tokens = kTileTokens;
   p.abi_version = MLA_ABI_VERSION;
   p.qo_len = qo_len;
   const uint64_t g = static_cast<uint64_t>(p.grid);
-  // partials of one launch: up to two query tokens per row
-  const uint64_t nq = static_cast<uint64_t>(qo_len < kMaxLaunchTokens ? qo_len : kMaxLaunchTokens);
+  const uint64_t nq = static_cast<uint64_t>(qo_len);
   uint64_t off = kAlign;  // error word + reserved header
   p.ws_prefix_offset = off;
   off += round_up((static_cast<uint64_t>(batch) + 1) * sizeof(int32_t));
@@ -300,9 +292,8 @@ mla_status_t mla_decode_stage1(const void* q_bf16, const void* kv_fp8, const flo
                                cudaStream_t stream, const mla_plan_t* plan,
                                const int32_t* kv_indices, int64_t kv_indices_len, int64_t kv_rows,
                                void* workspace, size_t workspace_bytes) {
-  if (!one_launch(plan)) return MLA_ERR_INVALID_ARG;
   return run_stage1(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream, plan,
-                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, false, 0);
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, false);
 }
 
 mla_status_t mla_decode_stage1_bf16kv(const void* q_bf16, const void* kv_bf16,
@@ -310,20 +301,19 @@ mla_status_t mla_decode_stage1_bf16kv(const void* q_bf16, const void* kv_bf16,
                                       void* out_bf16, cudaStream_t stream, const mla_plan_t* plan,
                                       const int32_t* kv_indices, int64_t kv_indices_len,
                                       int64_t kv_rows, void* workspace, size_t workspace_bytes) {
-  if (!one_launch(plan)) return MLA_ERR_INVALID_ARG;
   return run_stage1(q_bf16, kv_bf16, nullptr, qo_indptr, kv_indptr, out_bf16, stream, plan,
-                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, true, 0);
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, true);
 }
 
 mla_status_t mla_decode_stage2(const int32_t* qo_indptr, void* out_bf16, cudaStream_t stream,
                                const mla_plan_t* plan, void* workspace, size_t workspace_bytes) {
   mla_status_t st = check_plan(plan);
   if (st != MLA_OK) return st;
-  if (!one_launch(plan) || qo_indptr == nullptr || out_bf16 == nullptr || !aligned(out_bf16, 16))
+  if (qo_indptr == nullptr || out_bf16 == nullptr || !aligned(out_bf16, 16))
     return MLA_ERR_INVALID_ARG;
   st = check_workspace(plan, workspace, workspace_bytes);
   if (st != MLA_OK) return st;
-  return run_stage2(qo_indptr, out_bf16, stream, plan, workspace, false, 0);
+  return run_stage2(qo_indptr, out_bf16, stream, plan, workspace, false);
 }
 
 mla_status_t mla_decode_fwd(const void* q_bf16, const void* kv_fp8, const float* kv_scale,

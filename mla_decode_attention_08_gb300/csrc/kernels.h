@@ -33,8 +33,11 @@ struct Stage1Params {
   int32_t batch;
   int32_t grid;
   int32_t row_tokens;         // query tokens per row (1 to 4)
-  int32_t q_off;              // first of the row's tokens this launch handles (0 or 2);
-                              // it handles kQ = min(2, row_tokens - q_off) of them
+  int32_t q_off;              // first of the row's tokens this launch handles
+  int32_t siblings;           // CTAs per worker (1, or 2 for rows of 3-4 tokens: CTA
+                              // 2c + s takes tokens q_off + 2s, up to two of them)
+  int32_t slot_tokens;        // query tokens per partial slot (the row's tokens this
+                              // launch handles, all siblings together)
   int32_t stall_stream;       // test hook: the producers issue no cache loads, so the
                               // pipeline waits run out (bounded) and the call gives up
 };

@@ -317,14 +317,33 @@ __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity) {
   }
 }
 
-// ------------------------------------------------------------ schedule prologue
-// This launch's first query token of a row whose query tokens span
+// ------------------------------------------------------------ this CTA's share
+// A worker's tile range is covered by `siblings` CTAs (2c, 2c + 1 with two):
+// each takes up to kQ of the row's query tokens, from q_off on, and the
+// siblings stream the same tiles (the second one's copies mostly hit L2).
+__device__ __forceinline__ int32_t cta_worker(const Stage1Params& p) {
+  return static_cast<int32_t>(p.siblings == 2 ? blockIdx.x >> 1 : blockIdx.x);
+}
+__device__ __forceinline__ int32_t cta_sibling(const Stage1Params& p) {
+  return p.siblings == 2 ? static_cast<int32_t>(blockIdx.x & 1) : 0;
+}
+__device__ __forceinline__ int32_t cta_q_off(const Stage1Params& p) { return p.q_off + 2 * cta_sibling(p); }
+template <int kQ>
+__device__ __forceinline__ int32_t cta_tokens(const Stage1Params& p) {
+  const int32_t left = p.row_tokens - cta_q_off(p);
+  return left < kQ ? left : kQ;
+}
+
+// The first query token at q_off of a row whose query tokens span
 // [q_lo, q_hi), or -1 when that span is not the row_tokens tokens it must be.
-__device__ __forceinline__ int32_t launch_token(const Stage1Params& p, int32_t q_lo, int32_t q_hi) {
+__device__ __forceinline__ int32_t row_token(const Stage1Params& p, int32_t q_off, int32_t q_lo,
+                                             int32_t q_hi) {
   const int32_t n = p.row_tokens;
   const bool ok = q_hi - q_lo == n && q_lo >= 0 && q_lo <= p.batch * n - n;
-  return ok ? q_lo + p.q_off : -1;
+  return ok ? q_lo + q_off : -1;
 }
+
+// ------------------------------------------------------------ schedule prologue
 
 // All threads.  Tile counts of every row, their prefix, this worker's range
 // [t0, t1) and the rows holding its first and last tile.  Worker 0 also stores
@@ -334,10 +353,11 @@ __device__ __forceinline__ int32_t launch_token(const Stage1Params& p, int32_t q
 // finds it.
 template <int kQ>
 __device__ __forceinline__ void zero_row(const Stage1Params& p, int32_t b) {
-  const int32_t tq = launch_token(p, ldg_i32(p.qo_indptr + b), ldg_i32(p.qo_indptr + b + 1));
+  const int32_t tq = row_token(p, cta_q_off(p), ldg_i32(p.qo_indptr + b), ldg_i32(p.qo_indptr + b + 1));
   if (tq < 0) return;
   uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(tq) * kNumHeads * kVDim);
-  for (int i = 0; i < kQ * kNumHeads * kVDim * 2 / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+  const int n = cta_tokens<kQ>(p) * kNumHeads * kVDim * 2 / 16;
+  for (int i = 0; i < n; ++i) dst[i] = make_uint4(0, 0, 0, 0);
 }
 
 template <int kQ>
@@ -386,7 +406,7 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
     total += s;
   }
   if (bad) total = 0;
-  const int32_t c = static_cast<int32_t>(blockIdx.x);
+  const int32_t c = cta_worker(p);
   const int32_t t0 = worker_begin(c, total, p.grid);
   const int32_t t1 = worker_begin(c + 1, total, p.grid);
   if (tid == 0) {
@@ -420,7 +440,7 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
             q_lo = ldg_i32(p.qo_indptr + b);
             q_hi = ldg_i32(p.qo_indptr + b + 1);
           }
-          ms->first_tq = launch_token(p, q_lo, q_hi);
+          ms->first_tq = row_token(p, cta_q_off(p), q_lo, q_hi);
         }
         if (a <= t1 - 1 && t1 - 1 < a + nt) ms->last_row = b;
       }
@@ -442,14 +462,14 @@ __device__ __forceinline__ void write_worker_record(const Stage1Params& p, const
 // warp, and the prologue's thread 0 writes them before the pipeline starts.
 template <int kQ>
 __device__ __forceinline__ void write_worker_record(const Stage1Params& p, const Misc* ms) {
-  const int32_t c = static_cast<int32_t>(blockIdx.x);
+  const int32_t c = cta_worker(p);
   const int32_t total = ms->total_tiles, t0 = ms->t0, t1 = ms->t1;
   int32_t job[4] = {-1, 0, 0, 0};
   const int32_t b = ms->first_row, a0 = ms->first_prefix;
   if (t1 > t0 && b >= 0 && a0 < t0) {
     const int32_t c_first = worker_of_tile(a0, total, p.grid);
     if (worker_of_tile(t0 - 1, total, p.grid) == c_first) {
-      job[0] = launch_token(p, ldg_i32(p.qo_indptr + b), ldg_i32(p.qo_indptr + b + 1));
+      job[0] = row_token(p, p.q_off, ldg_i32(p.qo_indptr + b), ldg_i32(p.qo_indptr + b + 1));
       job[1] = c_first;
       job[2] = worker_of_tile(a0 + ms->first_tiles - 1, total, p.grid);
       job[3] = partial_slot(c_first, worker_begin(c_first, total, p.grid), a0);
@@ -931,12 +951,12 @@ __device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 
   named_bar_sync(kBarSoftmax, kSoftmaxThreads);
 }
 
-// Loads the row's query tokens tq .. tq + kQ - 1 (16 heads x 576 bf16 each)
-// and writes the Q operand of the cache format.  Sets qk_scale[qi], the factor
-// turning the QK accumulator of token qi into base-2 softmax exponent units.
-// tq < 0 writes a zero query.
+// Loads the row's query tokens tq .. tq + nq - 1 (16 heads x 576 bf16 each;
+// nq <= kQ, the other operand rows stay zero) and writes the Q operand of the
+// cache format.  Sets qk_scale[qi], the factor turning the QK accumulator of
+// token qi into base-2 softmax exponent units.  tq < 0 writes a zero query.
 template <int kQ, Kv kFmt>
-__device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq,
+__device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq, int32_t nq,
                           float kv_scale, float (&qk_scale)[kQ]) {
   const int t = threadIdx.x;
   uint4 raw[kQ][5][2];
@@ -946,7 +966,7 @@ __device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t 
     for (int r = 0; r < 5; ++r) {
       const int job = t + 128 * r;
       raw[qi][r][0] = raw[qi][r][1] = make_uint4(0, 0, 0, 0);
-      if (job < 576 && tq >= 0) {
+      if (job < 576 && tq >= 0 && qi < nq) {
         const int head = job / 36, ch = job % 36;
         const uint4* src = reinterpret_cast<const uint4*>(
             p.q + (static_cast<size_t>(tq + qi) * kNumHeads + head) * kQkDim + ch * 16);
@@ -1037,7 +1057,10 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;  // TMEM lane quarter
   const int token = warp * 32 + lane;  // S row (token) / O row (dim within a chunk) of this thread
-  const int32_t c = static_cast<int32_t>(blockIdx.x);
+  const int32_t c = cta_worker(p);
+  const int32_t q_off = cta_q_off(p);   // the row's first query token this CTA handles
+  const int32_t nq = kQ == 1 ? 1 : cta_tokens<kQ>(p);  // and how many (the rest of the kQ columns idle)
+  const int32_t slot_q = q_off - p.q_off;  // their first index within a partial slot
 
   Cursor cur;
   cursor_start(cur, ms);
@@ -1058,12 +1081,12 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     const int32_t b = cur.b;
     // This launch's first query token of the row.
     const int32_t tq = cur.seg == 0 ? ms->first_tq
-                                    : launch_token(p, ldg_i32(p.qo_indptr + b), ldg_i32(p.qo_indptr + b + 1));
+                                    : row_token(p, q_off, ldg_i32(p.qo_indptr + b), ldg_i32(p.qo_indptr + b + 1));
     const bool row_ok = tq >= 0;
     if (!row_ok && t == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
     if (cur.seg > 0) softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
     float qk_scale[kQ];
-    prepare_q<kQ, kFmt>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, kv_scale, qk_scale);
+    prepare_q<kQ, kFmt>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, nq, kv_scale, qk_scale);
     if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 1));
 
     float m_ref[kQ][16], l[kQ][16];
@@ -1079,7 +1102,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     // Query token i of the row's n sees its first len - n + 1 + i tokens
     // (causal, aligned to the end of the row; for n = 1 the whole row); this
     // launch's token qi is token q_off + qi and sees vis0 + qi of them.
-    const int32_t vis0 = cur.len - p.row_tokens + 1 + p.q_off;
+    const int32_t vis0 = cur.len - p.row_tokens + 1 + q_off;
 
     // ------------------------------------------------ tiles
     for (;;) {
@@ -1093,7 +1116,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
 #pragma unroll
       for (int qi = 0; qi < kQ; ++qi) {
         const uint32_t addr = tmem + lane_base + G::kColS + G::kN * sb + G::kTokCols * qi;
-        tok_ok[qi] = pos < vis0 + qi;
+        tok_ok[qi] = qi < nq && pos < vis0 + qi;
         const float sc = qk_scale[qi];
         if constexpr (G::kSplit) {
           uint32_t r[32];
@@ -1255,7 +1278,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     if (cur.next_a < ms->t1 && b + 1 < p.batch) {
       // More segments follow: bring the next row's query into L2 now, so that
       // its Q preparation after this epilogue reads it from there.
-      const int32_t tq_next = ldg_i32(p.qo_indptr + b + 1) + p.q_off;
+      const int32_t tq_next = ldg_i32(p.qo_indptr + b + 1) + q_off;
       if (tq_next >= 0 && tq_next <= p.batch * p.row_tokens - kQ) {
         const char* qn = reinterpret_cast<const char*>(p.q + static_cast<size_t>(tq_next) * kNumHeads * kQkDim);
         for (int i = t; i < kQ * kNumHeads * kQkDim * 2 / 128; i += kSoftmaxThreads) prefetch_l2(qn + 128 * i);
@@ -1292,11 +1315,12 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     tc_fence_after();
     const uint32_t stage_q = sbase + G::kOffQ;
     if (cur.whole) {
-      // bf16 rows [kQ tokens][16 heads][512 dims] (16 KB each), staged in the Q region.
+      // bf16 rows [nq tokens][16 heads][512 dims] (16 KB each), staged in the Q region.
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll
         for (int qi = 0; qi < kQ; ++qi) {
+          if (qi >= nq) continue;  // the same for every softmax thread
           float o[16];
           tmem_ld_heads<kFmt>(tmem + lane_base + G::kColO + G::kN * cc + G::kTokCols * qi, o);
           const int dim = 128 * cc + token;
@@ -1311,19 +1335,19 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);
       if (t == 0 && write) {
         bulk_store(p.out + static_cast<size_t>(tq) * kNumHeads * kVDim, stage_q,
-                   kQ * kNumHeads * kVDim * 2);
+                   nq * kNumHeads * kVDim * 2);
         bulk_commit();
       }
     } else {
       // bf16 partial of query token qi (as the pages keep their split
-      // outputs), stored [slot][qi][dim / 128][head / 8][dim % 128][head % 8]:
+      // outputs), stored [slot][slot_q + qi][dim / 128][head / 8][dim % 128][head % 8]:
       // each 128-dim chunk is 4 KB of contiguous memory, staged in the 8 KB
       // buffers of Geo (the Q region, then the P buffers), reused once their
       // bulk store has read them.  The float base-2 log-sum-exps follow the
       // last chunk in the same bulk group.
       const int32_t slot = partial_slot(c, ms->t0, cur.row_a);
 #pragma unroll 1
-      for (int k = 0; k < 4 * kQ; ++k) {
+      for (int k = 0; k < 4 * nq; ++k) {
         const int qi = k >> 2, cc = k & 3;
         float o[16];
         tmem_ld_heads<kFmt>(tmem + lane_base + G::kColO + G::kN * cc + G::kTokCols * qi, o);
@@ -1342,7 +1366,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
                          pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
                          pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
                          pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-          if (k == 4 * kQ - 1 && t < 16 * kQ) {
+          if (k == 4 * nq - 1 && t < 16 * nq) {
             // thread t stages the LSE of (token t / 16, head t % 16); -inf when it saw nothing
             float mm = m_ref[0][0], ll = l_tot[0][0];
 #pragma unroll
@@ -1356,11 +1380,10 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         fence_proxy_async_smem();
         named_bar_sync(kBarSoftmax, kSoftmaxThreads);
         if (t == 0 && write) {
-          bulk_store(p.partial + ((static_cast<size_t>(slot) * kQ + qi) * 4 + cc) * (kNumHeads * 128),
-                     buf, kNumHeads * 128 * 2);
-          if (k == 4 * kQ - 1)
-            bulk_store(p.lse + static_cast<size_t>(slot) * kQ * kNumHeads, smem_u32(ms->lse_stage),
-                       kQ * kNumHeads * 4);
+          const size_t piece = static_cast<size_t>(slot) * p.slot_tokens + slot_q;  // (slot, token)
+          bulk_store(p.partial + ((piece + qi) * 4 + cc) * (kNumHeads * 128), buf, kNumHeads * 128 * 2);
+          if (k == 4 * nq - 1)
+            bulk_store(p.lse + piece * kNumHeads, smem_u32(ms->lse_stage), nq * kNumHeads * 4);
           bulk_commit();
         }
       }
@@ -1421,7 +1444,7 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ>()), 1)
   schedule_prologue<kQ>(p, ms);
   if constexpr (kGather) {
     __syncthreads();
-    if (tid == 0) write_worker_record<kQ>(p, ms);
+    if (tid == 0 && cta_sibling(p) == 0) write_worker_record<kQ>(p, ms);
   }
   tc_fence_before();
   __syncthreads();
@@ -1446,7 +1469,7 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ>()), 1)
       run_mma_pv<kQ, kFmt>(p, ms, sbase, tmem);
     } else if (warp == kMmaQkWarp && lane == 0) {
       run_mma_qk<kQ, kFmt>(p, ms, sbase, tmem);
-    } else if (!kGather && warp == kIdleWarp && lane == 0) {
+    } else if (!kGather && warp == kIdleWarp && lane == 0 && cta_sibling(p) == 0) {
       write_worker_record<kQ>(p, ms);
     }
   }
@@ -1484,7 +1507,7 @@ cudaError_t launch(const Stage1Params& p, const CUtensorMap& map_v, const CUtens
   // may be scheduled while that kernel finishes, and wait for it (griddepcontrol
   // .wait) before touching global memory.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+  cfg.gridDim = dim3(static_cast<unsigned>(p.grid * p.siblings));
   cfg.blockDim = dim3(stage1_threads<kGather, kQ>());
   cfg.dynamicSmemBytes = smem_alloc<kQ, kFmt>();
   cfg.stream = stream;
@@ -1514,7 +1537,7 @@ cudaError_t stage1_prepare(int device) {
 cudaError_t launch_stage1(const Stage1Params& p, const CUtensorMap& map_v,
                           const CUtensorMap& map_r, bool gather, bool bf16_cache,
                           cudaStream_t stream) {
-  const bool two = p.row_tokens - p.q_off >= 2;
+  const bool two = p.row_tokens - p.q_off >= 2;  // each CTA takes up to two tokens
   if (bf16_cache) {
     if (gather) return cudaErrorNotSupported;  // the host rejects this before launching
     return two ? launch<false, 2, Kv::kBf16>(p, map_v, map_r, stream)

@@ -122,21 +122,12 @@ def test_binding_refuses_cpu_tensors(lib):
 @pytest.mark.parametrize("qo_len", [1, 2, 3, 4])
 def test_plan_mtp_sizes_the_partials_by_query_tokens(lib, qo_len):
     plan = binding.mla_decode_plan(64, 8192, 152, qo_len=qo_len)
-    assert plan.qo_len == qo_len and plan.grid == plan_grid(64, 8192, 152)
-    g, nq = plan.grid, min(qo_len, 2)  # one launch's tokens
-    assert plan.ws_partial_offset >= plan.ws_lse_offset + 4 * 2 * g * nq * 16
-    assert plan.ws_bytes >= plan.ws_partial_offset + 2 * 2 * g * nq * 16 * 512
-
-
-def test_separate_stages_take_one_launch_plans_only(lib):
-    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the checks fail first
-    plan = binding.mla_decode_plan(8, 1024, 152, qo_len=3)
-    p = ctypes.byref(plan)
-    assert lib.mla_decode_stage1(fake, fake, fake, fake, fake, fake, None, p, None, 0, 4096,
-                                 fake, plan.ws_bytes) == 1
-    assert lib.mla_decode_stage1_bf16kv(fake, fake, fake, fake, fake, None, p, None, 0, 4096,
-                                        fake, plan.ws_bytes) == 1
-    assert lib.mla_decode_stage2(fake, fake, None, p, fake, plan.ws_bytes) == 1
+    # rows of three or four tokens take two sibling CTAs per worker
+    workers = plan_grid(64, 8192, 152 if qo_len <= 2 else 76)
+    assert plan.qo_len == qo_len and plan.grid == workers
+    g = plan.grid
+    assert plan.ws_partial_offset >= plan.ws_lse_offset + 4 * 2 * g * qo_len * 16
+    assert plan.ws_bytes >= plan.ws_partial_offset + 2 * 2 * g * qo_len * 16 * 512
 
 
 def test_plan_mtp_rejects_unsupported_token_counts(lib):

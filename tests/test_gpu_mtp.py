@@ -2,8 +2,8 @@
 
 Each row holds n query tokens; token i sees the row's first L - n + 1 + i
 cached tokens (the oracle's causal, end-aligned reading).  One KV tile serves
-two tokens' 16 heads (MMA N = 64); rows of three or four tokens take two
-launches (tokens 0-1, then 2-3)."""
+two tokens' 16 heads (MMA N = 64); rows of three or four tokens are shared by
+two sibling CTAs per worker (tokens 0-1 and 2-3)."""
 import numpy as np
 import pytest
 import torch
@@ -84,6 +84,27 @@ def test_three_and_four_token_decode_matches_oracle(qo_len, name, lengths, paged
     dev.out.fill_(float("nan"))
     gpu, err, plan, _ = dev.run(sms=sms)
     assert err == 0 and plan.qo_len == qo_len
+    assert_close(gpu, OracleCase(inp).reference())
+
+
+@pytest.mark.parametrize("qo_len", [3, 4])
+def test_sibling_stages_give_the_same_bits(qo_len):
+    """Rows of three or four tokens: two sibling CTAs per worker write one
+    partial slot; stage 1 + stage 2 launched separately equal the fused call."""
+    inp = make_from_lengths([300, 1000, 17, 4500, 129, 0, 2000], seed=4400 + qo_len, paged=True,
+                            qo_len=qo_len)
+    dev = DeviceCase(inp)
+    plan = binding.mla_decode_plan(inp.batch, inp.max_kv_len, 14, qo_len=qo_len)
+    assert plan.grid == 7
+    ws = binding.new_workspace(plan)
+    gpu, err, _, _ = dev.run(plan=plan, workspace=ws)
+    assert err == 0
+    out2 = torch.full_like(dev.out, float("nan"))
+    binding.mla_decode_stage1(dev.q, dev.kv_codes, dev.kv_scale, dev.qo_indptr, dev.kv_indptr,
+                              out2, plan=plan, workspace=ws, kv_indices=dev.kv_indices)
+    binding.mla_decode_stage2(dev.qo_indptr, out2, plan=plan, workspace=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(out2.float().cpu().numpy(), gpu)
     assert_close(gpu, OracleCase(inp).reference())
 
 
