@@ -53,7 +53,7 @@ struct Stage2Params {
   const uint16_t* partial;  // bf16 bits
   int32_t batch;
   int32_t grid;
-  int32_t qo_len;  // tokens per row combined by this launch (1 or 2)
+  int32_t qo_len;  // query tokens per row (1 to 4), all in one partial slot
 };
 
 size_t stage1_smem_bytes();

@@ -1,7 +1,8 @@
 // Stage 1 of the MLA forward_absorb decode step on sm_103a: split attention.
 //
 // One persistent CTA per worker of the token-balanced schedule walks its tile
-// range.  Per 128-token tile of the FP8 latent cache:
+// range (two sibling CTAs for rows of three or four query tokens, each taking
+// up to two of them).  Per 128-token tile of the latent cache:
 //   * warp 4 streams the tile once through TMA into a ring of swizzled panels
 //     (four 128-dim latent panels + one 64-dim rope panel; page-table rows are
 //     fetched with tile::gather4, the panels spread over several producer
@@ -22,8 +23,8 @@
 // e4m3: per query token the 16 "hi" and 16 "lo" heads, so N = 32 per token of
 // the row.  A bf16 cache (the pages' choice for small batches, submission
 // 722089 `_aiter_path`): bf16 Q and P operands (kind::f16), N = 16 per token,
-// and every tile moves twice the bytes.  One or two query tokens per row
-// (Geo<kQ, kFmt>).
+// and every tile moves twice the bytes.  A CTA takes one or two of the row's
+// query tokens (Geo<kQ, kFmt>).
 #include <cstddef>
 
 #include <cuda_bf16.h>
