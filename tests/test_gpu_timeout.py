@@ -5,7 +5,8 @@ load the cache, so the waits on those loads (a flag nothing sets) reach their
 time limit.  The kernel must report MLA_DERR_TIMEOUT in the workspace error
 word, return, and leave the context usable: the next call on the same
 workspace gives the right answer.  Both the contiguous and the page-table
-kernels, with one and two query tokens, are covered.
+kernels, with one, two and four query tokens (two sibling CTAs per worker),
+are covered.
 """
 import time
 
@@ -27,7 +28,8 @@ def _lib(built_library):
     binding.load_library(built_library)
 
 
-@pytest.mark.parametrize("paged,qo_len", [(False, 1), (True, 1), (False, 2), (True, 2)])
+@pytest.mark.parametrize("paged,qo_len", [(False, 1), (True, 1), (False, 2), (True, 2), (False, 4),
+                                          (True, 4)])
 def test_stalled_stream_times_out_and_the_context_survives(paged, qo_len):
     inp = make_from_lengths([700, 300, 2000, 5], seed=31, paged=paged, qo_len=qo_len)
     dev = DeviceCase(inp)
