@@ -10,6 +10,8 @@ arithmetic.
 Modules
   fp8        e4m3fn decode / encode written from the format's definition.
   quant      per-tensor absmax FP8 quantisation of the bf16 latent cache.
+  mxfp4      MXFP4 (E2M1 elements, E8M0 scale per 32) codec, block
+             quantiser and the decode step over an MXFP4 cache.
   attention  exact softmax attention over the dequantised e4m3 cache or the
              bf16 cache (float64), and the split-KV partial / log-sum-exp
              combine restated.
