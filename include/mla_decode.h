@@ -52,6 +52,8 @@ typedef enum {
 #define MLA_DERR_KV_INDPTR 2  /* kv_indptr decreases, or its end exceeds kv_rows / kv_indices_len */
 #define MLA_DERR_KV_INDEX 4   /* a page-table entry lies outside [0, kv_rows)                */
 #define MLA_DERR_TIMEOUT 8    /* a pipeline wait ran past its time limit; the call gave up  */
+#define MLA_DERR_MX_SCALE 16  /* MXFP4 cache: a block holding a nonzero element has a scale
+                                 outside the exact window of mla_decode_fwd_mxfp4 (or NaN)  */
 
 /*
  * Launch plan for a batch shape.  The split-KV schedule (flash-decoding split,
@@ -186,6 +188,37 @@ mla_status_t mla_decode_fwd_bf16kv(const void* q_bf16, const void* kv_bf16,
                                    const int32_t* kv_indices, int64_t kv_indices_len,
                                    int64_t kv_rows, void* workspace, size_t workspace_bytes);
 
+/*
+ * mla_decode_fwd_mxfp4 — the decode step over an MXFP4 latent cache, the
+ * harness's third cache format (submission 738050: `custom_kernel` docstring,
+ * `kv_data["mxfp4"]`; `_dequantize_mxfp4_inplace` docstring for the format;
+ * submission 722089 `_custom_multihead_path` / `_mla_multihead_stage1` read it).
+ * A cached row is 576 E2M1 elements (2 per byte, the even element in the low
+ * nibble: 288 bytes) and 18 E8M0 scales, one per 32 consecutive elements; its
+ * value is element * 2^(scale - 127).  K is the whole row and V its first 512
+ * values, as for mla_decode_fwd.
+ *   kv_fp4     device uint8 [kv_rows, 288], 16-byte aligned.
+ *   kv_scales  device uint8 [kv_rows, 18] (row stride 18 bytes), 16-byte aligned.
+ *   scale_bias each tile is converted in shared memory to the e4m3 codes of
+ *              element * 2^(scale - 127 - scale_bias) and attended with the
+ *              per-tensor scale 2^scale_bias: exact while every block holding a
+ *              nonzero element has scale - 127 - scale_bias in [-8, 6] (block
+ *              scales 2^-8 ... 2^6 with the bias 0, which covers blocks whose
+ *              largest magnitude lies in [2^-6, 2^9)).  A block outside that
+ *              window sets MLA_DERR_MX_SCALE; its values then saturate at
+ *              448 * 2^scale_bias or round toward zero.  |scale_bias| <= 100.
+ *   kv_rows    rows of the pool, at most 119,304,419.
+ *   The rows of the batch are contiguous in the pool (no page table, as in the
+ *   pages' MXFP4 kernel); plan->qo_len must be 1 (else MLA_ERR_UNSUPPORTED).
+ *   Every other argument, the workspace, the error word and the status codes
+ *   are those of mla_decode_fwd.
+ */
+mla_status_t mla_decode_fwd_mxfp4(const void* q_bf16, const void* kv_fp4, const void* kv_scales,
+                                  int32_t scale_bias, const int32_t* qo_indptr,
+                                  const int32_t* kv_indptr, void* out_bf16, cudaStream_t stream,
+                                  const mla_plan_t* plan, int64_t kv_rows, void* workspace,
+                                  size_t workspace_bytes);
+
 /* The two stages of mla_decode_fwd launched separately (same arguments); the
  * pair is equivalent to one mla_decode_fwd call.  Used to time stage 1 alone.
  * mla_decode_stage1_bf16kv is stage 1 of mla_decode_fwd_bf16kv; stage 2 is
@@ -200,6 +233,11 @@ mla_status_t mla_decode_stage1_bf16kv(const void* q_bf16, const void* kv_bf16,
                                       void* out_bf16, cudaStream_t stream, const mla_plan_t* plan,
                                       const int32_t* kv_indices, int64_t kv_indices_len,
                                       int64_t kv_rows, void* workspace, size_t workspace_bytes);
+mla_status_t mla_decode_stage1_mxfp4(const void* q_bf16, const void* kv_fp4, const void* kv_scales,
+                                     int32_t scale_bias, const int32_t* qo_indptr,
+                                     const int32_t* kv_indptr, void* out_bf16, cudaStream_t stream,
+                                     const mla_plan_t* plan, int64_t kv_rows, void* workspace,
+                                     size_t workspace_bytes);
 mla_status_t mla_decode_stage2(const int32_t* qo_indptr, void* out_bf16, cudaStream_t stream,
                                const mla_plan_t* plan, void* workspace, size_t workspace_bytes);
 
@@ -232,6 +270,22 @@ mla_status_t mla_decode_fwd_stall_stream(const void* q_bf16, const void* kv_fp8,
 mla_status_t mla_fp8_quantize_per_tensor(const void* src_bf16, int64_t n, void* dst_fp8,
                                          float* scale_out, void* tmp, size_t tmp_bytes,
                                          cudaStream_t stream);
+
+/*
+ * mla_mxfp4_quantize — MXFP4 quantisation of bf16 rows of 576 values (input
+ * preparation; the pages' harness supplies the cache already quantised, see
+ * mla_decode_fwd_mxfp4).  Per block of 32 consecutive values of a row: scale
+ * exponent e = floor(log2 max|x|) - 2 clamped to [-127, 127] (-127 for an
+ * all-zero block), stored as the byte e + 127; elements x / 2^e rounded to the
+ * nearest E2M1 value, ties to even, saturating at +-6 (the OCP Microscaling
+ * conversion).
+ *   src_bf16   device bf16 [rows, 576], 16-byte aligned (finite values).
+ *   dst_fp4    device uint8 [rows, 288], 16-byte aligned.
+ *   dst_scales device uint8 [rows, 18].
+ * One kernel on `stream`.
+ */
+mla_status_t mla_mxfp4_quantize(const void* src_bf16, int64_t rows, void* dst_fp4, void* dst_scales,
+                                cudaStream_t stream);
 
 /* Zero a workspace (cudaMemsetAsync of ws_bytes on `stream`). */
 mla_status_t mla_decode_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream);

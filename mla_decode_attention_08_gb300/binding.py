@@ -18,7 +18,7 @@ NUM_HEADS, QK_HEAD_DIM, V_HEAD_DIM, TILE_TOKENS = 16, 576, 512, 128
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported device", 3: "workspace too small",
           4: "CUDA call failed"}
-DERR = {1: "qo_indptr", 2: "kv_indptr", 4: "kv_index", 8: "timeout"}
+DERR = {1: "qo_indptr", 2: "kv_indptr", 4: "kv_index", 8: "timeout", 16: "mx_scale"}
 
 
 class MlaError(RuntimeError):
@@ -41,6 +41,8 @@ _VP, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c
 _PLANP = ctypes.POINTER(mla_plan_t)
 _FWD_ARGS = [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _PLANP, _VP, _I64, _I64, _VP, _SZ]
 _FWD_BF16KV_ARGS = _FWD_ARGS[:2] + _FWD_ARGS[3:]  # no kv_scale
+# q, kv_fp4, kv_scales, scale_bias, qo_indptr, kv_indptr, out, stream, plan, kv_rows, ws, ws_bytes
+_FWD_MXFP4_ARGS = [_VP, _VP, _VP, _I32, _VP, _VP, _VP, _VP, _PLANP, _I64, _VP, _SZ]
 SIGNATURES = {
     "mla_decode_plan": (ctypes.c_int, [_I32, _I32, _I32, _PLANP]),
     "mla_decode_plan_mtp": (ctypes.c_int, [_I32, _I32, _I32, _I32, _PLANP]),
@@ -50,6 +52,9 @@ SIGNATURES = {
     "mla_decode_fwd_bf16kv": (ctypes.c_int, _FWD_BF16KV_ARGS),
     "mla_decode_stage1_bf16kv": (ctypes.c_int, _FWD_BF16KV_ARGS),
     "mla_decode_fwd_static_scratch": (ctypes.c_int, _FWD_ARGS[:-2]),
+    "mla_decode_fwd_mxfp4": (ctypes.c_int, _FWD_MXFP4_ARGS),
+    "mla_decode_stage1_mxfp4": (ctypes.c_int, _FWD_MXFP4_ARGS),
+    "mla_mxfp4_quantize": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP]),
     "mla_decode_stage2": (ctypes.c_int, [_VP, _VP, _VP, _PLANP, _VP, _SZ]),
     "mla_fp8_quantize_per_tensor": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP, _SZ, _VP]),
     "mla_decode_workspace_init": (ctypes.c_int, [_VP, _SZ, _VP]),
@@ -135,6 +140,46 @@ def _fwd_bf16kv_args(q, kv_bf16, qo_indptr, kv_indptr, out, stream, plan, kv_ind
             _dev_ptr(kv_indices, "kv_indices", torch.int32),
             0 if kv_indices is None else int(kv_indices.numel()), int(kv_bf16.shape[0]),
             _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size())
+
+
+def _fwd_mxfp4_args(q, kv_fp4, kv_scales, qo_indptr, kv_indptr, out, stream, plan, workspace,
+                    scale_bias):
+    kv_fp4 = kv_fp4.reshape(kv_fp4.shape[0], -1)
+    if kv_fp4.shape[1] != QK_HEAD_DIM // 2 or kv_scales.numel() != kv_fp4.shape[0] * 18:
+        raise ValueError("kv_fp4 must be [N, 288] uint8 and kv_scales [N, 18] uint8")
+    return (_dev_ptr(q, "q", torch.bfloat16), _dev_ptr(kv_fp4, "kv_fp4", torch.uint8),
+            _dev_ptr(kv_scales, "kv_scales", torch.uint8), int(scale_bias),
+            _dev_ptr(qo_indptr, "qo_indptr", torch.int32),
+            _dev_ptr(kv_indptr, "kv_indptr", torch.int32), _dev_ptr(out, "out", torch.bfloat16),
+            _stream(stream), ctypes.byref(plan), int(kv_fp4.shape[0]),
+            _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size())
+
+
+def mla_decode_fwd_mxfp4(q, kv_fp4, kv_scales, qo_indptr, kv_indptr, out, stream=None, *, plan,
+                         workspace, scale_bias: int = 0) -> torch.Tensor:
+    """Decode step over an MXFP4 cache (elements ``[N, 288]``, scales ``[N, 18]``); returns ``out``."""
+    _check("mla_decode_fwd_mxfp4", load_library().mla_decode_fwd_mxfp4(
+        *_fwd_mxfp4_args(q, kv_fp4, kv_scales, qo_indptr, kv_indptr, out, stream, plan, workspace,
+                         scale_bias)))
+    return out
+
+
+def mla_decode_stage1_mxfp4(q, kv_fp4, kv_scales, qo_indptr, kv_indptr, out, stream=None, *,
+                            plan, workspace, scale_bias: int = 0) -> None:
+    _check("mla_decode_stage1_mxfp4", load_library().mla_decode_stage1_mxfp4(
+        *_fwd_mxfp4_args(q, kv_fp4, kv_scales, qo_indptr, kv_indptr, out, stream, plan, workspace,
+                         scale_bias)))
+
+
+def mla_mxfp4_quantize(src_bf16, dst_fp4, dst_scales, stream=None) -> None:
+    """MXFP4 of bf16 rows ``[N, 576]`` into ``dst_fp4 [N, 288]`` and ``dst_scales [N, 18]``."""
+    src = src_bf16.reshape(-1, QK_HEAD_DIM)
+    rows = int(src.shape[0])
+    if dst_fp4.numel() != rows * 288 or dst_scales.numel() != rows * 18:
+        raise ValueError("dst_fp4 must hold [N, 288] and dst_scales [N, 18] bytes")
+    _check("mla_mxfp4_quantize", load_library().mla_mxfp4_quantize(
+        _dev_ptr(src, "src_bf16", torch.bfloat16), rows, _dev_ptr(dst_fp4, "dst_fp4", torch.uint8),
+        _dev_ptr(dst_scales, "dst_scales", torch.uint8), _stream(stream)))
 
 
 def mla_decode_fwd_bf16kv(q, kv_bf16, qo_indptr, kv_indptr, out, stream=None, *, plan,

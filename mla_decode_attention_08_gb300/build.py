@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmla_decode.so")
-SOURCES = ["stage1.cu", "stage2.cu", "fp8_quant.cu", "api.cu", "static_scratch.cu"]
+SOURCES = ["stage1.cu", "stage2.cu", "fp8_quant.cu", "mxfp4_quant.cu", "api.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

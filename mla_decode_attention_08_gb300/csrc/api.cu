@@ -96,6 +96,67 @@ bool kv_maps(const void* kv, int64_t rows, bool gather, bool bf16, int device, C
   return true;
 }
 
+// MXFP4 cache: the elements [kv_rows, 288] uint8 in boxes of 128 rows, 64 bytes
+// wide (64-byte swizzle) and 32 bytes wide (32-byte swizzle), and the scale
+// bytes [kv_rows * 18] as one flat array in 256-byte boxes (zero fill past its
+// end, so a tile's boxes never read beyond the caller's array).
+bool encode_mx_maps(const void* fp4, const void* scales, int64_t rows, mla::Stage1Maps* m) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t row_bytes = kQkDim / 2;
+  const cuuint64_t gdim[2] = {row_bytes, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t gstride[1] = {row_bytes};
+  const cuuint32_t estride[2] = {1, 1};
+  const cuuint32_t box_v[2] = {64, static_cast<cuuint32_t>(kTileTokens)};
+  const cuuint32_t box_r[2] = {32, static_cast<cuuint32_t>(kTileTokens)};
+  if (fn(&m->v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(fp4), gdim, gstride, box_v,
+         estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  if (fn(&m->r, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(fp4), gdim, gstride, box_r,
+         estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const cuuint64_t sdim[1] = {static_cast<cuuint64_t>(rows) * (kQkDim / 32)};
+  // A rank-1 map has no strides, but the encoder rejects a null array.
+  const cuuint64_t sstride[1] = {16};
+  const cuuint32_t sbox[1] = {256};
+  const cuuint32_t sestride[1] = {1};
+  return fn(&m->s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, const_cast<void*>(scales), sdim, sstride,
+            sbox, sestride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct MxMapEntry {
+  const void* fp4 = nullptr;
+  const void* scales = nullptr;
+  int64_t rows = 0;
+  int device = -1;
+  mla::Stage1Maps maps;
+};
+
+bool mx_maps(const void* fp4, const void* scales, int64_t rows, int device, mla::Stage1Maps* m) {
+  constexpr int kEntries = 4;
+  thread_local MxMapEntry cache[kEntries];
+  thread_local int next = 0;
+  for (auto& e : cache) {
+    if (e.fp4 == fp4 && e.scales == scales && e.rows == rows && e.device == device) {
+      *m = e.maps;
+      return true;
+    }
+  }
+  MxMapEntry e;
+  e.fp4 = fp4;
+  e.scales = scales;
+  e.rows = rows;
+  e.device = device;
+  if (!encode_mx_maps(fp4, scales, rows, &e.maps)) return false;
+  cache[next] = e;
+  next = (next + 1) % kEntries;
+  *m = e.maps;
+  return true;
+}
+
 // Checks the current device is an sm_103 part and sets the kernels' shared
 // memory limit once per device.
 mla_status_t prepare_device(int* device_out) {
@@ -153,22 +214,35 @@ mla::Stage2Params stage2_params(const int32_t* qo_indptr, void* out, const mla_p
   return s;
 }
 
-// kv_scale is required for an e4m3 cache and ignored for a bf16 one.
+// The largest MXFP4 pool: the kernel addresses the flat scale array (18 bytes a
+// row) with 32-bit box coordinates.
+constexpr int64_t kMaxMxRows = (INT32_MAX - 4096) / (kQkDim / 32);
+
+// kv_scale is required for an e4m3 cache and ignored for the others; an MXFP4
+// cache passes its elements as kv, its scale bytes as mx_scales and the bias.
 mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
                         const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
                         cudaStream_t stream, const mla_plan_t* plan, const int32_t* kv_indices,
                         int64_t kv_indices_len, int64_t kv_rows, void* workspace,
-                        size_t workspace_bytes, bool bf16_cache, bool stall_stream = false) {
+                        size_t workspace_bytes, mla::CacheFormat fmt, bool stall_stream = false,
+                        const void* mx_scales = nullptr, int32_t mx_bias = 0) {
+  using mla::CacheFormat;
   mla_status_t st = check_plan(plan);
   if (st != MLA_OK) return st;
-  if (q == nullptr || kv == nullptr || (kv_scale == nullptr && !bf16_cache) ||
-      qo_indptr == nullptr || kv_indptr == nullptr || out == nullptr)
+  if (q == nullptr || kv == nullptr || (kv_scale == nullptr && fmt == CacheFormat::kE4m3) ||
+      (mx_scales == nullptr && fmt == CacheFormat::kMxfp4) || qo_indptr == nullptr ||
+      kv_indptr == nullptr || out == nullptr)
     return MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16)) return MLA_ERR_INVALID_ARG;
   if (kv_rows < 1 || kv_rows > INT32_MAX) return MLA_ERR_INVALID_ARG;
   if (kv_indices != nullptr && (kv_indices_len < 0 || kv_indices_len > INT32_MAX))
     return MLA_ERR_INVALID_ARG;
-  if (bf16_cache && kv_indices != nullptr) return MLA_ERR_UNSUPPORTED;
+  if (fmt != CacheFormat::kE4m3 && kv_indices != nullptr) return MLA_ERR_UNSUPPORTED;
+  if (fmt == CacheFormat::kMxfp4) {
+    if (kv_rows > kMaxMxRows || mx_bias < -100 || mx_bias > 100 || !aligned(mx_scales, 16))
+      return MLA_ERR_INVALID_ARG;
+    if (plan->qo_len != 1) return MLA_ERR_UNSUPPORTED;
+  }
   st = check_workspace(plan, workspace, workspace_bytes);
   if (st != MLA_OK) return st;
   int device = 0;
@@ -176,13 +250,19 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
   if (st != MLA_OK) return st;
 
   const bool gather = kv_indices != nullptr;
-  CUtensorMap map_v, map_r;
-  if (!kv_maps(kv, kv_rows, gather, bf16_cache, device, &map_v, &map_r)) return MLA_ERR_CUDA;
+  mla::Stage1Maps maps;
+  if (fmt == CacheFormat::kMxfp4) {
+    if (!mx_maps(kv, mx_scales, kv_rows, device, &maps)) return MLA_ERR_CUDA;
+  } else {
+    if (!kv_maps(kv, kv_rows, gather, fmt == CacheFormat::kBf16, device, &maps.v, &maps.r))
+      return MLA_ERR_CUDA;
+    maps.s = maps.v;
+  }
 
   auto* ws = static_cast<uint8_t*>(workspace);
   mla::Stage1Params p;
   p.q = static_cast<const uint16_t*>(q);
-  p.kv_scale = bf16_cache ? nullptr : kv_scale;
+  p.kv_scale = fmt == CacheFormat::kE4m3 ? kv_scale : nullptr;
   p.qo_indptr = qo_indptr;
   p.kv_indptr = kv_indptr;
   p.kv_indices = kv_indices;
@@ -201,7 +281,8 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
   p.siblings = siblings_of(plan);
   p.slot_tokens = plan->qo_len;
   p.stall_stream = stall_stream ? 1 : 0;
-  return mla::launch_stage1(p, map_v, map_r, gather, bf16_cache, stream) == cudaSuccess
+  p.mx_bias = mx_bias;
+  return mla::launch_stage1(p, maps, gather, fmt, stream) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
 }
@@ -219,10 +300,11 @@ mla_status_t run_decode(const void* q, const void* kv, const float* kv_scale,
                         const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
                         cudaStream_t stream, const mla_plan_t* plan, const int32_t* kv_indices,
                         int64_t kv_indices_len, int64_t kv_rows, void* workspace,
-                        size_t workspace_bytes, bool bf16_cache, bool stall_stream = false) {
+                        size_t workspace_bytes, mla::CacheFormat fmt, bool stall_stream = false,
+                        const void* mx_scales = nullptr, int32_t mx_bias = 0) {
   mla_status_t st = run_stage1(q, kv, kv_scale, qo_indptr, kv_indptr, out, stream, plan,
                                kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes,
-                               bf16_cache, stall_stream);
+                               fmt, stall_stream, mx_scales, mx_bias);
   if (st == MLA_OK) st = run_stage2(qo_indptr, out, stream, plan, workspace, true);
   return st;
 }
@@ -293,7 +375,8 @@ mla_status_t mla_decode_stage1(const void* q_bf16, const void* kv_fp8, const flo
                                const int32_t* kv_indices, int64_t kv_indices_len, int64_t kv_rows,
                                void* workspace, size_t workspace_bytes) {
   return run_stage1(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream, plan,
-                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, false);
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes,
+                    mla::CacheFormat::kE4m3);
 }
 
 mla_status_t mla_decode_stage1_bf16kv(const void* q_bf16, const void* kv_bf16,
@@ -302,7 +385,8 @@ mla_status_t mla_decode_stage1_bf16kv(const void* q_bf16, const void* kv_bf16,
                                       const int32_t* kv_indices, int64_t kv_indices_len,
                                       int64_t kv_rows, void* workspace, size_t workspace_bytes) {
   return run_stage1(q_bf16, kv_bf16, nullptr, qo_indptr, kv_indptr, out_bf16, stream, plan,
-                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, true);
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes,
+                    mla::CacheFormat::kBf16);
 }
 
 mla_status_t mla_decode_stage2(const int32_t* qo_indptr, void* out_bf16, cudaStream_t stream,
@@ -322,7 +406,8 @@ mla_status_t mla_decode_fwd(const void* q_bf16, const void* kv_fp8, const float*
                             const int32_t* kv_indices, int64_t kv_indices_len, int64_t kv_rows,
                             void* workspace, size_t workspace_bytes) {
   return run_decode(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream, plan,
-                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, false);
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes,
+                    mla::CacheFormat::kE4m3);
 }
 
 mla_status_t mla_decode_fwd_bf16kv(const void* q_bf16, const void* kv_bf16,
@@ -331,7 +416,8 @@ mla_status_t mla_decode_fwd_bf16kv(const void* q_bf16, const void* kv_bf16,
                                    const int32_t* kv_indices, int64_t kv_indices_len,
                                    int64_t kv_rows, void* workspace, size_t workspace_bytes) {
   return run_decode(q_bf16, kv_bf16, nullptr, qo_indptr, kv_indptr, out_bf16, stream, plan,
-                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, true);
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes,
+                    mla::CacheFormat::kBf16);
 }
 
 mla_status_t mla_decode_fwd_stall_stream(const void* q_bf16, const void* kv_fp8,
@@ -341,7 +427,43 @@ mla_status_t mla_decode_fwd_stall_stream(const void* q_bf16, const void* kv_fp8,
                                          const int32_t* kv_indices, int64_t kv_indices_len,
                                          int64_t kv_rows, void* workspace, size_t workspace_bytes) {
   return run_decode(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream, plan,
-                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes, false, true);
+                    kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes,
+                    mla::CacheFormat::kE4m3, true);
+}
+
+mla_status_t mla_decode_fwd_mxfp4(const void* q_bf16, const void* kv_fp4, const void* kv_scales,
+                                  int32_t scale_bias, const int32_t* qo_indptr,
+                                  const int32_t* kv_indptr, void* out_bf16, cudaStream_t stream,
+                                  const mla_plan_t* plan, int64_t kv_rows, void* workspace,
+                                  size_t workspace_bytes) {
+  return run_decode(q_bf16, kv_fp4, nullptr, qo_indptr, kv_indptr, out_bf16, stream, plan, nullptr,
+                    0, kv_rows, workspace, workspace_bytes, mla::CacheFormat::kMxfp4, false,
+                    kv_scales, scale_bias);
+}
+
+mla_status_t mla_decode_stage1_mxfp4(const void* q_bf16, const void* kv_fp4, const void* kv_scales,
+                                     int32_t scale_bias, const int32_t* qo_indptr,
+                                     const int32_t* kv_indptr, void* out_bf16, cudaStream_t stream,
+                                     const mla_plan_t* plan, int64_t kv_rows, void* workspace,
+                                     size_t workspace_bytes) {
+  return run_stage1(q_bf16, kv_fp4, nullptr, qo_indptr, kv_indptr, out_bf16, stream, plan, nullptr,
+                    0, kv_rows, workspace, workspace_bytes, mla::CacheFormat::kMxfp4, false,
+                    kv_scales, scale_bias);
+}
+
+mla_status_t mla_mxfp4_quantize(const void* src_bf16, int64_t rows, void* dst_fp4, void* dst_scales,
+                                cudaStream_t stream) {
+  if (src_bf16 == nullptr || dst_fp4 == nullptr || dst_scales == nullptr || rows < 1 ||
+      rows > (INT64_C(1) << 36) || !aligned(src_bf16, 16) || !aligned(dst_fp4, 16))
+    return MLA_ERR_INVALID_ARG;
+  int device = 0;
+  mla_status_t st = prepare_device(&device);
+  if (st != MLA_OK) return st;
+  return mla::launch_mxfp4_quantize(static_cast<const uint16_t*>(src_bf16), rows,
+                                    static_cast<uint8_t*>(dst_fp4),
+                                    static_cast<uint8_t*>(dst_scales), stream) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 mla_status_t mla_fp8_quantize_per_tensor(const void* src_bf16, int64_t n, void* dst_fp8,

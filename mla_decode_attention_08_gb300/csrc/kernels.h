@@ -40,6 +40,16 @@ struct Stage1Params {
                               // launch handles, all siblings together)
   int32_t stall_stream;       // test hook: the producers issue no cache loads, so the
                               // pipeline waits run out (bounded) and the call gives up
+  int32_t mx_bias;            // MXFP4 cache: e4m3 panels hold e2m1 * 2^(e - 127 - mx_bias)
+};
+
+enum class CacheFormat { kE4m3, kBf16, kMxfp4 };
+
+// TMA descriptors of one call: the cache's latent and rope boxes (e4m3: 128-
+// and 64-byte wide; bf16: both 64 dims; MXFP4 elements: 64 and 32 bytes) and,
+// for an MXFP4 cache, the flat scale array in 256-byte boxes (else a copy of v).
+struct Stage1Maps {
+  CUtensorMap v, r, s;
 };
 
 struct Stage2Params {
@@ -58,12 +68,11 @@ struct Stage2Params {
 
 size_t stage1_smem_bytes();
 cudaError_t stage1_prepare(int device);  // sets the dynamic shared memory limit once
-// map_v / map_r: the cache's latent and rope boxes (e4m3: 128- and 64-byte
-// wide; bf16: both 64 dims); bf16_cache selects the bf16-cache kernels.
-cudaError_t launch_stage1(const Stage1Params& p, const CUtensorMap& map_v,
-                          const CUtensorMap& map_r, bool gather, bool bf16_cache,
-                          cudaStream_t stream);
+cudaError_t launch_stage1(const Stage1Params& p, const Stage1Maps& maps, bool gather,
+                          CacheFormat format, cudaStream_t stream);
 cudaError_t launch_stage2(const Stage2Params& p, bool programmatic, cudaStream_t stream);
+cudaError_t launch_mxfp4_quantize(const uint16_t* src, int64_t rows, uint8_t* dst, uint8_t* scales,
+                                  cudaStream_t stream);
 cudaError_t launch_fp8_quantize(const uint16_t* src, int64_t n, uint8_t* dst, float* scale_out,
                                 uint32_t* amax_bits, cudaStream_t stream);
 

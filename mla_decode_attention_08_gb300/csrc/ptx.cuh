@@ -124,6 +124,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar) : "memory");
 }
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2}], [%3];"
+      ::"r"(dst), "l"(map), "r"(x), "r"(bar) : "memory");
+}
 // Four rows y0..y3 of width box[0] at column x, stored consecutively at dst.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int32_t x,
                                             int32_t y0, int32_t y1, int32_t y2, int32_t y3,

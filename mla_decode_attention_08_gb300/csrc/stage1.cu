@@ -23,8 +23,13 @@
 // e4m3: per query token the 16 "hi" and 16 "lo" heads, so N = 32 per token of
 // the row.  A bf16 cache (the pages' choice for small batches, submission
 // 722089 `_aiter_path`): bf16 Q and P operands (kind::f16), N = 16 per token,
-// and every tile moves twice the bytes.  A CTA takes one or two of the row's
-// query tokens (Geo<kQ, kFmt>).
+// and every tile moves twice the bytes.  An MXFP4 cache (submission 738050,
+// `_dequantize_mxfp4_inplace`; submission 722089 `_mla_multihead_stage1`):
+// E2M1 elements with one E8M0 scale per 32; the tile streams in at 306 bytes a
+// token and four converter warps rewrite each panel in place as the e4m3 panel
+// the e4m3 path reads (exact while the block scales stay in a 15-binade
+// window), so the MMAs and the softmax are the e4m3 ones.  A CTA takes one or
+// two of the row's query tokens (Geo<kQ, kFmt>); an MXFP4 cache takes one.
 #include <cstddef>
 
 #include <cuda_bf16.h>
@@ -46,7 +51,17 @@ constexpr int kMaxQ = 2;          // query tokens per row handled by one CTA til
 constexpr int kMaxVSlots = 11;    // latent ring slots (e4m3, kQ = 1)
 
 // Latent cache formats.
-enum class Kv { kE4m3, kBf16 };
+enum class Kv { kE4m3, kBf16, kMx4 };
+
+// MXFP4 cache: each tile's 128 x 18 scale bytes land, by ten 256-byte boxes of
+// the flat scale array starting at the 16-byte boundary at or below the tile's
+// first byte, in one of four scale slots.
+constexpr int kNumSclSlots = 4;
+constexpr int kSclBoxes = 10;
+constexpr int kSclSlotBytes = 256 * kSclBoxes;
+static_assert(kSclSlotBytes >= 15 + kTileTokens * 18, "a tile's scale bytes fit a slot");
+constexpr int kConverterWarps = 4;
+constexpr int kFirstConverterWarp = 8;
 
 // Everything that depends on the cache format and on the number kQ of query
 // tokens per row.  The MMA N dimension holds, for each query token, the 16
@@ -55,7 +70,9 @@ enum class Kv { kE4m3, kBf16 };
 template <int kQ, Kv kFmt>
 struct Geo {
   static_assert(kQ == 1 || kQ == 2, "one or two query tokens per row");
-  static constexpr bool kSplit = kFmt == Kv::kE4m3;  // two-term Q and P operands
+  static_assert(kFmt != Kv::kMx4 || kQ == 1, "an MXFP4 cache takes one query token per row");
+  static constexpr bool kMx = kFmt == Kv::kMx4;        // elements converted in shared memory
+  static constexpr bool kSplit = kFmt != Kv::kBf16;  // two-term Q and P operands
   static constexpr int kElem = kSplit ? 1 : 2;         // bytes per cache / operand element
   static constexpr int kTokCols = kSplit ? 32 : 16;    // operand columns per query token
   static constexpr int kN = kTokCols * kQ;             // MMA N / operand rows of Q and P
@@ -64,7 +81,7 @@ struct Geo {
   // 64 bf16 dims, so a bf16 latent slot is two panels 16 KB apart.
   static constexpr int kVSlotBytes = 128 * 128 * kElem;
   static constexpr int kRSlotBytes = 128 * 64 * kElem;
-  static constexpr int kNumV = kSplit ? (kQ == 1 ? 11 : 9) : (kQ == 1 ? 5 : 4);
+  static constexpr int kNumV = kMx ? 10 : (kSplit ? (kQ == 1 ? 11 : 9) : (kQ == 1 ? 5 : 4));
   static constexpr int kPanelDims = 128 / kElem;
   // Q operand: kN rows; the 512 latent dims in 128-byte-wide panels, the 64
   // rope dims in one more (64 bytes wide, swizzle 64B, for e4m3; 128 for bf16).
@@ -82,7 +99,12 @@ struct Geo {
   static constexpr int kOffQ = kOffR + kNumRSlots * kRSlotBytes;
   static constexpr int kOffQRope = kOffQ + kQLatentPanels * kQPanelBytes;
   static constexpr int kOffP = kOffQRope + kQRopeBytes;
-  static constexpr int kOffMisc = kOffP + 2 * kPBytes;
+  static constexpr int kOffScl = kOffP + 2 * kPBytes;  // MXFP4 scale slots
+  static constexpr int kOffMisc = kOffScl + (kMx ? kNumSclSlots * kSclSlotBytes : 0);
+  // MXFP4: a panel's elements land in the upper half of its slot (a latent row
+  // is 64 bytes of elements, a rope row 32), below the e4m3 panel they become.
+  static constexpr int kVRawOff = kVSlotBytes / 2;
+  static constexpr int kRRawOff = kRSlotBytes / 2;
   static_assert(kOffP - kOffQ >= kQ * kNumHeads * kVDim * 2, "the Q region stages a bf16 output row");
 
   // TMEM columns: two S buffers (kN each) then O (4 chunks x kN).
@@ -109,6 +131,8 @@ struct Misc {
   uint64_t v_full[kMaxVSlots];
   uint64_t v_empty[kMaxVSlots];
   uint64_t r_full[kNumRSlots];
+  uint64_t raw_full[kMaxVSlots];   // MXFP4: a latent panel's elements landed
+  uint64_t rraw_full[kNumRSlots];  // MXFP4: a rope panel's elements and its tile's scales landed
   uint64_t s_full[2];   // QK of tile i landed in S[i & 1]
   uint64_t pv_done[2];  // PV of tile i completed (P[i & 1] free again)
   uint64_t q_empty;     // the segment's last QK completed (Q operand free)
@@ -153,7 +177,7 @@ constexpr bool geo_fits() {
   return G::kOffMisc % 16 == 0 && smem_alloc<kQ, kFmt>() <= 232448 && G::kNumV <= kMaxVSlots;
 }
 static_assert(geo_fits<1, Kv::kE4m3>() && geo_fits<2, Kv::kE4m3>() && geo_fits<1, Kv::kBf16>() &&
-                  geo_fits<2, Kv::kBf16>(),
+                  geo_fits<2, Kv::kBf16>() && geo_fits<1, Kv::kMx4>(),
               "stage-1 shared memory: per-CTA limit, 16-byte aligned barrier block, ring slots");
 
 constexpr int kSoftmaxThreads = 128;
@@ -163,16 +187,18 @@ constexpr int kMmaQkWarp = 6;  // QK issuer
 constexpr int kIdleWarp = 7;   // contiguous rows: writes the worker record for stage 2
 constexpr uint32_t kBarSoftmax = 1;  // named barrier id of warps 0-3
 constexpr uint32_t kBarProducers = 2;  // named barrier id of the page-table producers
+constexpr uint32_t kBarConverters = 3;  // named barrier id of the MXFP4 converter warps
 // Page-table mode with one query token: 12 warps, six producer warps (4, 7,
 // 8, 9, 10, 11) taking panels round-robin; the softmax warpgroup gets 240
 // registers and the other two 128 (launched with 168 each: 128 x 240 + 256 x 128
 // <= 384 x 168).
 // With two query tokens the softmax needs more than 240 registers, so that
 // kernel keeps 8 warps and two producers (warps 4 and 7).
-template <bool kGather, int kQ>
-__host__ __device__ constexpr bool wide_gather() { return kGather && kQ == 1; }
-template <bool kGather, int kQ>
-__host__ __device__ constexpr int stage1_threads() { return wide_gather<kGather, kQ>() ? kStage1ThreadsGather : kStage1Threads; }
+// An MXFP4 cache also runs 12 warps: warps 8-11 convert its panels.
+template <bool kGather, int kQ, Kv kFmt>
+__host__ __device__ constexpr bool wide_block() { return (kGather && kQ == 1) || kFmt == Kv::kMx4; }
+template <bool kGather, int kQ, Kv kFmt>
+__host__ __device__ constexpr int stage1_threads() { return wide_block<kGather, kQ, kFmt>() ? kStage1ThreadsGather : kStage1Threads; }
 template <bool kGather, int kQ>
 __host__ __device__ constexpr uint32_t num_producers() { return !kGather ? 1 : (kQ == 1 ? 6 : 2); }
 // Producer index of a warp in page-table mode (warps 4, 7, 8, ...), or -1.
@@ -624,11 +650,216 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
   }
 }
 
+// ------------------------------------------------------------ MXFP4 cache (warp 4 producer, warps 8-11 converters)
+// Producer (lane 0 of warp 4; contiguous rows only).  Per tile: the rope
+// panel's elements (32 bytes a row, 32-byte swizzle) into the upper half of its
+// rope slot together with the tile's scale bytes (scale slot tile % 4), then
+// each latent panel's elements (64 bytes a row, 64-byte swizzle) into the upper
+// half of its latent slot.  A slot is refilled only after the MMAs consumed the
+// e4m3 panel converted from its previous fill (which the converters read before
+// writing it), exactly as for the e4m3 cache; a scale slot is refilled four
+// tiles later, after the QK of two tiles later, so the converters have long
+// finished with it.
+template <int kQ>
+__device__ void run_producer_mx(const Stage1Params& p, const CUtensorMap* map_v,
+                                const CUtensorMap* map_r, const CUtensorMap* map_s, Misc* ms,
+                                uint32_t sbase) {
+  using G = Geo<kQ, Kv::kMx4>;
+  if ((threadIdx.x & 31) != 0) return;
+  Cursor cur;
+  cursor_start(cur, ms);
+  uint32_t tile = 0;
+  uint32_t v_fills = 0, r_fills = 0;  // latent / rope panels issued
+  bool ok = true;
+  while (cur.live && ok) {
+    const int32_t tok0 = cur.kb + cur.j * kTileTokens;
+    {
+      const uint32_t slot = tile % kNumRSlots, use = tile / kNumRSlots;
+      if (use > 0) ok = wait_phase(smem_u32(&ms->s_full[slot]), (use - 1) & 1, ms, p.err);
+      if (!ok) break;
+      const uint32_t full = smem_u32(&ms->rraw_full[slot]);
+      mbar_arrive_expect_tx(full, kTileTokens * 32 + kSclSlotBytes);
+      tma_load_2d(sbase + G::kOffR + slot * G::kRSlotBytes + G::kRRawOff, map_r, kVDim / 2, tok0,
+                  full);
+      const uint32_t sdst = sbase + G::kOffScl + (tile % kNumSclSlots) * kSclSlotBytes;
+      const int32_t x0 = (18 * tok0) & ~15;  // the host bounds 18 * kv_rows well below 2^31
+#pragma unroll 1
+      for (int i = 0; i < kSclBoxes; ++i) tma_load_1d(sdst + 256 * i, map_s, x0 + 256 * i, full);
+      r_fills = tile + 1;
+    }
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t g = tile * 4 + c, slot = g % G::kNumV, use = g / G::kNumV;
+      if (use > 0) ok = wait_phase(smem_u32(&ms->v_empty[slot]), (use - 1) & 1, ms, p.err);
+      if (!ok) break;
+      const uint32_t full = smem_u32(&ms->raw_full[slot]);
+      mbar_arrive_expect_tx(full, kTileTokens * 64);
+      tma_load_2d(sbase + G::kOffV + slot * G::kVSlotBytes + G::kVRawOff, map_v, 64 * c, tok0, full);
+      v_fills = g + 1;
+    }
+    if (!ok) break;
+    ++tile;
+    if (!cursor_next_tile(cur, ms, p.kv_indptr, p.batch)) break;
+  }
+  if (!ms->abort_flag) return;
+  // An abandoned call: only the last fill of each slot can still be in flight.
+  for (uint32_t n = 0; n < static_cast<uint32_t>(G::kNumV) && n < v_fills; ++n) {
+    const uint32_t g = v_fills - 1 - n;
+    drain_phase(smem_u32(&ms->raw_full[g % G::kNumV]), (g / G::kNumV) & 1);
+  }
+  for (uint32_t n = 0; n < static_cast<uint32_t>(kNumRSlots) && n < r_fills; ++n) {
+    const uint32_t t = r_fills - 1 - n;
+    drain_phase(smem_u32(&ms->rraw_full[t % kNumRSlots]), (t / kNumRSlots) & 1);
+  }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Eight E2M1 elements (a 32-bit word, element 0 in the low nibble) times the
+// power of two f2 (a half2 pair) -> eight e4m3 codes (element 0 in the low byte).
+// Both conversions are the hardware's; the product is exact in half precision.
+__device__ __forceinline__ uint2 e2m1x8_to_e4m3x8(uint32_t w, uint32_t f2) {
+  uint32_t h0, h1, h2, h3;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3) : "r"(w));
+  asm("mul.rn.f16x2 %0, %0, %4;\n mul.rn.f16x2 %1, %1, %4;\n"
+      " mul.rn.f16x2 %2, %2, %4;\n mul.rn.f16x2 %3, %3, %4;"
+      : "+r"(h0), "+r"(h1), "+r"(h2), "+r"(h3) : "r"(f2));
+  const uint32_t e0 = cvt_f16x2_to_e4m3x2(h0), e1 = cvt_f16x2_to_e4m3x2(h1);
+  const uint32_t e2 = cvt_f16x2_to_e4m3x2(h2), e3 = cvt_f16x2_to_e4m3x2(h3);
+  return make_uint2(e0 | (e1 << 16), e2 | (e3 << 16));
+}
+
+// One 32-element block (16 bytes of elements, scale byte sb) -> 32 e4m3 codes
+// e2m1 * 2^(sb - 127 - bias), stored as 16-byte chunks at a0 and a1.  Exact
+// while the shift lies in [-8, 6]: e2m1 magnitudes 0.5 ... 6 times 2^shift then
+// lie on the e4m3 grid (2^-9 ... 384).  Outside it (or for the NaN scale 0xFF)
+// a block holding a nonzero element raises *bad; the codes then saturate at 448
+// or round toward zero (a shift below -14 rounds every element to zero, as the
+// exact value would).
+__device__ __forceinline__ void mx_block_store(uint4 raw, uint32_t sb, int32_t bias, uint32_t a0,
+                                               uint32_t a1, int32_t& bad) {
+  const int32_t shift = static_cast<int32_t>(sb) - 127 - bias;
+  if ((shift < -8 || shift > 6) && (raw.x | raw.y | raw.z | raw.w) != 0) bad = 1;
+  const uint32_t f = static_cast<uint32_t>(min(max(shift, -14), 15) + 15) << 10;  // half 2^shift
+  const uint32_t f2 = f | (f << 16);
+  const uint2 c0 = e2m1x8_to_e4m3x8(raw.x, f2), c1 = e2m1x8_to_e4m3x8(raw.y, f2);
+  const uint2 c2 = e2m1x8_to_e4m3x8(raw.z, f2), c3 = e2m1x8_to_e4m3x8(raw.w, f2);
+  st_shared_v4(a0, c0.x, c0.y, c1.x, c1.y);
+  st_shared_v4(a1, c2.x, c2.y, c3.x, c3.y);
+}
+
+// Named-barrier arrival of the converter warps that also ORs a predicate.
+__device__ __forceinline__ bool converters_bar_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; bar.red.or.pred po, %2, %3, pi;"
+      " selp.u32 %0, 1, 0, po; }"
+      : "=r"(r) : "r"(static_cast<uint32_t>(v)), "r"(kBarConverters), "r"(kConverterWarps * 32)
+      : "memory");
+  return r != 0;
+}
+
+// Converters (warps 8-11): thread i owns row (token) i of every panel.  For each
+// panel, in fill order: wait for its elements (and, with the rope panel, read the
+// token's 18 scale bytes), load the row's elements, then meet the other
+// converters (the vote also ends the call for all of them together when a wait
+// gave up); only then write the e4m3 row over the slot, in the swizzled layouts
+// the e4m3 cache's TMA boxes produce (latent rows 128 bytes, 128-byte swizzle;
+// rope rows 64 bytes, 64-byte swizzle), and arrive, one lane per warp, on the
+// panel's full barrier that the QK issuer waits on.
+template <int kQ>
+__device__ void run_converter(const Stage1Params& p, Misc* ms, uint32_t sbase) {
+  using G = Geo<kQ, Kv::kMx4>;
+  const int i = static_cast<int>(threadIdx.x) - kFirstConverterWarp * 32;
+  const int lane = threadIdx.x & 31;
+  const int32_t bias = p.mx_bias;
+  Cursor cur;
+  cursor_start(cur, ms);
+  uint32_t tile = 0;
+  int32_t bad = 0;
+  bool stop = !cur.live;
+  while (!stop) {
+    const int32_t tok0 = cur.kb + cur.j * kTileTokens;
+    const uint32_t rslot = tile % kNumRSlots;
+    const uint32_t rs = sbase + G::kOffR + rslot * G::kRSlotBytes;
+    bool ok = wait_phase(smem_u32(&ms->rraw_full[rslot]), (tile / kNumRSlots) & 1, ms, p.err);
+    uint32_t sc[9];  // the token's scale bytes: blocks 2k and 2k + 1 in sc[k]
+    uint4 rr[2];
+    if (ok) {
+      const uint32_t sb = sbase + G::kOffScl + (tile % kNumSclSlots) * kSclSlotBytes +
+                          ((18 * tok0) & 15) + 18 * i;
+#pragma unroll
+      for (int k = 0; k < 9; ++k) sc[k] = ld_shared_u16(sb + 2 * k);
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        rr[j] = ld_shared_v4(rs + G::kRRawOff + 32 * i + 16 * (j ^ ((i >> 2) & 1)));
+    }
+    if (converters_bar_or(!ok)) break;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {  // rope dims 512 + 32 j ... (blocks 16, 17)
+      const uint32_t k0 = 2 * j, k1 = 2 * j + 1, sw = (i >> 1) & 3;
+      mx_block_store(rr[j], (sc[8] >> (8 * j)) & 0xFFu, bias, rs + 64 * i + 16 * (k0 ^ sw),
+                     rs + 64 * i + 16 * (k1 ^ sw), bad);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ms->r_full[rslot]));
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t g = tile * 4 + c, slot = g % G::kNumV;
+      const uint32_t vs = sbase + G::kOffV + slot * G::kVSlotBytes;
+      ok = wait_phase(smem_u32(&ms->raw_full[slot]), (g / G::kNumV) & 1, ms, p.err);
+      uint4 lr[4];
+      if (ok) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          lr[j] = ld_shared_v4(vs + G::kVRawOff + 64 * i + 16 * (j ^ ((i >> 1) & 3)));
+      }
+      if (converters_bar_or(!ok)) {
+        stop = true;
+        break;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // dims 128 c + 32 j ... (block 4 c + j)
+        const int blk = 4 * c + j;
+        const uint32_t k0 = 2 * j, k1 = 2 * j + 1, sw = i & 7;
+        mx_block_store(lr[j], (sc[blk >> 1] >> (8 * (blk & 1))) & 0xFFu, bias,
+                       vs + 128 * i + 16 * (k0 ^ sw), vs + 128 * i + 16 * (k1 ^ sw), bad);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ms->v_full[slot]));
+    }
+    if (stop) break;
+    ++tile;
+    stop = !cursor_next_tile(cur, ms, p.kv_indptr, p.batch);
+  }
+  if (bad) set_error(p.err, MLA_DERR_MX_SCALE);
+}
+
 // ------------------------------------------------------------ MMA issuers (warp 6: QK, warp 5: PV; lane 0)
 template <Kv kFmt>
 __device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                      uint32_t accumulate) {
-  if constexpr (kFmt == Kv::kE4m3)
+  if constexpr (kFmt != Kv::kBf16)
     umma_f8(d, a, b, idesc, accumulate);
   else
     umma_f16(d, a, b, idesc, accumulate);
@@ -838,11 +1069,6 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
   const __nv_bfloat16 h = __float2bfloat16_rn(x);
   return *reinterpret_cast<const uint16_t*>(&h);
 }
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d) : "memory");
-}
 
 // Two-term e4m3 split of 16 floats x (|x| <= 448): hi = e4m3(x), lo = e4m3(16 (x - hi)),
 // so x ~= hi + lo / 16 with about 8 significant bits.  Packs codes 4 per word.
@@ -1029,7 +1255,7 @@ __device__ __forceinline__ void split_p_16(const float (&x)[16], uint32_t (&hi)[
 // operands one column per head.
 template <Kv kFmt>
 __device__ __forceinline__ void tmem_ld_heads(uint32_t addr, float (&v)[16]) {
-  if constexpr (kFmt == Kv::kE4m3) {
+  if constexpr (kFmt != Kv::kBf16) {
     uint32_t r[32];
     tmem_ld32(addr, r);
     tmem_wait_ld();
@@ -1404,9 +1630,10 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
 
 // ------------------------------------------------------------ kernel
 template <bool kGather, int kQ, Kv kFmt>
-__global__ void __launch_bounds__((stage1_threads<kGather, kQ>()), 1)
+__global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
     mla_decode_stage1_kernel(const __grid_constant__ CUtensorMap map_v,
-                             const __grid_constant__ CUtensorMap map_r, const Stage1Params p) {
+                             const __grid_constant__ CUtensorMap map_r,
+                             const __grid_constant__ CUtensorMap map_s, const Stage1Params p) {
   using G = Geo<kQ, kFmt>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1417,11 +1644,18 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ>()), 1)
 
   if (warp == kMmaWarp) tmem_alloc(smem_u32(&ms->tmem_base), G::kTmemCols);
   if (tid == kProducerWarp * 32) {
+    // The e4m3 panels are complete when their copy lands, or (MXFP4) when
+    // every converter warp has written its rows.
+    constexpr uint32_t kFullArrivals = G::kMx ? kConverterWarps : 1;
     for (int s = 0; s < G::kNumV; ++s) {
-      mbar_init(smem_u32(&ms->v_full[s]), 1);
+      mbar_init(smem_u32(&ms->v_full[s]), kFullArrivals);
       mbar_init(smem_u32(&ms->v_empty[s]), 1);
+      if (G::kMx) mbar_init(smem_u32(&ms->raw_full[s]), 1);
     }
-    for (int s = 0; s < kNumRSlots; ++s) mbar_init(smem_u32(&ms->r_full[s]), 1);
+    for (int s = 0; s < kNumRSlots; ++s) {
+      mbar_init(smem_u32(&ms->r_full[s]), kFullArrivals);
+      if (G::kMx) mbar_init(smem_u32(&ms->rraw_full[s]), 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ms->s_full[i]), 1);
       mbar_init(smem_u32(&ms->pv_done[i]), 1);
@@ -1433,6 +1667,7 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ>()), 1)
     fence_mbar_init();
     prefetch_tensormap(&map_v);
     prefetch_tensormap(&map_r);
+    if (G::kMx) prefetch_tensormap(&map_s);
   }
   // Launched as a programmatic dependent, this grid may start while the
   // previous kernel of the stream is finishing: everything above touches only
@@ -1452,20 +1687,28 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ>()), 1)
   tc_fence_after();
   const uint32_t tmem = ms->tmem_base;
 
-  // Page-table mode runs 12 warps: registers move from the producers and MMA
-  // issuers to the softmax warpgroup, inside the role branches so that each
-  // role's code is compiled under its own count.
-  constexpr bool kWide = wide_gather<kGather, kQ>();
+  // Page-table mode and the MXFP4 cache run 12 warps: registers move from the
+  // producers, MMA issuers and converters to the softmax warpgroup, inside the
+  // role branches so that each role's code is compiled under its own count.
+  // An MXFP4 cache's e4m3 panels hold e2m1 * 2^(e - 127 - bias): its scale is
+  // 2^bias.
+  constexpr bool kWide = wide_block<kGather, kQ, kFmt>();
   if (warp < 4) {
     if constexpr (kWide) setmaxnreg_inc<kSoftmaxRegs>();
-    run_softmax<kQ, kFmt, kWide || kQ == 2>(p, ms, sbase, tmem,
-                                            G::kSplit ? __ldg(p.kv_scale) : 1.0f);
+    const float kv_scale = G::kMx ? __int_as_float((127 + p.mx_bias) << 23)
+                                  : (G::kSplit ? __ldg(p.kv_scale) : 1.0f);
+    run_softmax<kQ, kFmt, kWide || kQ == 2>(p, ms, sbase, tmem, kv_scale);
   } else {
     if constexpr (kWide) setmaxnreg_dec<kOtherRegs>();
     const int who = kGather ? gather_producer_of_warp(warp, num_producers<kGather, kQ>())
                             : (warp == kProducerWarp ? 0 : -1);
     if (who >= 0) {
-      run_producer<kGather, kQ, kFmt>(p, &map_v, &map_r, ms, sbase, static_cast<uint32_t>(who));
+      if constexpr (G::kMx)
+        run_producer_mx<kQ>(p, &map_v, &map_r, &map_s, ms, sbase);
+      else
+        run_producer<kGather, kQ, kFmt>(p, &map_v, &map_r, ms, sbase, static_cast<uint32_t>(who));
+    } else if (G::kMx && warp >= kFirstConverterWarp) {
+      if constexpr (G::kMx) run_converter<kQ>(p, ms, sbase);
     } else if (warp == kMmaWarp && lane == 0) {
       run_mma_pv<kQ, kFmt>(p, ms, sbase, tmem);
     } else if (warp == kMmaQkWarp && lane == 0) {
@@ -1498,18 +1741,18 @@ cudaError_t set_smem_limits() {
   if (e == cudaSuccess) e = set_smem_limit<true, 2, Kv::kE4m3>();
   if (e == cudaSuccess) e = set_smem_limit<false, 1, Kv::kBf16>();
   if (e == cudaSuccess) e = set_smem_limit<false, 2, Kv::kBf16>();
+  if (e == cudaSuccess) e = set_smem_limit<false, 1, Kv::kMx4>();
   return e;
 }
 
 template <bool kGather, int kQ, Kv kFmt>
-cudaError_t launch(const Stage1Params& p, const CUtensorMap& map_v, const CUtensorMap& map_r,
-                   cudaStream_t stream) {
+cudaError_t launch(const Stage1Params& p, const Stage1Maps& maps, cudaStream_t stream) {
   // A programmatic dependent of the previous kernel in the stream: its CTAs
   // may be scheduled while that kernel finishes, and wait for it (griddepcontrol
   // .wait) before touching global memory.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.grid * p.siblings));
-  cfg.blockDim = dim3(stage1_threads<kGather, kQ>());
+  cfg.blockDim = dim3(stage1_threads<kGather, kQ, kFmt>());
   cfg.dynamicSmemBytes = smem_alloc<kQ, kFmt>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1517,7 +1760,8 @@ cudaError_t launch(const Stage1Params& p, const CUtensorMap& map_v, const CUtens
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_decode_stage1_kernel<kGather, kQ, kFmt>, map_v, map_r, p);
+  return cudaLaunchKernelEx(&cfg, mla_decode_stage1_kernel<kGather, kQ, kFmt>, maps.v, maps.r,
+                            maps.s, p);
 }
 
 
@@ -1526,8 +1770,9 @@ constexpr int cmax(int a, int b) { return a > b ? a : b; }
 }  // namespace
 
 size_t stage1_smem_bytes() {
-  return static_cast<size_t>(cmax(cmax(smem_alloc<1, Kv::kE4m3>(), smem_alloc<2, Kv::kE4m3>()),
-                                  cmax(smem_alloc<1, Kv::kBf16>(), smem_alloc<2, Kv::kBf16>())));
+  return static_cast<size_t>(cmax(cmax(cmax(smem_alloc<1, Kv::kE4m3>(), smem_alloc<2, Kv::kE4m3>()),
+                                       cmax(smem_alloc<1, Kv::kBf16>(), smem_alloc<2, Kv::kBf16>())),
+                                  smem_alloc<1, Kv::kMx4>()));
 }
 
 cudaError_t stage1_prepare(int device) {
@@ -1535,20 +1780,23 @@ cudaError_t stage1_prepare(int device) {
   return set_smem_limits();
 }
 
-cudaError_t launch_stage1(const Stage1Params& p, const CUtensorMap& map_v,
-                          const CUtensorMap& map_r, bool gather, bool bf16_cache,
-                          cudaStream_t stream) {
+cudaError_t launch_stage1(const Stage1Params& p, const Stage1Maps& maps, bool gather,
+                          CacheFormat format, cudaStream_t stream) {
   const bool two = p.row_tokens - p.q_off >= 2;  // each CTA takes up to two tokens
-  if (bf16_cache) {
+  if (format == CacheFormat::kMxfp4) {
+    if (gather || two) return cudaErrorNotSupported;  // the host rejects these before launching
+    return launch<false, 1, Kv::kMx4>(p, maps, stream);
+  }
+  if (format == CacheFormat::kBf16) {
     if (gather) return cudaErrorNotSupported;  // the host rejects this before launching
-    return two ? launch<false, 2, Kv::kBf16>(p, map_v, map_r, stream)
-               : launch<false, 1, Kv::kBf16>(p, map_v, map_r, stream);
+    return two ? launch<false, 2, Kv::kBf16>(p, maps, stream)
+               : launch<false, 1, Kv::kBf16>(p, maps, stream);
   }
   if (two)
-    return gather ? launch<true, 2, Kv::kE4m3>(p, map_v, map_r, stream)
-                  : launch<false, 2, Kv::kE4m3>(p, map_v, map_r, stream);
-  return gather ? launch<true, 1, Kv::kE4m3>(p, map_v, map_r, stream)
-                : launch<false, 1, Kv::kE4m3>(p, map_v, map_r, stream);
+    return gather ? launch<true, 2, Kv::kE4m3>(p, maps, stream)
+                  : launch<false, 2, Kv::kE4m3>(p, maps, stream);
+  return gather ? launch<true, 1, Kv::kE4m3>(p, maps, stream)
+                : launch<false, 1, Kv::kE4m3>(p, maps, stream);
 }
 
 }  // namespace mla

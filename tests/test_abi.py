@@ -111,6 +111,29 @@ def test_host_side_argument_errors(lib):
                                      fake, plan.ws_bytes) == 2
 
 
+def test_mxfp4_host_side_argument_errors(lib):
+    plan = binding.mla_decode_plan(4, 1024, 152)
+    p = ctypes.byref(plan)
+    fake = ctypes.c_void_p(1 << 20)
+    ws = plan.ws_bytes
+
+    def fwd(*, scales=fake, bias=0, rows=4096, plan_ref=p, ws_bytes=ws, fn=lib.mla_decode_fwd_mxfp4):
+        return fn(fake, fake, scales, bias, fake, fake, fake, None, plan_ref, rows, fake, ws_bytes)
+
+    assert fwd(scales=None) == 1
+    assert fwd(scales=ctypes.c_void_p((1 << 20) + 2)) == 1          # scales not 16-byte aligned
+    assert fwd(bias=101) == 1 and fwd(bias=-101) == 1
+    assert fwd(rows=119_304_420) == 1                               # scale bytes past 2^31
+    assert fwd(rows=0) == 1
+    assert fwd(ws_bytes=ws - 1) == 3
+    assert fwd(fn=lib.mla_decode_stage1_mxfp4, ws_bytes=ws - 1) == 3
+    plan2 = binding.mla_decode_plan(4, 1024, 152, qo_len=2)
+    assert fwd(plan_ref=ctypes.byref(plan2), ws_bytes=plan2.ws_bytes) == 2  # one query token only
+    assert lib.mla_mxfp4_quantize(None, 4, fake, fake, None) == 1
+    assert lib.mla_mxfp4_quantize(fake, 0, fake, fake, None) == 1
+    assert lib.mla_mxfp4_quantize(fake, 4, ctypes.c_void_p((1 << 20) + 4), fake, None) == 1
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     plan = binding.mla_decode_plan(1, 128, 152)
