@@ -48,12 +48,15 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 
 
-def algorithmic_bytes(inp, bf16_cache: bool = False) -> int:
+CACHE_ROW_BYTES = {"e4m3": 576, "bf16": 1152, "mxfp4": 288 + 18}
+
+
+def algorithmic_bytes(inp, cache: str = "e4m3") -> int:
     """Bytes one call must move: every cached token's row (576 bytes of e4m3
-    codes, or 1152 of bf16; +4 for its page-table entry), the bf16 query and
-    output rows, and both indptr arrays."""
+    codes, 1152 of bf16, or 288 of E2M1 elements plus 18 scale bytes; +4 for its
+    page-table entry), the bf16 query and output rows, and both indptr arrays."""
     tokens = int(inp.kv_indptr[-1])
-    per_token = 576 * (2 if bf16_cache else 1) + (4 if inp.kv_indices is not None else 0)
+    per_token = CACHE_ROW_BYTES[cache] + (4 if inp.kv_indices is not None else 0)
     queries = inp.batch * getattr(inp, "qo_len", 1)
     return tokens * per_token + queries * 16 * (576 + 512) * 2 + 2 * (inp.batch + 1) * 4
 
@@ -169,6 +172,13 @@ class DeviceWorkload:
         binding.mla_fp8_quantize_per_tensor(kv, self.kv, self.kv_scale,
                                             torch.empty(16, dtype=torch.uint8, device=dev))
         self.kv_bf16 = kv  # the bf16 cache the e4m3 codes came from (the bf16-cache step's input)
+        # The MXFP4 cache of the same source (mla_decode_fwd_mxfp4: contiguous rows,
+        # one query token).
+        self.mx = inp.kv_indices is None and inp.qo_len == 1
+        if self.mx:
+            self.kv_fp4 = torch.empty((kv.shape[0], 288), dtype=torch.uint8, device=dev)
+            self.kv_mxs = torch.empty((kv.shape[0], 18), dtype=torch.uint8, device=dev)
+            binding.mla_mxfp4_quantize(kv, self.kv_fp4, self.kv_mxs)
         self.qo_indptr = torch.from_numpy(inp.qo_indptr).to(dev)
         self.kv_indptr = torch.from_numpy(inp.kv_indptr).to(dev)
         self.kv_indices = None if inp.kv_indices is None else torch.from_numpy(inp.kv_indices).to(dev)
@@ -176,7 +186,8 @@ class DeviceWorkload:
         self.plan = binding.mla_decode_plan(inp.batch, inp.max_kv_len, sms, qo_len=inp.qo_len)
         self.ws = binding.new_workspace(self.plan)
         self.bytes = algorithmic_bytes(inp)
-        self.bytes_bf16 = algorithmic_bytes(inp, bf16_cache=True)
+        self.bytes_bf16 = algorithmic_bytes(inp, "bf16")
+        self.bytes_mx = algorithmic_bytes(inp, "mxfp4")
         self.binding = binding
         torch.cuda.synchronize()
         self.inp.kv_bits = None  # release the host copy of the cache source
@@ -190,6 +201,16 @@ class DeviceWorkload:
         self.binding.mla_decode_fwd_bf16kv(self.q, self.kv_bf16, self.qo_indptr, self.kv_indptr,
                                            self.out, stream, plan=self.plan, workspace=self.ws,
                                            kv_indices=self.kv_indices)
+
+    def call_mxfp4(self, stream=None):
+        self.binding.mla_decode_fwd_mxfp4(self.q, self.kv_fp4, self.kv_mxs, self.qo_indptr,
+                                          self.kv_indptr, self.out, stream, plan=self.plan,
+                                          workspace=self.ws)
+
+    def stage1_mxfp4(self, stream=None):
+        self.binding.mla_decode_stage1_mxfp4(self.q, self.kv_fp4, self.kv_mxs, self.qo_indptr,
+                                             self.kv_indptr, self.out, stream, plan=self.plan,
+                                             workspace=self.ws)
 
     def stage1(self, stream=None):
         self.binding.mla_decode_stage1(self.q, self.kv, self.kv_scale, self.qo_indptr,
@@ -469,6 +490,20 @@ def ours_main(args) -> None:
             # the same step over the bf16 cache (mla_decode_fwd_bf16kv; contiguous caches only)
             entry["bf16_cache"] = (cold(ww.call_bf16kv, ww.bytes_bf16) if ww.kv_indices is None
                                    else {"unsupported": "page table (bf16 caches are read contiguously)"})
+            # and over the MXFP4 cache (mla_decode_fwd_mxfp4), with its stage 1 timed
+            # alone back to back (the MXFP4 kernel's roofline)
+            if ww.mx:
+                mx = cold(ww.call_mxfp4, ww.bytes_mx)
+                ms_mx = time_loop(torch, ww.call_mxfp4, 50, stream) / 50
+                ms_mx1 = time_loop(torch, ww.stage1_mxfp4, 50, stream) / 50
+                mx["us_back_to_back"] = round(ms_mx * 1e3, 2)
+                mx["stage1_us_back_to_back"] = round(ms_mx1 * 1e3, 2)
+                mx["stage1_frac_of_peak"] = round(ww.bytes_mx / (ms_mx1 * 1e-3) / 1e9 / peak, 3)
+                if binding.mla_decode_read_error(ww.ws) != 0:
+                    raise SystemExit("device error word set during the MXFP4 timing")
+                entry["mxfp4_cache"] = mx
+            else:
+                entry["mxfp4_cache"] = {"unsupported": "page table or several query tokens per row"}
             per_config.append(entry)
             if ww is not w:
                 del ww
@@ -476,6 +511,7 @@ def ours_main(args) -> None:
         del flush
 
     w.kv_bf16 = None
+    w.kv_fp4 = w.kv_mxs = None
     torch.cuda.empty_cache()
     e2e = e2e_timing(torch, w, args.e2e_steps, stream)
     cpu = None

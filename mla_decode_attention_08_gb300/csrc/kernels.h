@@ -10,10 +10,12 @@ namespace mla {
 // every size depend on the cache format (stage1.cu, Geo).
 constexpr int kNumRSlots = 2;
 // warps 0-3 softmax/epilogue, 4 TMA producer, 5 PV MMA issuer, 6 QK MMA issuer;
-// page-table mode adds TMA producers in warps 7, 8 and 9 (12 warps, registers
-// rebalanced with setmaxnreg).
+// page-table mode with one query token adds TMA producers in warps 7-11 (12
+// warps), an MXFP4 cache converter warps 8-15 (16 warps); registers rebalanced
+// with setmaxnreg in both.
 constexpr int kStage1Threads = 256;
 constexpr int kStage1ThreadsGather = 384;
+constexpr int kStage1ThreadsMx = 512;  // MXFP4 cache: warps 8-15 convert its panels
 constexpr long long kWaitLimitCycles = 2000000000LL;  // ~1 s per pipeline wait at 2 GHz
 
 struct Stage1Params {

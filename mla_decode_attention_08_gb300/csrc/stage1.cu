@@ -26,7 +26,7 @@
 // and every tile moves twice the bytes.  An MXFP4 cache (submission 738050,
 // `_dequantize_mxfp4_inplace`; submission 722089 `_mla_multihead_stage1`):
 // E2M1 elements with one E8M0 scale per 32; the tile streams in at 306 bytes a
-// token and four converter warps rewrite each panel in place as the e4m3 panel
+// token and eight converter warps rewrite each panel in place as the e4m3 panel
 // the e4m3 path reads (exact while the block scales stay in a 15-binade
 // window), so the MMAs and the softmax are the e4m3 ones.  A CTA takes one or
 // two of the row's query tokens (Geo<kQ, kFmt>); an MXFP4 cache takes one.
@@ -60,7 +60,7 @@ constexpr int kNumSclSlots = 4;
 constexpr int kSclBoxes = 10;
 constexpr int kSclSlotBytes = 256 * kSclBoxes;
 static_assert(kSclSlotBytes >= 15 + kTileTokens * 18, "a tile's scale bytes fit a slot");
-constexpr int kConverterWarps = 4;
+constexpr int kConverterWarps = 8;
 constexpr int kFirstConverterWarp = 8;
 
 // Everything that depends on the cache format and on the number kQ of query
@@ -146,7 +146,7 @@ struct Misc {
   alignas(16) float red_max[2][4][16 * kMaxQ];  // read and written as float4
   alignas(16) float red_sum[4][16 * kMaxQ];
   uint32_t red_u32[8];
-  int32_t scan[kStage1ThreadsGather / 32];  // per warp of the prologue's block scan
+  int32_t scan[kStage1ThreadsMx / 32];  // per warp of the prologue's block scan (largest block)
   uint32_t tmem_base;
   volatile int32_t abort_flag;
   int32_t total_tiles;
@@ -194,11 +194,14 @@ constexpr uint32_t kBarConverters = 3;  // named barrier id of the MXFP4 convert
 // <= 384 x 168).
 // With two query tokens the softmax needs more than 240 registers, so that
 // kernel keeps 8 warps and two producers (warps 4 and 7).
-// An MXFP4 cache also runs 12 warps: warps 8-11 convert its panels.
+// An MXFP4 cache runs 16 warps: warps 8-15 convert its panels.
 template <bool kGather, int kQ, Kv kFmt>
 __host__ __device__ constexpr bool wide_block() { return (kGather && kQ == 1) || kFmt == Kv::kMx4; }
 template <bool kGather, int kQ, Kv kFmt>
-__host__ __device__ constexpr int stage1_threads() { return wide_block<kGather, kQ, kFmt>() ? kStage1ThreadsGather : kStage1Threads; }
+__host__ __device__ constexpr int stage1_threads() {
+  return kFmt == Kv::kMx4 ? kStage1ThreadsMx
+                          : (wide_block<kGather, kQ, kFmt>() ? kStage1ThreadsGather : kStage1Threads);
+}
 template <bool kGather, int kQ>
 __host__ __device__ constexpr uint32_t num_producers() { return !kGather ? 1 : (kQ == 1 ? 6 : 2); }
 // Producer index of a warp in page-table mode (warps 4, 7, 8, ...), or -1.
@@ -209,6 +212,11 @@ __device__ __forceinline__ int gather_producer_of_warp(int warp, uint32_t produc
 constexpr int kSoftmaxRegs = 240, kOtherRegs = 128;
 static_assert(128 * kSoftmaxRegs + 256 * kOtherRegs <= kStage1ThreadsGather * 168,
               "register split exceeds the launch allocation");
+// MXFP4 (16 warps, launched with 128 registers a thread): 240 for the softmax
+// warpgroup, 88 for the other twelve warps.
+constexpr int kOtherRegsMx = 88;
+static_assert(128 * kSoftmaxRegs + 384 * kOtherRegsMx <= kStage1ThreadsMx * 128,
+              "MXFP4 register split exceeds the launch allocation");
 
 // log2(e) / sqrt(576): converts a dot product to base-2 softmax exponent units.
 constexpr float kSmScaleLog2 = 1.4426950408889634f / 24.0f;
@@ -650,7 +658,7 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
   }
 }
 
-// ------------------------------------------------------------ MXFP4 cache (warp 4 producer, warps 8-11 converters)
+// ------------------------------------------------------------ MXFP4 cache (warp 4 producer, warps 8-15 converters)
 // Producer (lane 0 of warp 4; contiguous rows only).  Per tile: the rope
 // panel's elements (32 bytes a row, 32-byte swizzle) into the upper half of its
 // rope slot together with the tile's scale bytes (scale slot tile % 4), then
@@ -777,18 +785,20 @@ __device__ __forceinline__ bool converters_bar_or(bool v) {
   return r != 0;
 }
 
-// Converters (warps 8-11): thread i owns row (token) i of every panel.  For each
-// panel, in fill order: wait for its elements (and, with the rope panel, read the
-// token's 18 scale bytes), load the row's elements, then meet the other
-// converters (the vote also ends the call for all of them together when a wait
-// gave up); only then write the e4m3 row over the slot, in the swizzled layouts
-// the e4m3 cache's TMA boxes produce (latent rows 128 bytes, 128-byte swizzle;
-// rope rows 64 bytes, 64-byte swizzle), and arrive, one lane per warp, on the
-// panel's full barrier that the QK issuer waits on.
+// Converters (warps 8-15): thread t owns row (token) i = t % 128 of every
+// panel and its half h = t / 128 (blocks 2h, 2h + 1 of a latent panel, block
+// 16 + h of the rope panel).  For each panel, in fill order: wait for its
+// elements, load the thread's blocks (and the scale bytes they need), then meet
+// the other converters (the vote also ends the call for all of them together
+// when a wait gave up); only then write the e4m3 codes over the slot, in the
+// swizzled layouts the e4m3 cache's TMA boxes produce (latent rows 128 bytes,
+// 128-byte swizzle; rope rows 64 bytes, 64-byte swizzle), and arrive, one lane
+// per warp, on the panel's full barrier that the QK issuer waits on.
 template <int kQ>
 __device__ void run_converter(const Stage1Params& p, Misc* ms, uint32_t sbase) {
   using G = Geo<kQ, Kv::kMx4>;
-  const int i = static_cast<int>(threadIdx.x) - kFirstConverterWarp * 32;
+  const int t = static_cast<int>(threadIdx.x) - kFirstConverterWarp * 32;
+  const int i = t & (kTileTokens - 1), h = t >> 7;
   const int lane = threadIdx.x & 31;
   const int32_t bias = p.mx_bias;
   Cursor cur;
@@ -801,23 +811,20 @@ __device__ void run_converter(const Stage1Params& p, Misc* ms, uint32_t sbase) {
     const uint32_t rslot = tile % kNumRSlots;
     const uint32_t rs = sbase + G::kOffR + rslot * G::kRSlotBytes;
     bool ok = wait_phase(smem_u32(&ms->rraw_full[rslot]), (tile / kNumRSlots) & 1, ms, p.err);
-    uint32_t sc[9];  // the token's scale bytes: blocks 2k and 2k + 1 in sc[k]
-    uint4 rr[2];
+    // The token's scale bytes (the slot stays put until the tile's panels are done).
+    const uint32_t sb = sbase + G::kOffScl + (tile % kNumSclSlots) * kSclSlotBytes +
+                        ((18 * tok0) & 15) + 18 * i;
+    uint32_t sc_rope = 0;
+    uint4 rr;
     if (ok) {
-      const uint32_t sb = sbase + G::kOffScl + (tile % kNumSclSlots) * kSclSlotBytes +
-                          ((18 * tok0) & 15) + 18 * i;
-#pragma unroll
-      for (int k = 0; k < 9; ++k) sc[k] = ld_shared_u16(sb + 2 * k);
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-        rr[j] = ld_shared_v4(rs + G::kRRawOff + 32 * i + 16 * (j ^ ((i >> 2) & 1)));
+      sc_rope = ld_shared_u16(sb + 16);  // blocks 16, 17
+      rr = ld_shared_v4(rs + G::kRRawOff + 32 * i + 16 * (h ^ ((i >> 2) & 1)));
     }
     if (converters_bar_or(!ok)) break;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {  // rope dims 512 + 32 j ... (blocks 16, 17)
-      const uint32_t k0 = 2 * j, k1 = 2 * j + 1, sw = (i >> 1) & 3;
-      mx_block_store(rr[j], (sc[8] >> (8 * j)) & 0xFFu, bias, rs + 64 * i + 16 * (k0 ^ sw),
-                     rs + 64 * i + 16 * (k1 ^ sw), bad);
+    {  // rope dims 512 + 32 h ... (block 16 + h)
+      const uint32_t sw = (i >> 1) & 3;
+      mx_block_store(rr, (sc_rope >> (8 * h)) & 0xFFu, bias, rs + 64 * i + 16 * ((2 * h) ^ sw),
+                     rs + 64 * i + 16 * ((2 * h + 1) ^ sw), bad);
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -827,22 +834,26 @@ __device__ void run_converter(const Stage1Params& p, Misc* ms, uint32_t sbase) {
       const uint32_t g = tile * 4 + c, slot = g % G::kNumV;
       const uint32_t vs = sbase + G::kOffV + slot * G::kVSlotBytes;
       ok = wait_phase(smem_u32(&ms->raw_full[slot]), (g / G::kNumV) & 1, ms, p.err);
-      uint4 lr[4];
+      uint4 lr[2];
+      uint32_t sc = 0;  // blocks 4c + 2h, 4c + 2h + 1
       if (ok) {
+        sc = ld_shared_u16(sb + 4 * c + 2 * h);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          lr[j] = ld_shared_v4(vs + G::kVRawOff + 64 * i + 16 * (j ^ ((i >> 1) & 3)));
+        for (int k = 0; k < 2; ++k) {
+          const int j = 2 * h + k;
+          lr[k] = ld_shared_v4(vs + G::kVRawOff + 64 * i + 16 * (j ^ ((i >> 1) & 3)));
+        }
       }
       if (converters_bar_or(!ok)) {
         stop = true;
         break;
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {  // dims 128 c + 32 j ... (block 4 c + j)
-        const int blk = 4 * c + j;
-        const uint32_t k0 = 2 * j, k1 = 2 * j + 1, sw = i & 7;
-        mx_block_store(lr[j], (sc[blk >> 1] >> (8 * (blk & 1))) & 0xFFu, bias,
-                       vs + 128 * i + 16 * (k0 ^ sw), vs + 128 * i + 16 * (k1 ^ sw), bad);
+      for (int k = 0; k < 2; ++k) {  // dims 128 c + 32 j ... (block 4 c + j)
+        const int j = 2 * h + k;
+        const uint32_t sw = i & 7;
+        mx_block_store(lr[k], (sc >> (8 * k)) & 0xFFu, bias, vs + 128 * i + 16 * ((2 * j) ^ sw),
+                       vs + 128 * i + 16 * ((2 * j + 1) ^ sw), bad);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -1699,7 +1710,10 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
                                   : (G::kSplit ? __ldg(p.kv_scale) : 1.0f);
     run_softmax<kQ, kFmt, kWide || kQ == 2>(p, ms, sbase, tmem, kv_scale);
   } else {
-    if constexpr (kWide) setmaxnreg_dec<kOtherRegs>();
+    if constexpr (G::kMx)
+      setmaxnreg_dec<kOtherRegsMx>();
+    else if constexpr (kWide)
+      setmaxnreg_dec<kOtherRegs>();
     const int who = kGather ? gather_producer_of_warp(warp, num_producers<kGather, kQ>())
                             : (warp == kProducerWarp ? 0 : -1);
     if (who >= 0) {
