@@ -139,10 +139,11 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, cache: str = "e4m3"):
     """Per-launch DRAM bytes of stage 1 from the committed ncu summary, if it
     was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"stage1_{workload}_traffic.json")
+    tag = "" if cache == "e4m3" else f"{cache}_"
+    path = os.path.join(ROOT, "profiles", f"stage1_{tag}{workload}_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -217,6 +218,19 @@ class DeviceWorkload:
                                        self.kv_indptr, self.out, stream, plan=self.plan,
                                        workspace=self.ws, kv_indices=self.kv_indices)
 
+    def stage1_bf16kv(self, stream=None):
+        self.binding.mla_decode_stage1_bf16kv(self.q, self.kv_bf16, self.qo_indptr,
+                                              self.kv_indptr, self.out, stream, plan=self.plan,
+                                              workspace=self.ws, kv_indices=self.kv_indices)
+
+    def timed(self, cache: str):
+        """(whole step, stage 1 alone, algorithmic bytes) for the selected cache format."""
+        if cache == "bf16":
+            return self.call_bf16kv, self.stage1_bf16kv, self.bytes_bf16
+        if cache == "mxfp4":
+            return self.call_mxfp4, self.stage1_mxfp4, self.bytes_mx
+        return self.call, self.stage1, self.bytes
+
 
 def time_loop(torch, fn, steps: int, stream) -> float:
     """Milliseconds for `steps` back-to-back calls, CUDA events on `stream`."""
@@ -247,7 +261,10 @@ def per_call_cold(torch, call, reps: int, stream, flush) -> list:
 def e2e_timing(torch, w: DeviceWorkload, steps: int, stream) -> dict:
     """Host-buffer round trip per call: pinned H2D of the step's inputs, the
     decode call, D2H of the output, all inside the timed region."""
-    host = {k: getattr(w, k).cpu().pin_memory() for k in ("q", "kv", "kv_scale", "qo_indptr", "kv_indptr")}
+    cache = getattr(w, "cache", "e4m3")
+    keys = {"e4m3": ("q", "kv", "kv_scale"), "bf16": ("q", "kv_bf16"),
+            "mxfp4": ("q", "kv_fp4", "kv_mxs")}[cache] + ("qo_indptr", "kv_indptr")
+    host = {k: getattr(w, k).cpu().pin_memory() for k in keys}
     if w.kv_indices is not None:
         host["kv_indices"] = w.kv_indices.cpu().pin_memory()
     out_host = torch.empty(w.out.shape, dtype=w.out.dtype).pin_memory()
@@ -258,9 +275,18 @@ def e2e_timing(torch, w: DeviceWorkload, steps: int, stream) -> dict:
     def step():
         for k, v in host.items():
             dev[k].copy_(v, non_blocking=True)
-        w.binding.mla_decode_fwd(dev["q"], dev["kv"], dev["kv_scale"], dev["qo_indptr"],
-                                 dev["kv_indptr"], w.out, stream, plan=w.plan, workspace=w.ws,
-                                 kv_indices=dev.get("kv_indices"))
+        if cache == "mxfp4":
+            w.binding.mla_decode_fwd_mxfp4(dev["q"], dev["kv_fp4"], dev["kv_mxs"], dev["qo_indptr"],
+                                           dev["kv_indptr"], w.out, stream, plan=w.plan,
+                                           workspace=w.ws)
+        elif cache == "bf16":
+            w.binding.mla_decode_fwd_bf16kv(dev["q"], dev["kv_bf16"], dev["qo_indptr"],
+                                            dev["kv_indptr"], w.out, stream, plan=w.plan,
+                                            workspace=w.ws, kv_indices=dev.get("kv_indices"))
+        else:
+            w.binding.mla_decode_fwd(dev["q"], dev["kv"], dev["kv_scale"], dev["qo_indptr"],
+                                     dev["kv_indptr"], w.out, stream, plan=w.plan, workspace=w.ws,
+                                     kv_indices=dev.get("kv_indices"))
         out_host.copy_(w.out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -282,10 +308,11 @@ class OracleSample:
     """The float64 oracle on single batch rows of a workload (quantisation is
     input preparation and stays outside the timed calls)."""
 
-    def __init__(self, name: str):
+    def __init__(self, name: str, cache: str = "e4m3"):
         from mla_decode_attention_08_gb300.inputs import bf16_bits_to_f32
         from oracle.attention import bf16_bits_to_f64
         from oracle.quant import per_tensor_scale
+        self.cache = cache
         self.inp = make_inputs(name)
         self.kv_f32 = bf16_bits_to_f32(self.inp.kv_bits)
         self.inp.kv_bits = None
@@ -293,26 +320,41 @@ class OracleSample:
         self.q = bf16_bits_to_f64(self.inp.q_bits)
 
     def prepare(self, b: int):
+        """The row's cache in the selected format (a tuple of arrays) and its length."""
+        from mla_decode_attention_08_gb300.inputs import f32_to_bf16_bits
+        from oracle.mxfp4 import quantize_rows
         from oracle.quant import encode_with_scale
         inp = self.inp
         j0, j1 = int(inp.kv_indptr[b]), int(inp.kv_indptr[b + 1])
         slots = np.arange(j0, j1) if inp.kv_indices is None else inp.kv_indices[j0:j1].astype(np.int64)
-        return encode_with_scale(self.kv_f32[slots], self.scale), j1 - j0
+        rows = self.kv_f32[slots]
+        if self.cache == "mxfp4":
+            return quantize_rows(rows.astype(np.float64)), j1 - j0
+        if self.cache == "bf16":
+            return (f32_to_bf16_bits(rows),), j1 - j0
+        return (encode_with_scale(rows, self.scale),), j1 - j0
 
     def run_row(self, b: int, prepared) -> float:
         """Seconds of one oracle call restricted to row b."""
-        from oracle.attention import mla_decode_ref
-        codes, length = prepared
+        from oracle.attention import mla_decode_ref, mla_decode_ref_bf16kv
+        from oracle.mxfp4 import mla_decode_ref_mxfp4
+        data, length = prepared
         n = self.inp.qo_len
         t0 = int(self.inp.qo_indptr[b])
+        q, qo, kv = self.q[t0:t0 + n], np.array([0, n]), np.array([0, length])
         t = time.perf_counter()
-        mla_decode_ref(self.q[t0:t0 + n], codes, self.scale, np.array([0, n]), np.array([0, length]))
+        if self.cache == "mxfp4":
+            mla_decode_ref_mxfp4(q, data[0], data[1], qo, kv)
+        elif self.cache == "bf16":
+            mla_decode_ref_bf16kv(q, data[0], qo, kv)
+        else:
+            mla_decode_ref(q, data[0], self.scale, qo, kv)
         return time.perf_counter() - t
 
 
-def oracle_sample_main(name: str, budget_s: float) -> None:
+def oracle_sample_main(name: str, budget_s: float, cache: str = "e4m3") -> None:
     """Worker: time the oracle on as many rows as fit the budget; print JSON."""
-    o = OracleSample(name)
+    o = OracleSample(name, cache)
     batch = o.inp.batch
     first = o.run_row(0, o.prepare(0))
     n = int(max(1, min(batch, budget_s / max(first, 1e-6))))
@@ -329,8 +371,9 @@ def oracle_sample_main(name: str, budget_s: float) -> None:
                                 f"{total:.1f} s, extrapolated by cached tokens"}))
 
 
-def cpu_baseline(name: str, budget_s: float = 15.0):
-    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", name, "--budget", str(budget_s)]
+def cpu_baseline(name: str, budget_s: float = 15.0, cache: str = "e4m3"):
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", name, "--budget", str(budget_s),
+           "--cache", cache]
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
         tail = r.stderr.strip().splitlines()[-1][:200] if r.stderr.strip() else "no output"
@@ -348,20 +391,20 @@ def reference_main(args) -> None:
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if int(os.environ.get("RANK", "0")) != 0:
         return
-    o = OracleSample(args.workload)
+    o = OracleSample(args.workload, args.cache)
     batch = o.inp.batch
     tok = np.diff(o.inp.kv_indptr.astype(np.int64))
     calib_row = int(np.argmax(tok))
-    codes_c, len_c = o.prepare(calib_row)
-    per_tok = o.run_row(calib_row, (codes_c, len_c)) / max(1, len_c)
+    data_c, len_c = o.prepare(calib_row)
+    per_tok = o.run_row(calib_row, (data_c, len_c)) / max(1, len_c)
     n_steps = args.warmup + args.steps
     cap = int(args.ref_budget / max(n_steps * per_tok, 1e-12))
     rows = [(i * 37) % batch for i in range(n_steps)]
     prepared = {}
     for b in set(rows):
-        codes, length = o.prepare(b)
+        data, length = o.prepare(b)
         n = max(1, min(length, cap))
-        prepared[b] = (codes[:n], n)
+        prepared[b] = (tuple(a[:n] for a in data), n)
     for b in rows[:args.warmup]:
         o.run_row(b, prepared[b])
     timed = rows[args.warmup:]
@@ -377,7 +420,7 @@ def reference_main(args) -> None:
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total * 1e3 / max(1, len(timed)), 3), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(args.workload, world),
+            "config": workload_config(args.workload, world, args.cache),
             "cpu_baseline": {"value": round(call_us, 1), "unit": "us/call", "cores": 1,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(call_us, 1), "unit": "us/call", "h2d_bytes_per_step": 0,
@@ -385,13 +428,21 @@ def reference_main(args) -> None:
     print(json.dumps(line), flush=True)
 
 
-def workload_config(name: str, world: int) -> dict:
+CACHE_DESC = {"e4m3": "e4m3fn, per-tensor scale", "bf16": "bf16",
+              "mxfp4": "MXFP4 (E2M1 elements, E8M0 scale per 32)"}
+DTYPE_DESC = {"e4m3": "e4m3 x e4m3 -> f32 (tcgen05 kind::f8f6f4), bf16 out",
+              "bf16": "bf16 x bf16 -> f32 (tcgen05 kind::f16), bf16 out",
+              "mxfp4": "MXFP4 converted to e4m3 in shared memory; e4m3 x e4m3 -> f32 "
+                       "(tcgen05 kind::f8f6f4), bf16 out"}
+
+
+def workload_config(name: str, world: int, cache: str = "e4m3") -> dict:
     w = WORKLOADS[name]
     return {"workload": name, "batch": w.batch, "kv_len": w.kv_len,
             "kv_len_dist": "uniform 1..kv_len" if w.ragged else "fixed",
             "page_table": "random permutation, page size 1" if w.paged else "identity",
             "heads": 16, "qk_head_dim": 576, "v_head_dim": 512,
-            "kv_cache": "e4m3fn, per-tensor scale", "qseqlen": w.qo_len,
+            "kv_cache": CACHE_DESC[cache], "qseqlen": w.qo_len,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": "cache larger than L2, no flush between steps"}
 
@@ -407,7 +458,7 @@ def max_over_ranks(value: float, dist=None, device: str = "cpu") -> float:
     return float(t.item())
 
 
-def workload_bytes(name: str) -> int:
+def workload_bytes(name: str, cache: str = "e4m3") -> int:
     """Algorithmic bytes of a workload from its shapes only."""
     from mla_decode_attention_08_gb300.inputs import workload_lengths
     wl = WORKLOADS[name]
@@ -418,7 +469,7 @@ def workload_bytes(name: str) -> int:
         qo_len = wl.qo_len
         kv_indptr = np.concatenate([[0], np.cumsum(lengths)])
         kv_indices = np.zeros(1) if wl.paged else None
-    return algorithmic_bytes(_Shape)
+    return algorithmic_bytes(_Shape, cache)
 
 
 def ours_main(args) -> None:
@@ -444,14 +495,19 @@ def ours_main(args) -> None:
         torch.cuda.synchronize()
 
     w = DeviceWorkload(args.workload, torch, binding, sms)
+    if args.cache != "e4m3" and (w.kv_indices is not None or (args.cache == "mxfp4" and not w.mx)):
+        raise SystemExit(f"--cache {args.cache} takes contiguous workloads"
+                         + (" with one query token per row" if args.cache == "mxfp4" else ""))
+    w.cache = args.cache
+    step_fn, stage1_fn, step_bytes = w.timed(args.cache)
     for _ in range(args.warmup):
-        w.call(stream)
+        step_fn(stream)
     barrier()
     sampler = ClockSampler(local).start()
     time.sleep(0.3)  # let the sampler attach before the timed region
     barrier()
     t0 = time.time()
-    ms = time_loop(torch, w.call, args.steps, stream)
+    ms = time_loop(torch, step_fn, args.steps, stream)
     t1 = time.time()
     barrier()
     clocks = sampler.stop(t0, t1)
@@ -461,12 +517,12 @@ def ours_main(args) -> None:
 
     # stage 1 alone, the dominant kernel, for the roofline
     for _ in range(3):
-        w.stage1(stream)
-    ms1 = time_loop(torch, w.stage1, args.steps, stream) / args.steps
+        stage1_fn(stream)
+    ms1 = time_loop(torch, stage1_fn, args.steps, stream) / args.steps
     peak, peak_src = measured_peak()
-    achieved = w.bytes / (ms1 * 1e-3) / 1e9
+    achieved = step_bytes / (ms1 * 1e-3) / 1e9
     us_call = ms_step * 1e3
-    eff_tbps = w.bytes / (us_call * 1e-6) / 1e12
+    eff_tbps = step_bytes / (us_call * 1e-6) / 1e12
 
     per_config = []
     if not args.no_per_config and rank == 0:
@@ -510,15 +566,17 @@ def ours_main(args) -> None:
                 torch.cuda.empty_cache()
         del flush
 
-    w.kv_bf16 = None
-    w.kv_fp4 = w.kv_mxs = None
+    if args.cache != "bf16":
+        w.kv_bf16 = None
+    if args.cache != "mxfp4":
+        w.kv_fp4 = w.kv_mxs = None
     torch.cuda.empty_cache()
     e2e = e2e_timing(torch, w, args.e2e_steps, stream)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         del w
         torch.cuda.empty_cache()
-        cpu = cpu_baseline(args.workload, args.cpu_budget)
+        cpu = cpu_baseline(args.workload, args.cpu_budget, args.cache)
 
     if rank != 0:
         if dist is not None:
@@ -528,16 +586,16 @@ def ours_main(args) -> None:
         "metric": METRIC, "value": round(us_call, 2), "unit": "us/call", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 x e4m3 -> f32 (tcgen05 kind::f8f6f4), bf16 out", "data": "synthetic",
-        "config": workload_config(args.workload, world),
+        "dtype": DTYPE_DESC[args.cache], "data": "synthetic",
+        "config": workload_config(args.workload, world, args.cache),
         "effective_tbps": round(eff_tbps, 3),
         "aggregate_effective_tbps": round(eff_tbps * world, 3),
         "frac_of_peak": round(eff_tbps * 1e3 / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args.workload),
+                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args.workload, args.cache),
                      "kernel": "mla_decode_stage1_kernel", "peak_source": f"{peak_src} hbm_gbs",
                      "stage1_us_per_launch": round(ms1 * 1e3, 2),
-                     "algorithmic_bytes_per_launch": workload_bytes(args.workload)},
+                     "algorithmic_bytes_per_launch": workload_bytes(args.workload, args.cache)},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks,
         "per_config": per_config,
     }
@@ -553,6 +611,8 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=list(WORKLOADS))
+    ap.add_argument("--cache", default="e4m3", choices=["e4m3", "bf16", "mxfp4"],
+                    help="cache format of the timed step (the e4m3 cache is the headline)")
     ap.add_argument("--cold-reps", type=int, default=30)
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
@@ -563,7 +623,7 @@ def main() -> None:
     ap.add_argument("--budget", type=float, default=15.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_sample:
-        oracle_sample_main(args.oracle_sample, args.budget)
+        oracle_sample_main(args.oracle_sample, args.budget, args.cache)
     elif args.impl == "reference":
         reference_main(args)
     else:
