@@ -258,6 +258,21 @@ mla_status_t mla_decode_fwd_stall_stream(const void* q_bf16, const void* kv_fp8,
                                          int64_t kv_rows, void* workspace, size_t workspace_bytes);
 
 /*
+ * mla_decode_fwd_mxfp4_stall_stream — test hook for the bounded waits of the
+ * MXFP4 kernel (no counterpart on the pages): mla_decode_fwd_mxfp4 with a
+ * producer that loads nothing, so the converter warps' and MMA issuers' waits
+ * run out; as mla_decode_fwd_stall_stream, the call sets MLA_DERR_TIMEOUT,
+ * drains and returns without a fault, and the output is not meaningful.
+ * Arguments as mla_decode_fwd_mxfp4.
+ */
+mla_status_t mla_decode_fwd_mxfp4_stall_stream(const void* q_bf16, const void* kv_fp4,
+                                               const void* kv_scales, int32_t scale_bias,
+                                               const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                               void* out_bf16, cudaStream_t stream,
+                                               const mla_plan_t* plan, int64_t kv_rows,
+                                               void* workspace, size_t workspace_bytes);
+
+/*
  * mla_fp8_quantize_per_tensor — per-tensor absmax quantisation of a bf16 tensor
  * to e4m3fn (input preparation; the pages' harness supplies the cache already
  * quantised this way: submission 722089 `quantize_fp8`, submission 738050

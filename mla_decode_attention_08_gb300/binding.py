@@ -54,6 +54,7 @@ SIGNATURES = {
     "mla_decode_fwd_static_scratch": (ctypes.c_int, _FWD_ARGS[:-2]),
     "mla_decode_fwd_mxfp4": (ctypes.c_int, _FWD_MXFP4_ARGS),
     "mla_decode_stage1_mxfp4": (ctypes.c_int, _FWD_MXFP4_ARGS),
+    "mla_decode_fwd_mxfp4_stall_stream": (ctypes.c_int, _FWD_MXFP4_ARGS),
     "mla_mxfp4_quantize": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP]),
     "mla_decode_stage2": (ctypes.c_int, [_VP, _VP, _VP, _PLANP, _VP, _SZ]),
     "mla_fp8_quantize_per_tensor": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP, _SZ, _VP]),
@@ -167,6 +168,14 @@ def mla_decode_fwd_mxfp4(q, kv_fp4, kv_scales, qo_indptr, kv_indptr, out, stream
 def mla_decode_stage1_mxfp4(q, kv_fp4, kv_scales, qo_indptr, kv_indptr, out, stream=None, *,
                             plan, workspace, scale_bias: int = 0) -> None:
     _check("mla_decode_stage1_mxfp4", load_library().mla_decode_stage1_mxfp4(
+        *_fwd_mxfp4_args(q, kv_fp4, kv_scales, qo_indptr, kv_indptr, out, stream, plan, workspace,
+                         scale_bias)))
+
+
+def mla_decode_fwd_mxfp4_stall_stream(q, kv_fp4, kv_scales, qo_indptr, kv_indptr, out,
+                                      stream=None, *, plan, workspace, scale_bias: int = 0) -> None:
+    """Test hook: the MXFP4 step with a cache stream that never arrives."""
+    _check("mla_decode_fwd_mxfp4_stall_stream", load_library().mla_decode_fwd_mxfp4_stall_stream(
         *_fwd_mxfp4_args(q, kv_fp4, kv_scales, qo_indptr, kv_indptr, out, stream, plan, workspace,
                          scale_bias)))
 

@@ -441,6 +441,17 @@ mla_status_t mla_decode_fwd_mxfp4(const void* q_bf16, const void* kv_fp4, const 
                     kv_scales, scale_bias);
 }
 
+mla_status_t mla_decode_fwd_mxfp4_stall_stream(const void* q_bf16, const void* kv_fp4,
+                                               const void* kv_scales, int32_t scale_bias,
+                                               const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                               void* out_bf16, cudaStream_t stream,
+                                               const mla_plan_t* plan, int64_t kv_rows,
+                                               void* workspace, size_t workspace_bytes) {
+  return run_decode(q_bf16, kv_fp4, nullptr, qo_indptr, kv_indptr, out_bf16, stream, plan, nullptr,
+                    0, kv_rows, workspace, workspace_bytes, mla::CacheFormat::kMxfp4, true,
+                    kv_scales, scale_bias);
+}
+
 mla_status_t mla_decode_stage1_mxfp4(const void* q_bf16, const void* kv_fp4, const void* kv_scales,
                                      int32_t scale_bias, const int32_t* qo_indptr,
                                      const int32_t* kv_indptr, void* out_bf16, cudaStream_t stream,

@@ -676,6 +676,7 @@ __device__ void run_producer_mx(const Stage1Params& p, const CUtensorMap* map_v,
   if ((threadIdx.x & 31) != 0) return;
   Cursor cur;
   cursor_start(cur, ms);
+  if (p.stall_stream) cur.live = false;  // test hook: nothing is ever loaded
   uint32_t tile = 0;
   uint32_t v_fills = 0, r_fills = 0;  // latent / rope panels issued
   bool ok = true;

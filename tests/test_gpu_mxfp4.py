@@ -213,3 +213,27 @@ def test_mxfp4_cache_workloads(name):
     ref = case.reference(None if full else rows)
     st = assert_close(gpu, ref, None if full else rows)
     print(name, "grid", plan.grid, st)
+
+
+def test_mxfp4_more_rows_than_prologue_threads():
+    """1,000 rows (several per thread of the 512-thread prologue), lengths 0..300."""
+    rng = np.random.default_rng(1214)
+    lengths = rng.integers(0, 301, size=1000)
+    inp = make_from_lengths(lengths, seed=1214)
+    case = MxCase(inp)
+    gpu, err, _, _ = case.run()
+    assert err == 0
+    assert_close(gpu, case.reference())
+
+
+@pytest.mark.parametrize("k", range(4))
+def test_mxfp4_randomised_shapes(k):
+    rng = np.random.default_rng(1300 + k)
+    batch = int(rng.integers(1, 200))
+    lengths = rng.integers(0, 3000, size=batch)
+    lengths[rng.random(batch) < 0.1] = 0
+    inp = make_from_lengths(lengths, seed=1300 + k)
+    case = MxCase(inp)
+    gpu, err, _, _ = case.run(sms=int(rng.integers(1, 153)))
+    assert err == 0
+    assert_close(gpu, case.reference())

@@ -6,7 +6,8 @@ time limit.  The kernel must report MLA_DERR_TIMEOUT in the workspace error
 word, return, and leave the context usable: the next call on the same
 workspace gives the right answer.  Both the contiguous and the page-table
 kernels, with one, two and four query tokens (two sibling CTAs per worker),
-are covered.
+and the MXFP4 kernel (whose converter warps wait on the missing loads) are
+covered.
 """
 import time
 
@@ -48,3 +49,25 @@ def test_stalled_stream_times_out_and_the_context_survives(paged, qo_len):
     gpu, err, _, _ = dev.run(plan=plan, workspace=ws)
     assert err == 0
     assert_close(gpu, OracleCase(inp).reference())
+
+
+def test_mxfp4_stalled_stream_times_out_and_the_context_survives():
+    from oracle.mxfp4 import mla_decode_ref_mxfp4
+    from oracle.attention import bf16_bits_to_f64
+    from .test_gpu_mxfp4 import MxCase
+    inp = make_from_lengths([700, 300, 2000, 5], seed=32)
+    case = MxCase(inp)
+    plan = binding.mla_decode_plan(inp.batch, inp.max_kv_len, 6)
+    ws = binding.new_workspace(plan)
+    t0 = time.time()
+    binding.mla_decode_fwd_mxfp4_stall_stream(case.q, case.fp4, case.sc, case.qo_indptr,
+                                              case.kv_indptr, case.out, plan=plan, workspace=ws)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    err = binding.mla_decode_read_error(ws)
+    assert err == MLA_DERR_TIMEOUT, err
+    assert elapsed < 30.0
+    gpu, err, _, _ = case.run(plan=plan, workspace=ws)
+    assert err == 0
+    assert_close(gpu, mla_decode_ref_mxfp4(bf16_bits_to_f64(inp.q_bits), case.fp4_host, case.sc_host,
+                                           inp.qo_indptr, inp.kv_indptr))
