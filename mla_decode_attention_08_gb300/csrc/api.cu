@@ -282,6 +282,8 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
   p.slot_tokens = plan->qo_len;
   p.stall_stream = stall_stream ? 1 : 0;
   p.mx_bias = mx_bias;
+  p.kv_bytes = gather ? nullptr : static_cast<const uint8_t*>(kv);
+  p.kv_row_bytes = fmt == CacheFormat::kMxfp4 ? kQkDim / 2 : (fmt == CacheFormat::kBf16 ? 2 * kQkDim : kQkDim);
   return mla::launch_stage1(p, maps, gather, fmt, stream) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;

@@ -43,6 +43,9 @@ struct Stage1Params {
   int32_t stall_stream;       // test hook: the producers issue no cache loads, so the
                               // pipeline waits run out (bounded) and the call gives up
   int32_t mx_bias;            // MXFP4 cache: e4m3 panels hold e2m1 * 2^(e - 127 - mx_bias)
+  const uint8_t* kv_bytes;    // contiguous rows: the cache (or MXFP4 elements) for an L2
+                              // prefetch of the first tile; null with a page table
+  int32_t kv_row_bytes;       // bytes per cached row in kv_bytes (576, 1152 or 288)
 };
 
 enum class CacheFormat { kE4m3, kBf16, kMxfp4 };

@@ -95,6 +95,10 @@ __device__ __forceinline__ void bulk_wait_all() {
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
+// Bulk L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned address.
+__device__ __forceinline__ void prefetch_bulk_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // ---------------------------------------------------------------- register split
 // Executed by all four warps of a warpgroup; the block's registers (threads x

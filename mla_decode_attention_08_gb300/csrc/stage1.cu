@@ -475,7 +475,20 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
             q_lo = ldg_i32(p.qo_indptr + b);
             q_hi = ldg_i32(p.qo_indptr + b + 1);
           }
-          ms->first_tq = row_token(p, cta_q_off(p), q_lo, q_hi);
+          const int32_t tq = row_token(p, cta_q_off(p), q_lo, q_hi);
+          ms->first_tq = tq;
+          // Warm L2 with what the pipeline reads first: this CTA's query
+          // tokens of the row and (contiguous rows) the worker's first tile,
+          // while the roles are still starting up.
+          if (tq >= 0)
+            prefetch_bulk_l2(p.q + static_cast<size_t>(tq) * kNumHeads * kQkDim,
+                             static_cast<uint32_t>(cta_tokens<kQ>(p)) * kNumHeads * kQkDim * 2);
+          if (p.kv_bytes != nullptr) {
+            const int32_t j0 = t0 - a;
+            const int32_t rows = min(kTileTokens, (next - prev) - j0 * kTileTokens);
+            prefetch_bulk_l2(p.kv_bytes + (static_cast<int64_t>(prev) + j0 * kTileTokens) * p.kv_row_bytes,
+                             static_cast<uint32_t>(rows * p.kv_row_bytes));
+          }
         }
         if (a <= t1 - 1 && t1 - 1 < a + nt) ms->last_row = b;
       }
