@@ -118,13 +118,6 @@ struct Geo {
                                               : idesc_bf16(128, kN, false, false);
   static constexpr uint32_t kIdescPV = kSplit ? idesc_e4m3(128, kN, true, true)
                                               : idesc_bf16(128, kN, true, true);
-
-  // 8 KB staging buffers of the epilogue: the Q operand region (4 kQ panels of
-  // 4 KB) then the two P buffers.
-  static constexpr int kNumStage = 2 * kQ + 2 * kPBytes / 8192;
-  static __device__ __forceinline__ uint32_t stage_buf(uint32_t sbase, int k) {
-    return k < 2 * kQ ? sbase + kOffQ + 8192 * k : sbase + kOffP + 8192 * (k - 2 * kQ);
-  }
 };
 
 struct Misc {
@@ -158,7 +151,6 @@ struct Misc {
   int32_t first_kb, first_len, first_tq;
   int32_t bad;
   uint32_t next_panel[6];  // per producer warp: one past its last issued panel
-  alignas(16) float lse_stage[16 * kMaxQ];  // a split piece's base-2 LSE on its way out (bulk store)
   alignas(16) float alpha_stage[16 * kMaxQ];  // O rescale factors of the current tile (thread 0 writes)
 };
 
@@ -1227,9 +1219,9 @@ __device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t 
       }
     }
   }
-  // The previous segment's output may still be leaving the Q and P regions
-  // through bulk stores (the loads above are already in flight); the barrier
-  // below orders every write to them after this wait.
+  // The previous segment's output row may still be leaving the Q region
+  // through a bulk store (the loads above are already in flight); the barrier
+  // below orders every write to it after this wait.
   if (t == 0) bulk_wait_read<0>();
   if constexpr (kFmt == Kv::kBf16)
     store_q_bf16<kQ>(sq, raw, qk_scale);
@@ -1523,10 +1515,10 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     }
 
     // ------------------------------------------------ segment epilogue
-    // The output leaves through the TMA engine: O is staged in shared memory
-    // (the Q and P regions are free once the segment's last PV has completed)
-    // and one thread issues bulk stores, so the warps do not wait for their
-    // global stores to drain before the next segment.
+    // A row held whole leaves through the TMA engine (staged in the Q region,
+    // free once the segment's last PV has completed; one bulk store); a split
+    // piece leaves through every thread's own global stores.  Neither waits
+    // for its stores to drain before the next segment.
     if (cur.next_a < ms->t1 && b + 1 < p.batch) {
       // More segments follow: bring the next row's query into L2 now, so that
       // its Q preparation after this epilogue reads it from there.
@@ -1593,51 +1585,40 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     } else {
       // bf16 partial of query token qi (as the pages keep their split
       // outputs), stored [slot][slot_q + qi][dim / 128][head / 8][dim % 128][head % 8]:
-      // each 128-dim chunk is 4 KB of contiguous memory, staged in the 8 KB
-      // buffers of Geo (the Q region, then the P buffers), reused once their
-      // bulk store has read them.  The float base-2 log-sum-exps follow the
-      // last chunk in the same bulk group.
+      // each 128-dim chunk is 4 KB of contiguous memory, in which this thread's
+      // dim owns two 16-byte pieces (heads 0-7 and 8-15), so every thread
+      // stores its own values straight from registers (a warp's stores are
+      // 512 contiguous bytes) and nothing waits for them to drain.  The float
+      // base-2 log-sum-exps follow, one per (token, head).
       const int32_t slot = partial_slot(c, ms->t0, cur.row_a);
+      const size_t piece = static_cast<size_t>(slot) * p.slot_tokens + slot_q;  // (slot, token)
 #pragma unroll 1
       for (int k = 0; k < 4 * nq; ++k) {
         const int qi = k >> 2, cc = k & 3;
         float o[16];
         tmem_ld_heads<kFmt>(tmem + lane_base + G::kColO + G::kN * cc + G::kTokCols * qi, o);
-        const uint32_t buf = G::stage_buf(sbase, k % G::kNumStage);
-        if (k >= G::kNumStage) {  // reuses the buffer of chunk k - kNumStage
-          if (t == 0) bulk_wait_read<G::kNumStage - 1>();
-          named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-        }
         if (write) {
           float v[16];
 #pragma unroll
           for (int h = 0; h < 16; ++h) v[h] = o[h] * inv[qi][h];
+          uint4* dst = reinterpret_cast<uint4*>(p.partial + ((piece + qi) * 4 + cc) * (kNumHeads * 128));
 #pragma unroll
           for (int j = 0; j < 2; ++j)
-            st_shared_v4(buf + (j * 128 + token) * 16, pack_bf16x2(v[8 * j], v[8 * j + 1]),
-                         pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                         pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
-                         pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-          if (k == 4 * nq - 1 && t < 16 * nq) {
-            // thread t stages the LSE of (token t / 16, head t % 16); -inf when it saw nothing
-            float mm = m_ref[0][0], ll = l_tot[0][0];
+            dst[j * 128 + token] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                                              pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                              pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                                              pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+        }
+      }
+      if (write && t < 16 * nq) {
+        // thread t writes the LSE of (token t / 16, head t % 16); -inf when it saw nothing
+        float mm = m_ref[0][0], ll = l_tot[0][0];
 #pragma unroll
-            for (int e = 1; e < 16 * kQ; ++e) {
-              mm = t == e ? m_ref[e >> 4][e & 15] : mm;
-              ll = t == e ? l_tot[e >> 4][e & 15] : ll;
-            }
-            ms->lse_stage[t] = mm + log2f(ll);
-          }
+        for (int e = 1; e < 16 * kQ; ++e) {
+          mm = t == e ? m_ref[e >> 4][e & 15] : mm;
+          ll = t == e ? l_tot[e >> 4][e & 15] : ll;
         }
-        fence_proxy_async_smem();
-        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-        if (t == 0 && write) {
-          const size_t piece = static_cast<size_t>(slot) * p.slot_tokens + slot_q;  // (slot, token)
-          bulk_store(p.partial + ((piece + qi) * 4 + cc) * (kNumHeads * 128), buf, kNumHeads * 128 * 2);
-          if (k == 4 * nq - 1)
-            bulk_store(p.lse + piece * kNumHeads, smem_u32(ms->lse_stage), nq * kNumHeads * 4);
-          bulk_commit();
-        }
+        p.lse[piece * kNumHeads + t] = mm + log2f(ll);
       }
     }
     // O has been read out (tcgen05.wait::ld above): the next segment's PV may
