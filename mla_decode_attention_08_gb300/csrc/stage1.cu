@@ -1320,18 +1320,29 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     }
   };
 
+  // A segment's Q operand is normally prepared at its start; with one query
+  // token per CTA, after a split piece (whose epilogue uses no shared memory)
+  // the next segment's is prepared before that epilogue instead, so that its
+  // first QKs overlap the epilogue.
+  bool q_early = false;
+  int32_t tq_early = -1;
+  float qk_scale[kQ];
   while (cur.live) {
     // ------------------------------------------------ segment start
     const int32_t b = cur.b;
     // This launch's first query token of the row.
-    const int32_t tq = cur.seg == 0 ? ms->first_tq
-                                    : row_token(p, q_off, ldg_i32(p.qo_indptr + b), ldg_i32(p.qo_indptr + b + 1));
+    const int32_t tq = q_early ? tq_early
+                               : (cur.seg == 0 ? ms->first_tq
+                                               : row_token(p, q_off, ldg_i32(p.qo_indptr + b),
+                                                           ldg_i32(p.qo_indptr + b + 1)));
     const bool row_ok = tq >= 0;
     if (!row_ok && t == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
-    if (cur.seg > 0) softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
-    float qk_scale[kQ];
-    prepare_q<kQ, kFmt>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, nq, kv_scale, qk_scale);
-    if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 1));
+    if (!q_early) {
+      if (cur.seg > 0) softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
+      prepare_q<kQ, kFmt>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, nq, kv_scale, qk_scale);
+      if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 1));
+    }
+    q_early = false;
 
     float m_ref[kQ][16], l[kQ][16];
 #pragma unroll
@@ -1514,12 +1525,27 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       ++cur.j;
     }
 
+    // ------------------------------------------------ next segment's Q, early
+    // (one query token per CTA: with two, the early preparation measured slower,
+    // 70.8 -> 82.9 us of stage 1 on bs64 with two tokens per row)
+    if (kQ == 1 && !cur.whole) {
+      Cursor nxt = cur;
+      if (cursor_next_tile(nxt, ms, p.kv_indptr, p.batch)) {
+        tq_early = row_token(p, q_off, ldg_i32(p.qo_indptr + nxt.b), ldg_i32(p.qo_indptr + nxt.b + 1));
+        // the QK of this segment's last tile has released the Q region
+        softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), cur.seg & 1, ms, p.err);
+        prepare_q<kQ, kFmt>(p, ms, sbase + G::kOffQ, tq_early, nq, kv_scale, qk_scale);
+        if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 2));
+        q_early = true;
+      }
+    }
+
     // ------------------------------------------------ segment epilogue
     // A row held whole leaves through the TMA engine (staged in the Q region,
     // free once the segment's last PV has completed; one bulk store); a split
     // piece leaves through every thread's own global stores.  Neither waits
     // for its stores to drain before the next segment.
-    if (cur.next_a < ms->t1 && b + 1 < p.batch) {
+    if ((kQ > 1 || cur.whole) && cur.next_a < ms->t1 && b + 1 < p.batch) {
       // More segments follow: bring the next row's query into L2 now, so that
       // its Q preparation after this epilogue reads it from there.
       const int32_t tq_next = ldg_i32(p.qo_indptr + b + 1) + q_off;
