@@ -54,6 +54,8 @@ typedef enum {
 #define MLA_DERR_TIMEOUT 8    /* a pipeline wait ran past its time limit; the call gave up  */
 #define MLA_DERR_MX_SCALE 16  /* MXFP4 cache: a block holding a nonzero element has a scale
                                  outside the exact window of mla_decode_fwd_mxfp4 (or NaN)  */
+#define MLA_DERR_DEBUG_BOUNDS 32 /* debug builds only: an index failed its bounds check and the
+                                    access was skipped (never set by release builds)        */
 
 /*
  * Launch plan for a batch shape.  The split-KV schedule (flash-decoding split,

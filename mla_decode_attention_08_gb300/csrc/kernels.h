@@ -6,6 +6,18 @@
 
 namespace mla {
 
+// Debug builds (-DMLA_DEBUG, `build(debug=True)`): every global store of the
+// kernels, the query loads, the cache tile coordinates and the converters'
+// shared-memory addresses are checked against their buffers first; a failed
+// check sets MLA_DERR_DEBUG_BOUNDS in the workspace error word and skips the
+// access (a stand-in for a memory checker, which this toolchain's pool does not
+// offer).  Release builds compile the checks away.
+#ifdef MLA_DEBUG
+#define MLA_DCHECK(cond, err) ((cond) ? true : (atomicOr((err), MLA_DERR_DEBUG_BOUNDS), false))
+#else
+#define MLA_DCHECK(cond, err) true
+#endif
+
 // Stage 1 ring: two rope slots (128 tokens x 64 dims); the latent slots and
 // every size depend on the cache format (stage1.cu, Geo).
 constexpr int kNumRSlots = 2;

@@ -370,6 +370,15 @@ __device__ __forceinline__ int32_t row_token(const Stage1Params& p, int32_t q_of
   return ok ? q_lo + q_off : -1;
 }
 
+// Query tokens of the batch (rows x tokens per row), the bound of q and out.
+__device__ __forceinline__ int64_t total_tokens(const Stage1Params& p) {
+  return static_cast<int64_t>(p.batch) * p.row_tokens;
+}
+// bf16 elements of the split partials (2 slots per worker).
+__device__ __forceinline__ int64_t partial_elems(const Stage1Params& p) {
+  return 2LL * p.grid * p.slot_tokens * kNumHeads * kVDim;
+}
+
 // ------------------------------------------------------------ schedule prologue
 
 // All threads.  Tile counts of every row, their prefix, this worker's range
@@ -382,6 +391,7 @@ template <int kQ>
 __device__ __forceinline__ void zero_row(const Stage1Params& p, int32_t b) {
   const int32_t tq = row_token(p, cta_q_off(p), ldg_i32(p.qo_indptr + b), ldg_i32(p.qo_indptr + b + 1));
   if (tq < 0) return;
+  if (!MLA_DCHECK(tq + cta_tokens<kQ>(p) <= total_tokens(p), p.err)) return;
   uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(tq) * kNumHeads * kVDim);
   const int n = cta_tokens<kQ>(p) * kNumHeads * kVDim * 2 / 16;
   for (int i = 0; i < n; ++i) dst[i] = make_uint4(0, 0, 0, 0);
@@ -614,6 +624,11 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
         const int boxes = G::kSplit || c < 0 ? 1 : 2;
         if (use > 0) ok = wait_phase(empty, (use - 1) & 1, ms, p.err);
         if (!ok) break;
+        if (!MLA_DCHECK(tok0 >= 0 && tok0 < p.kv_rows && (x & 15) == 0, p.err)) {
+          ms->abort_flag = 1;  // the waiters on this panel see it and give up
+          ok = false;
+          break;
+        }
         mbar_arrive_expect_tx(full, bytes);
         for (int i = 0; i < boxes; ++i)
           tma_load_2d(dst + i * kTileTokens * 128, map, x + 128 * i, tok0, full);
@@ -691,6 +706,11 @@ __device__ void run_producer_mx(const Stage1Params& p, const CUtensorMap* map_v,
       const uint32_t slot = tile % kNumRSlots, use = tile / kNumRSlots;
       if (use > 0) ok = wait_phase(smem_u32(&ms->s_full[slot]), (use - 1) & 1, ms, p.err);
       if (!ok) break;
+      if (!MLA_DCHECK(tok0 >= 0 && tok0 < p.kv_rows, p.err)) {
+        ms->abort_flag = 1;
+        ok = false;
+        break;
+      }
       const uint32_t full = smem_u32(&ms->rraw_full[slot]);
       mbar_arrive_expect_tx(full, kTileTokens * 32 + kSclSlotBytes);
       tma_load_2d(sbase + G::kOffR + slot * G::kRSlotBytes + G::kRRawOff, map_r, kVDim / 2, tok0,
@@ -1210,7 +1230,7 @@ __device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t 
     for (int r = 0; r < 5; ++r) {
       const int job = t + 128 * r;
       raw[qi][r][0] = raw[qi][r][1] = make_uint4(0, 0, 0, 0);
-      if (job < 576 && tq >= 0 && qi < nq) {
+      if (job < 576 && tq >= 0 && qi < nq && MLA_DCHECK(tq + qi < total_tokens(p), p.err)) {
         const int head = job / 36, ch = job % 36;
         const uint4* src = reinterpret_cast<const uint4*>(
             p.q + (static_cast<size_t>(tq + qi) * kNumHeads + head) * kQkDim + ch * 16);
@@ -1603,7 +1623,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       }
       fence_proxy_async_smem();
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-      if (t == 0 && write) {
+      if (t == 0 && write && MLA_DCHECK(tq + nq <= total_tokens(p), p.err)) {
         bulk_store(p.out + static_cast<size_t>(tq) * kNumHeads * kVDim, stage_q,
                    nq * kNumHeads * kVDim * 2);
         bulk_commit();
@@ -1628,9 +1648,11 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
 #pragma unroll
           for (int h = 0; h < 16; ++h) v[h] = o[h] * inv[qi][h];
           uint4* dst = reinterpret_cast<uint4*>(p.partial + ((piece + qi) * 4 + cc) * (kNumHeads * 128));
+          const int64_t last = static_cast<int64_t>(((piece + qi) * 4 + cc) * (kNumHeads * 128)) +
+                               (128 + token) * 8 + 8;
 #pragma unroll
           for (int j = 0; j < 2; ++j)
-            dst[j * 128 + token] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
+            if (MLA_DCHECK(last <= partial_elems(p), p.err)) dst[j * 128 + token] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
                                               pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
                                               pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
                                               pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
@@ -1644,7 +1666,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
           mm = t == e ? m_ref[e >> 4][e & 15] : mm;
           ll = t == e ? l_tot[e >> 4][e & 15] : ll;
         }
-        p.lse[piece * kNumHeads + t] = mm + log2f(ll);
+        if (MLA_DCHECK(static_cast<int64_t>(piece) * kNumHeads + t < partial_elems(p) / kVDim, p.err))
+          p.lse[piece * kNumHeads + t] = mm + log2f(ll);
       }
     }
     // O has been read out (tcgen05.wait::ld above): the next segment's PV may

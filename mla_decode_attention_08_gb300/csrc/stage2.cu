@@ -43,6 +43,8 @@ __global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const
   const int4 job = rec[2 * c + 1];  // (output row, first worker, last worker, first slot)
   if (job.x < 0) return;
   const int32_t tq = job.x + qi;  // output row: query token qi of the row
+  if (!MLA_DCHECK(tq < p.batch * nq && job.y >= 0 && job.z < p.grid && job.w < 2 * p.grid, p.err))
+    return;
 
   const float4* lse4 = reinterpret_cast<const float4*>(p.lse);
   const uint2* part8 = reinterpret_cast<const uint2*>(p.partial);
@@ -61,8 +63,10 @@ __global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const
 #pragma unroll
     for (int u = 0; u < kStage2Unroll; ++u) {
       const int32_t cu = w0 + u;
+      wr[u] = make_int4(0, 0, 0, 0);  // an empty record: the slot is skipped below
       if (cu <= job.z) {
         const int32_t piece = (cu == job.y ? job.w : 2 * cu) * nq + qi;  // (slot, token)
+        if (!MLA_DCHECK(piece < 2 * p.grid * nq, p.err)) continue;
         wr[u] = rec[2 * cu];
         x[u] = lse4[piece * 4 + j];
         v[u] = part8[(((static_cast<size_t>(piece) * 4 + cc) * 2 + (j >> 1)) * kStage2Threads + dd) * 2 +
