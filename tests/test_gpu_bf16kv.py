@@ -142,3 +142,17 @@ def test_bf16_cache_workloads(name):
     toks = None if rows is None else [n * b + i for b in rows for i in range(n)]
     st = assert_close(gpu, ref, toks, rel_l2_max=REL_L2_BF16)
     print(name, "grid", plan.grid, st)
+
+
+@pytest.mark.parametrize("k", range(4))
+def test_bf16_cache_randomised_shapes(k):
+    rng = np.random.default_rng(1400 + k)
+    batch = int(rng.integers(1, 200))
+    qo_len = int(rng.integers(1, 5))
+    lengths = rng.integers(0, 3000, size=batch)
+    lengths[rng.random(batch) < 0.1] = 0
+    inp = make_from_lengths(lengths, seed=1400 + k, qo_len=qo_len)
+    case = Bf16Case(inp)
+    gpu, err, _, _ = case.run(sms=int(rng.integers(1, 153)))
+    assert err == 0
+    assert_close(gpu, case.reference(), rel_l2_max=REL_L2_BF16)
