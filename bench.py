@@ -543,9 +543,15 @@ def ours_main(args) -> None:
             ww = w if name == args.workload else DeviceWorkload(name, torch, binding, sms)
             entry = {"workload": name, **cold(ww.call, ww.bytes), "grid": int(ww.plan.grid),
                      "l2": "flushed before each call"}
+            # the same step back to back (L2 warm for the small workloads), for reference
+            entry["us_back_to_back"] = round(time_loop(torch, ww.call, 50, stream) / 50 * 1e3, 2)
             # the same step over the bf16 cache (mla_decode_fwd_bf16kv; contiguous caches only)
-            entry["bf16_cache"] = (cold(ww.call_bf16kv, ww.bytes_bf16) if ww.kv_indices is None
-                                   else {"unsupported": "page table (bf16 caches are read contiguously)"})
+            if ww.kv_indices is None:
+                bf = cold(ww.call_bf16kv, ww.bytes_bf16)
+                bf["us_back_to_back"] = round(time_loop(torch, ww.call_bf16kv, 50, stream) / 50 * 1e3, 2)
+                entry["bf16_cache"] = bf
+            else:
+                entry["bf16_cache"] = {"unsupported": "page table (bf16 caches are read contiguously)"}
             # and over the MXFP4 cache (mla_decode_fwd_mxfp4), with its stage 1 timed
             # alone back to back (the MXFP4 kernel's roofline)
             if ww.mx:
