@@ -69,8 +69,10 @@ typedef struct {
   int32_t batch;       /* B, rows (one query token each)                          */
   int32_t max_kv_len;  /* upper bound on any row's cached tokens (sizes the grid)  */
   int32_t num_sms;     /* SMs the grid is sized for                               */
-  int32_t grid;        /* persistent stage-1 workers: max(1, min(S, B*ceil(max_kv_len/128))),
-                        * S = num_sms, or num_sms/2 for qo_len >= 3 (two CTAs per worker) */
+  int32_t grid;        /* persistent stage-1 workers: with U = B*ceil(max_kv_len/128) and
+                        * S = num_sms (num_sms/2 for qo_len >= 3: two CTAs per worker),
+                        * k = ceil(U / min(S, U)) tiles for the longest range and
+                        * grid = max(1, ceil(U / k)): the fewest workers that keep it */
   int32_t tile_tokens; /* 128                                                      */
   int32_t abi_version; /* MLA_ABI_VERSION                                          */
   int32_t qo_len;      /* query tokens per row: 1 (decode) to 4 (multi-token decode) */

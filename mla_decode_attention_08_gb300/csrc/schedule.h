@@ -27,10 +27,18 @@ MLA_HD int32_t tiles_of_length(int64_t len) {
   return len > 0 ? static_cast<int32_t>((len + kTileTokens - 1) / kTileTokens) : 0;
 }
 
+// Workers for a batch: the fewest that still give no worker more than
+// k = ceil(U / min(num_sms, U)) tiles, U = B * ceil(max_kv_len / 128), i.e.
+// ceil(U / k).  Fewer workers than SMs when that does not lengthen the longest
+// range: the ranges then hold k tiles each and, for rows of a multiple of k
+// tiles, start at row starts (bs 32 x 1024: 128 workers of two tiles instead
+// of 152 of one or two, some of which straddle two rows).
 MLA_HD int32_t plan_grid(int32_t batch, int32_t max_kv_len, int32_t num_sms) {
-  int64_t upper = static_cast<int64_t>(batch) * tiles_of_length(max_kv_len);
-  int64_t g = upper < num_sms ? upper : num_sms;
-  return g < 1 ? 1 : static_cast<int32_t>(g);
+  const int64_t upper = static_cast<int64_t>(batch) * tiles_of_length(max_kv_len);
+  const int64_t g0 = upper < num_sms ? upper : num_sms;
+  if (g0 < 1) return 1;
+  const int64_t k = (upper + g0 - 1) / g0;
+  return static_cast<int32_t>((upper + k - 1) / k);
 }
 
 // floor(c * total / grid) for 0 <= c <= grid and total >= 0, without a 64-bit

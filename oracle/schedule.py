@@ -13,7 +13,9 @@ as follows (the pages print no formula for their persistent work map):
 * every row is cut into tiles of ``TILE_TOKENS`` tokens, ``ceil(L_b / 128)``
   tiles, the last one partial; the tiles of all rows, row after row, form one
   global sequence of ``T`` tiles;
-* the grid has ``G = max(1, min(num_sms, B * ceil(max_kv_len / 128)))`` workers;
+* the grid has the fewest workers ``G`` whose longest equal split of the
+  batch's upper bound ``U = B * ceil(max_kv_len / 128)`` tiles is no longer
+  than with ``min(num_sms, U)`` workers (1 for an empty batch);
   worker c takes the contiguous tile range ``[floor(c T / G), floor((c+1) T / G))``;
 * the part of a row inside one worker's range is a segment; a row covered by a
   single worker is "whole", otherwise "split" and each of its segments writes a
@@ -34,9 +36,18 @@ def ceil_div(a: int, b: int) -> int:
 
 
 def plan_grid(batch: int, max_kv_len: int, num_sms: int) -> int:
-    """Number of persistent workers for a batch of ``batch`` rows."""
+    """Number of persistent workers for a batch of ``batch`` rows: the fewest
+    that give no worker more tiles than spreading the batch's upper bound
+    ``U = batch * ceil(max_kv_len / 128)`` over ``min(num_sms, U)`` workers."""
     upper = batch * ceil_div(max(0, max_kv_len), TILE_TOKENS)
-    return max(1, min(num_sms, upper))
+    g0 = min(num_sms, upper)
+    if g0 < 1:
+        return 1
+    most = ceil_div(upper, g0)          # tiles of the longest range
+    for g in range(1, g0 + 1):          # the fewest workers with ranges no longer
+        if ceil_div(upper, g) <= most:
+            return g
+    return g0
 
 
 def row_tiles(kv_indptr) -> list[int]:

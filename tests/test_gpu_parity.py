@@ -327,7 +327,7 @@ def test_one_very_long_row_among_short_ones():
     inp = make_from_lengths([100_000, 3, 0, 129], seed=73)
     dev = DeviceCase(inp)
     gpu, err, plan, _ = dev.run()
-    assert err == 0 and plan.grid == num_sms()
+    assert err == 0 and plan.grid == plan_grid(inp.batch, inp.max_kv_len, num_sms()) >= 140
     assert_close(gpu, OracleCase(inp).reference())
 
 

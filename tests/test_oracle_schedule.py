@@ -19,8 +19,8 @@ def test_hand_derived_case():
 
 
 @pytest.mark.parametrize("batch,max_len,sms,want", [
-    (4, 1024, 152, 32), (32, 1024, 152, 152), (256, 8192, 152, 152),
-    (1, 0, 152, 1), (3, 1, 152, 3), (0, 100, 152, 1)])
+    (4, 1024, 152, 32), (32, 1024, 152, 128), (64, 8192, 152, 152), (256, 8192, 152, 152),
+    (64, 8192, 76, 76), (1, 0, 152, 1), (3, 1, 152, 3), (0, 100, 152, 1), (200, 128, 152, 100)])
 def test_plan_grid(batch, max_len, sms, want):
     assert plan_grid(batch, max_len, sms) == want
 
