@@ -137,6 +137,13 @@ mla_status_t mla_decode_plan_mtp(int32_t batch, int32_t qo_len, int32_t max_kv_l
  *              error word starts clear.  Calls sharing a workspace must not
  *              overlap on the GPU.
  * Output is deterministic for a given plan.  Returns MLA_OK after launching.
+ * Calls with their own workspaces may run concurrently on different streams.
+ * The call allocates nothing and never synchronises, so it can be captured into
+ * a CUDA graph (make one call on the device outside capture first).  The split
+ * schedule is derived on the device from kv_indptr, so a replayed graph follows
+ * new values in the same buffers (query, cache, kv_indptr, page table) as long
+ * as every row stays within plan->max_kv_len, kv_indptr[B] within
+ * kv_indices_len (page table) or kv_rows (contiguous rows).
  */
 mla_status_t mla_decode_fwd(const void* q_bf16, const void* kv_fp8, const float* kv_scale,
                             const int32_t* qo_indptr, const int32_t* kv_indptr, void* out_bf16,
