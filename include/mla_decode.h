@@ -165,11 +165,14 @@ mla_status_t mla_decode_fwd(const void* q_bf16, const void* kv_fp8, const float*
  *   MLA_STATIC_SCRATCH_BYTES (on a 152-SM GB300 every batch of up to ~600,000
  *   rows fits).
  *   The first call on a device looks up that device's copy of the array; make
- *   that first call before any stream capture.
+ *   that first call before any stream capture.  A device other than sm_103
+ *   returns MLA_ERR_UNSUPPORTED.
  *   All calls share the one array: calls that may overlap on the GPU (different
  *   streams, or different host threads on the same device) race and must be
- *   ordered by the caller.  Device-side input errors (MLA_DERR_*) are not
- *   reported through this entry point; use mla_decode_fwd to diagnose inputs.
+ *   ordered by the caller.  The array's error word collects the MLA_DERR_*
+ *   bits of every call (it starts clear when the library is loaded); read and
+ *   clear it with mla_decode_static_scratch_read_error, e.g. to learn that a
+ *   call gave up on a wait (MLA_DERR_TIMEOUT) and its output is not valid.
  */
 #define MLA_STATIC_SCRATCH_BYTES (12u * 1024u * 1024u)
 mla_status_t mla_decode_fwd_static_scratch(const void* q_bf16, const void* kv_fp8,
@@ -178,6 +181,13 @@ mla_status_t mla_decode_fwd_static_scratch(const void* q_bf16, const void* kv_fp
                                            cudaStream_t stream, const mla_plan_t* plan,
                                            const int32_t* kv_indices, int64_t kv_indices_len,
                                            int64_t kv_rows);
+
+/* Read (and, when clear != 0, reset) the error word of the current device's
+ * static scratch, as mla_decode_read_error does for a workspace.  Synchronises
+ * `stream` (order it after the calls to be checked); off the hot path.  Copies
+ * four bytes to the host and allocates nothing. */
+mla_status_t mla_decode_static_scratch_read_error(int32_t* err_host, int32_t clear,
+                                                  cudaStream_t stream);
 
 /*
  * mla_decode_fwd_bf16kv — the decode step over a bf16 latent cache, as the
@@ -282,6 +292,46 @@ mla_status_t mla_decode_fwd_mxfp4_stall_stream(const void* q_bf16, const void* k
                                                void* out_bf16, cudaStream_t stream,
                                                const mla_plan_t* plan, int64_t kv_rows,
                                                void* workspace, size_t workspace_bytes);
+
+/*
+ * mla_debug_q_operand — test hook (no counterpart on the pages): the query
+ * operand of the e4m3-cache step exactly as a stage-1 CTA builds it in shared
+ * memory, copied out.  The pages hand the tensor cores an FP8 query (submission
+ * 722089 `_mla_multihead_stage1` casts each query chunk to float8e4nv;
+ * submissions 663509 and 738050 quantise Q per tensor); this library keeps the
+ * bf16 query's precision with two e4m3 terms per value.  Per query token:
+ * a = max |q| over its 16 x 576 values, k2 the integer with
+ * 224 < a * 2^k2 <= 448 (clamped to [-126, 126]; 0 when a = 0),
+ * x = float32(q * 2^k2), hi = e4m3(x), lo = e4m3(float32(16 * (x - hi))), both
+ * rounded to nearest even and saturating; the QK accumulator of the token is
+ * turned into base-2 softmax units by qk_scale = 2^-k2 * kv_scale * log2(e) / 24.
+ *   q_bf16         device bf16 [num_tokens, 16, 576], 16-byte aligned.
+ *   num_tokens     1 .. 2^24.
+ *   tokens_per_cta 1 or 2: run the one- or two-token form of the operand code
+ *                  (a stage-1 CTA takes up to two query tokens of a row).
+ *   kv_scale       device float[1].
+ *   codes_out      device uint8 [num_tokens, 2, 16, 576]: hi codes of the 16
+ *                  heads, then lo codes; 16-byte aligned.
+ *   qk_scale_out   device float [num_tokens].
+ * One kernel on `stream`; returns MLA_OK after launching.
+ */
+mla_status_t mla_debug_q_operand(const void* q_bf16, int32_t num_tokens, int32_t tokens_per_cta,
+                                 const float* kv_scale, void* codes_out, float* qk_scale_out,
+                                 cudaStream_t stream);
+
+/*
+ * mla_debug_p_split — test hook (no counterpart on the pages): the two-term
+ * e4m3 probability operand of the e4m3-cache step, by stage 1's own code.  The
+ * pages round P to bf16 before P . V (submission 722089 `_mla_multihead_stage1`);
+ * here p16 = float16(p), hi = e4m3(p16), lo = e4m3(float16(16 * (p16 - hi))),
+ * every step rounded to nearest even in half precision.
+ *   p       device float [n] (0 <= p <= 256 in the kernel), 16-byte aligned.
+ *   n       a multiple of 16, >= 16.
+ *   hi_out, lo_out  device uint8 [n], 16-byte aligned.
+ * One kernel on `stream`; returns MLA_OK after launching.
+ */
+mla_status_t mla_debug_p_split(const float* p, int64_t n, void* hi_out, void* lo_out,
+                               cudaStream_t stream);
 
 /*
  * mla_fp8_quantize_per_tensor — per-tensor absmax quantisation of a bf16 tensor

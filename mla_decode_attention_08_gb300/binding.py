@@ -52,10 +52,13 @@ SIGNATURES = {
     "mla_decode_fwd_bf16kv": (ctypes.c_int, _FWD_BF16KV_ARGS),
     "mla_decode_stage1_bf16kv": (ctypes.c_int, _FWD_BF16KV_ARGS),
     "mla_decode_fwd_static_scratch": (ctypes.c_int, _FWD_ARGS[:-2]),
+    "mla_decode_static_scratch_read_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), _I32, _VP]),
     "mla_decode_fwd_mxfp4": (ctypes.c_int, _FWD_MXFP4_ARGS),
     "mla_decode_stage1_mxfp4": (ctypes.c_int, _FWD_MXFP4_ARGS),
     "mla_decode_fwd_mxfp4_stall_stream": (ctypes.c_int, _FWD_MXFP4_ARGS),
     "mla_mxfp4_quantize": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP]),
+    "mla_debug_q_operand": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP, _VP, _VP]),
+    "mla_debug_p_split": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP]),
     "mla_decode_stage2": (ctypes.c_int, [_VP, _VP, _VP, _PLANP, _VP, _SZ]),
     "mla_fp8_quantize_per_tensor": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP, _SZ, _VP]),
     "mla_decode_workspace_init": (ctypes.c_int, [_VP, _SZ, _VP]),
@@ -116,10 +119,21 @@ def mla_decode_plan(batch: int, max_kv_len: int, num_sms: int = 0, qo_len: int =
     return plan
 
 
+def _e4m3_cache(kv_fp8) -> torch.Tensor:
+    """The e4m3 cache as [rows, 576] bytes; anything else is refused (a bf16 or
+    MXFP4 cache passed here would otherwise be read as e4m3 codes)."""
+    if not isinstance(kv_fp8, torch.Tensor):
+        raise TypeError("kv_fp8 must be a CUDA tensor")
+    if kv_fp8.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError(f"kv_fp8 must hold e4m3fn codes (uint8 or float8_e4m3fn), got {kv_fp8.dtype}")
+    if kv_fp8.dim() not in (2, 3) or kv_fp8.numel() != kv_fp8.shape[0] * QK_HEAD_DIM:
+        raise ValueError(f"kv_fp8 must be [rows, 576] or [rows, 1, 576], got {tuple(kv_fp8.shape)}")
+    return kv_fp8.reshape(kv_fp8.shape[0], QK_HEAD_DIM)
+
+
 def _fwd_args(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream, plan, kv_indices,
               workspace):
-    if kv_fp8.dim() == 3:
-        kv_fp8 = kv_fp8.reshape(kv_fp8.shape[0], -1)
+    kv_fp8 = _e4m3_cache(kv_fp8)
     kv_rows = int(kv_fp8.shape[0])
     return (_dev_ptr(q, "q", torch.bfloat16), _dev_ptr(kv_fp8, "kv_fp8"),
             _dev_ptr(kv_scale, "kv_scale", torch.float32),
@@ -229,8 +243,7 @@ def mla_decode_fwd_static_scratch(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out
                                   plan, kv_indices=None) -> torch.Tensor:
     """Decode step with the library's own static scratch instead of a workspace,
     for callers that may not allocate device memory (see the C header)."""
-    if kv_fp8.dim() == 3:
-        kv_fp8 = kv_fp8.reshape(kv_fp8.shape[0], -1)
+    kv_fp8 = _e4m3_cache(kv_fp8)
     _check("mla_decode_fwd_static_scratch", load_library().mla_decode_fwd_static_scratch(
         _dev_ptr(q, "q", torch.bfloat16), _dev_ptr(kv_fp8, "kv_fp8"),
         _dev_ptr(kv_scale, "kv_scale", torch.float32), _dev_ptr(qo_indptr, "qo_indptr", torch.int32),
@@ -238,6 +251,15 @@ def mla_decode_fwd_static_scratch(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out
         _stream(stream), ctypes.byref(plan), _dev_ptr(kv_indices, "kv_indices", torch.int32),
         0 if kv_indices is None else int(kv_indices.numel()), int(kv_fp8.shape[0])))
     return out
+
+
+def mla_decode_static_scratch_read_error(clear: bool = True, stream=None) -> int:
+    """Error word of the current device's static scratch (MLA_DERR_* bits)."""
+    v = ctypes.c_int32(0)
+    _check("mla_decode_static_scratch_read_error",
+           load_library().mla_decode_static_scratch_read_error(ctypes.byref(v), int(clear),
+                                                               _stream(stream)))
+    return int(v.value)
 
 
 def mla_decode_stage1(q, kv_fp8, kv_scale, qo_indptr, kv_indptr, out, stream=None, *, plan,
@@ -260,6 +282,30 @@ def mla_fp8_quantize_per_tensor(src_bf16, dst_fp8, scale_out, tmp, stream=None) 
         _dev_ptr(src_bf16, "src", torch.bfloat16), src_bf16.numel(), _dev_ptr(dst_fp8, "dst"),
         _dev_ptr(scale_out, "scale_out", torch.float32), _dev_ptr(tmp, "tmp"),
         tmp.numel() * tmp.element_size(), _stream(stream)))
+
+
+def mla_debug_q_operand(q, kv_scale, tokens_per_cta: int = 1, stream=None):
+    """Test hook: stage 1's query operand of an e4m3 cache for every token of
+    ``q`` [T, 16, 576]: (codes uint8 [T, 2, 16, 576] = hi then lo, qk_scale float [T])."""
+    t = int(q.shape[0])
+    codes = torch.empty((t, 2, NUM_HEADS, QK_HEAD_DIM), dtype=torch.uint8, device=q.device)
+    qk_scale = torch.empty(t, dtype=torch.float32, device=q.device)
+    _check("mla_debug_q_operand", load_library().mla_debug_q_operand(
+        _dev_ptr(q, "q", torch.bfloat16), t, int(tokens_per_cta),
+        _dev_ptr(kv_scale, "kv_scale", torch.float32), _dev_ptr(codes, "codes"),
+        _dev_ptr(qk_scale, "qk_scale"), _stream(stream)))
+    return codes, qk_scale
+
+
+def mla_debug_p_split(p, stream=None):
+    """Test hook: stage 1's two-term e4m3 split of float probabilities ``p``
+    (numel a multiple of 16): (hi uint8, lo uint8), shaped like ``p``."""
+    hi = torch.empty(p.shape, dtype=torch.uint8, device=p.device)
+    lo = torch.empty(p.shape, dtype=torch.uint8, device=p.device)
+    _check("mla_debug_p_split", load_library().mla_debug_p_split(
+        _dev_ptr(p, "p", torch.float32), p.numel(), _dev_ptr(hi, "hi"), _dev_ptr(lo, "lo"),
+        _stream(stream)))
+    return hi, lo
 
 
 def mla_decode_workspace_init(workspace, stream=None) -> None:

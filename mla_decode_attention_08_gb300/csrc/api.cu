@@ -454,6 +454,37 @@ mla_status_t mla_decode_fwd_mxfp4_stall_stream(const void* q_bf16, const void* k
                     kv_scales, scale_bias);
 }
 
+mla_status_t mla_debug_q_operand(const void* q_bf16, int32_t num_tokens, int32_t tokens_per_cta,
+                                 const float* kv_scale, void* codes_out, float* qk_scale_out,
+                                 cudaStream_t stream) {
+  if (q_bf16 == nullptr || kv_scale == nullptr || codes_out == nullptr || qk_scale_out == nullptr ||
+      num_tokens < 1 || num_tokens > (1 << 24) || (tokens_per_cta != 1 && tokens_per_cta != 2) ||
+      !aligned(q_bf16, 16) || !aligned(codes_out, 16))
+    return MLA_ERR_INVALID_ARG;
+  int device = 0;
+  mla_status_t st = prepare_device(&device);
+  if (st != MLA_OK) return st;
+  return mla::launch_debug_q_operand(static_cast<const uint16_t*>(q_bf16), num_tokens,
+                                     tokens_per_cta, kv_scale, static_cast<uint8_t*>(codes_out),
+                                     qk_scale_out, stream) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+mla_status_t mla_debug_p_split(const float* p, int64_t n, void* hi_out, void* lo_out,
+                               cudaStream_t stream) {
+  if (p == nullptr || hi_out == nullptr || lo_out == nullptr || n < 16 || n % 16 != 0 ||
+      n > (INT64_C(1) << 34) || !aligned(p, 16) || !aligned(hi_out, 16) || !aligned(lo_out, 16))
+    return MLA_ERR_INVALID_ARG;
+  int device = 0;
+  mla_status_t st = prepare_device(&device);
+  if (st != MLA_OK) return st;
+  return mla::launch_debug_p_split(p, n / 16, static_cast<uint8_t*>(hi_out),
+                                   static_cast<uint8_t*>(lo_out), stream) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
 mla_status_t mla_decode_stage1_mxfp4(const void* q_bf16, const void* kv_fp4, const void* kv_scales,
                                      int32_t scale_bias, const int32_t* qo_indptr,
                                      const int32_t* kv_indptr, void* out_bf16, cudaStream_t stream,

@@ -88,6 +88,12 @@ cudaError_t stage1_prepare(int device);  // sets the dynamic shared memory limit
 cudaError_t launch_stage1(const Stage1Params& p, const Stage1Maps& maps, bool gather,
                           CacheFormat format, cudaStream_t stream);
 cudaError_t launch_stage2(const Stage2Params& p, bool programmatic, cudaStream_t stream);
+// Test hooks: stage 1's own two-term operand code run on caller buffers.
+cudaError_t launch_debug_q_operand(const uint16_t* q, int32_t tokens, int32_t per_cta,
+                                   const float* kv_scale, uint8_t* codes, float* qk_scale,
+                                   cudaStream_t stream);
+cudaError_t launch_debug_p_split(const float* p, int64_t groups, uint8_t* hi, uint8_t* lo,
+                                 cudaStream_t stream);
 cudaError_t launch_mxfp4_quantize(const uint16_t* src, int64_t rows, uint8_t* dst, uint8_t* scales,
                                   cudaStream_t stream);
 cudaError_t launch_fp8_quantize(const uint16_t* src, int64_t n, uint8_t* dst, float* scale_out,

@@ -1683,6 +1683,65 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
   if (t == 0) bulk_wait_all();
 }
 
+// ------------------------------------------------------------ test hooks: the two-term operands
+// The Q operand of an e4m3 cache exactly as a stage-1 CTA prepares it: CTA i
+// runs prepare_q for query tokens kQ i .. kQ i + kQ - 1 (one 128-thread
+// warpgroup, as the softmax warps do) and copies the swizzled operand back out
+// as codes [token][hi, lo][head][576] with the token's qk_scale.  The query
+// bounds check of prepare_q always holds here (nq stops at the last token), so
+// p.err is never written.
+template <int kQ>
+__global__ void __launch_bounds__(kSoftmaxThreads) debug_q_operand_kernel(const Stage1Params p,
+                                                                          uint8_t* codes,
+                                                                          float* qk_scale_out) {
+  using G = Geo<kQ, Kv::kE4m3>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sq = smem_u32(smem);
+  Misc* ms = reinterpret_cast<Misc*>(smem + (G::kOffP - G::kOffQ));
+  const int32_t tokens = p.batch;
+  const int32_t tq = static_cast<int32_t>(blockIdx.x) * kQ;
+  const int32_t nq = min(kQ, tokens - tq);
+  float qk_scale[kQ];
+  prepare_q<kQ, Kv::kE4m3>(p, ms, sq, tq, nq, __ldg(p.kv_scale), qk_scale);
+  constexpr int kChunks = kQkDim / 16;  // 16-byte chunks of an operand row
+  for (int job = threadIdx.x; job < nq * 32 * kChunks; job += kSoftmaxThreads) {
+    const int row = job / kChunks, ch = job % kChunks;  // row = 32 qi + 16 lo + head
+    const uint4 v = ld_shared_v4(q_chunk_addr<kQ, Kv::kE4m3>(sq, row, ch));
+    *reinterpret_cast<uint4*>(codes + (static_cast<size_t>(tq) * 32 + row) * kQkDim + 16 * ch) = v;
+  }
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int qi = 0; qi < kQ; ++qi)
+      if (qi < nq) qk_scale_out[tq + qi] = qk_scale[qi];
+  }
+}
+
+constexpr int debug_q_smem(int q) {
+  return (q == 1 ? Geo<1, Kv::kE4m3>::kOffP - Geo<1, Kv::kE4m3>::kOffQ
+                 : Geo<2, Kv::kE4m3>::kOffP - Geo<2, Kv::kE4m3>::kOffQ) +
+         static_cast<int>(sizeof(Misc)) + 1024;
+}
+static_assert(debug_q_smem(2) <= 48 * 1024, "the Q-operand hook runs without a shared-memory opt-in");
+static_assert((Geo<1, Kv::kE4m3>::kOffP - Geo<1, Kv::kE4m3>::kOffQ) % 16 == 0 &&
+                  (Geo<2, Kv::kE4m3>::kOffP - Geo<2, Kv::kE4m3>::kOffQ) % 16 == 0,
+              "the hook's barrier block follows the Q region 16-byte aligned");
+
+// The P operand split of the softmax warps: each thread takes 16 consecutive
+// probabilities and writes their hi and lo e4m3 codes (16 bytes each).
+__global__ void debug_p_split_kernel(const float* p, int64_t groups, uint8_t* hi, uint8_t* lo) {
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (g >= groups) return;
+  float x[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) x[k] = p[16 * g + k];
+  uint32_t h[4], l[4];
+  split_p_16(x, h, l);
+  reinterpret_cast<uint4*>(hi)[g] = make_uint4(h[0], h[1], h[2], h[3]);
+  reinterpret_cast<uint4*>(lo)[g] = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
 // ------------------------------------------------------------ kernel
 template <bool kGather, int kQ, Kv kFmt>
 __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
@@ -1855,6 +1914,29 @@ cudaError_t launch_stage1(const Stage1Params& p, const Stage1Maps& maps, bool ga
                   : launch<false, 2, Kv::kE4m3>(p, maps, stream);
   return gather ? launch<true, 1, Kv::kE4m3>(p, maps, stream)
                 : launch<false, 1, Kv::kE4m3>(p, maps, stream);
+}
+
+cudaError_t launch_debug_q_operand(const uint16_t* q, int32_t tokens, int32_t per_cta,
+                                   const float* kv_scale, uint8_t* codes, float* qk_scale,
+                                   cudaStream_t stream) {
+  Stage1Params p = {};
+  p.q = q;
+  p.kv_scale = kv_scale;
+  p.batch = tokens;
+  p.row_tokens = 1;
+  const unsigned grid = static_cast<unsigned>((tokens + per_cta - 1) / per_cta);
+  if (per_cta == 2)
+    debug_q_operand_kernel<2><<<grid, kSoftmaxThreads, debug_q_smem(2), stream>>>(p, codes, qk_scale);
+  else
+    debug_q_operand_kernel<1><<<grid, kSoftmaxThreads, debug_q_smem(1), stream>>>(p, codes, qk_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_p_split(const float* p, int64_t groups, uint8_t* hi, uint8_t* lo,
+                                 cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>((groups + 255) / 256);
+  debug_p_split_kernel<<<grid, 256, 0, stream>>>(p, groups, hi, lo);
+  return cudaGetLastError();
 }
 
 }  // namespace mla

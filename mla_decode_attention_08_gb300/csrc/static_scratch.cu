@@ -26,7 +26,9 @@ ScratchAddress g_scratch_address[kMaxDevices];
 
 // Device address of this GPU's copy of the array.  Host code cannot use the
 // array's name as a pointer (it is a host-side stand-in), so it is looked up
-// once per device, with that device current.
+// once per device, with that device current.  A device this library has no
+// kernels for is refused first: the lookup would fail there with a
+// missing-image error.
 mla_status_t scratch_on_current_device(void** out) {
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return MLA_ERR_CUDA;
@@ -34,9 +36,16 @@ mla_status_t scratch_on_current_device(void** out) {
   ScratchAddress& a = g_scratch_address[device];
   std::lock_guard<std::mutex> guard(a.lock);
   if (a.ptr == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress((void**)&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr)
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess)
       return MLA_ERR_CUDA;
+    if (major != 10 || minor != 3) return MLA_ERR_UNSUPPORTED;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress((void**)&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
+      (void)cudaGetLastError();  // leave no runtime error behind for the caller
+      return MLA_ERR_CUDA;
+    }
     a.ptr = ptr;
   }
   *out = a.ptr;
@@ -55,8 +64,17 @@ extern "C" mla_status_t mla_decode_fwd_static_scratch(
   const mla_status_t st = scratch_on_current_device(&scratch);
   if (st != MLA_OK) return st;
   // Nothing in the scratch has to start at zero: every region a call reads is
-  // written earlier in the same call, and the error word it accumulates is not
-  // reported through this entry point.
+  // written earlier in the same call.  The error word only accumulates bits;
+  // mla_decode_static_scratch_read_error reads and clears it.
   return mla_decode_fwd(q_bf16, kv_fp8, kv_scale, qo_indptr, kv_indptr, out_bf16, stream, plan,
                         kv_indices, kv_indices_len, kv_rows, scratch, MLA_STATIC_SCRATCH_BYTES);
+}
+
+extern "C" mla_status_t mla_decode_static_scratch_read_error(int32_t* err_host, int32_t clear,
+                                                             cudaStream_t stream) {
+  if (err_host == nullptr) return MLA_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  const mla_status_t st = scratch_on_current_device(&scratch);
+  if (st != MLA_OK) return st;
+  return mla_decode_read_error(scratch, err_host, clear, stream);
 }

@@ -192,6 +192,16 @@ def workload_lengths(w: Workload) -> np.ndarray:
     return np.full(w.batch, w.kv_len, dtype=np.int64)
 
 
+def workload_query_bits(w) -> np.ndarray:
+    """The query of a named workload alone (the same draw as ``make_inputs``,
+    without generating its cache): uint16 bf16 bits ``[B * qo_len, 16, 576]``."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    q = np.empty((w.batch * w.qo_len, NUM_HEADS, QK_HEAD_DIM), dtype=np.float32)
+    _rng(w.seed, 0).standard_normal(out=q, dtype=np.float32)
+    return f32_to_bf16_bits(q)
+
+
 def make_inputs(w) -> Inputs:
     """Inputs of a named workload (see ``WORKLOADS``)."""
     if isinstance(w, str):

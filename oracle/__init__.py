@@ -10,6 +10,8 @@ arithmetic.
 Modules
   fp8        e4m3fn decode / encode written from the format's definition.
   quant      per-tensor absmax FP8 quantisation of the bf16 latent cache.
+  qsplit     the two-term e4m3 query and probability operands of the
+             e4m3-cache step (per-token power-of-two scale, hi / lo split).
   mxfp4      MXFP4 (E2M1 elements, E8M0 scale per 32) codec, block
              quantiser and the decode step over an MXFP4 cache.
   attention  exact softmax attention over the dequantised e4m3 cache or the

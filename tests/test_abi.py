@@ -157,3 +157,23 @@ def test_plan_mtp_rejects_unsupported_token_counts(lib):
     plan = binding.mla_plan_t()
     for n in (0, 5, 8, -1):
         assert lib.mla_decode_plan_mtp(8, n, 1024, 152, ctypes.byref(plan)) == 1
+
+
+@pytest.mark.parametrize("kv", [
+    lambda torch: torch.zeros((8, 576), dtype=torch.bfloat16),   # a bf16 cache
+    lambda torch: torch.zeros((8, 576), dtype=torch.float32),
+    lambda torch: torch.zeros((8, 288), dtype=torch.uint8),      # MXFP4 elements
+])
+def test_binding_refuses_a_cache_that_is_not_e4m3(lib, kv):
+    torch = pytest.importorskip("torch")
+    cache = kv(torch)
+    q = torch.zeros((1, 16, 576), dtype=torch.bfloat16)
+    ind = torch.zeros(2, dtype=torch.int32)
+    out = torch.zeros((1, 16, 512), dtype=torch.bfloat16)
+    plan = binding.mla_decode_plan(1, 8, 152)
+    err = TypeError if cache.dtype != torch.uint8 else ValueError
+    with pytest.raises(err):
+        binding.mla_decode_fwd(q, cache, torch.ones(1), ind, ind, out, plan=plan,
+                               workspace=torch.zeros(16, dtype=torch.uint8))
+    with pytest.raises(err):
+        binding.mla_decode_fwd_static_scratch(q, cache, torch.ones(1), ind, ind, out, plan=plan)
