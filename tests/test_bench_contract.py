@@ -31,7 +31,8 @@ def test_reference_arm_line():
     assert line["higher_is_better"] is False and line["value"] > 0
     assert line["config"]["workload"] == "bs4_kv1024"
     cb = line["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"]
+    assert cb["cores"] == len(os.sched_getaffinity(0))  # every host core this process may use
     assert line["e2e"] == {"value": line["value"], "unit": "us/call", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
 
@@ -50,3 +51,13 @@ def test_gpu_arm_line(cache):
     assert e2e["value"] > line["value"] and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert line["gpu_launches"] == 2 * 20
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(line["clocks"])
+
+
+def test_cpu_baseline_leg_uses_every_host_core():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-sample",
+                        "bs4_kv1024", "--budget", "1"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    cb = json.loads(r.stdout.strip().splitlines()[-1])
+    assert cb["kind"] == "oracle" and cb["cores"] == len(os.sched_getaffinity(0))
+    assert cb["value"] > 0 and cb["single_core_value"] > 0
