@@ -37,7 +37,7 @@ extern "C" {
 #define MLA_QK_HEAD_DIM 576
 #define MLA_V_HEAD_DIM 512
 #define MLA_TILE_TOKENS 128
-#define MLA_ABI_VERSION 4
+#define MLA_ABI_VERSION 5
 
 typedef enum {
   MLA_OK = 0,
@@ -64,6 +64,20 @@ typedef enum {
  * tiles of 128 tokens, the tiles of all rows form one sequence of T tiles, and
  * `grid` persistent workers take equal contiguous ranges of it.  A row covered
  * by more than one worker is combined by the second stage.
+ *
+ * Small batches instead take the cluster split (`cluster` = s > 0): row b is
+ * shared by a thread-block cluster of s CTAs, the CTA of rank r taking the
+ * row's tiles [r k, min((r + 1) k, nt)) with nt = ceil(L_b / 128) and
+ * k = ceil(nt / s); the s partial results are combined inside the cluster
+ * through distributed shared memory, and no second kernel runs.  The plan
+ * chooses s as the largest of 8, 4, 2 with s <= ceil(max_kv_len / 128) whose
+ * clusters for the whole batch fit the GPU at once (at most num_sms / 10
+ * clusters of 8, 7 num_sms / 32 of 4, num_sms / 2 of 2), and only when its
+ * longest share ceil(ceil(max_kv_len / 128) / s) is at most two tiles longer
+ * than the persistent split's longest range; rows of one query token only.
+ * The cluster split serves the contiguous e4m3 and bf16 caches; with a page
+ * table or an MXFP4 cache the same plan runs the persistent split.  A caller
+ * may set `cluster` to 0 to force the persistent split.
  */
 typedef struct {
   int32_t batch;       /* B, rows (one query token each)                          */
@@ -76,7 +90,8 @@ typedef struct {
   int32_t tile_tokens; /* 128                                                      */
   int32_t abi_version; /* MLA_ABI_VERSION                                          */
   int32_t qo_len;      /* query tokens per row: 1 (decode) to 4 (multi-token decode) */
-  int32_t reserved;    /* 0                                                        */
+  int32_t cluster;     /* CTAs per row of the cluster split (2, 4 or 8), or 0: the
+                        * persistent split (see above)                            */
   uint64_t ws_bytes;   /* workspace bytes mla_decode_fwd needs                      */
   uint64_t ws_prefix_offset;  /* int32[B+1]   tile prefix over rows                 */
   uint64_t ws_workers_offset; /* int32[grid*8] per worker: (t0, t1, first_row, last_row)
@@ -332,6 +347,31 @@ mla_status_t mla_debug_q_operand(const void* q_bf16, int32_t num_tokens, int32_t
  */
 mla_status_t mla_debug_p_split(const float* p, int64_t n, void* hi_out, void* lo_out,
                                cudaStream_t stream);
+
+/*
+ * mla_decode_trace_read — start-up trace of trace builds (no counterpart on the
+ * pages): a library compiled with -DMLA_TRACE stamps, for each of the first
+ * MLA_TRACE_CTAS stage-1 CTAs, MLA_TRACE_EVENTS events (entry and exit on the
+ * global timer in ns; the milestones between them in SM cycles: before and
+ * after the wait for the previous kernel, prologue done, first cache copy
+ * issued, Q operand ready, first rope panel landed, first QK issued, first
+ * scores read, first P published, first PV issued, first epilogue start and
+ * end, exit; then the row-pointer loads returned, the prologue's scan barrier,
+ * the first query loads returned, the first rope and last latent panel
+ * arrived; for the cluster split the cluster barrier passed and the combine
+ * written), and for each of the first
+ * MLA_TRACE2_BLOCKS stage-2 blocks
+ * (numbered y * grid_x + x) the global timer at entry, after its wait for
+ * stage 1 and at exit.  Each call's stamps overwrite the previous call's.
+ *   stage1_host  host uint64 [MLA_TRACE_CTAS * MLA_TRACE_EVENTS]
+ *   stage2_host  host uint64 [MLA_TRACE2_BLOCKS * 3]
+ *   clear        nonzero: zero the device copies after reading.
+ * Synchronous.  Release builds return MLA_ERR_UNSUPPORTED.
+ */
+#define MLA_TRACE_CTAS 320
+#define MLA_TRACE_EVENTS 24
+#define MLA_TRACE2_BLOCKS 4096
+mla_status_t mla_decode_trace_read(uint64_t* stage1_host, uint64_t* stage2_host, int32_t clear);
 
 /*
  * mla_fp8_quantize_per_tensor — per-tensor absmax quantisation of a bf16 tensor

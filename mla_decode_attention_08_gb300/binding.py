@@ -31,7 +31,7 @@ class mla_plan_t(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("max_kv_len", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("tile_tokens", ctypes.c_int32), ("abi_version", ctypes.c_int32),
-                ("qo_len", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("qo_len", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("ws_bytes", ctypes.c_uint64), ("ws_prefix_offset", ctypes.c_uint64),
                 ("ws_workers_offset", ctypes.c_uint64), ("ws_lse_offset", ctypes.c_uint64),
                 ("ws_partial_offset", ctypes.c_uint64)]
@@ -58,6 +58,7 @@ SIGNATURES = {
     "mla_decode_fwd_mxfp4_stall_stream": (ctypes.c_int, _FWD_MXFP4_ARGS),
     "mla_mxfp4_quantize": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP]),
     "mla_debug_q_operand": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP, _VP, _VP]),
+    "mla_decode_trace_read": (ctypes.c_int, [_VP, _VP, _I32]),
     "mla_debug_p_split": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP]),
     "mla_decode_stage2": (ctypes.c_int, [_VP, _VP, _VP, _PLANP, _VP, _SZ]),
     "mla_fp8_quantize_per_tensor": (ctypes.c_int, [_VP, _I64, _VP, _VP, _VP, _SZ, _VP]),
@@ -80,7 +81,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                "(python -m mla_decode_attention_08_gb300.build)")
         lib = ctypes.CDLL(path)
         for name, (res, args) in SIGNATURES.items():
-            fn = getattr(lib, name)
+            fn = getattr(lib, name, None)
+            if fn is None:  # a library from before this entry point; calling it raises
+                continue
             fn.restype, fn.argtypes = res, args
         _lib = lib
     return _lib
@@ -111,11 +114,17 @@ def _stream(stream) -> Optional[int]:
     return int(stream)
 
 
-def mla_decode_plan(batch: int, max_kv_len: int, num_sms: int = 0, qo_len: int = 1) -> mla_plan_t:
-    """Plan for ``batch`` rows of ``qo_len`` query tokens (1 to 4; 2-4 for multi-token decode)."""
+def mla_decode_plan(batch: int, max_kv_len: int, num_sms: int = 0, qo_len: int = 1,
+                    persistent: bool = False) -> mla_plan_t:
+    """Plan for ``batch`` rows of ``qo_len`` query tokens (1 to 4; 2-4 for multi-token decode).
+
+    ``persistent=True`` forces the persistent split (``plan.cluster = 0``) where
+    the plan would take the cluster split of small batches."""
     plan = mla_plan_t()
     _check("mla_decode_plan_mtp", load_library().mla_decode_plan_mtp(batch, qo_len, max_kv_len,
                                                                     num_sms, ctypes.byref(plan)))
+    if persistent:
+        plan.cluster = 0
     return plan
 
 
@@ -306,6 +315,19 @@ def mla_debug_p_split(p, stream=None):
         _dev_ptr(p, "p", torch.float32), p.numel(), _dev_ptr(hi, "hi"), _dev_ptr(lo, "lo"),
         _stream(stream)))
     return hi, lo
+
+
+TRACE_CTAS, TRACE_EVENTS, TRACE2_BLOCKS = 320, 24, 4096
+
+
+def mla_decode_trace_read(clear: bool = True):
+    """Trace builds only: (stage-1 stamps uint64 [320, 24], stage-2 stamps uint64 [4096, 3])."""
+    import numpy as np
+    s1 = np.zeros((TRACE_CTAS, TRACE_EVENTS), dtype=np.uint64)
+    s2 = np.zeros((TRACE2_BLOCKS, 3), dtype=np.uint64)
+    _check("mla_decode_trace_read", load_library().mla_decode_trace_read(
+        s1.ctypes.data, s2.ctypes.data, int(clear)))
+    return s1, s2
 
 
 def mla_decode_workspace_init(workspace, stream=None) -> None:

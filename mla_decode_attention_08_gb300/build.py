@@ -22,6 +22,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmla_decode.so")
 BUILD_DEBUG = os.path.join(PKG, "_build_debug")
 LIB_DEBUG = os.path.join(PKG, "libmla_decode_debug.so")
+BUILD_TRACE = os.path.join(PKG, "_build_trace")
+LIB_TRACE = os.path.join(PKG, "libmla_decode_trace.so")
 SOURCES = ["stage1.cu", "stage2.cu", "fp8_quant.cu", "mxfp4_quant.cu", "api.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -45,9 +47,17 @@ def _stale(out: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, debug: bool = False) -> str:
-    """Compile (if anything changed) and return the path of the shared library."""
-    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+def build(verbose: bool = False, force: bool = False, debug: bool = False,
+          trace: bool = False) -> str:
+    """Compile (if anything changed) and return the path of the shared library.
+
+    ``trace=True`` builds ``libmla_decode_trace.so`` with ``-DMLA_TRACE``: the
+    kernels stamp their start-up milestones (``mla_decode_trace_read``)."""
+    if debug and trace:
+        raise ValueError("build either the debug or the trace variant")
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else ((BUILD_TRACE, LIB_TRACE) if trace
+                                                             else (BUILD, LIB))
+    extra = ["-DMLA_DEBUG"] if debug else (["-DMLA_TRACE"] if trace else [])
     os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(ROOT, "include", "mla_decode.h"))
@@ -57,7 +67,7 @@ def build(verbose: bool = False, force: bool = False, debug: bool = False) -> st
         s = os.path.join(CSRC, src)
         o = os.path.join(build_dir, src.replace(".cu", ".o"))
         if force or _stale(o, [s] + headers):
-            cmd = [exe] + _flags() + (["-DMLA_DEBUG"] if debug else []) + ["-c", s, "-o", o]
+            cmd = [exe] + _flags() + extra + ["-c", s, "-o", o]
             if verbose:
                 print(" ".join(cmd), flush=True)
             r = subprocess.run(cmd, capture_output=True, text=True)
@@ -78,4 +88,5 @@ def build(verbose: bool = False, force: bool = False, debug: bool = False) -> st
 
 
 if __name__ == "__main__":
-    print(build(verbose=True, force="--force" in sys.argv, debug="--debug" in sys.argv))
+    print(build(verbose=True, force="--force" in sys.argv, debug="--debug" in sys.argv,
+                trace="--trace" in sys.argv))

@@ -181,9 +181,19 @@ mla_status_t prepare_device(int* device_out) {
 mla_status_t check_plan(const mla_plan_t* plan) {
   if (plan == nullptr || plan->abi_version != MLA_ABI_VERSION || plan->batch < 1 ||
       plan->grid < 1 || plan->tile_tokens != kTileTokens || plan->max_kv_len < 0 ||
-      plan->qo_len < 1 || plan->qo_len > 4)
+      plan->qo_len < 1 || plan->qo_len > 4 || plan->num_sms < 1)
+    return MLA_ERR_INVALID_ARG;
+  // The cluster split: the planned size, or 0 (the caller forced the persistent split).
+  if (plan->cluster != 0 &&
+      plan->cluster != mla::plan_cluster(plan->batch, plan->qo_len, plan->max_kv_len, plan->num_sms))
     return MLA_ERR_INVALID_ARG;
   return MLA_OK;
+}
+
+// CTAs per row of the cluster split for this call, or 0 for the persistent split:
+// the cluster split takes contiguous e4m3 and bf16 caches.
+int32_t cluster_of(const mla_plan_t* plan, mla::CacheFormat fmt, const int32_t* kv_indices) {
+  return kv_indices == nullptr && fmt != mla::CacheFormat::kMxfp4 ? plan->cluster : 0;
 }
 
 mla_status_t check_workspace(const mla_plan_t* plan, void* workspace, size_t workspace_bytes) {
@@ -283,6 +293,7 @@ mla_status_t run_stage1(const void* q, const void* kv, const float* kv_scale,
   p.stall_stream = stall_stream ? 1 : 0;
   p.mx_bias = mx_bias;
   p.kv_bytes = gather ? nullptr : static_cast<const uint8_t*>(kv);
+  p.cluster = cluster_of(plan, fmt, kv_indices);
   p.kv_row_bytes = fmt == CacheFormat::kMxfp4 ? kQkDim / 2 : (fmt == CacheFormat::kBf16 ? 2 * kQkDim : kQkDim);
   return mla::launch_stage1(p, maps, gather, fmt, stream) == cudaSuccess
              ? MLA_OK
@@ -307,7 +318,9 @@ mla_status_t run_decode(const void* q, const void* kv, const float* kv_scale,
   mla_status_t st = run_stage1(q, kv, kv_scale, qo_indptr, kv_indptr, out, stream, plan,
                                kv_indices, kv_indices_len, kv_rows, workspace, workspace_bytes,
                                fmt, stall_stream, mx_scales, mx_bias);
-  if (st == MLA_OK) st = run_stage2(qo_indptr, out, stream, plan, workspace, true);
+  // The cluster split combines inside stage 1: no second kernel.
+  if (st == MLA_OK && cluster_of(plan, fmt, kv_indices) == 0)
+    st = run_stage2(qo_indptr, out, stream, plan, workspace, true);
   return st;
 }
 
@@ -355,6 +368,7 @@ mla_status_t mla_decode_plan_mtp(int32_t batch, int32_t qo_len, int32_t max_kv_l
   p.tile_tokens = kTileTokens;
   p.abi_version = MLA_ABI_VERSION;
   p.qo_len = qo_len;
+  p.cluster = mla::plan_cluster(batch, qo_len, max_kv_len, num_sms);
   const uint64_t g = static_cast<uint64_t>(p.grid);
   const uint64_t nq = static_cast<uint64_t>(qo_len);
   uint64_t off = kAlign;  // error word + reserved header
@@ -469,6 +483,16 @@ mla_status_t mla_debug_q_operand(const void* q_bf16, int32_t num_tokens, int32_t
                                      qk_scale_out, stream) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
+}
+
+mla_status_t mla_decode_trace_read(uint64_t* stage1_host, uint64_t* stage2_host, int32_t clear) {
+  if (stage1_host == nullptr || stage2_host == nullptr) return MLA_ERR_INVALID_ARG;
+  static_assert(sizeof(uint64_t) == sizeof(unsigned long long), "trace stamps are 64-bit");
+  cudaError_t e = mla::trace_read_stage1(reinterpret_cast<unsigned long long*>(stage1_host), clear != 0);
+  if (e == cudaSuccess)
+    e = mla::trace_read_stage2(reinterpret_cast<unsigned long long*>(stage2_host), clear != 0);
+  if (e == cudaErrorNotSupported) return MLA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 mla_status_t mla_debug_p_split(const float* p, int64_t n, void* hi_out, void* lo_out,

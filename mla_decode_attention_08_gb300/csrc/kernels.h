@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
+#include "../../include/mla_decode.h"
+
 namespace mla {
 
 // Debug builds (-DMLA_DEBUG, `build(debug=True)`): every global store of the
@@ -29,6 +31,43 @@ constexpr int kStage1Threads = 256;
 constexpr int kStage1ThreadsGather = 384;
 constexpr int kStage1ThreadsMx = 512;  // MXFP4 cache: warps 8-15 convert its panels
 constexpr long long kWaitLimitCycles = 2000000000LL;  // ~1 s per pipeline wait at 2 GHz
+
+// Start-up trace of trace builds (-DMLA_TRACE, `build(trace=True)`): per stage-1
+// CTA (the first kTraceCtas) kTraceEvents stamps, per stage-2 block (the first
+// kTrace2Blocks, numbered y * gridDim.x + x) three global-timer stamps.
+constexpr int kTraceCtas = MLA_TRACE_CTAS;
+constexpr int kTraceEvents = MLA_TRACE_EVENTS;
+constexpr int kTrace2Blocks = MLA_TRACE2_BLOCKS;
+constexpr int kTrace2Events = 3;
+enum TraceEvent {
+  kTrEntryNs = 0,      // global timer at entry (ns)
+  kTrEntry = 1,        // the rest: SM cycles (clock64); entry
+  kTrPreWait = 2,      // thread 0 before waiting for the previous kernel of the stream
+  kTrPostWait = 3,     // ... after it
+  kTrPrologue = 4,     // schedule prologue done (after the block barrier)
+  kTrFirstCopy = 5,    // producer: first cache copy issued
+  kTrQReady = 6,       // softmax: the first segment's Q operand published
+  kTrRopeLanded = 7,   // QK issuer: the first rope panel landed
+  kTrQkIssued = 8,     // QK issuer: the first tile's QK issued and committed
+  kTrSRead = 9,        // softmax: the first tile's scores read out of TMEM
+  kTrPReady = 10,      // softmax: the first tile's P published
+  kTrPvIssued = 11,    // PV issuer: the first tile's PV issued
+  kTrEpilogue = 12,    // softmax: the first segment's epilogue starts (its last PV done)
+  kTrEpilogueDone = 13,  // softmax: the first segment's output stores issued
+  kTrExit = 14,        // thread 0 after the final block barrier
+  kTrExitNs = 15,      // global timer at exit (ns)
+  kTrIndptrLoaded = 16,  // thread 0: its rows' kv_indptr entries returned
+  kTrScanBarrier = 17,   // thread 0: past the prologue's first block barrier
+  kTrQLoaded = 18,       // softmax: the first query loads returned
+  kTrRopeArrived = 19,   // observer lane: the first rope panel's copy completed
+  kTrTileArrived = 20,   // observer lane: the first tile's last latent panel completed
+  kTrClusterBarrier = 21,  // cluster split: thread 0 past the cluster barrier
+  kTrCombineDone = 22,     // ... its share of the combine written
+};
+// Copy the trace out (host arrays of kTraceCtas * kTraceEvents and kTrace2Blocks
+// * kTrace2Events entries) and zero it; cudaErrorNotSupported without -DMLA_TRACE.
+cudaError_t trace_read_stage1(unsigned long long* host, bool clear);
+cudaError_t trace_read_stage2(unsigned long long* host, bool clear);
 
 struct Stage1Params {
   const uint16_t* q;          // bf16 bits [B, 16, 576]
@@ -58,6 +97,7 @@ struct Stage1Params {
   const uint8_t* kv_bytes;    // contiguous rows: the cache (or MXFP4 elements) for an L2
                               // prefetch of the first tile; null with a page table
   int32_t kv_row_bytes;       // bytes per cached row in kv_bytes (576, 1152 or 288)
+  int32_t cluster;            // CTAs per row of the cluster split (2, 4, 8), or 0: persistent
 };
 
 enum class CacheFormat { kE4m3, kBf16, kMxfp4 };

@@ -100,6 +100,19 @@ __device__ __forceinline__ void prefetch_bulk_l2(const void* p, uint32_t bytes) 
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// ---------------------------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Executed by every thread of every CTA of the cluster: each thread's earlier
+// memory writes are released at cluster scope and the others' acquired.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
 // ---------------------------------------------------------------- register split
 // Executed by all four warps of a warpgroup; the block's registers (threads x
 // the launch count) must cover the sum of every warpgroup's count after it.

@@ -41,6 +41,33 @@ MLA_HD int32_t plan_grid(int32_t batch, int32_t max_kv_len, int32_t num_sms) {
   return static_cast<int32_t>((upper + k - 1) / k);
 }
 
+// Clusters of s CTAs (one 227 KB CTA per SM) that a GPU of num_sms SMs runs at
+// once, estimated from the GB300 GPC layout (measured: 15 clusters of 8, 36 of
+// 4 and 76 of 2 on 152 SMs): num_sms / 10, 7 num_sms / 32 and num_sms / 2.
+MLA_HD int32_t cluster_capacity(int32_t s, int32_t num_sms) {
+  return s == 8 ? num_sms / 10 : (s == 4 ? num_sms * 7 / 32 : num_sms / 2);
+}
+
+// Cluster split for small batches of one query token per row: every row gets
+// a cluster of s CTAs that share its tiles (rank r takes the row's tiles
+// [r k, min((r + 1) k, nt)), k = ceil(nt / s)) and combine their partial
+// results through distributed shared memory, with no second kernel.  s is the
+// largest of 8, 4, 2 with s <= ceil(max_kv_len / 128) whose clusters for the
+// whole batch fit the GPU at once; it is used (else 0: the persistent split)
+// when its longest share, ceil(nt / s) tiles, is at most two tiles longer than
+// the persistent schedule's longest range.
+MLA_HD int32_t plan_cluster(int32_t batch, int32_t qo_len, int32_t max_kv_len, int32_t num_sms) {
+  const int32_t nt = tiles_of_length(max_kv_len);
+  if (qo_len != 1 || batch < 1 || num_sms < 1 || nt < 2) return 0;
+  int32_t s = 8;
+  while (s >= 2 && (s > nt || batch > cluster_capacity(s, num_sms))) s >>= 1;
+  if (s < 2) return 0;
+  const int64_t upper = static_cast<int64_t>(batch) * nt;
+  const int64_t g0 = upper < num_sms ? upper : num_sms;
+  const int64_t longest = (upper + g0 - 1) / g0;
+  return (nt + s - 1) / s <= longest + 2 ? s : 0;
+}
+
 // floor(c * total / grid) for 0 <= c <= grid and total >= 0, without a 64-bit
 // division (a slow call on the GPU): with total = q * grid + r it is
 // c * q + floor(c * r / grid), and c * r < grid^2 fits 32 bits whenever

@@ -48,6 +48,7 @@ namespace {
 constexpr uint32_t kLayoutSw128 = 2, kLayoutSw64 = 4, kLayoutSw32 = 6;
 
 constexpr int kMaxQ = 2;          // query tokens per row handled by one CTA tile
+constexpr int kMaxCluster = 8;    // CTAs per row of the cluster split
 constexpr int kMaxVSlots = 11;    // latent ring slots (e4m3, kQ = 1)
 
 // Latent cache formats.
@@ -150,6 +151,8 @@ struct Misc {
   // again before its first tile.
   int32_t first_kb, first_len, first_tq;
   int32_t bad;
+  int32_t tile0_issued;    // the prologue issued the first tile's copies (contiguous rows)
+  alignas(16) float cl_w[kMaxCluster][16];  // cluster split: combine weights [rank][head]
   uint32_t next_panel[6];  // per producer warp: one past its last issued panel
   alignas(16) float alpha_stage[16 * kMaxQ];  // O rescale factors of the current tile (thread 0 writes)
 };
@@ -217,6 +220,22 @@ constexpr float kSmScaleLog2 = 1.4426950408889634f / 24.0f;
 constexpr float kRescaleThreshold = 8.0f;
 
 __device__ __forceinline__ int32_t ldg_i32(const int32_t* p) { return __ldg(p); }
+
+// ------------------------------------------------------------ start-up trace (-DMLA_TRACE only)
+// Clock stamps of one CTA's way to its first output, per role, in SM cycles
+// (clock64), plus the global timer at entry and exit; read back with
+// mla_decode_trace_read.  Release builds compile the stamps away.
+#ifdef MLA_TRACE
+__device__ unsigned long long g_trace_stage1[kTraceCtas * kTraceEvents];
+__device__ __forceinline__ void trace_put(int ev, unsigned long long v) {
+  if (blockIdx.x < static_cast<unsigned>(kTraceCtas)) g_trace_stage1[blockIdx.x * kTraceEvents + ev] = v;
+}
+#define MLA_TRACE_CLK(ev) trace_put((ev), static_cast<unsigned long long>(clock64()))
+#define MLA_TRACE_NS(ev) trace_put((ev), global_timer_ns())
+#else
+#define MLA_TRACE_CLK(ev) ((void)0)
+#define MLA_TRACE_NS(ev) ((void)0)
+#endif
 
 __device__ __forceinline__ void set_error(int32_t* err, int32_t bits) { atomicOr(err, bits); }
 
@@ -397,8 +416,36 @@ __device__ __forceinline__ void zero_row(const Stage1Params& p, int32_t b) {
   for (int i = 0; i < n; ++i) dst[i] = make_uint4(0, 0, 0, 0);
 }
 
-template <int kQ>
-__device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
+// Contiguous rows: the worker's first tile, issued by the prologue thread that
+// finds the worker's first row (tile 0's ring slots start empty), so that its
+// copies are in flight while the roles start; the producer begins with the
+// second tile.  Not used for an MXFP4 cache or the stall test hook.
+template <int kQ, Kv kFmt>
+__device__ __forceinline__ void issue_first_tile(const Stage1Params& p, const CUtensorMap* map_v,
+                                                 const CUtensorMap* map_r, Misc* ms, uint32_t sbase,
+                                                 int32_t tok0) {
+  using G = Geo<kQ, kFmt>;
+  static_assert(G::kNumV >= 4, "tile 0 takes latent slots 0-3");
+  if (!MLA_DCHECK(tok0 >= 0 && tok0 < p.kv_rows, p.err)) return;  // the producer then aborts
+  const uint32_t rfull = smem_u32(&ms->r_full[0]);
+  mbar_arrive_expect_tx(rfull, G::kRSlotBytes);
+  tma_load_2d(sbase + G::kOffR, map_r, kVDim * G::kElem, tok0, rfull);
+  constexpr int kBoxes = G::kSplit ? 1 : 2;  // 128-byte-wide boxes per latent slot
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t full = smem_u32(&ms->v_full[c]);
+    mbar_arrive_expect_tx(full, G::kVSlotBytes);
+#pragma unroll
+    for (int i = 0; i < kBoxes; ++i)
+      tma_load_2d(sbase + G::kOffV + c * G::kVSlotBytes + i * kTileTokens * 128, map_v,
+                  128 * c * G::kElem + 128 * i, tok0, full);
+  }
+  ms->tile0_issued = 1;
+}
+
+template <int kQ, Kv kFmt>
+__device__ void schedule_prologue(const Stage1Params& p, const CUtensorMap* map_v,
+                                  const CUtensorMap* map_r, Misc* ms, uint32_t sbase) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, nwarps = nthreads >> 5;
   const int32_t batch = p.batch;
@@ -414,9 +461,30 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
     q_lo = ldg_i32(p.qo_indptr + r0);
     q_hi = ldg_i32(p.qo_indptr + r0 + 1);
   }
+  // The row pointers of up to kKeep rows per thread stay in registers for the
+  // second pass (batches of up to kKeep x the block's threads need one round
+  // trip to global memory); beyond that they are loaded again.
+  constexpr int kKeep = 4;
+  int32_t keep[kKeep + 1];
   if (r0 < r1) {
     int32_t prev = ldg_i32(p.kv_indptr + r0);
-    for (int32_t b = r0; b < r1; ++b) {
+    keep[0] = prev;
+#pragma unroll
+    for (int i = 0; i < kKeep; ++i) {
+      if (r0 + i < r1) {
+        keep[i + 1] = ldg_i32(p.kv_indptr + r0 + i + 1);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kKeep; ++i) {
+      if (r0 + i < r1) {
+        const int32_t next = keep[i + 1];
+        if (next < prev) bad = 1;
+        local += tiles_of_length(static_cast<int64_t>(next) - prev);
+        prev = next;
+      }
+    }
+    for (int32_t b = r0 + kKeep; b < r1; ++b) {
       const int32_t next = ldg_i32(p.kv_indptr + b + 1);
       if (next < prev) bad = 1;
       local += tiles_of_length(static_cast<int64_t>(next) - prev);
@@ -425,7 +493,10 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
   }
   if (tid == 0) {
     const int64_t limit = p.kv_indices != nullptr ? p.kv_indices_len : p.kv_rows;
-    if (ldg_i32(p.kv_indptr) < 0 || ldg_i32(p.kv_indptr + batch) > limit) bad = 1;
+    const int32_t e0 = ldg_i32(p.kv_indptr), e1 = ldg_i32(p.kv_indptr + batch);
+    if (e0 < 0 || e1 > limit) bad = 1;
+    // (the stamp depends on the loaded values, so it follows their arrival)
+    if (e0 != INT32_MIN && local != INT32_MIN) MLA_TRACE_CLK(kTrIndptrLoaded);
   }
   int32_t incl = local;
 #pragma unroll
@@ -434,7 +505,10 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
     if (lane >= off) incl += v;
   }
   if (lane == 31) ms->scan[warp] = incl;
+  // (first_row / last_row were set to -1 before the wait for the previous
+  // kernel; this barrier orders that before the second pass below.)
   bad = __syncthreads_or(bad);
+  if (tid == 0) MLA_TRACE_CLK(kTrScanBarrier);
 
   int32_t warp_off = 0, total = 0;
   for (int w = 0; w < nwarps; ++w) {
@@ -450,19 +524,19 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
     ms->total_tiles = total;
     ms->t0 = t0;
     ms->t1 = t1;
-    ms->first_row = -1;
-    ms->last_row = -1;
-    ms->first_prefix = 0;
     ms->bad = bad;
     if (bad) set_error(p.err, MLA_DERR_KV_INDPTR);
   }
-  __syncthreads();
 
   int32_t a = bad ? 0 : warp_off + incl - local;
   if (r0 < r1) {
-    int32_t prev = ldg_i32(p.kv_indptr + r0);
+    int32_t prev = keep[0];
     for (int32_t b = r0; b < r1; ++b) {
-      const int32_t next = ldg_i32(p.kv_indptr + b + 1);
+      int32_t next = 0;
+#pragma unroll
+      for (int i = 0; i < kKeep; ++i)
+        if (b - r0 == i) next = keep[i + 1];
+      if (b - r0 >= kKeep) next = ldg_i32(p.kv_indptr + b + 1);
       const int32_t nt = bad ? 0 : tiles_of_length(static_cast<int64_t>(next) - prev);
       if (c == 0) p.prefix[b] = a;
       if (nt == 0 && b % p.grid == c) zero_row<kQ>(p, b);  // no cached token: zero output
@@ -481,7 +555,10 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
           ms->first_tq = tq;
           // Warm L2 with what the pipeline reads first: this CTA's query
           // tokens of the row and (contiguous rows) the worker's first tile,
-          // while the roles are still starting up.
+          // while the roles are still starting up.  (Issuing the tile's copies
+          // or a bulk copy of the query from here instead measured slower: the
+          // block barrier after the prologue, which every role waits for, then
+          // ends later, and the query copy lands after the tile.)
           if (tq >= 0)
             prefetch_bulk_l2(p.q + static_cast<size_t>(tq) * kNumHeads * kQkDim,
                              static_cast<uint32_t>(cta_tokens<kQ>(p)) * kNumHeads * kQkDim * 2);
@@ -499,6 +576,159 @@ __device__ void schedule_prologue(const Stage1Params& p, Misc* ms) {
     }
   }
   if (c == 0 && tid == 0) p.prefix[batch] = total;
+}
+
+// ------------------------------------------------------------ cluster split prologue
+// Row b = blockIdx.x / s is shared by the s CTAs of one cluster (blockIdx.x =
+// s b + rank); the CTA of rank r takes the row's tiles [r k, min((r + 1) k, nt)),
+// k = ceil(nt / s).  Every CTA checks the whole kv_indptr, as the persistent
+// prologue does (a bad one empties every row), in one round trip: thread i
+// loads the pointers of row i (the plan keeps the batch within the block), the
+// owner of row b also its query bounds.  The roles then see the CTA's share as
+// a one-segment tile range starting at prefix 0.  With contiguous rows thread 0
+// also issues the share's first tile, so that its copies fly while the roles
+// start.  The persistent split's worker records are marked empty so that a
+// separately launched stage 2 finds no combine job.
+template <int kQ, Kv kFmt>
+__device__ void cluster_prologue(const Stage1Params& p, const CUtensorMap* map_v,
+                                 const CUtensorMap* map_r, Misc* ms, uint32_t sbase) {
+  const int tid = threadIdx.x;
+  const int32_t batch = p.batch, s = p.cluster;
+  const int32_t b = static_cast<int32_t>(blockIdx.x) / s, rank = static_cast<int32_t>(blockIdx.x) % s;
+  int bad = 0;
+  for (int32_t r = tid; r < batch; r += blockDim.x) {
+    const int32_t x0 = ldg_i32(p.kv_indptr + r), x1 = ldg_i32(p.kv_indptr + r + 1);
+    if (x1 < x0) bad = 1;
+    if (r == b) {
+      const int32_t q_lo = ldg_i32(p.qo_indptr + b), q_hi = ldg_i32(p.qo_indptr + b + 1);
+      ms->first_kb = x0;
+      ms->first_len = x1 - x0;
+      ms->first_tq = row_token(p, cta_q_off(p), q_lo, q_hi);
+    }
+  }
+  if (tid == 0) {
+    const int64_t limit = p.kv_indices != nullptr ? p.kv_indices_len : p.kv_rows;
+    if (ldg_i32(p.kv_indptr) < 0 || ldg_i32(p.kv_indptr + batch) > limit) bad = 1;
+  }
+  if (blockIdx.x == 0)
+    for (int32_t c = tid; c < p.grid; c += blockDim.x) p.workers[8 * c + 4] = -1;
+  bad = __syncthreads_or(bad);
+  if (tid == 0) MLA_TRACE_CLK(kTrScanBarrier);
+  if (tid == 0) {
+    const int32_t nt = bad ? 0 : tiles_of_length(ms->first_len);
+    const int32_t k = (nt + s - 1) / s;
+    const int32_t j0 = min(rank * k, nt), j1 = min(j0 + k, nt);
+    ms->total_tiles = nt;
+    ms->t0 = j0;
+    ms->t1 = j1;
+    ms->first_prefix = 0;
+    ms->first_tiles = nt;
+    ms->first_row = j1 > j0 ? b : -1;
+    ms->last_row = ms->first_row;
+    ms->bad = bad;
+    if (bad) set_error(p.err, MLA_DERR_KV_INDPTR);
+    if (j1 > j0) {
+      const int32_t tq = ms->first_tq;
+      if (tq >= 0)
+        prefetch_bulk_l2(p.q + static_cast<size_t>(tq) * kNumHeads * kQkDim,
+                         static_cast<uint32_t>(cta_tokens<kQ>(p)) * kNumHeads * kQkDim * 2);
+      if (kFmt != Kv::kMx4 && p.kv_bytes != nullptr && !p.stall_stream)
+        issue_first_tile<kQ, kFmt>(p, map_v, map_r, ms, sbase, ms->first_kb + j0 * kTileTokens);
+    }
+  }
+}
+
+// ------------------------------------------------------------ cluster split combine
+// Every thread of the CTA of rank r, after the cluster barrier that publishes
+// the cluster's partials: the output dims [r D, (r + 1) D), D = 512 / s, of all
+// 16 heads of the row's query token, combined from the s CTAs' partials (the
+// workspace's partial slots s b .. s b + s - 1: normalised bf16 outputs and
+// base-2 log-sum-exps, written by the epilogues) with the weights
+// w_i = 2^(lse_i - M) / sum_j 2^(lse_j - M), M = max_i lse_i (submission 722089,
+// `_mla_reduce`).  A CTA without tokens (lse = -inf) weighs 0 and its slot is
+// not read; a row with none outputs zeros.  The partials go through L2 (loads
+// that bypass L1, which may hold an earlier call's values): an SM pulls them
+// from L2 several times faster than from its peers' shared memory.
+template <int kQ, Kv kFmt>
+__device__ void cluster_combine(const Stage1Params& p, Misc* ms) {
+  const int tid = threadIdx.x;
+  const int32_t s = p.cluster;
+  const int32_t rank = static_cast<int32_t>(cluster_ctarank());
+  const int32_t slot0 = static_cast<int32_t>(blockIdx.x) - rank;  // the row's first slot
+  const size_t slot_lse = static_cast<size_t>(p.slot_tokens) * kNumHeads;
+  const size_t slot_part = static_cast<size_t>(p.slot_tokens) * (kNumHeads * kVDim / 4);  // uint2s
+  // Item = (dim, quarter of the heads): one 8-byte piece (4 heads) of each
+  // slot's partial, stored [slot][token][dim / 128][head / 8][dim % 128][head % 8].
+  // The pieces are loaded first and are in flight while the weights form.
+  const int32_t dims = kVDim / s;
+  const int32_t items = 4 * dims;
+  constexpr int kPerThread = 4;  // items per thread: 4 x 512 / s <= 1024 with s >= 2, 256 threads
+  uint2 v[kPerThread][kMaxCluster];
+#pragma unroll
+  for (int k = 0; k < kPerThread; ++k) {
+    const int32_t it = tid + k * static_cast<int32_t>(blockDim.x);
+    const int32_t quarter = it / dims, d = rank * dims + it % dims;
+    const size_t piece = ((static_cast<size_t>(d >> 7) * 2 + (quarter >> 1)) * 128 + (d & 127)) * 2 +
+                         (quarter & 1);
+#pragma unroll
+    for (int i = 0; i < kMaxCluster; ++i)
+      v[k][i] = it < items && i < s
+                    ? __ldcg(reinterpret_cast<const uint2*>(p.partial) + (slot0 + i) * slot_part + piece)
+                    : make_uint2(0, 0);
+  }
+  // Weights of (slot, head), one thread each: w = 2^(lse - M) / sum over the
+  // row's slots, M the largest; a slot without tokens (lse = -inf) weighs 0.
+  if (tid < 16 * s) {
+    const int i = tid >> 4, h = tid & 15;
+    float lse[kMaxCluster];
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j) {
+      lse[j] = j < s ? __ldcg(p.lse + (slot0 + j) * slot_lse + h) : -INFINITY;
+      m = fmaxf(m, lse[j]);
+    }
+    float sum = 0.0f, mine = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j) {
+      const float e = lse[j] != -INFINITY ? exp2f(lse[j] - m) : 0.0f;
+      sum += e;
+      mine = j == i ? e : mine;
+    }
+    ms->cl_w[i][h] = sum > 0.0f ? mine / sum : 0.0f;
+  }
+  __syncthreads();
+  const int32_t tq = ms->first_tq;
+  if (tq < 0) {  // the row's query tokens are malformed: the row is not written
+    if (tid == 0 && rank == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < kPerThread; ++k) {
+    const int32_t it = tid + k * static_cast<int32_t>(blockDim.x);
+    if (it >= items) continue;
+    const int32_t quarter = it / dims, d = rank * dims + it % dims;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < kMaxCluster; ++i) {
+      if (i >= s) continue;
+      const float4 w = *reinterpret_cast<const float4*>(&ms->cl_w[i][4 * quarter]);
+      const float x[4] = {__uint_as_float(v[k][i].x << 16), __uint_as_float(v[k][i].x & 0xFFFF0000u),
+                          __uint_as_float(v[k][i].y << 16), __uint_as_float(v[k][i].y & 0xFFFF0000u)};
+      // (an empty or abandoned piece is never written: its weight 0 keeps it out)
+      acc[0] = w.x != 0.0f ? fmaf(w.x, x[0], acc[0]) : acc[0];
+      acc[1] = w.y != 0.0f ? fmaf(w.y, x[1], acc[1]) : acc[1];
+      acc[2] = w.z != 0.0f ? fmaf(w.z, x[2], acc[2]) : acc[2];
+      acc[3] = w.w != 0.0f ? fmaf(w.w, x[3], acc[3]) : acc[3];
+    }
+    if (MLA_DCHECK(tq < total_tokens(p), p.err)) {
+      uint16_t* dst = p.out + (static_cast<size_t>(tq) * kNumHeads + 4 * quarter) * kVDim + d;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const __nv_bfloat16 y = __float2bfloat16_rn(acc[h]);
+        dst[h * kVDim] = *reinterpret_cast<const uint16_t*>(&y);
+      }
+    }
+  }
 }
 
 template <int kQ>
@@ -554,12 +784,21 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
   constexpr uint32_t kProducers = num_producers<kGather, kQ>();
   static_assert(kProducers <= sizeof(Misc::next_panel) / sizeof(uint32_t), "producer slots");
   const int lane = threadIdx.x & 31;
+#ifdef MLA_TRACE
+  // Trace builds: an idle lane of the contiguous-rows producer watches the
+  // first tile's copies land (bounded waits).
+  if (!kGather && lane == 1 && !p.stall_stream && ms->t1 > ms->t0 && ms->first_row >= 0) {
+    if (drain_phase(smem_u32(&ms->r_full[0]), 0)) MLA_TRACE_CLK(kTrRopeArrived);
+    if (drain_phase(smem_u32(&ms->v_full[3 % G::kNumV]), 0)) MLA_TRACE_CLK(kTrTileArrived);
+  }
+#endif
   if (!kGather && lane != 0) return;
   Cursor cur;
   cursor_start(cur, ms);
   if (p.stall_stream) cur.live = false;  // test hook: nothing is ever loaded
   uint32_t tile = 0;
   uint32_t next_k = 0;  // one past the last panel this warp issued
+  const bool tile0_issued = !kGather && ms->tile0_issued;  // by the prologue
   bool ok = true;
   while (cur.live && ok) {
     const int32_t tok0 = cur.kb + cur.j * kTileTokens;
@@ -582,6 +821,10 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
     for (int c = -1; c < 4 && ok; ++c) {  // c = -1: rope panel, 0..3: latent panels
       const uint32_t k = tile * 5 + 1 + c;
       if (kProducers > 1 && k % kProducers != who) continue;
+      if (tile == 0 && tile0_issued) {
+        next_k = k + 1;
+        continue;
+      }
       uint32_t slot, use, bytes, dst, full, empty;
       int32_t x;
       const CUtensorMap* map;
@@ -634,6 +877,7 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
           tma_load_2d(dst + i * kTileTokens * 128, map, x + 128 * i, tok0, full);
       }
       next_k = k + 1;
+      if (k == 0 && lane == 0) MLA_TRACE_CLK(kTrFirstCopy);
     }
     if (!ok) break;
     ++tile;
@@ -720,6 +964,7 @@ __device__ void run_producer_mx(const Stage1Params& p, const CUtensorMap* map_v,
 #pragma unroll 1
       for (int i = 0; i < kSclBoxes; ++i) tma_load_1d(sdst + 256 * i, map_s, x0 + 256 * i, full);
       r_fills = tile + 1;
+      if (tile == 0) MLA_TRACE_CLK(kTrFirstCopy);
     }
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
@@ -1017,6 +1262,7 @@ __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
     if (ok) ok = wait_phase(smem_u32(&ms->r_full[qk_n % kNumRSlots]), (qk_n / kNumRSlots) & 1, ms,
                             p.err);
     if (!ok) break;
+    if (qk_n == 0) MLA_TRACE_CLK(kTrRopeLanded);
     tc_fence_after();
     issue_qk_rope<kQ, kFmt>(tmem, sbase, qk_n);
     for (int c = 0; c < 4 && ok; ++c) {
@@ -1029,6 +1275,7 @@ __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
     if (!ok) break;
     umma_commit(smem_u32(&ms->s_full[qk_n & 1]));  // also frees rope slot qk_n & 1
     if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
+    if (qk_n == 0) MLA_TRACE_CLK(kTrQkIssued);
     ++qk_n;
     cursor_next_tile(qc, ms, p.kv_indptr, p.batch);
   }
@@ -1053,6 +1300,7 @@ __device__ void run_mma_pv(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
     tc_fence_after();
     issue_pv<kQ, kFmt>(tmem, sbase, pv_n, first, ms);
     umma_commit(smem_u32(&ms->pv_done[pv_n & 1]));
+    if (pv_n == 0) MLA_TRACE_CLK(kTrPvIssued);
     ++pv_n;
     cursor_next_tile(pc, ms, p.kv_indptr, p.batch);
   }
@@ -1173,6 +1421,7 @@ __device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 
       }
     }
     amax = __reduce_max_sync(0xffffffffu, amax);
+    if (t == 0 && qi == 0 && ms->q_ready == 0 && amax != 0xFFFFFFFFu) MLA_TRACE_CLK(kTrQLoaded);
     if (lane == 0) ms->red_u32[4 * qi + warp] = amax;
   }
   named_bar_sync(kBarSoftmax, kSoftmaxThreads);
@@ -1219,11 +1468,12 @@ __device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 
 // nq <= kQ, the other operand rows stay zero) and writes the Q operand of the
 // cache format.  Sets qk_scale[qi], the factor turning the QK accumulator of
 // token qi into base-2 softmax exponent units.  tq < 0 writes a zero query.
-template <int kQ, Kv kFmt>
-__device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq, int32_t nq,
-                          float kv_scale, float (&qk_scale)[kQ]) {
+// This thread's share of the query tokens (16-dim chunks `t + 128 r` of the
+// 16 x 36 per token) into registers.
+template <int kQ>
+__device__ __forceinline__ void load_q(const Stage1Params& p, int32_t tq, int32_t nq,
+                                       uint4 (&raw)[kQ][5][2]) {
   const int t = threadIdx.x;
-  uint4 raw[kQ][5][2];
 #pragma unroll
   for (int qi = 0; qi < kQ; ++qi) {
 #pragma unroll
@@ -1239,6 +1489,14 @@ __device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t 
       }
     }
   }
+}
+
+template <int kQ, Kv kFmt>
+__device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq, int32_t nq,
+                          float kv_scale, float (&qk_scale)[kQ]) {
+  const int t = threadIdx.x;
+  uint4 raw[kQ][5][2];
+  load_q<kQ>(p, tq, nq, raw);
   // The previous segment's output row may still be leaving the Q region
   // through a bulk store (the loads above are already in flight); the barrier
   // below orders every write to it after this wait.
@@ -1314,7 +1572,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // kInlineWaits: the waits' slow paths inlined (required where setmaxnreg raised
 // the register count: a call out of such a region does not compile).
-template <int kQ, Kv kFmt, bool kInlineWaits>
+template <int kQ, Kv kFmt, bool kInlineWaits, bool kCluster>
 __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem,
                             float kv_scale) {
   using G = Geo<kQ, kFmt>;
@@ -1361,6 +1619,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       if (cur.seg > 0) softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
       prepare_q<kQ, kFmt>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, nq, kv_scale, qk_scale);
       if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 1));
+      if (t == 0 && cur.seg == 0) MLA_TRACE_CLK(kTrQReady);
     }
     q_early = false;
 
@@ -1415,6 +1674,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         }
       }
       tc_fence_before();
+      if (t == 0 && tile == 0) MLA_TRACE_CLK(kTrSRead);
 
       // The reference maximum moves only when some score exceeds it by more
       // than the threshold (always on a segment's first tile); then the tile
@@ -1540,6 +1800,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       tc_fence_before();
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);
       if (t == 0) st_release_u32(&ms->p_ready, tile + 1);
+      if (t == 0 && tile == 0) MLA_TRACE_CLK(kTrPReady);
       ++tile;
       if (cur.j + 1 == cur.j1) break;
       ++cur.j;
@@ -1603,8 +1864,9 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     }
     wait_pv(tile - 1);  // PV of the segment's last tile (and so of all before it)
     tc_fence_after();
+    if (t == 0 && cur.seg == 0) MLA_TRACE_CLK(kTrEpilogue);
     const uint32_t stage_q = sbase + G::kOffQ;
-    if (cur.whole) {
+    if (!kCluster && cur.whole) {
       // bf16 rows [nq tokens][16 heads][512 dims] (16 KB each), staged in the Q region.
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
@@ -1636,7 +1898,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       // stores its own values straight from registers (a warp's stores are
       // 512 contiguous bytes) and nothing waits for them to drain.  The float
       // base-2 log-sum-exps follow, one per (token, head).
-      const int32_t slot = partial_slot(c, ms->t0, cur.row_a);
+      // (the cluster split: CTA i's piece goes to slot i, combined in this kernel)
+      const int32_t slot = kCluster ? static_cast<int32_t>(blockIdx.x) : partial_slot(c, ms->t0, cur.row_a);
       const size_t piece = static_cast<size_t>(slot) * p.slot_tokens + slot_q;  // (slot, token)
 #pragma unroll 1
       for (int k = 0; k < 4 * nq; ++k) {
@@ -1658,8 +1921,10 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
                                               pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
         }
       }
-      if (write && t < 16 * nq) {
-        // thread t writes the LSE of (token t / 16, head t % 16); -inf when it saw nothing
+      if ((write || kCluster) && t < 16 * nq) {
+        // thread t writes the LSE of (token t / 16, head t % 16); -inf when it saw
+        // nothing (or, for the cluster split, when the call gave up: the piece is
+        // then not written and weighs 0)
         float mm = m_ref[0][0], ll = l_tot[0][0];
 #pragma unroll
         for (int e = 1; e < 16 * kQ; ++e) {
@@ -1667,7 +1932,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
           ll = t == e ? l_tot[e >> 4][e & 15] : ll;
         }
         if (MLA_DCHECK(static_cast<int64_t>(piece) * kNumHeads + t < partial_elems(p) / kVDim, p.err))
-          p.lse[piece * kNumHeads + t] = mm + log2f(ll);
+          p.lse[piece * kNumHeads + t] = write ? mm + log2f(ll) : -INFINITY;
       }
     }
     // O has been read out (tcgen05.wait::ld above): the next segment's PV may
@@ -1676,6 +1941,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     tc_fence_before();
     named_bar_sync(kBarSoftmax, kSoftmaxThreads);
     if (t == 0) st_relaxed_u32(&ms->o_free, static_cast<uint32_t>(cur.seg + 1));
+    if (t == 0 && cur.seg == 0) MLA_TRACE_CLK(kTrEpilogueDone);
     cursor_next_tile(cur, ms, p.kv_indptr, p.batch);
   }
   // The bulk stores have read their staging and written global memory before
@@ -1743,7 +2009,7 @@ __global__ void debug_p_split_kernel(const float* p, int64_t groups, uint8_t* hi
 }
 
 // ------------------------------------------------------------ kernel
-template <bool kGather, int kQ, Kv kFmt>
+template <bool kGather, int kQ, Kv kFmt, bool kCluster>
 __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
     mla_decode_stage1_kernel(const __grid_constant__ CUtensorMap map_v,
                              const __grid_constant__ CUtensorMap map_r,
@@ -1755,6 +2021,10 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
   Misc* ms = reinterpret_cast<Misc*>(smem + G::kOffMisc);
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    MLA_TRACE_NS(kTrEntryNs);
+    MLA_TRACE_CLK(kTrEntry);
+  }
 
   if (warp == kMmaWarp) tmem_alloc(smem_u32(&ms->tmem_base), G::kTmemCols);
   if (tid == kProducerWarp * 32) {
@@ -1778,6 +2048,10 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
     ms->q_ready = ms->s_read = ms->p_ready = ms->o_free = 0;
     mbar_init(smem_u32(&ms->mma_done), 2);  // one commit from each MMA issuer
     ms->abort_flag = 0;
+    ms->first_row = -1;
+    ms->last_row = -1;
+    ms->first_prefix = 0;
+    ms->tile0_issued = 0;
     fence_mbar_init();
     prefetch_tensormap(&map_v);
     prefetch_tensormap(&map_r);
@@ -1787,11 +2061,16 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
   // previous kernel of the stream is finishing: everything above touches only
   // this CTA's own resources, everything below may read that kernel's results
   // or write what it reads.  (Without the launch attribute the wait is a no-op.)
+  if (tid == 0) MLA_TRACE_CLK(kTrPreWait);
   pdl_wait_primary();
+  if (tid == 0) MLA_TRACE_CLK(kTrPostWait);
   // Stage 2 may start launching now; it waits for this grid's completion
   // before it reads anything this grid writes.
   pdl_launch_dependents();
-  schedule_prologue<kQ>(p, ms);
+  if constexpr (kCluster)
+    cluster_prologue<kQ, kFmt>(p, &map_v, &map_r, ms, sbase);
+  else
+    schedule_prologue<kQ, kFmt>(p, &map_v, &map_r, ms, sbase);
   if constexpr (kGather) {
     __syncthreads();
     if (tid == 0 && cta_sibling(p) == 0) write_worker_record<kQ>(p, ms);
@@ -1799,6 +2078,7 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0) MLA_TRACE_CLK(kTrPrologue);
   const uint32_t tmem = ms->tmem_base;
 
   // Page-table mode and the MXFP4 cache run 12 warps: registers move from the
@@ -1811,7 +2091,7 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
     if constexpr (kWide) setmaxnreg_inc<kSoftmaxRegs>();
     const float kv_scale = G::kMx ? __int_as_float((127 + p.mx_bias) << 23)
                                   : (G::kSplit ? __ldg(p.kv_scale) : 1.0f);
-    run_softmax<kQ, kFmt, kWide || kQ == 2>(p, ms, sbase, tmem, kv_scale);
+    run_softmax<kQ, kFmt, kWide || kQ == 2, kCluster>(p, ms, sbase, tmem, kv_scale);
   } else {
     if constexpr (G::kMx)
       setmaxnreg_dec<kOtherRegsMx>();
@@ -1830,13 +2110,29 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
       run_mma_pv<kQ, kFmt>(p, ms, sbase, tmem);
     } else if (warp == kMmaQkWarp && lane == 0) {
       run_mma_qk<kQ, kFmt>(p, ms, sbase, tmem);
-    } else if (!kGather && warp == kIdleWarp && lane == 0 && cta_sibling(p) == 0) {
+    } else if (!kGather && !kCluster && warp == kIdleWarp && lane == 0 && cta_sibling(p) == 0) {
       write_worker_record<kQ>(p, ms);
     }
   }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if constexpr (kCluster) {
+    // A CTA without tokens marks its slot empty; then the barrier publishes
+    // every CTA's partial (its global writes, released at cluster scope) and
+    // the row is combined.
+    if (ms->first_row < 0 && tid < 16 &&
+        MLA_DCHECK(static_cast<int64_t>(blockIdx.x) * p.slot_tokens < 2LL * p.grid * p.slot_tokens, p.err))
+      p.lse[static_cast<size_t>(blockIdx.x) * p.slot_tokens * kNumHeads + tid] = -INFINITY;
+    cluster_sync_all();
+    if (tid == 0) MLA_TRACE_CLK(kTrClusterBarrier);
+    cluster_combine<kQ, kFmt>(p, ms);
+    if (tid == 0) MLA_TRACE_CLK(kTrCombineDone);
+  }
+  if (tid == 0) {
+    MLA_TRACE_CLK(kTrExit);
+    MLA_TRACE_NS(kTrExitNs);
+  }
   if (warp == kMmaWarp) {
     if (lane == 0) drain_phase(smem_u32(&ms->mma_done), 0);
     __syncwarp();
@@ -1845,9 +2141,9 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
   }
 }
 
-template <bool kGather, int kQ, Kv kFmt>
+template <bool kGather, int kQ, Kv kFmt, bool kCluster = false>
 cudaError_t set_smem_limit() {
-  return cudaFuncSetAttribute(mla_decode_stage1_kernel<kGather, kQ, kFmt>,
+  return cudaFuncSetAttribute(mla_decode_stage1_kernel<kGather, kQ, kFmt, kCluster>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem_alloc<kQ, kFmt>());
 }
 
@@ -1859,26 +2155,33 @@ cudaError_t set_smem_limits() {
   if (e == cudaSuccess) e = set_smem_limit<false, 1, Kv::kBf16>();
   if (e == cudaSuccess) e = set_smem_limit<false, 2, Kv::kBf16>();
   if (e == cudaSuccess) e = set_smem_limit<false, 1, Kv::kMx4>();
+  if (e == cudaSuccess) e = set_smem_limit<false, 1, Kv::kE4m3, true>();
+  if (e == cudaSuccess) e = set_smem_limit<false, 1, Kv::kBf16, true>();
   return e;
 }
 
-template <bool kGather, int kQ, Kv kFmt>
+template <bool kGather, int kQ, Kv kFmt, bool kCluster = false>
 cudaError_t launch(const Stage1Params& p, const Stage1Maps& maps, cudaStream_t stream) {
   // A programmatic dependent of the previous kernel in the stream: its CTAs
   // may be scheduled while that kernel finishes, and wait for it (griddepcontrol
-  // .wait) before touching global memory.
+  // .wait) before touching global memory.  The cluster split launches one
+  // cluster of p.cluster CTAs per row.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.grid * p.siblings));
+  cfg.gridDim = dim3(static_cast<unsigned>(kCluster ? p.batch * p.cluster : p.grid * p.siblings));
   cfg.blockDim = dim3(stage1_threads<kGather, kQ, kFmt>());
   cfg.dynamicSmemBytes = smem_alloc<kQ, kFmt>();
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kCluster ? static_cast<unsigned>(p.cluster) : 1u;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_decode_stage1_kernel<kGather, kQ, kFmt>, maps.v, maps.r,
-                            maps.s, p);
+  cfg.numAttrs = kCluster ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, mla_decode_stage1_kernel<kGather, kQ, kFmt, kCluster>, maps.v,
+                            maps.r, maps.s, p);
 }
 
 
@@ -1904,6 +2207,12 @@ cudaError_t launch_stage1(const Stage1Params& p, const Stage1Maps& maps, bool ga
     if (gather || two) return cudaErrorNotSupported;  // the host rejects these before launching
     return launch<false, 1, Kv::kMx4>(p, maps, stream);
   }
+  if (p.cluster > 0) {  // contiguous rows, one query token (the host checks)
+    if (gather || two || p.cluster > kMaxCluster || (p.cluster & (p.cluster - 1)) != 0)
+      return cudaErrorNotSupported;
+    return format == CacheFormat::kBf16 ? launch<false, 1, Kv::kBf16, true>(p, maps, stream)
+                                        : launch<false, 1, Kv::kE4m3, true>(p, maps, stream);
+  }
   if (format == CacheFormat::kBf16) {
     if (gather) return cudaErrorNotSupported;  // the host rejects this before launching
     return two ? launch<false, 2, Kv::kBf16>(p, maps, stream)
@@ -1915,6 +2224,19 @@ cudaError_t launch_stage1(const Stage1Params& p, const Stage1Maps& maps, bool ga
   return gather ? launch<true, 1, Kv::kE4m3>(p, maps, stream)
                 : launch<false, 1, Kv::kE4m3>(p, maps, stream);
 }
+
+#ifdef MLA_TRACE
+cudaError_t trace_read_stage1(unsigned long long* host, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(host, g_trace_stage1, sizeof(g_trace_stage1));
+  if (e == cudaSuccess && clear) {
+    static const unsigned long long zeros[kTraceCtas * kTraceEvents] = {};
+    e = cudaMemcpyToSymbol(g_trace_stage1, zeros, sizeof(zeros));
+  }
+  return e;
+}
+#else
+cudaError_t trace_read_stage1(unsigned long long*, bool) { return cudaErrorNotSupported; }
+#endif
 
 cudaError_t launch_debug_q_operand(const uint16_t* q, int32_t tokens, int32_t per_cta,
                                    const float* kv_scale, uint8_t* codes, float* qk_scale,

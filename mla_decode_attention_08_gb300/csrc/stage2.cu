@@ -28,20 +28,39 @@ namespace {
 constexpr int kStage2Threads = 128;  // one thread per dim of a 128-dim chunk
 constexpr int kStage2Unroll = 4;     // partials loaded together
 
+// Start-up trace (-DMLA_TRACE only): global-timer stamps of each block at entry,
+// after the wait for stage 1 and at exit (see kernels.h).
+#ifdef MLA_TRACE
+__device__ unsigned long long g_trace_stage2[kTrace2Blocks * kTrace2Events];
+__device__ __forceinline__ void trace2_put(int ev) {
+  const unsigned blk = blockIdx.y * gridDim.x + blockIdx.x;
+  if (threadIdx.x == 0 && blk < static_cast<unsigned>(kTrace2Blocks))
+    g_trace_stage2[blk * kTrace2Events + ev] = global_timer_ns();
+}
+#define MLA_TRACE2(ev) trace2_put(ev)
+#else
+#define MLA_TRACE2(ev) ((void)0)
+#endif
+
 __global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const Stage2Params p) {
   __shared__ __align__(16) uint16_t blk[4 * kStage2Threads];  // bf16 [4 heads][128 dims]
+  MLA_TRACE2(0);
   // The next kernel of the stream may start launching; it waits for this
   // grid's completion before it touches global memory.
   pdl_launch_dependents();
   // Everything read below is written by stage 1.
   pdl_wait_primary();
+  MLA_TRACE2(1);
 
   const int32_t c = blockIdx.x;
   const int qi = blockIdx.y >> 4, cc = (blockIdx.y >> 2) & 3, j = blockIdx.y & 3, dd = threadIdx.x;
   const int32_t nq = p.qo_len;
   const int4* rec = reinterpret_cast<const int4*>(p.workers);
   const int4 job = rec[2 * c + 1];  // (output row, first worker, last worker, first slot)
-  if (job.x < 0) return;
+  if (job.x < 0) {
+    MLA_TRACE2(2);
+    return;
+  }
   const int32_t tq = job.x + qi;  // output row: query token qi of the row
   if (!MLA_DCHECK(tq < p.batch * nq && job.y >= 0 && job.z < p.grid && job.w < 2 * p.grid, p.err))
     return;
@@ -102,9 +121,23 @@ __global__ void __launch_bounds__(kStage2Threads) mla_decode_stage2_kernel(const
     uint16_t* dst = p.out + (static_cast<size_t>(tq) * kNumHeads + 4 * j + h) * kVDim + 128 * cc + part * 8;
     *reinterpret_cast<uint4*>(dst) = reinterpret_cast<const uint4*>(blk)[dd];
   }
+  MLA_TRACE2(2);
 }
 
 }  // namespace
+
+#ifdef MLA_TRACE
+cudaError_t trace_read_stage2(unsigned long long* host, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(host, g_trace_stage2, sizeof(g_trace_stage2));
+  if (e == cudaSuccess && clear) {
+    static const unsigned long long zeros[kTrace2Blocks * kTrace2Events] = {};
+    e = cudaMemcpyToSymbol(g_trace_stage2, zeros, sizeof(zeros));
+  }
+  return e;
+}
+#else
+cudaError_t trace_read_stage2(unsigned long long*, bool) { return cudaErrorNotSupported; }
+#endif
 
 cudaError_t launch_stage2(const Stage2Params& p, bool programmatic, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};

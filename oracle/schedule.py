@@ -22,6 +22,12 @@ as follows (the pages print no formula for their persistent work map):
   partial (normalised output and base-2 log-sum-exp) to a workspace slot:
   slot ``2c`` when worker c's range begins inside that row, else ``2c + 1``.
 
+Small batches of one query token per row take the cluster split instead
+(``plan_cluster``): each row is shared by ``size`` CTAs of one thread-block
+cluster, rank r taking the row's tiles ``[r k, min((r + 1) k, n))`` with
+``k = ceil(n / size)``, and their partials are combined inside the cluster;
+the size follows the rule stated in ``plan_cluster``.
+
 This module is the restatement the CUDA path's schedule must match bit for bit.
 """
 from __future__ import annotations
@@ -48,6 +54,47 @@ def plan_grid(batch: int, max_kv_len: int, num_sms: int) -> int:
         if ceil_div(upper, g) <= most:
             return g
     return g0
+
+
+def cluster_capacity(size: int, num_sms: int) -> int:
+    """Clusters of ``size`` CTAs the GPU runs at once (the library's estimate):
+    num_sms // 10 of 8, 7 num_sms // 32 of 4, num_sms // 2 of 2."""
+    return {8: num_sms // 10, 4: (7 * num_sms) // 32, 2: num_sms // 2}[size]
+
+
+def plan_cluster(batch: int, qo_len: int, max_kv_len: int, num_sms: int) -> int:
+    """CTAs per row of the cluster split, or 0 for the persistent split.
+
+    Rows of one query token only.  The candidate sizes 8, 4, 2 are tried from
+    the largest: a size must not exceed the tiles of the longest row and its
+    clusters for the whole batch must fit the GPU at once.  The first that does
+    is taken when the longest share it gives, ceil(tiles / size), is at most two
+    tiles longer than the persistent split's longest range; otherwise 0.
+    """
+    tiles = ceil_div(max(0, max_kv_len), TILE_TOKENS)
+    if qo_len != 1 or batch < 1 or num_sms < 1 or tiles < 2:
+        return 0
+    chosen = 0
+    for size in (8, 4, 2):
+        if size <= tiles and batch <= cluster_capacity(size, num_sms):
+            chosen = size
+            break
+    if chosen == 0:
+        return 0
+    upper = batch * tiles
+    longest = ceil_div(upper, min(num_sms, upper))
+    return chosen if ceil_div(tiles, chosen) <= longest + 2 else 0
+
+
+def cluster_shares(kv_indptr, size: int) -> dict:
+    """(row, rank) -> (first tile, end tile) of each CTA's share under the cluster split."""
+    out = {}
+    for b, n in enumerate(row_tiles(kv_indptr)):
+        k = ceil_div(n, size)
+        for r in range(size):
+            j0 = min(r * k, n)
+            out[(b, r)] = (j0, min(j0 + k, n))
+    return out
 
 
 def row_tiles(kv_indptr) -> list[int]:

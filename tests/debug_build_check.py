@@ -43,6 +43,24 @@ def main() -> None:
     torch.cuda.synchronize()
     ref = mla_decode_ref_bf16kv(bf16_bits_to_f64(inp.q_bits), inp.kv_bits, inp.qo_indptr, inp.kv_indptr)
     results["bf16 q=2"] = {"err": binding.mla_decode_read_error(ws), **compare(out.float().cpu().numpy(), ref)}
+    # the cluster split (e4m3 and bf16 caches, sizes 8, 4 and 2)
+    for size_lengths, sms in (([1024, 1, 0, 700], 152), (list(range(3, 1024, 37)), 152),
+                              ([300, 299, 1], 152)):
+        inp = make_from_lengths(size_lengths, seed=82, max_kv_len=max(size_lengths))
+        dev = DeviceCase(inp)
+        gpu, err, plan, _ = dev.run(sms=sms)
+        st = compare(gpu, OracleCase(inp).reference())
+        results[f"e4m3 cluster={plan.cluster}"] = {"err": err, **st}
+        q, kv = bits_to_bf16(inp.q_bits), bits_to_bf16(inp.kv_bits)
+        qo, kvp = torch.from_numpy(inp.qo_indptr).cuda(), torch.from_numpy(inp.kv_indptr).cuda()
+        out = torch.empty((inp.batch, 16, 512), dtype=torch.bfloat16, device="cuda")
+        ws = binding.new_workspace(plan)
+        binding.mla_decode_fwd_bf16kv(q, kv, qo, kvp, out, plan=plan, workspace=ws)
+        torch.cuda.synchronize()
+        ref = mla_decode_ref_bf16kv(bf16_bits_to_f64(inp.q_bits), inp.kv_bits, inp.qo_indptr,
+                                    inp.kv_indptr)
+        results[f"bf16 cluster={plan.cluster}"] = {"err": binding.mla_decode_read_error(ws),
+                                                   **compare(out.float().cpu().numpy(), ref)}
     inp = make_from_lengths(lengths, seed=81)
     case = MxCase(inp)
     for sms in (3, 152):

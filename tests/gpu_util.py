@@ -48,9 +48,10 @@ class DeviceCase:
         self.out = torch.empty((inp.batch * inp.qo_len, 16, 512), dtype=torch.bfloat16,
                                device=device)
 
-    def run(self, sms: int | None = None, workspace=None, plan=None):
+    def run(self, sms: int | None = None, workspace=None, plan=None, persistent: bool = False):
         plan = plan or binding.mla_decode_plan(self.inp.batch, self.inp.max_kv_len,
-                                               sms or num_sms(), qo_len=self.inp.qo_len)
+                                               sms or num_sms(), qo_len=self.inp.qo_len,
+                                               persistent=persistent)
         ws = workspace if workspace is not None else binding.new_workspace(plan)
         binding.mla_decode_fwd(self.q, self.kv_codes, self.kv_scale, self.qo_indptr,
                                self.kv_indptr, self.out, plan=plan, workspace=ws,

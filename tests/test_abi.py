@@ -8,7 +8,7 @@ import pytest
 
 from mla_decode_attention_08_gb300 import binding
 from mla_decode_attention_08_gb300.build import ROOT
-from oracle.schedule import plan_grid, worker_table
+from oracle.schedule import plan_cluster, plan_grid, worker_table
 from oracle.schedule import schedule as oracle_schedule
 
 HEADER = os.path.join(ROOT, "include", "mla_decode.h")
@@ -34,7 +34,7 @@ def test_every_declared_function_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.mla_decode_abi_version() == 4
+    assert lib.mla_decode_abi_version() == 5
     for s in range(5):
         assert lib.mla_status_string(s)
 
@@ -177,3 +177,13 @@ def test_binding_refuses_a_cache_that_is_not_e4m3(lib, kv):
                                workspace=torch.zeros(16, dtype=torch.uint8))
     with pytest.raises(err):
         binding.mla_decode_fwd_static_scratch(q, cache, torch.ones(1), ind, ind, out, plan=plan)
+
+
+@pytest.mark.parametrize("qo_len", [1, 2])
+def test_plan_cluster_matches_oracle(lib, qo_len):
+    for sms in (152, 148, 40, 7, 1):
+        for batch in (1, 2, 3, 4, 5, 8, 15, 16, 32, 33, 34, 64, 76, 77, 256):
+            for max_len in (0, 1, 128, 129, 300, 512, 1024, 2048, 4096, 8192):
+                plan = binding.mla_decode_plan(batch, max_len, sms, qo_len=qo_len)
+                assert plan.cluster == plan_cluster(batch, qo_len, max_len, sms), (batch, max_len, sms)
+                assert plan.grid == plan_grid(batch, max_len, sms if qo_len <= 2 else sms // 2)

@@ -19,7 +19,7 @@ def test_debug_build_reports_no_out_of_bounds_access():
                        capture_output=True, text=True, timeout=1800, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     results = json.loads(r.stdout.strip().splitlines()[-1])
-    assert len(results) == 15
+    assert len(results) == 21
     for name, st in results.items():
         assert st["err"] == 0, (name, st)
         assert st["finite"] and st["violations"] == 0 and st["rel_l2"] <= 1e-2, (name, st)

@@ -32,13 +32,16 @@ SMALL = [
 
 @pytest.mark.parametrize("name,lengths,paged", SMALL, ids=[s[0] for s in SMALL])
 @pytest.mark.parametrize("sms", [1, 5, None])
-def test_small_shapes(name, lengths, paged, sms):
+@pytest.mark.parametrize("persistent", [False, True], ids=["planned", "persistent"])
+def test_small_shapes(name, lengths, paged, sms, persistent):
     inp = make_from_lengths(lengths, seed=777 + len(lengths), paged=paged)
     dev = DeviceCase(inp)
-    gpu, err, plan, ws = dev.run(sms=sms)
+    gpu, err, plan, ws = dev.run(sms=sms, persistent=persistent)
     assert err == 0
     ref = OracleCase(inp).reference()
     assert_close(gpu, ref)
+    if plan.cluster and not paged:
+        return  # the cluster split writes no persistent schedule (tests/test_gpu_cluster.py)
     # the schedule the kernel used, bit for bit
     views = binding.workspace_views(plan, ws)
     assert np.array_equal(views["workers"].cpu().numpy(), worker_table(inp.kv_indptr, plan.grid))
@@ -221,8 +224,9 @@ def test_workload_parity(name):
     check = np.arange(min(4096, inp.kv_bits.shape[0]))
     assert np.float32(dev.kv_scale.item()) == ora.scale
     assert np.array_equal(dev.kv_codes[: check.size].cpu().numpy(), ora.codes(check))
-    views = binding.workspace_views(plan, ws)
-    assert np.array_equal(views["workers"].cpu().numpy(), worker_table(inp.kv_indptr, plan.grid))
+    if plan.cluster == 0 or inp.kv_indices is not None:
+        views = binding.workspace_views(plan, ws)
+        assert np.array_equal(views["workers"].cpu().numpy(), worker_table(inp.kv_indptr, plan.grid))
     # rows of three or four query tokens take two sibling CTAs per worker
     sms = num_sms() if inp.qo_len <= 2 else num_sms() // 2
     assert plan.grid == plan_grid(inp.batch, inp.max_kv_len, sms)

@@ -2,7 +2,8 @@
 import numpy as np
 import pytest
 
-from oracle.schedule import TILE_TOKENS, plan_grid, schedule, token_segments, worker_table
+from oracle.schedule import (TILE_TOKENS, cluster_shares, plan_cluster, plan_grid, schedule,
+                             token_segments, worker_table)
 
 from .golden_util import load_table
 
@@ -68,3 +69,38 @@ def test_partition_invariants(seed):
     for b, ws in sch["covers"].items():
         if ws:
             assert ws == [c for c in nonempty if ws[0] <= c <= ws[-1]]
+
+
+# The cluster split's size, worked out by hand from its rule (largest of 8, 4, 2
+# not above the longest row's tiles whose clusters fit at once: num_sms // 10 of
+# 8, 7 num_sms // 32 of 4, num_sms // 2 of 2; taken when ceil(tiles / size) <=
+# the persistent longest range + 2).
+@pytest.mark.parametrize("batch,max_len,sms,qo_len,want", [
+    (4, 1024, 152, 1, 8),      # 8 tiles; 4 <= 15 clusters of 8; share 1 <= 1 + 2
+    (32, 1024, 152, 1, 4),     # 32 > 15 of 8; 32 <= 33 of 4; share 2 <= ceil(256/152) + 2
+    (34, 1024, 152, 1, 2),     # 34 > 33 of 4; 34 <= 76 of 2; share 4 <= 2 + 2
+    (64, 8192, 152, 1, 0),     # of 2 only; share 32 > ceil(4096/152) + 2 = 29
+    (256, 8192, 152, 1, 0),    # no size fits
+    (4, 8192, 152, 1, 0),      # share 8 > ceil(256/152) + 2 = 4
+    (4, 1024, 152, 2, 0),      # two query tokens per row
+    (1, 128, 152, 1, 0),       # one tile
+    (3, 300, 152, 1, 2),       # 3 tiles: 8 and 4 exceed them; share 2 <= 1 + 2
+    (8, 2048, 148, 1, 8),      # 148 // 10 = 14 clusters of 8; share 2 <= 1 + 2
+    (16, 2048, 152, 1, 4),     # 16 > 15 of 8; share 4 <= ceil(256/152) + 2 = 4
+    (5, 1024, 40, 1, 4),       # 40 // 10 = 4 < 5 of 8; 7*40 // 32 = 8 of 4; share 2 <= 1 + 2
+])
+def test_plan_cluster_by_hand(batch, max_len, sms, qo_len, want):
+    assert plan_cluster(batch, qo_len, max_len, sms) == want
+
+
+def test_cluster_shares_partition_each_row():
+    indptr = [0, 1000, 1000, 1001, 3000, 3129]
+    for size in (2, 4, 8):
+        sh = cluster_shares(indptr, size)
+        for b, n in enumerate([8, 0, 1, 16, 2]):
+            ranges = [sh[(b, r)] for r in range(size)]
+            assert ranges[0][0] == 0 and ranges[-1][1] == n
+            assert all(r0 <= r1 for r0, r1 in ranges)
+            assert all(ranges[i][1] == ranges[i + 1][0] for i in range(size - 1))
+            k = -(-n // size)
+            assert max(r1 - r0 for r0, r1 in ranges) == k
