@@ -246,11 +246,17 @@ def time_loop(torch, fn, steps: int, stream) -> float:
     return start.elapsed_time(end)
 
 
-def per_call_cold(torch, call, reps: int, stream, flush) -> list:
-    """Per-call device times (µs) of ``call(stream)`` with L2 flushed before each call."""
+def per_call_cold(torch, call, reps: int, stream, flush, clean=None) -> list:
+    """Per-call device times (µs) of ``call(stream)`` with L2 flushed before each call.
+
+    The flush writes a buffer of twice the L2 size; ``clean`` (as large) is then
+    read, so that the flush's dirty lines are written back before the timed
+    call rather than while it reads its inputs (both outside the events)."""
     times = []
     for _ in range(reps):
         flush.add_(1)
+        if clean is not None:
+            clean.max()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
         call(stream)
@@ -556,10 +562,11 @@ def ours_main(args) -> None:
     per_config = []
     if not args.no_per_config and rank == 0:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+        clean = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
         def cold(call, nbytes):
             for _ in range(5):
                 call(stream)
-            times = per_call_cold(torch, call, args.cold_reps, stream, flush)
+            times = per_call_cold(torch, call, args.cold_reps, stream, flush, clean)
             med = statistics.median(times)
             return {"us_median": round(med, 2),
                     "us_p10": round(float(np.percentile(times, 10)), 2),
@@ -571,7 +578,8 @@ def ours_main(args) -> None:
         for name in WORKLOADS:
             ww = w if name == args.workload else DeviceWorkload(name, torch, binding, sms)
             entry = {"workload": name, **cold(ww.call, ww.bytes), "grid": int(ww.plan.grid),
-                     "l2": "flushed before each call"}
+                     "cluster": int(ww.plan.cluster),
+                     "l2": "flushed before each call (2x L2 written, then 2x L2 of other data read)"}
             # the same step back to back (L2 warm for the small workloads), for reference
             entry["us_back_to_back"] = round(time_loop(torch, ww.call, 50, stream) / 50 * 1e3, 2)
             # the same step over the bf16 cache (mla_decode_fwd_bf16kv; contiguous caches only)
@@ -599,7 +607,7 @@ def ours_main(args) -> None:
             if ww is not w:
                 del ww
                 torch.cuda.empty_cache()
-        del flush
+        del flush, clean
 
     if args.cache != "bf16":
         w.kv_bf16 = None

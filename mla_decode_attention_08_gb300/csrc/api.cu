@@ -47,8 +47,15 @@ bool encode_kv_map(CUtensorMap* map, const void* kv, int64_t rows, bool bf16, ui
   const cuuint64_t gstride[1] = {row_bytes};
   const cuuint32_t box[2] = {box_w, box_h};
   const cuuint32_t estride[2] = {1, 1};
+  // Page-table rows (boxes one row high) sit at random places in the pool: a
+  // 64-byte promotion fetches exactly a row (576 = 9 x 64 bytes, rows 64-byte
+  // aligned), where 128- and 256-byte promotions also fetch parts of
+  // neighbouring rows (DRAM reads measured 313.5 MB against 341.6 MB with 256
+  // bytes for the ragged 128-row workload, whose algorithmic bytes are 313.9 MB).
+  const CUtensorMapL2promotion promo =
+      box_h == 1 ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), gdim, gstride, box,
-            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -737,9 +737,10 @@ __device__ __forceinline__ void write_worker_record(const Stage1Params& p, const
 // The worker record, then the combine job of the split row (if any) whose
 // first worker boundary is this worker's start: output row, first and last
 // worker of the row, partial slot of the first worker (the others use 2c).
-// Only stage 2 reads them: with contiguous rows the otherwise idle warp 7
-// writes them while the pipeline starts; the page-table kernels have no idle
-// warp, and the prologue's thread 0 writes them before the pipeline starts.
+// Only stage 2 reads them, so they are written off the start-up path while the
+// pipeline starts: by the otherwise idle warp 7 with contiguous rows, by an
+// idle lane of the PV issuer's warp in the page-table kernels (whose warp 7
+// produces).
 template <int kQ>
 __device__ __forceinline__ void write_worker_record(const Stage1Params& p, const Misc* ms) {
   const int32_t c = cta_worker(p);
@@ -2071,10 +2072,6 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
     cluster_prologue<kQ, kFmt>(p, &map_v, &map_r, ms, sbase);
   else
     schedule_prologue<kQ, kFmt>(p, &map_v, &map_r, ms, sbase);
-  if constexpr (kGather) {
-    __syncthreads();
-    if (tid == 0 && cta_sibling(p) == 0) write_worker_record<kQ>(p, ms);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -2110,7 +2107,8 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
       run_mma_pv<kQ, kFmt>(p, ms, sbase, tmem);
     } else if (warp == kMmaQkWarp && lane == 0) {
       run_mma_qk<kQ, kFmt>(p, ms, sbase, tmem);
-    } else if (!kGather && !kCluster && warp == kIdleWarp && lane == 0 && cta_sibling(p) == 0) {
+    } else if (!kCluster && cta_sibling(p) == 0 &&
+               (kGather ? warp == kMmaWarp && lane == 1 : warp == kIdleWarp && lane == 0)) {
       write_worker_record<kQ>(p, ms);
     }
   }
