@@ -257,6 +257,11 @@ def per_call_cold(torch, call, reps: int, stream, flush, clean=None) -> list:
         flush.add_(1)
         if clean is not None:
             clean.max()
+        # The flush kernels end before the start event (the call, a programmatic
+        # dependent launch, must not overlap them), and a short device-side wait
+        # keeps the host's launch latency out of the timed region.
+        torch.cuda.synchronize()
+        torch.cuda._sleep(50_000)
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
         call(stream)

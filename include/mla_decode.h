@@ -358,8 +358,12 @@ mla_status_t mla_debug_p_split(const float* p, int64_t n, void* hi_out, void* lo
  * scores read, first P published, first PV issued, first epilogue start and
  * end, exit; then the row-pointer loads returned, the prologue's scan barrier,
  * the first query loads returned, the first rope and last latent panel
- * arrived; for the cluster split the cluster barrier passed and the combine
- * written), and for each of the first
+ * arrived (an otherwise idle producer lane watching them); for the cluster split the cluster barrier passed and the combine
+ * written; not a clock, segments * 65536 + tiles of the CTA's range; then the
+ * boundary into the second segment: the first segment's last P published, the
+ * second segment's Q operand published, its first scores read, P published
+ * and PV issued, its Q preparation started and its query loads returned),
+ * and for each of the first
  * MLA_TRACE2_BLOCKS stage-2 blocks
  * (numbered y * grid_x + x) the global timer at entry, after its wait for
  * stage 1 and at exit.  Each call's stamps overwrite the previous call's.
@@ -369,7 +373,7 @@ mla_status_t mla_debug_p_split(const float* p, int64_t n, void* hi_out, void* lo
  * Synchronous.  Release builds return MLA_ERR_UNSUPPORTED.
  */
 #define MLA_TRACE_CTAS 320
-#define MLA_TRACE_EVENTS 24
+#define MLA_TRACE_EVENTS 32
 #define MLA_TRACE2_BLOCKS 4096
 mla_status_t mla_decode_trace_read(uint64_t* stage1_host, uint64_t* stage2_host, int32_t clear);
 

@@ -63,6 +63,14 @@ enum TraceEvent {
   kTrTileArrived = 20,   // observer lane: the first tile's last latent panel completed
   kTrClusterBarrier = 21,  // cluster split: thread 0 past the cluster barrier
   kTrCombineDone = 22,     // ... its share of the combine written
+  kTrShape = 23,           // not a clock: segments * 65536 + tiles of this CTA's range
+  kTrPLast0 = 24,          // softmax: the first segment's last P published
+  kTrQReady1 = 25,         // softmax: the second segment's Q operand published
+  kTrSRead1 = 26,          // softmax: the second segment's first scores read
+  kTrPReady1 = 27,         // softmax: the second segment's first P published
+  kTrPvIssued1 = 28,       // PV issuer: the second segment's first PV issued
+  kTrQStart1 = 29,         // softmax: the second segment's Q preparation starts
+  kTrQLoaded1 = 30,        // softmax: ... its query loads returned
 };
 // Copy the trace out (host arrays of kTraceCtas * kTraceEvents and kTrace2Blocks
 // * kTrace2Events entries) and zero it; cudaErrorNotSupported without -DMLA_TRACE.

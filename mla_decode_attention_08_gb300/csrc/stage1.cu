@@ -232,9 +232,13 @@ __device__ __forceinline__ void trace_put(int ev, unsigned long long v) {
 }
 #define MLA_TRACE_CLK(ev) trace_put((ev), static_cast<unsigned long long>(clock64()))
 #define MLA_TRACE_NS(ev) trace_put((ev), global_timer_ns())
+__device__ __forceinline__ void trace_shape(int32_t segments, int32_t tiles) {
+  trace_put(kTrShape, static_cast<unsigned long long>(segments) * 65536ull + static_cast<uint32_t>(tiles));
+}
 #else
 #define MLA_TRACE_CLK(ev) ((void)0)
 #define MLA_TRACE_NS(ev) ((void)0)
+__device__ __forceinline__ void trace_shape(int32_t, int32_t) {}
 #endif
 
 __device__ __forceinline__ void set_error(int32_t* err, int32_t bits) { atomicOr(err, bits); }
@@ -1302,6 +1306,7 @@ __device__ void run_mma_pv(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
     issue_pv<kQ, kFmt>(tmem, sbase, pv_n, first, ms);
     umma_commit(smem_u32(&ms->pv_done[pv_n & 1]));
     if (pv_n == 0) MLA_TRACE_CLK(kTrPvIssued);
+    if (first && pc.seg == 1) MLA_TRACE_CLK(kTrPvIssued1);
     ++pv_n;
     cursor_next_tile(pc, ms, p.kv_indptr, p.batch);
   }
@@ -1423,6 +1428,7 @@ __device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 
     }
     amax = __reduce_max_sync(0xffffffffu, amax);
     if (t == 0 && qi == 0 && ms->q_ready == 0 && amax != 0xFFFFFFFFu) MLA_TRACE_CLK(kTrQLoaded);
+    if (t == 0 && qi == 0 && ms->q_ready == 1 && amax != 0xFFFFFFFFu) MLA_TRACE_CLK(kTrQLoaded1);
     if (lane == 0) ms->red_u32[4 * qi + warp] = amax;
   }
   named_bar_sync(kBarSoftmax, kSoftmaxThreads);
@@ -1496,6 +1502,7 @@ template <int kQ, Kv kFmt>
 __device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq, int32_t nq,
                           float kv_scale, float (&qk_scale)[kQ]) {
   const int t = threadIdx.x;
+  if (t == 0 && ms->q_ready == 1) MLA_TRACE_CLK(kTrQStart1);
   uint4 raw[kQ][5][2];
   load_q<kQ>(p, tq, nq, raw);
   // The previous segment's output row may still be leaving the Q region
@@ -1621,6 +1628,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       prepare_q<kQ, kFmt>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, nq, kv_scale, qk_scale);
       if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 1));
       if (t == 0 && cur.seg == 0) MLA_TRACE_CLK(kTrQReady);
+      if (t == 0 && cur.seg == 1) MLA_TRACE_CLK(kTrQReady1);
     }
     q_early = false;
 
@@ -1676,6 +1684,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       }
       tc_fence_before();
       if (t == 0 && tile == 0) MLA_TRACE_CLK(kTrSRead);
+      if (t == 0 && cur.seg == 1 && tile == seg_first_tile) MLA_TRACE_CLK(kTrSRead1);
 
       // The reference maximum moves only when some score exceeds it by more
       // than the threshold (always on a segment's first tile); then the tile
@@ -1802,6 +1811,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);
       if (t == 0) st_release_u32(&ms->p_ready, tile + 1);
       if (t == 0 && tile == 0) MLA_TRACE_CLK(kTrPReady);
+      if (t == 0 && cur.seg == 1 && tile == seg_first_tile) MLA_TRACE_CLK(kTrPReady1);
+      if (t == 0 && cur.seg == 0 && cur.j + 1 == cur.j1) MLA_TRACE_CLK(kTrPLast0);
       ++tile;
       if (cur.j + 1 == cur.j1) break;
       ++cur.j;
@@ -1818,6 +1829,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), cur.seg & 1, ms, p.err);
         prepare_q<kQ, kFmt>(p, ms, sbase + G::kOffQ, tq_early, nq, kv_scale, qk_scale);
         if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 2));
+        if (t == 0 && cur.seg == 0) MLA_TRACE_CLK(kTrQReady1);
         q_early = true;
       }
     }
@@ -1948,6 +1960,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
   // The bulk stores have read their staging and written global memory before
   // the CTA exits.
   if (t == 0) bulk_wait_all();
+  if (t == 0) trace_shape(cur.seg + 1, static_cast<int32_t>(tile));
 }
 
 // ------------------------------------------------------------ test hooks: the two-term operands

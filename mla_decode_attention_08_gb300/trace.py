@@ -38,6 +38,11 @@ EVENTS = [
     (20, "observer: first tile's last latent panel arrived"),
     (21, "cluster split: cluster barrier passed"),
     (22, "cluster split: combine written"),
+    (24, "softmax: first segment's last P published"),
+    (25, "softmax: second segment's Q operand published"),
+    (26, "softmax: second segment's first scores read"),
+    (27, "softmax: second segment's first P published"),
+    (28, "PV issuer: second segment's first PV issued"),
 ]
 
 
@@ -59,6 +64,31 @@ def summarise(s1: np.ndarray, s2: np.ndarray, workload: str, mode: str) -> str:
             continue
         med, mx = float(np.median(col[ok])), float(np.max(col[ok]))
         lines.append(f"| {name} | {med:.0f} | {mx:.0f} | {med / mhz:.2f} |")
+    shape = t[:, 23]
+    if shape.any():
+        segs, tiles = shape >> 16, shape & 0xFFFF
+        exit_ns = t[:, 15] - e0
+        lines += ["", "| CTAs by (segments, tiles) | count | exit ns, median | exit ns, max |",
+                  "|---|---|---|---|"]
+        for key in sorted(set(zip(segs.tolist(), tiles.tolist()))):
+            sel = (segs == key[0]) & (tiles == key[1])
+            lines.append(f"| {key[0]} segments, {key[1]} tiles | {int(sel.sum())} | "
+                         f"{int(np.median(exit_ns[sel]))} | {int(exit_ns[sel].max())} |")
+    two = (shape >> 16) >= 2 if shape.any() else np.zeros(len(t), bool)
+    if two.any():
+        base = t[two, 24]
+        lines += ["", "| segment boundary (CTAs with two or more segments) | cycles after the first "
+                  "segment's last P, median | max |", "|---|---|---|"]
+        for ev, name in ((29, "second segment's Q preparation starts"),
+                         (30, "second segment's query loads returned"),
+                         (25, "second segment's Q operand published"),
+                         (12, "first segment's epilogue starts (its last PV done)"),
+                         (13, "first segment's output stores issued"),
+                         (26, "second segment's first scores read"),
+                         (27, "second segment's first P published"),
+                         (28, "second segment's first PV issued")):
+            d = t[two, ev] - base
+            lines.append(f"| {name} | {int(np.median(d))} | {int(d.max())} |")
     live2 = s2[:, 0] > 0
     u = s2[live2].astype(np.int64)
     lines += ["", "| global timer (ns from the first stage-1 CTA's entry) | first | last |",
