@@ -246,29 +246,74 @@ def time_loop(torch, fn, steps: int, stream) -> float:
     return start.elapsed_time(end)
 
 
-def per_call_cold(torch, call, reps: int, stream, flush, clean=None) -> list:
-    """Per-call device times (µs) of ``call(stream)`` with L2 flushed before each call.
+def per_call_cold(torch, call, reps: int, stream, flush, clean=None) -> tuple:
+    """Per-call device times (µs) of ``call(stream)`` with L2 flushed before each
+    call, and how many of the calls the host enqueued too late.
 
     The flush writes a buffer of twice the L2 size; ``clean`` (as large) is then
     read, so that the flush's dirty lines are written back before the timed
-    call rather than while it reads its inputs (both outside the events)."""
-    times = []
+    call rather than while it reads its inputs (both outside the events).  A
+    device-side wait of ~0.5 ms then holds the stream while the host records
+    the start event and enqueues the call, so that the host's launch path stays
+    outside the timed region; a call whose start event had already completed
+    when the host finished enqueueing it counts as late (its time holds host
+    latency)."""
+    times, late = [], 0
     for _ in range(reps):
         flush.add_(1)
         if clean is not None:
             clean.max()
         # The flush kernels end before the start event (the call, a programmatic
-        # dependent launch, must not overlap them), and a short device-side wait
-        # keeps the host's launch latency out of the timed region.
+        # dependent launch, must not overlap them).
         torch.cuda.synchronize()
-        torch.cuda._sleep(50_000)
+        torch.cuda._sleep(1_000_000)
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
         call(stream)
+        late += int(s.query())
         e.record(stream)
         torch.cuda.synchronize()
         times.append(s.elapsed_time(e) * 1e3)
-    return times
+    return times, late
+
+
+def graph_back_to_back(torch, call, n: int, reps: int = 5) -> float:
+    """Device µs per call of ``n`` calls back to back, captured once in a CUDA
+    graph and replayed (median of ``reps`` replays): the host's launch path,
+    longer than a small call, stays out of it.  A call that cannot be captured
+    is timed eagerly instead (a negative return marks that)."""
+    try:
+        return _graph_back_to_back(torch, call, n, reps)
+    except RuntimeError:
+        torch.cuda.synchronize()
+        return -time_loop(torch, call, n, torch.cuda.current_stream()) / n * 1e3
+
+
+def _graph_back_to_back(torch, call, n: int, reps: int) -> float:
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            call(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(n):
+            call(side)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(side)
+        with torch.cuda.stream(side):
+            g.replay()
+        e.record(side)
+        torch.cuda.synchronize()
+        out.append(s.elapsed_time(e) * 1e3 / n)
+    del g
+    return statistics.median(out)
 
 
 def e2e_timing(torch, w: DeviceWorkload, steps: int, stream) -> dict:
@@ -571,26 +616,27 @@ def ours_main(args) -> None:
         def cold(call, nbytes):
             for _ in range(5):
                 call(stream)
-            times = per_call_cold(torch, call, args.cold_reps, stream, flush, clean)
+            times, late = per_call_cold(torch, call, args.cold_reps, stream, flush, clean)
             med = statistics.median(times)
             return {"us_median": round(med, 2),
                     "us_p10": round(float(np.percentile(times, 10)), 2),
                     "us_p90": round(float(np.percentile(times, 90)), 2),
                     "effective_tbps": round(nbytes / (med * 1e-6) / 1e12, 3),
                     "frac_of_peak": round(nbytes / (med * 1e-6) / 1e9 / peak, 3),
-                    "algorithmic_bytes": nbytes}
+                    "algorithmic_bytes": nbytes, "host_late_calls": late}
 
         for name in WORKLOADS:
             ww = w if name == args.workload else DeviceWorkload(name, torch, binding, sms)
             entry = {"workload": name, **cold(ww.call, ww.bytes), "grid": int(ww.plan.grid),
                      "cluster": int(ww.plan.cluster),
                      "l2": "flushed before each call (2x L2 written, then 2x L2 of other data read)"}
-            # the same step back to back (L2 warm for the small workloads), for reference
-            entry["us_back_to_back"] = round(time_loop(torch, ww.call, 50, stream) / 50 * 1e3, 2)
+            # the same step back to back (L2 warm for the small workloads), for
+            # reference: 50 calls replayed from a CUDA graph
+            entry["us_back_to_back"] = round(graph_back_to_back(torch, ww.call, 50), 2)
             # the same step over the bf16 cache (mla_decode_fwd_bf16kv; contiguous caches only)
             if ww.kv_indices is None:
                 bf = cold(ww.call_bf16kv, ww.bytes_bf16)
-                bf["us_back_to_back"] = round(time_loop(torch, ww.call_bf16kv, 50, stream) / 50 * 1e3, 2)
+                bf["us_back_to_back"] = round(graph_back_to_back(torch, ww.call_bf16kv, 50), 2)
                 entry["bf16_cache"] = bf
             else:
                 entry["bf16_cache"] = {"unsupported": "page table (bf16 caches are read contiguously)"}
@@ -598,11 +644,11 @@ def ours_main(args) -> None:
             # alone back to back (the MXFP4 kernel's roofline)
             if ww.mx:
                 mx = cold(ww.call_mxfp4, ww.bytes_mx)
-                ms_mx = time_loop(torch, ww.call_mxfp4, 50, stream) / 50
-                ms_mx1 = time_loop(torch, ww.stage1_mxfp4, 50, stream) / 50
-                mx["us_back_to_back"] = round(ms_mx * 1e3, 2)
-                mx["stage1_us_back_to_back"] = round(ms_mx1 * 1e3, 2)
-                mx["stage1_frac_of_peak"] = round(ww.bytes_mx / (ms_mx1 * 1e-3) / 1e9 / peak, 3)
+                us_mx = graph_back_to_back(torch, ww.call_mxfp4, 50)
+                us_mx1 = graph_back_to_back(torch, ww.stage1_mxfp4, 50)
+                mx["us_back_to_back"] = round(us_mx, 2)
+                mx["stage1_us_back_to_back"] = round(us_mx1, 2)
+                mx["stage1_frac_of_peak"] = round(ww.bytes_mx / (us_mx1 * 1e-6) / 1e9 / peak, 3)
                 if binding.mla_decode_read_error(ww.ws) != 0:
                     raise SystemExit("device error word set during the MXFP4 timing")
                 entry["mxfp4_cache"] = mx

@@ -61,15 +61,21 @@ typedef enum {
  * Launch plan for a batch shape.  The split-KV schedule (flash-decoding split,
  * submission 722089 `_mla_multihead_stage1`; the persistent work maps of
  * submissions 663509 and 738050) is fixed analytically here: rows are cut into
- * tiles of 128 tokens, the tiles of all rows form one sequence of T tiles, and
- * `grid` persistent workers take equal contiguous ranges of it.  A row covered
+ * tiles of 128 tokens; the rows form one sequence of T units, each row with
+ * tiles contributing S start units and then its tiles, and `grid` persistent
+ * workers take equal contiguous ranges of it.  S = 3 when the batch's N tiles
+ * give ranges of at least 8 tiles (ceil(N / grid) >= 8), else 0: a worker
+ * whose range takes on a row start also prepares that row's query and writes
+ * the previous segment's output, and gets S fewer tiles for it.  A row covered
  * by more than one worker is combined by the second stage.
  *
  * Small batches instead take the cluster split (`cluster` = s > 0): row b is
  * shared by a thread-block cluster of s CTAs, the CTA of rank r taking the
  * row's tiles [r k, min((r + 1) k, nt)) with nt = ceil(L_b / 128) and
- * k = ceil(nt / s); the s partial results are combined inside the cluster
- * through distributed shared memory, and no second kernel runs.  The plan
+ * k = ceil(nt / s); each CTA writes its partial result to the workspace, the
+ * cluster meets at one barrier, and its CTAs then combine the row's s partials
+ * (read back through L2) into the output, each CTA a slice of it: no second
+ * kernel runs.  The plan
  * chooses s as the largest of 8, 4, 2 with s <= ceil(max_kv_len / 128) whose
  * clusters for the whole batch fit the GPU at once (at most num_sms / 10
  * clusters of 8, 7 num_sms / 32 of 4, num_sms / 2 of 2), and only when its
@@ -373,7 +379,7 @@ mla_status_t mla_debug_p_split(const float* p, int64_t n, void* hi_out, void* lo
  * Synchronous.  Release builds return MLA_ERR_UNSUPPORTED.
  */
 #define MLA_TRACE_CTAS 320
-#define MLA_TRACE_EVENTS 32
+#define MLA_TRACE_EVENTS 40
 #define MLA_TRACE2_BLOCKS 4096
 mla_status_t mla_decode_trace_read(uint64_t* stage1_host, uint64_t* stage2_host, int32_t clear);
 
@@ -419,8 +425,9 @@ mla_status_t mla_decode_read_error(void* workspace, int32_t* err_host, int32_t c
  * mla_decode_schedule_host — the stage-1 schedule computed on the host from a
  * host copy of kv_indptr, with the same integer formulas the kernel uses.
  *   workers_out int32 [grid*4]: (t0, t1, first_row, last_row) per worker
- *   (first_row = last_row = -1 for an empty range); prefix_out int32 [B+1]:
- *   tiles before each row.  Pure host; for tests and tools.
+ *   in schedule units (first_row = last_row = -1 for a range without tiles);
+ *   prefix_out int32 [B+1]: units before each row (tiles and start units of
+ *   the rows before it).  Pure host; for tests and tools.
  */
 mla_status_t mla_decode_schedule_host(const int32_t* kv_indptr_host, int32_t batch, int32_t grid,
                                       int32_t* workers_out, int32_t* prefix_out);

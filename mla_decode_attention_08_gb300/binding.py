@@ -317,7 +317,7 @@ def mla_debug_p_split(p, stream=None):
     return hi, lo
 
 
-TRACE_CTAS, TRACE_EVENTS, TRACE2_BLOCKS = 320, 32, 4096
+TRACE_CTAS, TRACE_EVENTS, TRACE2_BLOCKS = 320, 40, 4096
 
 
 def mla_decode_trace_read(clear: bool = True):

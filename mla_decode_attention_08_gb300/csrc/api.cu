@@ -584,10 +584,18 @@ mla_status_t mla_decode_schedule_host(const int32_t* kv_indptr_host, int32_t bat
   bool bad = kv_indptr_host[0] < 0;
   for (int32_t b = 0; b < batch; ++b)
     if (kv_indptr_host[b + 1] < kv_indptr_host[b]) bad = true;
+  auto row_tiles = [&](int32_t b) {
+    return bad ? 0 : mla::tiles_of_length(static_cast<int64_t>(kv_indptr_host[b + 1]) - kv_indptr_host[b]);
+  };
+  int32_t tiles = 0;
+  for (int32_t b = 0; b < batch; ++b) tiles += row_tiles(b);
+  // every row with tiles is preceded by `start` schedule units
+  const int32_t start = mla::row_start_units(tiles, grid);
   int32_t a = 0;
   for (int32_t b = 0; b < batch; ++b) {
     prefix_out[b] = a;
-    if (!bad) a += mla::tiles_of_length(static_cast<int64_t>(kv_indptr_host[b + 1]) - kv_indptr_host[b]);
+    const int32_t nt = row_tiles(b);
+    if (nt > 0) a += start + nt;
   }
   prefix_out[batch] = a;
   const int32_t total = a;
@@ -597,10 +605,13 @@ mla_status_t mla_decode_schedule_host(const int32_t* kv_indptr_host, int32_t bat
     int32_t first = -1, last = -1;
     if (t1 > t0) {
       for (int32_t b = 0; b < batch; ++b) {
-        const int32_t nt = prefix_out[b + 1] - prefix_out[b];
+        const int32_t nt = row_tiles(b);
         if (nt <= 0) continue;
-        if (prefix_out[b] <= t0 && t0 < prefix_out[b] + nt) first = b;
-        if (prefix_out[b] <= t1 - 1 && t1 - 1 < prefix_out[b] + nt) last = b;
+        const int32_t ra = prefix_out[b] + start;  // the row's first tile
+        if (ra < t1 && t0 < ra + nt) {  // the worker holds tiles of row b
+          if (first < 0) first = b;
+          last = b;
+        }
       }
     }
     workers_out[4 * c + 0] = t0;

@@ -71,6 +71,8 @@ enum TraceEvent {
   kTrPvIssued1 = 28,       // PV issuer: the second segment's first PV issued
   kTrQStart1 = 29,         // softmax: the second segment's Q preparation starts
   kTrQLoaded1 = 30,        // softmax: ... its query loads returned
+  kTrCombineW = 31,        // cluster split: thread 0's combine weight formed
+  kTrCombineLanded = 32,   // ... the partials landed in shared memory
 };
 // Copy the trace out (host arrays of kTraceCtas * kTraceEvents and kTrace2Blocks
 // * kTrace2Events entries) and zero it; cudaErrorNotSupported without -DMLA_TRACE.

@@ -2,7 +2,8 @@
 // planner and the kernels so both compute the same ranges.
 //
 // Rows are cut into tiles of kTileTokens tokens; all rows' tiles, row after
-// row, form one sequence of T tiles; worker c of a grid of G takes the tiles
+// row (each row with tiles preceded by row_start_units units for its start),
+// form one sequence of T units; worker c of a grid of G takes the units
 // [floor(c*T/G), floor((c+1)*T/G)).  This is the persistent form of the
 // flash-decoding split (kernelbot-amd-mixed-mla submission 722089,
 // `_mla_multihead_stage1` splits each row into contiguous ranges; submissions
@@ -51,7 +52,7 @@ MLA_HD int32_t cluster_capacity(int32_t s, int32_t num_sms) {
 // Cluster split for small batches of one query token per row: every row gets
 // a cluster of s CTAs that share its tiles (rank r takes the row's tiles
 // [r k, min((r + 1) k, nt)), k = ceil(nt / s)) and combine their partial
-// results through distributed shared memory, with no second kernel.  s is the
+// results after one cluster barrier, with no second kernel.  s is the
 // largest of 8, 4, 2 with s <= ceil(max_kv_len / 128) whose clusters for the
 // whole batch fit the GPU at once; it is used (else 0: the persistent split)
 // when its longest share, ceil(nt / s) tiles, is at most two tiles longer than
@@ -66,6 +67,25 @@ MLA_HD int32_t plan_cluster(int32_t batch, int32_t qo_len, int32_t max_kv_len, i
   const int64_t g0 = upper < num_sms ? upper : num_sms;
   const int64_t longest = (upper + g0 - 1) / g0;
   return (nt + s - 1) / s <= longest + 2 ? s : 0;
+}
+
+// Row starts.  A worker whose range takes on a new row pays for that row's
+// start (its query's preparation and the previous segment's epilogue, about
+// three tiles' streaming time) on top of its tiles, and such workers finished
+// last.  So when the ranges are long, every row with tiles is preceded in the
+// global sequence by kRowStartUnits units that stand for its start: a range
+// that takes on a row start gets that many fewer tiles.  With short ranges
+// (fewer than kRowStartMinRange tiles each) the units would cost more than
+// they balance (ranges of 2 tiles become 2 or 3), and rows start with their
+// tiles.  The rule depends only on the batch's tile count T and the grid:
+// units per row start = kRowStartUnits when ceil(T / grid) >= kRowStartMinRange,
+// else 0.
+constexpr int32_t kRowStartUnits = 3;
+constexpr int32_t kRowStartMinRange = 8;
+MLA_HD int32_t row_start_units(int32_t total_tiles, int32_t grid) {
+  if (grid < 1 || total_tiles < 1) return 0;
+  const int64_t k = (static_cast<int64_t>(total_tiles) + grid - 1) / grid;
+  return k >= kRowStartMinRange ? kRowStartUnits : 0;
 }
 
 // floor(c * total / grid) for 0 <= c <= grid and total >= 0, without a 64-bit

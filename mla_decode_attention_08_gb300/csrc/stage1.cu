@@ -140,7 +140,9 @@ struct Misc {
   alignas(16) float red_max[2][4][16 * kMaxQ];  // read and written as float4
   alignas(16) float red_sum[4][16 * kMaxQ];
   uint32_t red_u32[8];
-  int32_t scan[kStage1ThreadsMx / 32];  // per warp of the prologue's block scan (largest block)
+  int32_t scan[kStage1ThreadsMx / 32];       // per warp of the prologue's block scan (largest block):
+  int32_t scan_rows[kStage1ThreadsMx / 32];  // tiles, and rows with tiles
+  int32_t row_start;    // schedule units before each row's tiles (row_start_units)
   uint32_t tmem_base;
   volatile int32_t abort_flag;
   int32_t total_tiles;
@@ -152,7 +154,8 @@ struct Misc {
   int32_t first_kb, first_len, first_tq;
   int32_t bad;
   int32_t tile0_issued;    // the prologue issued the first tile's copies (contiguous rows)
-  alignas(16) float cl_w[kMaxCluster][16];  // cluster split: combine weights [rank][head]
+  alignas(16) float cl_w[kMaxCluster][16];    // cluster split: combine weights [rank][head]
+  alignas(16) float cl_lse[kMaxCluster][16];  // ... and the partials' log-sum-exps
   uint32_t next_panel[6];  // per producer warp: one past its last issued panel
   alignas(16) float alpha_stage[16 * kMaxQ];  // O rescale factors of the current tile (thread 0 writes)
 };
@@ -301,6 +304,7 @@ struct Cursor {
   int32_t kb, len;  // first flattened token and token count of row b
   int32_t j, j0, j1;  // current tile and this worker's tile range inside row b
   int32_t seg;      // segment counter (0-based)
+  int32_t start;    // schedule units before each row's tiles
   bool whole;       // row b lies entirely inside this worker
   bool live;
 };
@@ -315,9 +319,10 @@ __device__ __forceinline__ bool cursor_next_segment(Cursor& c, const int32_t* kv
     const int32_t ke = ldg_i32(kv_indptr + b + 1);
     const int32_t len = ke > kb ? ke - kb : 0;
     const int32_t nt = tiles_of_length(len);
-    const int32_t a = c.next_a;
-    c.next_a = a + nt;
     if (nt == 0) continue;
+    const int32_t a = c.next_a + c.start;  // the row's first tile, after its start units
+    c.next_a = a + nt;
+    if (a >= t1) return false;  // the range ends among the row's start units
     c.row_a = a;
     c.kb = kb;
     c.len = len;
@@ -335,6 +340,7 @@ __device__ __forceinline__ bool cursor_next_segment(Cursor& c, const int32_t* kv
 // same values cursor_next_segment would load).
 __device__ __forceinline__ void cursor_start(Cursor& c, const Misc* ms) {
   c.seg = -1;
+  c.start = ms->row_start;
   c.live = ms->t1 > ms->t0 && ms->first_row >= 0;
   if (!c.live) return;
   const int32_t a = ms->first_prefix, nt = ms->first_tiles, t0 = ms->t0, t1 = ms->t1;
@@ -343,7 +349,7 @@ __device__ __forceinline__ void cursor_start(Cursor& c, const Misc* ms) {
   c.row_a = a;
   c.kb = ms->first_kb;
   c.len = ms->first_len;
-  c.j0 = t0 - a;
+  c.j0 = (t0 > a ? t0 : a) - a;  // (t0 may lie among the row's start units)
   c.j1 = (t1 < a + nt ? t1 : a + nt) - a;
   c.j = c.j0;
   c.whole = a >= t0 && a + nt <= t1;
@@ -456,7 +462,7 @@ __device__ void schedule_prologue(const Stage1Params& p, const CUtensorMap* map_
   const int32_t per = (batch + nthreads - 1) / nthreads;
   const int32_t r0 = min(tid * per, batch), r1 = min(r0 + per, batch);
 
-  int32_t local = 0;
+  int32_t local = 0, local_rows = 0;  // tiles and rows with tiles of this thread's rows
   int bad = 0;
   // A thread owning a single row also loads its query-token bounds here, in the
   // same round trip (used if that row turns out to be the worker's first).
@@ -484,14 +490,18 @@ __device__ void schedule_prologue(const Stage1Params& p, const CUtensorMap* map_
       if (r0 + i < r1) {
         const int32_t next = keep[i + 1];
         if (next < prev) bad = 1;
-        local += tiles_of_length(static_cast<int64_t>(next) - prev);
+        const int32_t nt = tiles_of_length(static_cast<int64_t>(next) - prev);
+        local += nt;
+        local_rows += nt > 0;
         prev = next;
       }
     }
     for (int32_t b = r0 + kKeep; b < r1; ++b) {
       const int32_t next = ldg_i32(p.kv_indptr + b + 1);
       if (next < prev) bad = 1;
-      local += tiles_of_length(static_cast<int64_t>(next) - prev);
+      const int32_t nt = tiles_of_length(static_cast<int64_t>(next) - prev);
+      local += nt;
+      local_rows += nt > 0;
       prev = next;
     }
   }
@@ -502,25 +512,39 @@ __device__ void schedule_prologue(const Stage1Params& p, const CUtensorMap* map_
     // (the stamp depends on the loaded values, so it follows their arrival)
     if (e0 != INT32_MIN && local != INT32_MIN) MLA_TRACE_CLK(kTrIndptrLoaded);
   }
-  int32_t incl = local;
+  int32_t incl = local, incl_rows = local_rows;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += v;
+    const int32_t r = __shfl_up_sync(0xffffffffu, incl_rows, off);
+    if (lane >= off) {
+      incl += v;
+      incl_rows += r;
+    }
   }
-  if (lane == 31) ms->scan[warp] = incl;
+  if (lane == 31) {
+    ms->scan[warp] = incl;
+    ms->scan_rows[warp] = incl_rows;
+  }
   // (first_row / last_row were set to -1 before the wait for the previous
   // kernel; this barrier orders that before the second pass below.)
   bad = __syncthreads_or(bad);
   if (tid == 0) MLA_TRACE_CLK(kTrScanBarrier);
 
-  int32_t warp_off = 0, total = 0;
+  int32_t warp_off = 0, tiles = 0, warp_off_rows = 0, rows = 0;
   for (int w = 0; w < nwarps; ++w) {
-    const int32_t s = ms->scan[w];
-    if (w < warp) warp_off += s;
-    total += s;
+    const int32_t s = ms->scan[w], r = ms->scan_rows[w];
+    if (w < warp) {
+      warp_off += s;
+      warp_off_rows += r;
+    }
+    tiles += s;
+    rows += r;
   }
-  if (bad) total = 0;
+  if (bad) tiles = rows = 0;
+  // Schedule units: every row with tiles is preceded by `start` units.
+  const int32_t start = row_start_units(tiles, p.grid);
+  const int32_t total = tiles + start * rows;
   const int32_t c = cta_worker(p);
   const int32_t t0 = worker_begin(c, total, p.grid);
   const int32_t t1 = worker_begin(c + 1, total, p.grid);
@@ -529,10 +553,12 @@ __device__ void schedule_prologue(const Stage1Params& p, const CUtensorMap* map_
     ms->t0 = t0;
     ms->t1 = t1;
     ms->bad = bad;
+    ms->row_start = start;
     if (bad) set_error(p.err, MLA_DERR_KV_INDPTR);
   }
 
-  int32_t a = bad ? 0 : warp_off + incl - local;
+  // units before this thread's first row
+  int32_t a = bad ? 0 : (warp_off + incl - local) + start * (warp_off_rows + incl_rows - local_rows);
   if (r0 < r1) {
     int32_t prev = keep[0];
     for (int32_t b = r0; b < r1; ++b) {
@@ -542,12 +568,13 @@ __device__ void schedule_prologue(const Stage1Params& p, const CUtensorMap* map_
         if (b - r0 == i) next = keep[i + 1];
       if (b - r0 >= kKeep) next = ldg_i32(p.kv_indptr + b + 1);
       const int32_t nt = bad ? 0 : tiles_of_length(static_cast<int64_t>(next) - prev);
+      const int32_t ra = nt > 0 ? a + start : a;  // the row's first tile, after its start units
       if (c == 0) p.prefix[b] = a;
       if (nt == 0 && b % p.grid == c) zero_row<kQ>(p, b);  // no cached token: zero output
       if (nt > 0 && t1 > t0) {
-        if (a <= t0 && t0 < a + nt) {
+        if (a <= t0 && t0 < ra + nt && ra < t1) {
           ms->first_row = b;
-          ms->first_prefix = a;
+          ms->first_prefix = ra;
           ms->first_tiles = nt;
           ms->first_kb = prev;
           ms->first_len = next - prev;
@@ -567,15 +594,16 @@ __device__ void schedule_prologue(const Stage1Params& p, const CUtensorMap* map_
             prefetch_bulk_l2(p.q + static_cast<size_t>(tq) * kNumHeads * kQkDim,
                              static_cast<uint32_t>(cta_tokens<kQ>(p)) * kNumHeads * kQkDim * 2);
           if (p.kv_bytes != nullptr) {
-            const int32_t j0 = t0 - a;
+            const int32_t j0 = t0 > ra ? t0 - ra : 0;
             const int32_t rows = min(kTileTokens, (next - prev) - j0 * kTileTokens);
             prefetch_bulk_l2(p.kv_bytes + (static_cast<int64_t>(prev) + j0 * kTileTokens) * p.kv_row_bytes,
                              static_cast<uint32_t>(rows * p.kv_row_bytes));
           }
         }
-        if (a <= t1 - 1 && t1 - 1 < a + nt) ms->last_row = b;
+        // (the next row with tiles has its first tile at ra + nt + start)
+        if (ra < t1 && t0 < ra + nt && t1 <= ra + nt + start) ms->last_row = b;
       }
-      a += nt;
+      a = nt > 0 ? ra + nt : a;
       prev = next;
     }
   }
@@ -626,6 +654,7 @@ __device__ void cluster_prologue(const Stage1Params& p, const CUtensorMap* map_v
     ms->t0 = j0;
     ms->t1 = j1;
     ms->first_prefix = 0;
+    ms->row_start = 0;
     ms->first_tiles = nt;
     ms->first_row = j1 > j0 ? b : -1;
     ms->last_row = ms->first_row;
@@ -649,87 +678,100 @@ __device__ void cluster_prologue(const Stage1Params& p, const CUtensorMap* map_v
 // workspace's partial slots s b .. s b + s - 1: normalised bf16 outputs and
 // base-2 log-sum-exps, written by the epilogues) with the weights
 // w_i = 2^(lse_i - M) / sum_j 2^(lse_j - M), M = max_i lse_i (submission 722089,
-// `_mla_reduce`).  A CTA without tokens (lse = -inf) weighs 0 and its slot is
-// not read; a row with none outputs zeros.  The partials go through L2 (loads
-// that bypass L1, which may hold an earlier call's values): an SM pulls them
-// from L2 several times faster than from its peers' shared memory.
+// `_mla_reduce`).  A CTA without tokens (lse = -inf) weighs 0; a row with none
+// outputs zeros.
+//
+// Item (head half, dim): 8 heads of one output dim, a 16-byte piece of each
+// slot's partial ([dim / 128][head / 8][dim % 128][head % 8] per slot); a
+// thread copies its items' pieces into the ring's first latent slot (free once
+// every role has finished) with asynchronous copies, all in flight at once,
+// and combines them from there.  The loops over slots are unrolled so that
+// their shared-memory loads are all in flight at once: this step is a chain of
+// latencies, not of throughput.
 template <int kQ, Kv kFmt>
-__device__ void cluster_combine(const Stage1Params& p, Misc* ms) {
+__device__ __forceinline__ void cluster_combine(const Stage1Params& p, Misc* ms, const uint8_t* smem) {
+  using G = Geo<kQ, kFmt>;
+  static_assert(G::kVSlotBytes >= kNumHeads * kVDim * 2, "the pieces land in one latent slot");
   const int tid = threadIdx.x;
   const int32_t s = p.cluster;
   const int32_t rank = static_cast<int32_t>(cluster_ctarank());
   const int32_t slot0 = static_cast<int32_t>(blockIdx.x) - rank;  // the row's first slot
-  const size_t slot_lse = static_cast<size_t>(p.slot_tokens) * kNumHeads;
-  const size_t slot_part = static_cast<size_t>(p.slot_tokens) * (kNumHeads * kVDim / 4);  // uint2s
-  // Item = (dim, quarter of the heads): one 8-byte piece (4 heads) of each
-  // slot's partial, stored [slot][token][dim / 128][head / 8][dim % 128][head % 8].
-  // The pieces are loaded first and are in flight while the weights form.
-  const int32_t dims = kVDim / s;
-  const int32_t items = 4 * dims;
-  constexpr int kPerThread = 4;  // items per thread: 4 x 512 / s <= 1024 with s >= 2, 256 threads
-  uint2 v[kPerThread][kMaxCluster];
-#pragma unroll
-  for (int k = 0; k < kPerThread; ++k) {
-    const int32_t it = tid + k * static_cast<int32_t>(blockDim.x);
-    const int32_t quarter = it / dims, d = rank * dims + it % dims;
-    const size_t piece = ((static_cast<size_t>(d >> 7) * 2 + (quarter >> 1)) * 128 + (d & 127)) * 2 +
-                         (quarter & 1);
-#pragma unroll
-    for (int i = 0; i < kMaxCluster; ++i)
-      v[k][i] = it < items && i < s
-                    ? __ldcg(reinterpret_cast<const uint2*>(p.partial) + (slot0 + i) * slot_part + piece)
-                    : make_uint2(0, 0);
-  }
-  // Weights of (slot, head), one thread each: w = 2^(lse - M) / sum over the
-  // row's slots, M the largest; a slot without tokens (lse = -inf) weighs 0.
-  if (tid < 16 * s) {
-    const int i = tid >> 4, h = tid & 15;
-    float lse[kMaxCluster];
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kMaxCluster; ++j) {
-      lse[j] = j < s ? __ldcg(p.lse + (slot0 + j) * slot_lse + h) : -INFINITY;
-      m = fmaxf(m, lse[j]);
-    }
-    float sum = 0.0f, mine = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kMaxCluster; ++j) {
-      const float e = lse[j] != -INFINITY ? exp2f(lse[j] - m) : 0.0f;
-      sum += e;
-      mine = j == i ? e : mine;
-    }
-    ms->cl_w[i][h] = sum > 0.0f ? mine / sum : 0.0f;
-  }
-  __syncthreads();
+  const int32_t dims = kVDim / s, items = 2 * dims;
+  const size_t slot_elems = static_cast<size_t>(p.slot_tokens) * kNumHeads * kVDim;
+  const uint4* land = reinterpret_cast<const uint4*>(smem + G::kOffV);  // [slot][item]
   const int32_t tq = ms->first_tq;
   if (tq < 0) {  // the row's query tokens are malformed: the row is not written
     if (tid == 0 && rank == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
     return;
   }
+  if (MLA_DCHECK(static_cast<int64_t>(slot0 + s) * static_cast<int64_t>(slot_elems) <= partial_elems(p),
+                 p.err)) {
+#pragma unroll 1
+    for (int32_t it = tid; it < items; it += static_cast<int32_t>(blockDim.x)) {
+      const int32_t hh = it / dims, d = rank * dims + it % dims;
+      const uint16_t* src = p.partial + static_cast<size_t>(slot0) * slot_elems +
+                            (static_cast<size_t>(d >> 7) * 2 + hh) * (128 * 8) + (d & 127) * 8;
+#pragma unroll 1
+      for (int32_t i = 0; i < s; ++i)
+        cp_async_16(smem_u32(land + i * items + it), src + static_cast<size_t>(i) * slot_elems);
+    }
+    if (tid < 4 * s)  // 16 bytes (4 heads) of slot tid / 4's log-sum-exps
+      cp_async_16(smem_u32(&ms->cl_lse[tid >> 2][4 * (tid & 3)]),
+                  p.lse + static_cast<size_t>(slot0 + (tid >> 2)) * p.slot_tokens * kNumHeads + 4 * (tid & 3));
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  if (tid == 0) MLA_TRACE_CLK(kTrCombineLanded);
+  // Weights of (slot, head), one thread each: w = 2^(lse - M) / sum over the
+  // row's slots, M the largest; a slot without tokens (lse = -inf) weighs 0.
+  if (tid < 16 * s) {
+    const int i = tid >> 4, h = tid & 15;
+    float l[kMaxCluster];
+    float m = -INFINITY;
 #pragma unroll
-  for (int k = 0; k < kPerThread; ++k) {
-    const int32_t it = tid + k * static_cast<int32_t>(blockDim.x);
-    if (it >= items) continue;
-    const int32_t quarter = it / dims, d = rank * dims + it % dims;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int j = 0; j < kMaxCluster; ++j) {
+      l[j] = j < s ? ms->cl_lse[j][h] : -INFINITY;
+      m = fmaxf(m, l[j]);
+    }
+    float sum = 0.0f, mine = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j) {
+      const float e = l[j] != -INFINITY ? exp2f(l[j] - m) : 0.0f;
+      sum += e;
+      mine = j == i ? e : mine;
+    }
+    ms->cl_w[i][h] = sum > 0.0f ? mine / sum : 0.0f;
+    if (tid == 0) MLA_TRACE_CLK(kTrCombineW);
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int32_t it = tid; it < items; it += static_cast<int32_t>(blockDim.x)) {
+    const int32_t hh = it / dims, dl = it % dims;
+    float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    uint4 xs[kMaxCluster];
+#pragma unroll
+    for (int i = 0; i < kMaxCluster; ++i) xs[i] = i < s ? land[i * items + it] : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int i = 0; i < kMaxCluster; ++i) {
-      if (i >= s) continue;
-      const float4 w = *reinterpret_cast<const float4*>(&ms->cl_w[i][4 * quarter]);
-      const float x[4] = {__uint_as_float(v[k][i].x << 16), __uint_as_float(v[k][i].x & 0xFFFF0000u),
-                          __uint_as_float(v[k][i].y << 16), __uint_as_float(v[k][i].y & 0xFFFF0000u)};
+      if (i >= s) break;
+      const uint4 x = xs[i];
+      const float4 w0 = *reinterpret_cast<const float4*>(&ms->cl_w[i][8 * hh]);
+      const float4 w1 = *reinterpret_cast<const float4*>(&ms->cl_w[i][8 * hh + 4]);
+      const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
       // (an empty or abandoned piece is never written: its weight 0 keeps it out)
-      acc[0] = w.x != 0.0f ? fmaf(w.x, x[0], acc[0]) : acc[0];
-      acc[1] = w.y != 0.0f ? fmaf(w.y, x[1], acc[1]) : acc[1];
-      acc[2] = w.z != 0.0f ? fmaf(w.z, x[2], acc[2]) : acc[2];
-      acc[3] = w.w != 0.0f ? fmaf(w.w, x[3], acc[3]) : acc[3];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float xe = __uint_as_float((e & 1) ? (xw[e >> 1] & 0xFFFF0000u) : (xw[e >> 1] << 16));
+        acc[e] = w[e] != 0.0f ? fmaf(w[e], xe, acc[e]) : acc[e];
+      }
     }
     if (MLA_DCHECK(tq < total_tokens(p), p.err)) {
-      uint16_t* dst = p.out + (static_cast<size_t>(tq) * kNumHeads + 4 * quarter) * kVDim + d;
+      uint16_t* dst = p.out + (static_cast<size_t>(tq) * kNumHeads + 8 * hh) * kVDim + rank * dims + dl;
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const __nv_bfloat16 y = __float2bfloat16_rn(acc[h]);
-        dst[h * kVDim] = *reinterpret_cast<const uint16_t*>(&y);
+      for (int e = 0; e < 8; ++e) {
+        const __nv_bfloat16 y = __float2bfloat16_rn(acc[e]);
+        dst[e * kVDim] = *reinterpret_cast<const uint16_t*>(&y);
       }
     }
   }
@@ -1001,12 +1043,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d) : "memory");
-}
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
-  return v;
 }
 __device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
   uint16_t v;
@@ -2137,7 +2173,7 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
       p.lse[static_cast<size_t>(blockIdx.x) * p.slot_tokens * kNumHeads + tid] = -INFINITY;
     cluster_sync_all();
     if (tid == 0) MLA_TRACE_CLK(kTrClusterBarrier);
-    cluster_combine<kQ, kFmt>(p, ms);
+    cluster_combine<kQ, kFmt>(p, ms, smem);
     if (tid == 0) MLA_TRACE_CLK(kTrCombineDone);
   }
   if (tid == 0) {

@@ -37,6 +37,8 @@ EVENTS = [
     (19, "observer: first rope panel arrived"),
     (20, "observer: first tile's last latent panel arrived"),
     (21, "cluster split: cluster barrier passed"),
+    (32, "cluster split: the partials landed"),
+    (31, "cluster split: thread 0's combine weight formed"),
     (22, "cluster split: combine written"),
     (24, "softmax: first segment's last P published"),
     (25, "softmax: second segment's Q operand published"),
@@ -108,6 +110,9 @@ def main(argv=None) -> None:
     ap.add_argument("--workload", default="bs4_kv1024")
     ap.add_argument("--calls", type=int, default=20)
     ap.add_argument("--cold", action="store_true", help="one call on an idle GPU")
+    ap.add_argument("--flush", action="store_true",
+                    help="with --cold: write then read two L2-sized buffers before the call, "
+                         "as the benchmark's flushed timing does")
     ap.add_argument("--lib", default=None, help="a trace-built library to load instead of building one")
     args = ap.parse_args(argv)
 
@@ -144,13 +149,22 @@ def main(argv=None) -> None:
         call()
     torch.cuda.synchronize()
     binding.mla_decode_trace_read(clear=True)
+    if args.cold and args.flush:
+        l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 129 << 20)
+        flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device="cuda")
+        clean = torch.zeros_like(flush)
+        flush.add_(1)
+        clean.max()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(1_000_000)  # the call is enqueued before the stream reaches it
     for _ in range(1 if args.cold else args.calls):
         call()
     torch.cuda.synchronize()
     if binding.mla_decode_read_error(ws) != 0:
         raise SystemExit("device error word set")
     s1, s2 = binding.mla_decode_trace_read(clear=True)
-    mode = "one call on an idle GPU" if args.cold else f"last of {args.calls} calls back to back"
+    mode = ("one call on an idle GPU" + (", L2 flushed before it" if args.flush else "")
+            if args.cold else f"last of {args.calls} calls back to back")
     sys.stdout.write(summarise(s1, s2, args.workload, mode))
 
 

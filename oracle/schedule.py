@@ -11,16 +11,24 @@ The schedule here is the persistent, token-balanced form of that split, fixed
 as follows (the pages print no formula for their persistent work map):
 
 * every row is cut into tiles of ``TILE_TOKENS`` tokens, ``ceil(L_b / 128)``
-  tiles, the last one partial; the tiles of all rows, row after row, form one
-  global sequence of ``T`` tiles;
+  tiles, the last one partial;
 * the grid has the fewest workers ``G`` whose longest equal split of the
   batch's upper bound ``U = B * ceil(max_kv_len / 128)`` tiles is no longer
   than with ``min(num_sms, U)`` workers (1 for an empty batch);
-  worker c takes the contiguous tile range ``[floor(c T / G), floor((c+1) T / G))``;
+* the rows, row after row, form one global sequence of units: each row with
+  tiles contributes ``S`` start units followed by its tiles, where
+  ``S = ROW_START_UNITS`` (3) when the batch's ``N`` tiles give ranges of at
+  least ``ROW_START_MIN_RANGE`` (8) tiles, ``ceil(N / G) >= 8``, else 0 (a
+  worker whose range takes on a row start pays for that row's query
+  preparation and the previous segment's epilogue, and gets ``S`` fewer tiles
+  for it; this is a property of the library's kernel, not of the pages);
+  worker c takes the contiguous unit range ``[floor(c T / G), floor((c+1) T / G))``
+  of the ``T`` units;
 * the part of a row inside one worker's range is a segment; a row covered by a
   single worker is "whole", otherwise "split" and each of its segments writes a
   partial (normalised output and base-2 log-sum-exp) to a workspace slot:
-  slot ``2c`` when worker c's range begins inside that row, else ``2c + 1``.
+  slot ``2c`` when worker c's range begins at or after the row's first tile,
+  else ``2c + 1``.
 
 Small batches of one query token per row take the cluster split instead
 (``plan_cluster``): each row is shared by ``size`` CTAs of one thread-block
@@ -106,13 +114,35 @@ def row_tiles(kv_indptr) -> list[int]:
     return out
 
 
+ROW_START_UNITS = 3
+ROW_START_MIN_RANGE = 8
+
+
+def row_start_units(total_tiles: int, grid: int) -> int:
+    """Start units before each row with tiles: ROW_START_UNITS when the ranges
+    hold at least ROW_START_MIN_RANGE tiles (``ceil(N / G) >= 8``), else 0."""
+    if grid < 1 or total_tiles < 1:
+        return 0
+    return ROW_START_UNITS if ceil_div(total_tiles, grid) >= ROW_START_MIN_RANGE else 0
+
+
 def schedule(kv_indptr, grid: int) -> dict:
-    """Per-worker ranges, per-row covers and segment list, by enumeration."""
+    """Per-worker ranges, per-row covers and segment list, by enumeration of
+    the unit sequence (each unit labelled with its row and tile, or -1 for a
+    start unit)."""
     tiles = row_tiles(kv_indptr)
-    prefix = [0]
-    for n in tiles:
-        prefix.append(prefix[-1] + n)
-    total = prefix[-1]
+    start = row_start_units(sum(tiles), grid)
+    units = []                       # (row, tile) per unit; tile -1: a start unit
+    prefix = []                      # units before each row
+    first_tile = []                  # unit index of each row's first tile
+    for b, n in enumerate(tiles):
+        prefix.append(len(units))
+        if n > 0:
+            units.extend([(b, -1)] * start)
+        first_tile.append(len(units))
+        units.extend((b, j) for j in range(n))
+    prefix.append(len(units))
+    total = len(units)
 
     workers = []
     for c in range(grid):
@@ -120,35 +150,33 @@ def schedule(kv_indptr, grid: int) -> dict:
         t1 = ((c + 1) * total) // grid
         workers.append({"t0": t0, "t1": t1, "first_row": -1, "last_row": -1})
 
-    # Which workers touch which row: enumerate every tile.
-    owner = []                       # owner[t] = worker holding global tile t
+    # Which workers touch which row: enumerate every unit.
+    owner = []                       # owner[u] = worker holding unit u
     for c, w in enumerate(workers):
         owner.extend([c] * (w["t1"] - w["t0"]))
     assert len(owner) == total
 
-    covers = {}                      # row -> ordered list of workers
+    covers = {b: [] for b in range(len(tiles))}  # row -> ordered workers holding its tiles
+    for u, (b, j) in enumerate(units):
+        if j >= 0 and (not covers[b] or covers[b][-1] != owner[u]):
+            covers[b].append(owner[u])
     segments = []
-    for b, n in enumerate(tiles):
-        ws = []
-        for t in range(prefix[b], prefix[b] + n):
-            if not ws or ws[-1] != owner[t]:
-                ws.append(owner[t])
-        covers[b] = ws
     for c, w in enumerate(workers):
         rows = [b for b in range(len(tiles)) if c in covers[b]]
         if rows:
             w["first_row"], w["last_row"] = rows[0], rows[-1]
         for b in rows:
-            j0 = max(w["t0"], prefix[b]) - prefix[b]
-            j1 = min(w["t1"], prefix[b + 1]) - prefix[b]
+            f, n = first_tile[b], tiles[b]
+            j0 = max(w["t0"], f) - f
+            j1 = min(w["t1"], f + n) - f
             split = len(covers[b]) > 1
             slot = -1
             if split:
-                slot = 2 * c if w["t0"] >= prefix[b] else 2 * c + 1
+                slot = 2 * c if w["t0"] >= f else 2 * c + 1
             segments.append({"worker": c, "row": b, "tile_begin": j0, "tile_end": j1,
                              "split": split, "slot": slot})
-    return {"grid": grid, "total_tiles": total, "prefix": prefix, "workers": workers,
-            "covers": covers, "segments": segments}
+    return {"grid": grid, "total_tiles": total, "row_start": start, "prefix": prefix,
+            "workers": workers, "covers": covers, "segments": segments}
 
 
 def token_segments(kv_indptr, grid: int) -> dict:

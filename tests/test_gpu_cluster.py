@@ -1,8 +1,9 @@
 """The cluster split of small batches against the float64 oracle (GPU).
 
 A plan with ``cluster`` = s > 0 shares every row among the s CTAs of one
-thread-block cluster, which combine their partials through distributed shared
-memory, with no second kernel.  These tests run shapes that make the plan pick
+thread-block cluster, which meet at one cluster barrier and combine their
+partials (written to the workspace, read back through L2), with no second
+kernel.  These tests run shapes that make the plan pick
 s = 8, 4 and 2 (ragged rows, rows with fewer tiles than CTAs, empty rows), the
 bf16 cache, host-made input errors, the stall hook, a page table with a
 cluster plan (which runs the persistent split), the two stages launched apart,

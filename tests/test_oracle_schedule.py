@@ -2,8 +2,8 @@
 import numpy as np
 import pytest
 
-from oracle.schedule import (TILE_TOKENS, cluster_shares, plan_cluster, plan_grid, schedule,
-                             token_segments, worker_table)
+from oracle.schedule import (TILE_TOKENS, cluster_shares, plan_cluster, plan_grid, row_start_units,
+                             schedule, token_segments, worker_table)
 
 from .golden_util import load_table
 
@@ -17,6 +17,34 @@ def test_hand_derived_case():
     assert sch["prefix"] == [0, 3, 3, 9, 10]
     assert worker_table([0, 300, 300, 1000, 1128], 4).tolist() == [
         [0, 2, 0, 0], [2, 5, 0, 2], [5, 7, 2, 2], [7, 10, 2, 3]]
+
+
+@pytest.mark.parametrize("tiles,grid,want", [
+    (30, 3, 3),    # ranges of 10 tiles >= 8: three start units per row
+    (20, 3, 0),    # ceil(20 / 3) = 7 < 8
+    (8, 1, 3), (7, 1, 0), (0, 5, 0), (4096, 152, 3), (256, 128, 0), (16384, 152, 3)])
+def test_row_start_units_by_hand(tiles, grid, want):
+    assert row_start_units(tiles, grid) == want
+
+
+def test_hand_derived_case_with_row_start_units():
+    """Rows of 20 and 10 tiles over 3 workers: 30 tiles, ranges of 10 >= 8, so
+    each row is preceded by 3 start units.  Units: row 0 start [0, 3), tiles
+    [3, 23); row 1 start [23, 26), tiles [26, 36); 36 units, workers [0, 12),
+    [12, 24), [24, 36).  Worker 0 holds row 0's tiles 0-8, worker 1 its tiles
+    9-19 (and one start unit of row 1, no tile of it), worker 2 row 1 whole.
+    Row 0 is split: worker 0's range begins before the row's first tile (slot
+    2c + 1 = 1), worker 1's after it (slot 2c = 2)."""
+    indptr = [0, 2560, 3840]
+    sch = schedule(indptr, 3)
+    assert sch["row_start"] == 3
+    assert sch["prefix"] == [0, 23, 36]
+    assert worker_table(indptr, 3).tolist() == [[0, 12, 0, 0], [12, 24, 0, 0], [24, 36, 1, 1]]
+    got = [[s["worker"], s["row"], s["tile_begin"], s["tile_end"], int(s["split"]), s["slot"]]
+           for s in sch["segments"]]
+    assert got == [[0, 0, 0, 9, 1, 1], [1, 0, 9, 20, 1, 2], [2, 1, 0, 10, 0, -1]]
+    # an empty row in between takes no units: [0, 13, 13, 26] for 10, 0, 10 tiles
+    assert schedule([0, 1280, 1280, 2560], 2)["prefix"] == [0, 13, 13, 26]
 
 
 @pytest.mark.parametrize("batch,max_len,sms,want", [
@@ -37,9 +65,9 @@ def test_partition_invariants(seed):
     rng = np.random.default_rng(seed)
     batch = int(rng.integers(1, 40))
     indptr = random_indptr(rng, batch, int(rng.integers(1, 3000)))
-    grid = int(rng.integers(1, 160))
+    grid = int(rng.integers(1, 160)) if seed % 2 else int(rng.integers(1, 8))
     sch = schedule(indptr, grid)
-    total = sch["total_tiles"]
+    total = sch["total_tiles"]  # units: tiles and start units
     sizes = [w["t1"] - w["t0"] for w in sch["workers"]]
     assert sum(sizes) == total and max(sizes) - min(sizes) <= 1
     # segments tile every row exactly once, in order
