@@ -73,6 +73,11 @@ enum TraceEvent {
   kTrQLoaded1 = 30,        // softmax: ... its query loads returned
   kTrCombineW = 31,        // cluster split: thread 0's combine weight formed
   kTrCombineLanded = 32,   // ... the partials landed in shared memory
+  kTrScanTotals = 33,      // prologue: thread 0 has the batch's totals (after the first barrier)
+  kTrFirstRowFound = 34,   // prologue: the first row found and its L2 prefetches issued
+  kTrProducerStart = 35,   // producer: its loop starts
+  kTrSoftmaxStart = 36,    // softmax: its loop starts
+  kTrQIssued = 37,         // softmax: the first query loads issued
 };
 // Copy the trace out (host arrays of kTraceCtas * kTraceEvents and kTrace2Blocks
 // * kTrace2Events entries) and zero it; cudaErrorNotSupported without -DMLA_TRACE.

@@ -545,6 +545,7 @@ __device__ void schedule_prologue(const Stage1Params& p, const CUtensorMap* map_
   // Schedule units: every row with tiles is preceded by `start` units.
   const int32_t start = row_start_units(tiles, p.grid);
   const int32_t total = tiles + start * rows;
+  if (tid == 0) MLA_TRACE_CLK(kTrScanTotals);
   const int32_t c = cta_worker(p);
   const int32_t t0 = worker_begin(c, total, p.grid);
   const int32_t t1 = worker_begin(c + 1, total, p.grid);
@@ -599,6 +600,7 @@ __device__ void schedule_prologue(const Stage1Params& p, const CUtensorMap* map_
             prefetch_bulk_l2(p.kv_bytes + (static_cast<int64_t>(prev) + j0 * kTileTokens) * p.kv_row_bytes,
                              static_cast<uint32_t>(rows * p.kv_row_bytes));
           }
+          MLA_TRACE_CLK(kTrFirstRowFound);
         }
         // (the next row with tiles has its first tile at ra + nt + start)
         if (ra < t1 && t0 < ra + nt && t1 <= ra + nt + start) ms->last_row = b;
@@ -807,7 +809,21 @@ __device__ __forceinline__ void write_worker_record(const Stage1Params& p, const
   w[1] = make_int4(job[0], job[1], job[2], job[3]);
 }
 
+// Trace builds: lane 1 of the otherwise idle warp 7 (contiguous rows) watches
+// the first tile's copies land (bounded waits).
+template <int kQ, Kv kFmt>
+__device__ __forceinline__ void trace_observer(const Stage1Params& p, Misc* ms) {
+#ifdef MLA_TRACE
+  using G = Geo<kQ, kFmt>;
+  if (!p.stall_stream && ms->t1 > ms->t0 && ms->first_row >= 0) {
+    if (drain_phase(smem_u32(&ms->r_full[0]), 0)) MLA_TRACE_CLK(kTrRopeArrived);
+    if (drain_phase(smem_u32(&ms->v_full[3 % G::kNumV]), 0)) MLA_TRACE_CLK(kTrTileArrived);
+  }
+#endif
+}
+
 // ------------------------------------------------------------ producers (warp 4; page-table mode also 7-11)
+constexpr uint32_t kStartGateTile = 2;
 // Stream each tile once: the rope slot (64 dims) then four latent slots (128
 // dims each), slot fill k = 5 * tile + 1 + c in one sequence over the worker's
 // tiles (called "panels" below; a bf16 latent slot takes two boxes of 64 dims).
@@ -831,15 +847,8 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
   constexpr uint32_t kProducers = num_producers<kGather, kQ>();
   static_assert(kProducers <= sizeof(Misc::next_panel) / sizeof(uint32_t), "producer slots");
   const int lane = threadIdx.x & 31;
-#ifdef MLA_TRACE
-  // Trace builds: an idle lane of the contiguous-rows producer watches the
-  // first tile's copies land (bounded waits).
-  if (!kGather && lane == 1 && !p.stall_stream && ms->t1 > ms->t0 && ms->first_row >= 0) {
-    if (drain_phase(smem_u32(&ms->r_full[0]), 0)) MLA_TRACE_CLK(kTrRopeArrived);
-    if (drain_phase(smem_u32(&ms->v_full[3 % G::kNumV]), 0)) MLA_TRACE_CLK(kTrTileArrived);
-  }
-#endif
   if (!kGather && lane != 0) return;
+  MLA_TRACE_CLK(kTrProducerStart);
   Cursor cur;
   cursor_start(cur, ms);
   if (p.stall_stream) cur.live = false;  // test hook: nothing is ever loaded
@@ -848,6 +857,17 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
   const bool tile0_issued = !kGather && ms->tile0_issued;  // by the prologue
   bool ok = true;
   while (cur.live && ok) {
+    if (tile == kStartGateTile) {
+      // Start-up: every CTA starts at once, and a ring filled at once puts a
+      // few tiles per SM in flight, through which each CTA's first tile (which
+      // the pipeline waits for) lands only late.  Tiles from this one on are
+      // issued once the first tile's last latent panel has landed.
+      int w = 1;
+      if (lane == 0) w = wait_phase(smem_u32(&ms->v_full[3 % G::kNumV]), 0, ms, p.err);
+      if (kGather) w = __shfl_sync(0xffffffffu, w, 0);
+      ok = w != 0;
+      if (!ok) break;
+    }
     const int32_t tok0 = cur.kb + cur.j * kTileTokens;
     const int32_t valid = min(kTileTokens, cur.len - cur.j * kTileTokens);
     int32_t rows[4] = {0, 0, 0, 0};
@@ -1541,6 +1561,7 @@ __device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t 
   if (t == 0 && ms->q_ready == 1) MLA_TRACE_CLK(kTrQStart1);
   uint4 raw[kQ][5][2];
   load_q<kQ>(p, tq, nq, raw);
+  if (t == 0 && ms->q_ready == 0) MLA_TRACE_CLK(kTrQIssued);
   // The previous segment's output row may still be leaving the Q region
   // through a bulk store (the loads above are already in flight); the barrier
   // below orders every write to it after this wait.
@@ -1628,6 +1649,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
   const int32_t nq = kQ == 1 ? 1 : cta_tokens<kQ>(p);  // and how many (the rest of the kQ columns idle)
   const int32_t slot_q = q_off - p.q_off;  // their first index within a partial slot
 
+  if (t == 0) MLA_TRACE_CLK(kTrSoftmaxStart);
   Cursor cur;
   cursor_start(cur, ms);
   uint32_t tile = 0;                 // tiles processed by this CTA
@@ -2159,6 +2181,8 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
     } else if (!kCluster && cta_sibling(p) == 0 &&
                (kGather ? warp == kMmaWarp && lane == 1 : warp == kIdleWarp && lane == 0)) {
       write_worker_record<kQ>(p, ms);
+    } else if (!kGather && !G::kMx && warp == kIdleWarp && lane == 1) {
+      trace_observer<kQ, kFmt>(p, ms);
     }
   }
   __syncwarp();

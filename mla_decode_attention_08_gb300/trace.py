@@ -32,6 +32,11 @@ EVENTS = [
     (13, "softmax: first output stores issued"),
     (14, "exit barrier passed"),
     (16, "prologue: thread 0's kv_indptr loads returned"),
+    (33, "prologue: the batch's totals known"),
+    (34, "prologue: first row found, its L2 prefetches issued"),
+    (35, "producer: loop starts"),
+    (36, "softmax: loop starts"),
+    (37, "softmax: first query loads issued"),
     (17, "prologue: first block barrier passed"),
     (18, "softmax: first query loads returned"),
     (19, "observer: first rope panel arrived"),
