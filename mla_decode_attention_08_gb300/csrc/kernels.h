@@ -78,6 +78,7 @@ enum TraceEvent {
   kTrProducerStart = 35,   // producer: its loop starts
   kTrSoftmaxStart = 36,    // softmax: its loop starts
   kTrQIssued = 37,         // softmax: the first query loads issued
+  kTrFirstExpect = 38,     // producer: about to arm the first panel's barrier and issue its copy
 };
 // Copy the trace out (host arrays of kTraceCtas * kTraceEvents and kTrace2Blocks
 // * kTrace2Events entries) and zero it; cudaErrorNotSupported without -DMLA_TRACE.

@@ -939,6 +939,7 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
           ok = false;
           break;
         }
+        if (k == 0) MLA_TRACE_CLK(kTrFirstExpect);
         mbar_arrive_expect_tx(full, bytes);
         for (int i = 0; i < boxes; ++i)
           tma_load_2d(dst + i * kTileTokens * 128, map, x + 128 * i, tok0, full);

@@ -35,6 +35,7 @@ EVENTS = [
     (33, "prologue: the batch's totals known"),
     (34, "prologue: first row found, its L2 prefetches issued"),
     (35, "producer: loop starts"),
+    (38, "producer: first panel's barrier about to be armed"),
     (36, "softmax: loop starts"),
     (37, "softmax: first query loads issued"),
     (17, "prologue: first block barrier passed"),
