@@ -66,7 +66,8 @@ typedef enum {
  * workers take equal contiguous ranges of it.  S = 3 when the batch's N tiles
  * give ranges of at least 8 tiles (ceil(N / grid) >= 8), else 0: a worker
  * whose range takes on a row start also prepares that row's query and writes
- * the previous segment's output, and gets S fewer tiles for it.  A row covered
+ * the previous segment's output, and gets S fewer tiles for it.  (A bf16 cache,
+ * whose tiles take twice as long, uses S = 0.)  A row covered
  * by more than one worker is combined by the second stage.
  *
  * Small batches instead take the cluster split (`cluster` = s > 0): row b is
@@ -422,8 +423,9 @@ mla_status_t mla_decode_read_error(void* workspace, int32_t* err_host, int32_t c
                                    cudaStream_t stream);
 
 /*
- * mla_decode_schedule_host — the stage-1 schedule computed on the host from a
- * host copy of kv_indptr, with the same integer formulas the kernel uses.
+ * mla_decode_schedule_host — the stage-1 schedule of an e4m3 (or MXFP4) cache
+ * computed on the host from a host copy of kv_indptr, with the same integer
+ * formulas the kernel uses.
  *   workers_out int32 [grid*4]: (t0, t1, first_row, last_row) per worker
  *   in schedule units (first_row = last_row = -1 for a range without tiles);
  *   prefix_out int32 [B+1]: units before each row (tiles and start units of

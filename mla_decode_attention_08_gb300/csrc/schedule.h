@@ -79,7 +79,7 @@ MLA_HD int32_t plan_cluster(int32_t batch, int32_t qo_len, int32_t max_kv_len, i
 // they balance (ranges of 2 tiles become 2 or 3), and rows start with their
 // tiles.  The rule depends only on the batch's tile count T and the grid:
 // units per row start = kRowStartUnits when ceil(T / grid) >= kRowStartMinRange,
-// else 0.
+// else 0 (e4m3 and MXFP4 caches; a bf16 cache's rows start with their tiles).
 constexpr int32_t kRowStartUnits = 3;
 constexpr int32_t kRowStartMinRange = 8;
 MLA_HD int32_t row_start_units(int32_t total_tiles, int32_t grid) {

@@ -364,6 +364,25 @@ __device__ __forceinline__ bool cursor_next_tile(Cursor& c, const Misc* ms, cons
   return c.live;
 }
 
+// The same step with the segment change out of line, for the roles of the
+// MXFP4 kernel other than the softmax (whose raised register count admits no
+// calls).  That kernel runs sixteen warps of four roles, each with its own
+// copy of the segment change inlined, and it is bound by instruction issue
+// with instruction-fetch stalls: one shared copy measured 302 -> 276 us at
+// bs256.  (The e4m3 kernels measured the same or slower with it.)
+__device__ __noinline__ bool cursor_next_segment_call(Cursor& c, const int32_t* kv_indptr, int32_t batch,
+                                                      int32_t t0, int32_t t1) {
+  return cursor_next_segment(c, kv_indptr, batch, t0, t1);
+}
+template <bool kOutOfLine>
+__device__ __forceinline__ bool cursor_step(Cursor& c, const Misc* ms, const int32_t* kv_indptr,
+                                            int32_t batch) {
+  if (!kOutOfLine) return cursor_next_tile(c, ms, kv_indptr, batch);
+  if (++c.j < c.j1) return true;
+  c.live = cursor_next_segment_call(c, kv_indptr, batch, ms->t0, ms->t1);
+  return c.live;
+}
+
 // Bounded wait used only while draining at the end of a call.
 __device__ __noinline__ bool drain_phase(uint32_t bar, uint32_t parity) {
   const long long start = clock64();
@@ -542,8 +561,10 @@ __device__ void schedule_prologue(const Stage1Params& p, const CUtensorMap* map_
     rows += r;
   }
   if (bad) tiles = rows = 0;
-  // Schedule units: every row with tiles is preceded by `start` units.
-  const int32_t start = row_start_units(tiles, p.grid);
+  // Schedule units: every row with tiles is preceded by `start` units (none
+  // for a bf16 cache, whose tiles carry twice the bytes: there a row start
+  // costs little against them, and units measured slower).
+  const int32_t start = kFmt == Kv::kBf16 ? 0 : row_start_units(tiles, p.grid);
   const int32_t total = tiles + start * rows;
   if (tid == 0) MLA_TRACE_CLK(kTrScanTotals);
   const int32_t c = cta_worker(p);
@@ -815,7 +836,7 @@ template <int kQ, Kv kFmt>
 __device__ __forceinline__ void trace_observer(const Stage1Params& p, Misc* ms) {
 #ifdef MLA_TRACE
   using G = Geo<kQ, kFmt>;
-  if (!p.stall_stream && ms->t1 > ms->t0 && ms->first_row >= 0) {
+  if (G::kNumV >= 8 && !p.stall_stream && ms->t1 > ms->t0 && ms->first_row >= 0) {
     if (drain_phase(smem_u32(&ms->r_full[0]), 0)) MLA_TRACE_CLK(kTrRopeArrived);
     if (drain_phase(smem_u32(&ms->v_full[3 % G::kNumV]), 0)) MLA_TRACE_CLK(kTrTileArrived);
   }
@@ -857,11 +878,14 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
   const bool tile0_issued = !kGather && ms->tile0_issued;  // by the prologue
   bool ok = true;
   while (cur.live && ok) {
-    if (tile == kStartGateTile) {
+    if (G::kNumV >= 8 && tile == kStartGateTile) {
       // Start-up: every CTA starts at once, and a ring filled at once puts a
       // few tiles per SM in flight, through which each CTA's first tile (which
       // the pipeline waits for) lands only late.  Tiles from this one on are
-      // issued once the first tile's last latent panel has landed.
+      // issued once the first tile's last latent panel has landed.  (Phase 0
+      // of that slot is the first tile's only while the second tile fits in
+      // other slots: a ring of 8 or more latent slots.  A shallower ring
+      // bounds the look-ahead by itself.)
       int w = 1;
       if (lane == 0) w = wait_phase(smem_u32(&ms->v_full[3 % G::kNumV]), 0, ms, p.err);
       if (kGather) w = __shfl_sync(0xffffffffu, w, 0);
@@ -1046,7 +1070,7 @@ __device__ void run_producer_mx(const Stage1Params& p, const CUtensorMap* map_v,
     }
     if (!ok) break;
     ++tile;
-    if (!cursor_next_tile(cur, ms, p.kv_indptr, p.batch)) break;
+    if (!cursor_step<true>(cur, ms, p.kv_indptr, p.batch)) break;
   }
   if (!ms->abort_flag) return;
   // An abandoned call: only the last fill of each slot can still be in flight.
@@ -1194,7 +1218,7 @@ __device__ void run_converter(const Stage1Params& p, Misc* ms, uint32_t sbase) {
     }
     if (stop) break;
     ++tile;
-    stop = !cursor_next_tile(cur, ms, p.kv_indptr, p.batch);
+    stop = !cursor_step<true>(cur, ms, p.kv_indptr, p.batch);
   }
   if (bad) set_error(p.err, MLA_DERR_MX_SCALE);
 }
@@ -1339,7 +1363,7 @@ __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
     if (qc.j + 1 == qc.j1) umma_commit(smem_u32(&ms->q_empty));
     if (qk_n == 0) MLA_TRACE_CLK(kTrQkIssued);
     ++qk_n;
-    cursor_next_tile(qc, ms, p.kv_indptr, p.batch);
+    cursor_step<kFmt == Kv::kMx4>(qc, ms, p.kv_indptr, p.batch);
   }
   // Every MMA issued by this thread completes before TMEM is released.
   umma_commit(smem_u32(&ms->mma_done));
@@ -1365,7 +1389,7 @@ __device__ void run_mma_pv(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
     if (pv_n == 0) MLA_TRACE_CLK(kTrPvIssued);
     if (first && pc.seg == 1) MLA_TRACE_CLK(kTrPvIssued1);
     ++pv_n;
-    cursor_next_tile(pc, ms, p.kv_indptr, p.batch);
+    cursor_step<kFmt == Kv::kMx4>(pc, ms, p.kv_indptr, p.batch);
   }
   umma_commit(smem_u32(&ms->mma_done));
 }
