@@ -365,12 +365,16 @@ mla_status_t mla_debug_p_split(const float* p, int64_t n, void* hi_out, void* lo
  * scores read, first P published, first PV issued, first epilogue start and
  * end, exit; then the row-pointer loads returned, the prologue's scan barrier,
  * the first query loads returned, the first rope and last latent panel
- * arrived (an otherwise idle producer lane watching them); for the cluster split the cluster barrier passed and the combine
- * written; not a clock, segments * 65536 + tiles of the CTA's range; then the
- * boundary into the second segment: the first segment's last P published, the
- * second segment's Q operand published, its first scores read, P published
- * and PV issued, its Q preparation started and its query loads returned),
- * and for each of the first
+ * arrived (a lane of the otherwise idle warp 7 watching them); for the
+ * cluster split the cluster barrier passed and the combine written; not a
+ * clock, segments * 65536 + tiles of the CTA's range; then the boundary into
+ * the second segment: the first segment's last P published, the second
+ * segment's Q operand published, its first scores read, P published and PV
+ * issued, its Q preparation started and its query loads returned; then the
+ * cluster combine's weight formed and partials landed, the prologue's totals
+ * and first row, the producer's and the softmax's loop starts, the first
+ * query loads issued and the producer's first barrier arming; event indices
+ * as in the library's kernels.h), and for each of the first
  * MLA_TRACE2_BLOCKS stage-2 blocks
  * (numbered y * grid_x + x) the global timer at entry, after its wait for
  * stage 1 and at exit.  Each call's stamps overwrite the previous call's.

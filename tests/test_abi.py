@@ -187,3 +187,16 @@ def test_plan_cluster_matches_oracle(lib, qo_len):
                 plan = binding.mla_decode_plan(batch, max_len, sms, qo_len=qo_len)
                 assert plan.cluster == plan_cluster(batch, qo_len, max_len, sms), (batch, max_len, sms)
                 assert plan.grid == plan_grid(batch, max_len, sms if qo_len <= 2 else sms // 2)
+
+
+def test_trace_table_sizes_match_the_header():
+    """The binding sizes the host arrays of mla_decode_trace_read from the
+    header's MLA_TRACE_* constants; a drift would make the call write past
+    them.  The trace summariser's event indices stay inside the table."""
+    text = open(os.path.join(ROOT, "include", "mla_decode.h")).read()
+    want = {name: int(re.search(rf"#define {name} (\d+)", text).group(1))
+            for name in ("MLA_TRACE_CTAS", "MLA_TRACE_EVENTS", "MLA_TRACE2_BLOCKS")}
+    assert (binding.TRACE_CTAS, binding.TRACE_EVENTS, binding.TRACE2_BLOCKS) == (
+        want["MLA_TRACE_CTAS"], want["MLA_TRACE_EVENTS"], want["MLA_TRACE2_BLOCKS"])
+    from mla_decode_attention_08_gb300 import trace
+    assert all(0 < ev < want["MLA_TRACE_EVENTS"] for ev, _ in trace.EVENTS)
