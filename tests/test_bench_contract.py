@@ -38,18 +38,21 @@ def test_reference_arm_line():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("cache", ["e4m3", "mxfp4"])
-def test_gpu_arm_line(cache):
-    line = run_bench("--workload", "bs64_kv8192", "--steps", "20", "--warmup", "3",
+@pytest.mark.parametrize("workload,cache,kernels", [
+    ("bs64_kv8192", "e4m3", 2), ("bs64_kv8192", "mxfp4", 2),
+    ("bs4_kv1024", "e4m3", 1),    # the cluster split: stage 1 alone
+    ("bs4_kv1024", "mxfp4", 2)])  # an MXFP4 cache runs the persistent split
+def test_gpu_arm_line(workload, cache, kernels):
+    line = run_bench("--workload", workload, "--steps", "20", "--warmup", "3",
                      "--no-per-config", "--no-cpu-baseline", "--e2e-steps", "2", "--cache", cache)
     assert BASE_KEYS <= set(line) and line["n_gpus"] == 1 and line["steps"] == 20
-    assert line["config"]["workload"] == "bs64_kv8192"
+    assert line["config"]["workload"] == workload
     rf = line["roofline"]
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and 0 < rf["frac"] < 1.2
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
     e2e = line["e2e"]
     assert e2e["value"] > line["value"] and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
-    assert line["gpu_launches"] == 2 * 20
+    assert line["gpu_launches"] == kernels * 20
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(line["clocks"])
 
 
