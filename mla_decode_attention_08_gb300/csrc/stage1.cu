@@ -132,14 +132,15 @@ struct Misc {
   uint64_t q_empty;     // the segment's last QK completed (Q operand free)
   uint64_t mma_done;
   // Monotonic counters the MMA issuers poll (st.release, then relaxed loads
-  // followed by fence.acq_rel once a condition holds).
-  uint32_t q_ready;     // segments whose Q operand is written
-  uint32_t s_read;      // tiles whose S has been read out by every softmax warp
-  uint32_t p_ready;     // tiles whose P is published (and O rescaled)
-  uint32_t o_free;      // segments whose epilogue has read O out of TMEM
+  // followed by fence.acq_rel once a condition holds), one per softmax
+  // warpgroup (the two-token kernels on contiguous rows run two).
+  uint32_t q_ready[2];  // segments whose Q operand is written
+  uint32_t s_read[2];   // tiles whose S has been read out by every softmax warp
+  uint32_t p_ready[2];  // tiles whose P is published (and O rescaled)
+  uint32_t o_free[2];   // segments whose epilogue has read O out of TMEM
   alignas(16) float red_max[2][4][16 * kMaxQ];  // read and written as float4
   alignas(16) float red_sum[4][16 * kMaxQ];
-  uint32_t red_u32[8];
+  uint32_t red_u32[16];  // [4 token + warp]: a query token's |q| maxima; [8 + group]: abort flag
   int32_t scan[kStage1ThreadsMx / 32];       // per warp of the prologue's block scan (largest block):
   int32_t scan_rows[kStage1ThreadsMx / 32];  // tiles, and rows with tiles
   int32_t row_start;    // schedule units before each row's tiles (row_start_units)
@@ -186,6 +187,21 @@ constexpr int kIdleWarp = 7;   // contiguous rows: writes the worker record for 
 constexpr uint32_t kBarSoftmax = 1;  // named barrier id of warps 0-3
 constexpr uint32_t kBarProducers = 2;  // named barrier id of the page-table producers
 constexpr uint32_t kBarConverters = 3;  // named barrier id of the MXFP4 converter warps
+constexpr uint32_t kBarSoftmaxB = 4;     // named barrier id of the second softmax warpgroup (warps 8-11)
+constexpr uint32_t kBarSoftmaxPair = 5;  // ... of both softmax warpgroups together
+
+// A softmax warpgroup: its threads' index within it, the first of the query-
+// token columns it owns, its own named barrier, and the barrier it takes
+// before it writes the Q region (both warpgroups' when there are two: the
+// other's output staging must have been read first).
+struct SoftmaxGroup {
+  int t;
+  int q0;
+  uint32_t bar, pair, pair_threads;
+};
+__device__ __forceinline__ SoftmaxGroup single_softmax_group() {
+  return SoftmaxGroup{static_cast<int>(threadIdx.x), 0, kBarSoftmax, kBarSoftmax, 128u};
+}
 // Page-table mode with one query token: 12 warps, six producer warps (4, 7,
 // 8, 9, 10, 11) taking panels round-robin; the softmax warpgroup gets 240
 // registers and the other two 128 (launched with 168 each: 128 x 240 + 256 x 128
@@ -195,10 +211,26 @@ constexpr uint32_t kBarConverters = 3;  // named barrier id of the MXFP4 convert
 // An MXFP4 cache runs 16 warps: warps 8-15 convert its panels.
 template <bool kGather, int kQ, Kv kFmt>
 __host__ __device__ constexpr bool wide_block() { return (kGather && kQ == 1) || kFmt == Kv::kMx4; }
+// Two query tokens on contiguous rows: two softmax warpgroups, one token
+// each (warps 0-3 and 8-11), 12 warps: a warpgroup of 128 threads then does
+// the softmax of one token per tile, as in the one-token kernels, instead of
+// one warpgroup doing both tokens' (each warp the only one of its scheduler,
+// whose latencies nothing covered).
+// (Trace builds keep one warpgroup: with the stamps, ptxas finds no register
+// allocation for the two-warpgroup split at any softmax count up to 224.)
+template <bool kGather, int kQ, Kv kFmt>
+__host__ __device__ constexpr bool dual_softmax() {
+#ifdef MLA_TRACE
+  return false;
+#else
+  return !kGather && kQ == 2 && kFmt != Kv::kMx4;
+#endif
+}
 template <bool kGather, int kQ, Kv kFmt>
 __host__ __device__ constexpr int stage1_threads() {
   return kFmt == Kv::kMx4 ? kStage1ThreadsMx
-                          : (wide_block<kGather, kQ, kFmt>() ? kStage1ThreadsGather : kStage1Threads);
+                          : (wide_block<kGather, kQ, kFmt>() || dual_softmax<kGather, kQ, kFmt>()
+                                 ? kStage1ThreadsGather : kStage1Threads);
 }
 template <bool kGather, int kQ>
 __host__ __device__ constexpr uint32_t num_producers() { return !kGather ? 1 : (kQ == 1 ? 6 : 2); }
@@ -210,6 +242,11 @@ __device__ __forceinline__ int gather_producer_of_warp(int warp, uint32_t produc
 constexpr int kSoftmaxRegs = 240, kOtherRegs = 128;
 static_assert(128 * kSoftmaxRegs + 256 * kOtherRegs <= kStage1ThreadsGather * 168,
               "register split exceeds the launch allocation");
+// Two softmax warpgroups (12 warps, launched with 168 registers a thread):
+// 192 for each, 120 for the producer and MMA warpgroup.
+constexpr int kDualSoftmaxRegs = 192, kDualOtherRegs = 120;
+static_assert(2 * 128 * kDualSoftmaxRegs + 128 * kDualOtherRegs <= kStage1ThreadsGather * 168,
+              "two-warpgroup register split exceeds the launch allocation");
 // MXFP4 (16 warps, launched with 128 registers a thread): 240 for the softmax
 // warpgroup, 88 for the other twelve warps.
 constexpr int kOtherRegsMx = 88;
@@ -1351,6 +1388,14 @@ __device__ __forceinline__ bool spin_counter(const uint32_t* ctr, uint32_t targe
   return spin_counter_slow(ctr, target, ms, err);
 }
 
+// The same wait on a counter of every softmax warpgroup (two in the
+// two-token kernels on contiguous rows).
+template <bool kDual>
+__device__ __forceinline__ bool spin_groups(const uint32_t (&ctr)[2], uint32_t target, Misc* ms,
+                                            int32_t* err) {
+  return spin_counter(&ctr[0], target, ms, err) && (!kDual || spin_counter(&ctr[1], target, ms, err));
+}
+
 // Two threads issue tcgen05.mma, each for one product, so that neither
 // product's issue waits behind the other's (issuing one product blocks the
 // issuing thread for about its execution time, ~1200 cycles).
@@ -1360,7 +1405,7 @@ __device__ __forceinline__ bool spin_counter(const uint32_t* ctr, uint32_t targe
 // then each of its five slots is multiplied as soon as its copy has landed (the
 // issuer waits on the TMA barriers itself), so that the products overlap the
 // copies still in flight.
-template <int kQ, Kv kFmt, bool kRolled>
+template <int kQ, Kv kFmt, bool kRolled, bool kDual>
 __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
   using G = Geo<kQ, kFmt>;
   Cursor qc;
@@ -1368,8 +1413,8 @@ __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
   uint32_t qk_n = 0;  // tiles whose QK has been issued
   while (qc.live) {
     bool ok = true;
-    if (qc.j == qc.j0) ok = spin_counter(&ms->q_ready, static_cast<uint32_t>(qc.seg) + 1, ms, p.err);
-    if (ok && qk_n >= 2) ok = spin_counter(&ms->s_read, qk_n - 1, ms, p.err);
+    if (qc.j == qc.j0) ok = spin_groups<kDual>(ms->q_ready, static_cast<uint32_t>(qc.seg) + 1, ms, p.err);
+    if (ok && qk_n >= 2) ok = spin_groups<kDual>(ms->s_read, qk_n - 1, ms, p.err);
     if (ok) fence_acquire_cta();
     if (ok) ok = wait_phase(smem_u32(&ms->r_full[qk_n % kNumRSlots]), (qk_n / kNumRSlots) & 1, ms,
                             p.err);
@@ -1411,15 +1456,15 @@ __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
 // PV issuer (warp 5, lane 0): PV of tile i needs P[i & 1] published and, on
 // the first tile of a later segment, O read out by the previous segment's
 // epilogue.
-template <int kQ, Kv kFmt, bool kRolled>
+template <int kQ, Kv kFmt, bool kRolled, bool kDual>
 __device__ void run_mma_pv(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
   Cursor pc;
   cursor_start(pc, ms);
   uint32_t pv_n = 0;  // tiles whose PV has been issued
   while (pc.live) {
     const bool first = pc.j == pc.j0;
-    bool ok = spin_counter(&ms->p_ready, pv_n + 1, ms, p.err);
-    if (ok && first && pc.seg > 0) ok = spin_counter(&ms->o_free, static_cast<uint32_t>(pc.seg), ms, p.err);
+    bool ok = spin_groups<kDual>(ms->p_ready, pv_n + 1, ms, p.err);
+    if (ok && first && pc.seg > 0) ok = spin_groups<kDual>(ms->o_free, static_cast<uint32_t>(pc.seg), ms, p.err);
     if (!ok) break;
     fence_acquire_cta();
     tc_fence_after();
@@ -1502,58 +1547,62 @@ __device__ __forceinline__ void split_e4m3_16(const float (&x)[16], uint32_t (&h
 }
 
 // Q operand rows of a bf16 cache: the bf16 values themselves, row 16 qi + head.
-template <int kQ>
-__device__ __forceinline__ void store_q_bf16(uint32_t sq, const uint4 (&raw)[kQ][5][2],
-                                             float (&qk_scale)[kQ]) {
-  const int t = threadIdx.x;
-  named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+template <int kQ, int kQt>
+__device__ __forceinline__ void store_q_bf16(uint32_t sq, const uint4 (&raw)[kQt][5][2],
+                                             float (&qk_scale)[kQt], const SoftmaxGroup& sg) {
+  const int t = sg.t;
+  named_bar_sync(sg.pair, sg.pair_threads);
 #pragma unroll
-  for (int qi = 0; qi < kQ; ++qi) {
-    qk_scale[qi] = kSmScaleLog2;
+  for (int i = 0; i < kQt; ++i) {
+    const int qi = sg.q0 + i;
+    qk_scale[i] = kSmScaleLog2;
 #pragma unroll
     for (int r = 0; r < 5; ++r) {
       const int job = t + 128 * r;
       if (job < 576) {
         const int head = job / 36, ch = job % 36;  // ch: 16 dims = two 16-byte chunks
-        const uint4 a = raw[qi][r][0], b = raw[qi][r][1];
+        const uint4 a = raw[i][r][0], b = raw[i][r][1];
         st_shared_v4(q_chunk_addr<kQ, Kv::kBf16>(sq, 16 * qi + head, 2 * ch), a.x, a.y, a.z, a.w);
         st_shared_v4(q_chunk_addr<kQ, Kv::kBf16>(sq, 16 * qi + head, 2 * ch + 1), b.x, b.y, b.z, b.w);
       }
     }
   }
   fence_proxy_async_smem();
-  named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+  named_bar_sync(sg.bar, kSoftmaxThreads);
 }
 
 // Q operand rows of an e4m3 cache: each query token scaled by a power of two so
 // its largest magnitude lands in (224, 448], then split into hi / lo e4m3 rows
 // (32 qi + head for hi, 32 qi + 16 + head for lo).
-template <int kQ>
-__device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 (&raw)[kQ][5][2],
-                                             float kv_scale, float (&qk_scale)[kQ]) {
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+template <int kQ, int kQt>
+__device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 (&raw)[kQt][5][2],
+                                             float kv_scale, float (&qk_scale)[kQt],
+                                             const SoftmaxGroup& sg) {
+  const int t = sg.t, warp = t >> 5, lane = t & 31;
 #pragma unroll
-  for (int qi = 0; qi < kQ; ++qi) {
+  for (int i = 0; i < kQt; ++i) {
+    const int qi = sg.q0 + i;
     uint32_t amax = 0;
     auto fold = [&](uint32_t w) { amax = max(amax, max(w & 0x7FFFu, (w >> 16) & 0x7FFFu)); };
 #pragma unroll
     for (int r = 0; r < 5; ++r) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        fold(raw[qi][r][k].x);
-        fold(raw[qi][r][k].y);
-        fold(raw[qi][r][k].z);
-        fold(raw[qi][r][k].w);
+        fold(raw[i][r][k].x);
+        fold(raw[i][r][k].y);
+        fold(raw[i][r][k].z);
+        fold(raw[i][r][k].w);
       }
     }
     amax = __reduce_max_sync(0xffffffffu, amax);
-    if (t == 0 && qi == 0 && ms->q_ready == 0 && amax != 0xFFFFFFFFu) MLA_TRACE_CLK(kTrQLoaded);
-    if (t == 0 && qi == 0 && ms->q_ready == 1 && amax != 0xFFFFFFFFu) MLA_TRACE_CLK(kTrQLoaded1);
+    if (t == 0 && qi == 0 && ms->q_ready[0] == 0 && amax != 0xFFFFFFFFu) MLA_TRACE_CLK(kTrQLoaded);
+    if (t == 0 && qi == 0 && ms->q_ready[0] == 1 && amax != 0xFFFFFFFFu) MLA_TRACE_CLK(kTrQLoaded1);
     if (lane == 0) ms->red_u32[4 * qi + warp] = amax;
   }
-  named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+  named_bar_sync(sg.pair, sg.pair_threads);
 #pragma unroll
-  for (int qi = 0; qi < kQ; ++qi) {
+  for (int i = 0; i < kQt; ++i) {
+    const int qi = sg.q0 + i;
     const uint32_t amax = max(max(ms->red_u32[4 * qi], ms->red_u32[4 * qi + 1]),
                               max(ms->red_u32[4 * qi + 2], ms->red_u32[4 * qi + 3]));
     const float a = __uint_as_float(amax << 16);
@@ -1565,7 +1614,7 @@ __device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 
       k2 = min(max(k2, -126), 126);
     }
     const float up = __int_as_float((k2 + 127) << 23);
-    qk_scale[qi] = __int_as_float((127 - k2) << 23) * kv_scale * kSmScaleLog2;
+    qk_scale[i] = __int_as_float((127 - k2) << 23) * kv_scale * kSmScaleLog2;
 #pragma unroll
     for (int r = 0; r < 5; ++r) {
       const int job = t + 128 * r;
@@ -1576,10 +1625,10 @@ __device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 
           x[2 * i] = u2f(w << 16) * up;
           x[2 * i + 1] = u2f(w & 0xFFFF0000u) * up;
         };
-        unpack(raw[qi][r][0].x, 0); unpack(raw[qi][r][0].y, 1);
-        unpack(raw[qi][r][0].z, 2); unpack(raw[qi][r][0].w, 3);
-        unpack(raw[qi][r][1].x, 4); unpack(raw[qi][r][1].y, 5);
-        unpack(raw[qi][r][1].z, 6); unpack(raw[qi][r][1].w, 7);
+        unpack(raw[i][r][0].x, 0); unpack(raw[i][r][0].y, 1);
+        unpack(raw[i][r][0].z, 2); unpack(raw[i][r][0].w, 3);
+        unpack(raw[i][r][1].x, 4); unpack(raw[i][r][1].y, 5);
+        unpack(raw[i][r][1].z, 6); unpack(raw[i][r][1].w, 7);
         uint32_t hi[4], lo[4];
         split_e4m3_16(x, hi, lo);
         st_shared_v4(q_chunk_addr<kQ, Kv::kE4m3>(sq, 32 * qi + head, ch), hi[0], hi[1], hi[2], hi[3]);
@@ -1588,52 +1637,54 @@ __device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 
     }
   }
   fence_proxy_async_smem();
-  named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+  named_bar_sync(sg.bar, kSoftmaxThreads);
 }
 
-// Loads the row's query tokens tq .. tq + nq - 1 (16 heads x 576 bf16 each;
-// nq <= kQ, the other operand rows stay zero) and writes the Q operand of the
-// cache format.  Sets qk_scale[qi], the factor turning the QK accumulator of
-// token qi into base-2 softmax exponent units.  tq < 0 writes a zero query.
-// This thread's share of the query tokens (16-dim chunks `t + 128 r` of the
-// 16 x 36 per token) into registers.
-template <int kQ>
-__device__ __forceinline__ void load_q(const Stage1Params& p, int32_t tq, int32_t nq,
-                                       uint4 (&raw)[kQ][5][2]) {
-  const int t = threadIdx.x;
+// Loads the row's query tokens tq + q0 .. tq + q0 + kQt - 1 of the nq this CTA
+// takes (16 heads x 576 bf16 each; tokens past nq give zero operand rows) and
+// writes their rows of the Q operand of the cache format (kQ token columns).
+// Sets qk_scale[i], the factor turning the QK accumulator of token q0 + i into
+// base-2 softmax exponent units.  tq < 0 writes a zero query.  This thread's
+// share of each token (16-dim chunks `t + 128 r` of the 16 x 36 per token)
+// goes into registers first.
+template <int kQt>
+__device__ __forceinline__ void load_q(const Stage1Params& p, int t, int32_t tq, int32_t nq, int q0,
+                                       uint4 (&raw)[kQt][5][2]) {
 #pragma unroll
-  for (int qi = 0; qi < kQ; ++qi) {
+  for (int i = 0; i < kQt; ++i) {
+    const int qi = q0 + i;
 #pragma unroll
     for (int r = 0; r < 5; ++r) {
       const int job = t + 128 * r;
-      raw[qi][r][0] = raw[qi][r][1] = make_uint4(0, 0, 0, 0);
+      raw[i][r][0] = raw[i][r][1] = make_uint4(0, 0, 0, 0);
       if (job < 576 && tq >= 0 && qi < nq && MLA_DCHECK(tq + qi < total_tokens(p), p.err)) {
         const int head = job / 36, ch = job % 36;
         const uint4* src = reinterpret_cast<const uint4*>(
             p.q + (static_cast<size_t>(tq + qi) * kNumHeads + head) * kQkDim + ch * 16);
-        raw[qi][r][0] = __ldg(src);
-        raw[qi][r][1] = __ldg(src + 1);
+        raw[i][r][0] = __ldg(src);
+        raw[i][r][1] = __ldg(src + 1);
       }
     }
   }
 }
 
-template <int kQ, Kv kFmt>
+template <int kQ, int kQt, Kv kFmt>
 __device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq, int32_t nq,
-                          float kv_scale, float (&qk_scale)[kQ]) {
-  const int t = threadIdx.x;
-  if (t == 0 && ms->q_ready == 1) MLA_TRACE_CLK(kTrQStart1);
-  uint4 raw[kQ][5][2];
-  load_q<kQ>(p, tq, nq, raw);
-  if (t == 0 && ms->q_ready == 0) MLA_TRACE_CLK(kTrQIssued);
-  // The previous segment's output row may still be leaving the Q region
-  // through a bulk store (the loads above are already in flight); the barrier
-  // below orders every write to it after this wait.
-  if (t == 0) bulk_wait_read<0>();
+                          float kv_scale, float (&qk_scale)[kQt], const SoftmaxGroup& sg) {
+  const bool lead = sg.t == 0 && sg.q0 == 0;
+  if (lead && ms->q_ready[0] == 1) MLA_TRACE_CLK(kTrQStart1);
+  uint4 raw[kQt][5][2];
+  load_q<kQt>(p, sg.t, tq, nq, sg.q0, raw);
+  if (lead && ms->q_ready[0] == 0) MLA_TRACE_CLK(kTrQIssued);
+  // The previous segment's output rows may still be leaving the Q region
+  // through bulk stores (the loads above are already in flight); the barrier
+  // in the store below (both warpgroups', when there are two) orders every
+  // write to it after these waits.
+  if (sg.t == 0) bulk_wait_read<0>();
   if constexpr (kFmt == Kv::kBf16)
-    store_q_bf16<kQ>(sq, raw, qk_scale);
+    store_q_bf16<kQ, kQt>(sq, raw, qk_scale, sg);
   else
-    store_q_e4m3<kQ>(ms, sq, raw, kv_scale, qk_scale);
+    store_q_e4m3<kQ, kQt>(ms, sq, raw, kv_scale, qk_scale, sg);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -1643,12 +1694,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // Named-barrier arrival of the softmax warpgroup that also ORs a predicate.
-__device__ __forceinline__ bool softmax_bar_or(bool v) {
+__device__ __forceinline__ bool softmax_bar_or(bool v, uint32_t bar) {
   uint32_t r;
   asm volatile(
       "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; bar.red.or.pred po, %2, %3, pi;"
       " selp.u32 %0, 1, 0, po; }"
-      : "=r"(r) : "r"(static_cast<uint32_t>(v)), "r"(kBarSoftmax), "r"(kSoftmaxThreads) : "memory");
+      : "=r"(r) : "r"(static_cast<uint32_t>(v)), "r"(bar), "r"(kSoftmaxThreads) : "memory");
   return r != 0;
 }
 
@@ -1701,11 +1752,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // kInlineWaits: the waits' slow paths inlined (required where setmaxnreg raised
 // the register count: a call out of such a region does not compile).
-template <int kQ, Kv kFmt, bool kInlineWaits, bool kCluster>
+// kGroups softmax warpgroups share the CTA's query tokens: warpgroup g (warps
+// 0-3, and 8-11 for g = 1) owns token columns g kQt .. g kQt + kQt - 1 of the
+// kQ, reads their S columns, writes their P chunks and Q rows and their O
+// columns, and publishes its own progress counters; the MMA issuers wait for
+// every warpgroup's.
+template <int kQ, Kv kFmt, bool kInlineWaits, bool kCluster, int kGroups>
 __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem,
-                            float kv_scale) {
+                            float kv_scale, int g) {
   using G = Geo<kQ, kFmt>;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  static_assert(kGroups == 1 || (kGroups == 2 && kQ == 2 && !kCluster), "two warpgroups take one token each");
+  constexpr int kQt = kQ / kGroups;  // token columns of this warpgroup
+  const SoftmaxGroup sg{static_cast<int>(threadIdx.x) - 256 * g, g * kQt,
+                        g ? kBarSoftmaxB : kBarSoftmax, kGroups == 2 ? kBarSoftmaxPair : kBarSoftmax,
+                        kGroups == 2 ? 2u * kSoftmaxThreads : kSoftmaxThreads};
+  const int t = sg.t, warp = t >> 5, lane = t & 31, q0 = sg.q0;
+  const bool lead = t == 0 && g == 0;  // trace stamps
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;  // TMEM lane quarter
   const int token = warp * 32 + lane;  // S row (token) / O row (dim within a chunk) of this thread
   const int32_t c = cta_worker(p);
@@ -1713,7 +1775,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
   const int32_t nq = kQ == 1 ? 1 : cta_tokens<kQ>(p);  // and how many (the rest of the kQ columns idle)
   const int32_t slot_q = q_off - p.q_off;  // their first index within a partial slot
 
-  if (t == 0) MLA_TRACE_CLK(kTrSoftmaxStart);
+  if (lead) MLA_TRACE_CLK(kTrSoftmaxStart);
   Cursor cur;
   cursor_start(cur, ms);
   uint32_t tile = 0;                 // tiles processed by this CTA
@@ -1734,7 +1796,7 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
   // first QKs overlap the epilogue.
   bool q_early = false;
   int32_t tq_early = -1;
-  float qk_scale[kQ];
+  float qk_scale[kQt];
   while (cur.live) {
     // ------------------------------------------------ segment start
     const int32_t b = cur.b;
@@ -1747,20 +1809,20 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     if (!row_ok && t == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
     if (!q_early) {
       if (cur.seg > 0) softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
-      prepare_q<kQ, kFmt>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, nq, kv_scale, qk_scale);
-      if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 1));
-      if (t == 0 && cur.seg == 0) MLA_TRACE_CLK(kTrQReady);
-      if (t == 0 && cur.seg == 1) MLA_TRACE_CLK(kTrQReady1);
+      prepare_q<kQ, kQt, kFmt>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, nq, kv_scale, qk_scale, sg);
+      if (t == 0) st_release_u32(&ms->q_ready[g], static_cast<uint32_t>(cur.seg + 1));
+      if (lead && cur.seg == 0) MLA_TRACE_CLK(kTrQReady);
+      if (lead && cur.seg == 1) MLA_TRACE_CLK(kTrQReady1);
     }
     q_early = false;
 
-    float m_ref[kQ][16], l[kQ][16];
+    float m_ref[kQt][16], l[kQt][16];
 #pragma unroll
-    for (int qi = 0; qi < kQ; ++qi) {
+    for (int i = 0; i < kQt; ++i) {
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
-        m_ref[qi][h] = -INFINITY;
-        l[qi][h] = 0.0f;
+        m_ref[i][h] = -INFINITY;
+        l[i][h] = 0.0f;
       }
     }
     const uint32_t seg_first_tile = tile;
@@ -1775,14 +1837,15 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       softmax_wait<kInlineWaits>(smem_u32(&ms->s_full[sb]), (tile >> 1) & 1, ms, p.err);
       tc_fence_after();
       const int32_t pos = cur.j * kTileTokens + token;  // row-local token of this thread
-      bool tok_ok[kQ];
-      float s[kQ][16];
+      bool tok_ok[kQt];
+      float s[kQt][16];
       bool exceed = false;
 #pragma unroll
-      for (int qi = 0; qi < kQ; ++qi) {
+      for (int i = 0; i < kQt; ++i) {
+        const int qi = q0 + i;
         const uint32_t addr = tmem + lane_base + G::kColS + G::kN * sb + G::kTokCols * qi;
-        tok_ok[qi] = qi < nq && pos < vis0 + qi;
-        const float sc = qk_scale[qi];
+        tok_ok[i] = qi < nq && pos < vis0 + qi;
+        const float sc = qk_scale[i];
         if constexpr (G::kSplit) {
           uint32_t r[32];
           tmem_ld32(addr, r);
@@ -1790,8 +1853,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
           const float sc_lo = sc * 0.0625f;
 #pragma unroll
           for (int h = 0; h < 16; ++h) {
-            s[qi][h] = tok_ok[qi] ? fmaf(u2f(r[16 + h]), sc_lo, u2f(r[h]) * sc) : -INFINITY;
-            exceed |= s[qi][h] > m_ref[qi][h] + kRescaleThreshold;
+            s[i][h] = tok_ok[i] ? fmaf(u2f(r[16 + h]), sc_lo, u2f(r[h]) * sc) : -INFINITY;
+            exceed |= s[i][h] > m_ref[i][h] + kRescaleThreshold;
           }
         } else {
           uint32_t r[16];
@@ -1799,42 +1862,44 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
           tmem_wait_ld();
 #pragma unroll
           for (int h = 0; h < 16; ++h) {
-            s[qi][h] = tok_ok[qi] ? u2f(r[h]) * sc : -INFINITY;
-            exceed |= s[qi][h] > m_ref[qi][h] + kRescaleThreshold;
+            s[i][h] = tok_ok[i] ? u2f(r[h]) * sc : -INFINITY;
+            exceed |= s[i][h] > m_ref[i][h] + kRescaleThreshold;
           }
         }
       }
       tc_fence_before();
-      if (t == 0 && tile == 0) MLA_TRACE_CLK(kTrSRead);
-      if (t == 0 && cur.seg == 1 && tile == seg_first_tile) MLA_TRACE_CLK(kTrSRead1);
+      if (lead && tile == 0) MLA_TRACE_CLK(kTrSRead);
+      if (lead && cur.seg == 1 && tile == seg_first_tile) MLA_TRACE_CLK(kTrSRead1);
 
       // The reference maximum moves only when some score exceeds it by more
       // than the threshold (always on a segment's first tile); then the tile
       // maximum per column is reduced over the 128 tokens.
       bool moved = false;
-      const bool any_exceed = softmax_bar_or(exceed);
-      // Every softmax warp has read S[sb] (its tcgen05.ld completed before the barrier).
-      if (t == 0) st_release_u32(&ms->s_read, tile + 1);
+      const bool any_exceed = softmax_bar_or(exceed, sg.bar);
+      // Every warp of this warpgroup has read S[sb] (its tcgen05.ld completed before the barrier).
+      if (t == 0) st_release_u32(&ms->s_read[g], tile + 1);
       if (any_exceed) {
-        float mx[kQ][16];
+        float mx[kQt][16];
 #pragma unroll
-        for (int qi = 0; qi < kQ; ++qi) {
+        for (int i = 0; i < kQt; ++i) {
 #pragma unroll
-          for (int h = 0; h < 16; ++h) mx[qi][h] = warp_max(s[qi][h]);
+          for (int h = 0; h < 16; ++h) mx[i][h] = warp_max(s[i][h]);
         }
         if (lane == 0) {
           float4* dst = reinterpret_cast<float4*>(&ms->red_max[sb][warp][0]);
 #pragma unroll
-          for (int qi = 0; qi < kQ; ++qi) {
+          for (int i = 0; i < kQt; ++i) {
+            const int qi = q0 + i;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              dst[4 * qi + k] = make_float4(mx[qi][4 * k], mx[qi][4 * k + 1], mx[qi][4 * k + 2],
-                                            mx[qi][4 * k + 3]);
+              dst[4 * qi + k] = make_float4(mx[i][4 * k], mx[i][4 * k + 1], mx[i][4 * k + 2],
+                                            mx[i][4 * k + 3]);
           }
         }
-        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+        named_bar_sync(sg.bar, kSoftmaxThreads);
 #pragma unroll
-        for (int qi = 0; qi < kQ; ++qi) {
+        for (int i = 0; i < kQt; ++i) {
+          const int qi = q0 + i;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             float4 m4 = reinterpret_cast<const float4*>(&ms->red_max[sb][0][0])[4 * qi + k];
@@ -1844,18 +1909,18 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
               m4.x = fmaxf(m4.x, o4.x); m4.y = fmaxf(m4.y, o4.y);
               m4.z = fmaxf(m4.z, o4.z); m4.w = fmaxf(m4.w, o4.w);
             }
-            mx[qi][4 * k] = m4.x; mx[qi][4 * k + 1] = m4.y;
-            mx[qi][4 * k + 2] = m4.z; mx[qi][4 * k + 3] = m4.w;
+            mx[i][4 * k] = m4.x; mx[i][4 * k + 1] = m4.y;
+            mx[i][4 * k + 2] = m4.z; mx[i][4 * k + 3] = m4.w;
           }
           // The O rescale factors go to shared memory (every thread computes
           // the same ones), so that they hold no registers across the P work.
 #pragma unroll
           for (int h = 0; h < 16; ++h) {
             float alpha = 1.0f;
-            if (mx[qi][h] > m_ref[qi][h] + kRescaleThreshold) {
-              alpha = fast_exp2(m_ref[qi][h] - mx[qi][h]);  // 0 on a segment's first tile
-              m_ref[qi][h] = mx[qi][h];
-              l[qi][h] *= alpha;
+            if (mx[i][h] > m_ref[i][h] + kRescaleThreshold) {
+              alpha = fast_exp2(m_ref[i][h] - mx[i][h]);  // 0 on a segment's first tile
+              m_ref[i][h] = mx[i][h];
+              l[i][h] *= alpha;
               moved = true;
             }
             if (t == 0) ms->alpha_stage[16 * qi + h] = alpha;
@@ -1866,22 +1931,22 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
 
       // P row chunks of query token qi: e4m3 hi then lo (16 bytes each), or the
       // bf16 values of heads 0-7 then 8-15.
-      uint32_t phi[kQ][4], plo[kQ][4];
+      uint32_t phi[kQt][4], plo[kQt][4];
 #pragma unroll
-      for (int qi = 0; qi < kQ; ++qi) {
+      for (int i = 0; i < kQt; ++i) {
         float pr[16];
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
-          pr[h] = tok_ok[qi] ? fast_exp2(s[qi][h] - m_ref[qi][h]) : 0.0f;
-          l[qi][h] += pr[h];
+          pr[h] = tok_ok[i] ? fast_exp2(s[i][h] - m_ref[i][h]) : 0.0f;
+          l[i][h] += pr[h];
         }
         if constexpr (G::kSplit) {
-          split_p_16(pr, phi[qi], plo[qi]);
+          split_p_16(pr, phi[i], plo[i]);
         } else {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            phi[qi][k] = pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
-            plo[qi][k] = pack_bf16x2(pr[8 + 2 * k], pr[9 + 2 * k]);
+            phi[i][k] = pack_bf16x2(pr[2 * k], pr[2 * k + 1]);
+            plo[i][k] = pack_bf16x2(pr[8 + 2 * k], pr[9 + 2 * k]);
           }
         }
       }
@@ -1894,21 +1959,23 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         const uint32_t pa = sbase + G::kOffP + sb * G::kPBytes + token * G::kPRowBytes;
         const uint32_t sw = kQ == 1 ? (token >> 2) & 1 : (token >> 1) & 3;
 #pragma unroll
-        for (int qi = 0; qi < kQ; ++qi) {
-          st_shared_v4(pa + (((2 * qi) ^ sw) << 4), phi[qi][0], phi[qi][1], phi[qi][2], phi[qi][3]);
-          st_shared_v4(pa + (((2 * qi + 1) ^ sw) << 4), plo[qi][0], plo[qi][1], plo[qi][2], plo[qi][3]);
+        for (int i = 0; i < kQt; ++i) {
+          const int qi = q0 + i;
+          st_shared_v4(pa + (((2 * qi) ^ sw) << 4), phi[i][0], phi[i][1], phi[i][2], phi[i][3]);
+          st_shared_v4(pa + (((2 * qi + 1) ^ sw) << 4), plo[i][0], plo[i][1], plo[i][2], plo[i][3]);
         }
       }
       fence_proxy_async_smem();
       if (rescale_o) {  // the same for every softmax thread
         // O must hold every earlier tile before it is rescaled.
         wait_pv(tile - 1);
-        named_bar_sync(kBarSoftmax, kSoftmaxThreads);  // thread 0's alpha_stage is written
+        named_bar_sync(sg.bar, kSoftmaxThreads);  // thread 0's alpha_stage is written
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll
-          for (int qi = 0; qi < kQ; ++qi) {
+          for (int i = 0; i < kQt; ++i) {
+            const int qi = q0 + i;
             const uint32_t addr = tmem + lane_base + G::kColO + G::kN * cc + G::kTokCols * qi;
             if constexpr (G::kSplit) {
               uint32_t o[32];
@@ -1930,11 +1997,11 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         tmem_wait_st();
       }
       tc_fence_before();
-      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-      if (t == 0) st_release_u32(&ms->p_ready, tile + 1);
-      if (t == 0 && tile == 0) MLA_TRACE_CLK(kTrPReady);
-      if (t == 0 && cur.seg == 1 && tile == seg_first_tile) MLA_TRACE_CLK(kTrPReady1);
-      if (t == 0 && cur.seg == 0 && cur.j + 1 == cur.j1) MLA_TRACE_CLK(kTrPLast0);
+      named_bar_sync(sg.bar, kSoftmaxThreads);
+      if (t == 0) st_release_u32(&ms->p_ready[g], tile + 1);
+      if (lead && tile == 0) MLA_TRACE_CLK(kTrPReady);
+      if (lead && cur.seg == 1 && tile == seg_first_tile) MLA_TRACE_CLK(kTrPReady1);
+      if (lead && cur.seg == 0 && cur.j + 1 == cur.j1) MLA_TRACE_CLK(kTrPLast0);
       ++tile;
       if (cur.j + 1 == cur.j1) break;
       ++cur.j;
@@ -1949,9 +2016,9 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         tq_early = row_token(p, q_off, ldg_i32(p.qo_indptr + nxt.b), ldg_i32(p.qo_indptr + nxt.b + 1));
         // the QK of this segment's last tile has released the Q region
         softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), cur.seg & 1, ms, p.err);
-        prepare_q<kQ, kFmt>(p, ms, sbase + G::kOffQ, tq_early, nq, kv_scale, qk_scale);
-        if (t == 0) st_release_u32(&ms->q_ready, static_cast<uint32_t>(cur.seg + 2));
-        if (t == 0 && cur.seg == 0) MLA_TRACE_CLK(kTrQReady1);
+        prepare_q<kQ, kQt, kFmt>(p, ms, sbase + G::kOffQ, tq_early, nq, kv_scale, qk_scale, sg);
+        if (t == 0) st_release_u32(&ms->q_ready[g], static_cast<uint32_t>(cur.seg + 2));
+        if (lead && cur.seg == 0) MLA_TRACE_CLK(kTrQReady1);
         q_early = true;
       }
     }
@@ -1970,43 +2037,47 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         for (int i = t; i < kQ * kNumHeads * kQkDim * 2 / 128; i += kSoftmaxThreads) prefetch_l2(qn + 128 * i);
       }
     }
-    if (t == 0) ms->red_u32[4] = static_cast<uint32_t>(ms->abort_flag);
-    float l_tot[kQ][16];
+    if (t == 0) ms->red_u32[8 + g] = static_cast<uint32_t>(ms->abort_flag);
+    float l_tot[kQt][16];
 #pragma unroll
-    for (int qi = 0; qi < kQ; ++qi) {
+    for (int i = 0; i < kQt; ++i) {
       float v[16];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) v[h] = l[qi][h];
+      for (int h = 0; h < 16; ++h) v[h] = l[i][h];
       const float ws = warp_transpose_sum16(v);
-      if ((lane & 1) == 0) ms->red_sum[warp][16 * qi + (lane >> 1)] = ws;
+      if ((lane & 1) == 0) ms->red_sum[warp][16 * (q0 + i) + (lane >> 1)] = ws;
     }
-    named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+    named_bar_sync(sg.bar, kSoftmaxThreads);
 #pragma unroll
-    for (int qi = 0; qi < kQ; ++qi) {
+    for (int i = 0; i < kQt; ++i) {
+      const int qi = q0 + i;
 #pragma unroll
       for (int h = 0; h < 16; ++h)
-        l_tot[qi][h] = (ms->red_sum[0][16 * qi + h] + ms->red_sum[1][16 * qi + h]) +
-                       (ms->red_sum[2][16 * qi + h] + ms->red_sum[3][16 * qi + h]);
+        l_tot[i][h] = (ms->red_sum[0][16 * qi + h] + ms->red_sum[1][16 * qi + h]) +
+                      (ms->red_sum[2][16 * qi + h] + ms->red_sum[3][16 * qi + h]);
     }
-    const bool write = row_ok && ms->red_u32[4] == 0;  // the same for every softmax thread
+    const bool write = row_ok && ms->red_u32[8 + g] == 0;  // the same for every thread of the warpgroup
     // l >= 1 when the token saw a cached token here (its reference maximum
     // contributes 1): a fast divide suffices; l = 0 (nothing visible) gives 0.
-    float inv[kQ][16];
+    float inv[kQt][16];
 #pragma unroll
-    for (int qi = 0; qi < kQ; ++qi) {
+    for (int i = 0; i < kQt; ++i) {
 #pragma unroll
-      for (int h = 0; h < 16; ++h) inv[qi][h] = l_tot[qi][h] > 0.0f ? __fdividef(kv_scale, l_tot[qi][h]) : 0.0f;
+      for (int h = 0; h < 16; ++h) inv[i][h] = l_tot[i][h] > 0.0f ? __fdividef(kv_scale, l_tot[i][h]) : 0.0f;
     }
+    // this warpgroup's tokens that the CTA takes: q0 .. q0 + gn - 1
+    const int32_t gn = max(0, min(nq - q0, kQt));
     wait_pv(tile - 1);  // PV of the segment's last tile (and so of all before it)
     tc_fence_after();
-    if (t == 0 && cur.seg == 0) MLA_TRACE_CLK(kTrEpilogue);
+    if (lead && cur.seg == 0) MLA_TRACE_CLK(kTrEpilogue);
     const uint32_t stage_q = sbase + G::kOffQ;
     if (!kCluster && cur.whole) {
-      // bf16 rows [nq tokens][16 heads][512 dims] (16 KB each), staged in the Q region.
+      // bf16 rows [token][16 heads][512 dims] (16 KB each), staged in the Q region.
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll
-        for (int qi = 0; qi < kQ; ++qi) {
+        for (int i = 0; i < kQt; ++i) {
+          const int qi = q0 + i;
           if (qi >= nq) continue;  // the same for every softmax thread
           float o[16];
           tmem_ld_heads<kFmt>(tmem + lane_base + G::kColO + G::kN * cc + G::kTokCols * qi, o);
@@ -2014,15 +2085,15 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
           if (write) {
 #pragma unroll
             for (int h = 0; h < 16; ++h)
-              st_shared_u16(stage_q + ((16 * qi + h) * kVDim + dim) * 2, bf16_bits(o[h] * inv[qi][h]));
+              st_shared_u16(stage_q + ((16 * qi + h) * kVDim + dim) * 2, bf16_bits(o[h] * inv[i][h]));
           }
         }
       }
       fence_proxy_async_smem();
-      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-      if (t == 0 && write && MLA_DCHECK(tq + nq <= total_tokens(p), p.err)) {
-        bulk_store(p.out + static_cast<size_t>(tq) * kNumHeads * kVDim, stage_q,
-                   nq * kNumHeads * kVDim * 2);
+      named_bar_sync(sg.bar, kSoftmaxThreads);
+      if (t == 0 && write && gn > 0 && MLA_DCHECK(tq + q0 + gn <= total_tokens(p), p.err)) {
+        bulk_store(p.out + static_cast<size_t>(tq + q0) * kNumHeads * kVDim,
+                   stage_q + q0 * kNumHeads * kVDim * 2, gn * kNumHeads * kVDim * 2);
         bulk_commit();
       }
     } else {
@@ -2037,14 +2108,14 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
       const int32_t slot = kCluster ? static_cast<int32_t>(blockIdx.x) : partial_slot(c, ms->t0, cur.row_a);
       const size_t piece = static_cast<size_t>(slot) * p.slot_tokens + slot_q;  // (slot, token)
 #pragma unroll 1
-      for (int k = 0; k < 4 * nq; ++k) {
-        const int qi = k >> 2, cc = k & 3;
+      for (int k = 0; k < 4 * gn; ++k) {
+        const int i = kQt == 1 ? 0 : k >> 2, qi = q0 + i, cc = k & 3;
         float o[16];
         tmem_ld_heads<kFmt>(tmem + lane_base + G::kColO + G::kN * cc + G::kTokCols * qi, o);
         if (write) {
           float v[16];
 #pragma unroll
-          for (int h = 0; h < 16; ++h) v[h] = o[h] * inv[qi][h];
+          for (int h = 0; h < 16; ++h) v[h] = o[h] * inv[i][h];
           uint4* dst = reinterpret_cast<uint4*>(p.partial + ((piece + qi) * 4 + cc) * (kNumHeads * 128));
           const int64_t last = static_cast<int64_t>(((piece + qi) * 4 + cc) * (kNumHeads * 128)) +
                                (128 + token) * 8 + 8;
@@ -2056,33 +2127,34 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
                                               pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
         }
       }
-      if ((write || kCluster) && t < 16 * nq) {
-        // thread t writes the LSE of (token t / 16, head t % 16); -inf when it saw
-        // nothing (or, for the cluster split, when the call gave up: the piece is
-        // then not written and weighs 0)
+      if ((write || kCluster) && t < 16 * gn) {
+        // thread t writes the LSE of (token q0 + t / 16, head t % 16); -inf when
+        // it saw nothing (or, for the cluster split, when the call gave up: the
+        // piece is then not written and weighs 0)
         float mm = m_ref[0][0], ll = l_tot[0][0];
 #pragma unroll
-        for (int e = 1; e < 16 * kQ; ++e) {
+        for (int e = 1; e < 16 * kQt; ++e) {
           mm = t == e ? m_ref[e >> 4][e & 15] : mm;
           ll = t == e ? l_tot[e >> 4][e & 15] : ll;
         }
-        if (MLA_DCHECK(static_cast<int64_t>(piece) * kNumHeads + t < partial_elems(p) / kVDim, p.err))
-          p.lse[piece * kNumHeads + t] = write ? mm + log2f(ll) : -INFINITY;
+        const size_t at = (piece + q0) * kNumHeads + t;
+        if (MLA_DCHECK(static_cast<int64_t>(at) < partial_elems(p) / kVDim, p.err))
+          p.lse[at] = write ? mm + log2f(ll) : -INFINITY;
       }
     }
     // O has been read out (tcgen05.wait::ld above): the next segment's PV may
     // overwrite it.  Nothing else is published, so the flag is stored relaxed
     // and does not wait for the output stores to drain.
     tc_fence_before();
-    named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-    if (t == 0) st_relaxed_u32(&ms->o_free, static_cast<uint32_t>(cur.seg + 1));
-    if (t == 0 && cur.seg == 0) MLA_TRACE_CLK(kTrEpilogueDone);
+    named_bar_sync(sg.bar, kSoftmaxThreads);
+    if (t == 0) st_relaxed_u32(&ms->o_free[g], static_cast<uint32_t>(cur.seg + 1));
+    if (lead && cur.seg == 0) MLA_TRACE_CLK(kTrEpilogueDone);
     cursor_next_tile(cur, ms, p.kv_indptr, p.batch);
   }
   // The bulk stores have read their staging and written global memory before
   // the CTA exits.
   if (t == 0) bulk_wait_all();
-  if (t == 0) trace_shape(cur.seg + 1, static_cast<int32_t>(tile));
+  if (lead) trace_shape(cur.seg + 1, static_cast<int32_t>(tile));
 }
 
 // ------------------------------------------------------------ test hooks: the two-term operands
@@ -2106,7 +2178,7 @@ __global__ void __launch_bounds__(kSoftmaxThreads) debug_q_operand_kernel(const 
   const int32_t tq = static_cast<int32_t>(blockIdx.x) * kQ;
   const int32_t nq = min(kQ, tokens - tq);
   float qk_scale[kQ];
-  prepare_q<kQ, Kv::kE4m3>(p, ms, sq, tq, nq, __ldg(p.kv_scale), qk_scale);
+  prepare_q<kQ, kQ, Kv::kE4m3>(p, ms, sq, tq, nq, __ldg(p.kv_scale), qk_scale, single_softmax_group());
   constexpr int kChunks = kQkDim / 16;  // 16-byte chunks of an operand row
   for (int job = threadIdx.x; job < nq * 32 * kChunks; job += kSoftmaxThreads) {
     const int row = job / kChunks, ch = job % kChunks;  // row = 32 qi + 16 lo + head
@@ -2181,7 +2253,7 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
       mbar_init(smem_u32(&ms->pv_done[i]), 1);
     }
     mbar_init(smem_u32(&ms->q_empty), 1);
-    ms->q_ready = ms->s_read = ms->p_ready = ms->o_free = 0;
+    for (int g = 0; g < 2; ++g) ms->q_ready[g] = ms->s_read[g] = ms->p_ready[g] = ms->o_free[g] = 0;
     mbar_init(smem_u32(&ms->mma_done), 2);  // one commit from each MMA issuer
     ms->abort_flag = 0;
     ms->first_row = -1;
@@ -2219,16 +2291,21 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
   // An MXFP4 cache's e4m3 panels hold e2m1 * 2^(e - 127 - bias): its scale is
   // 2^bias.
   constexpr bool kWide = wide_block<kGather, kQ, kFmt>();
-  if (warp < 4) {
+  constexpr bool kDual = dual_softmax<kGather, kQ, kFmt>();
+  if (warp < 4 || (kDual && warp >= 8)) {
     if constexpr (kWide) setmaxnreg_inc<kSoftmaxRegs>();
+    if constexpr (kDual) setmaxnreg_inc<kDualSoftmaxRegs>();
     const float kv_scale = G::kMx ? __int_as_float((127 + p.mx_bias) << 23)
                                   : (G::kSplit ? __ldg(p.kv_scale) : 1.0f);
-    run_softmax<kQ, kFmt, kWide || kQ == 2, kCluster>(p, ms, sbase, tmem, kv_scale);
+    run_softmax<kQ, kFmt, kWide || kQ == 2, kCluster, kDual ? 2 : 1>(p, ms, sbase, tmem, kv_scale,
+                                                                      warp >= 8 ? 1 : 0);
   } else {
     if constexpr (G::kMx)
       setmaxnreg_dec<kOtherRegsMx>();
     else if constexpr (kWide)
       setmaxnreg_dec<kOtherRegs>();
+    else if constexpr (kDual)
+      setmaxnreg_dec<kDualOtherRegs>();
     const int who = kGather ? gather_producer_of_warp(warp, num_producers<kGather, kQ>())
                             : (warp == kProducerWarp ? 0 : -1);
     if (who >= 0) {
@@ -2239,9 +2316,9 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
     } else if (G::kMx && warp >= kFirstConverterWarp) {
       if constexpr (G::kMx) run_converter<kQ>(p, ms, sbase);
     } else if (warp == kMmaWarp && lane == 0) {
-      run_mma_pv<kQ, kFmt, kQ == 2 || kCluster>(p, ms, sbase, tmem);
+      run_mma_pv<kQ, kFmt, kQ == 2 || kCluster, kDual>(p, ms, sbase, tmem);
     } else if (warp == kMmaQkWarp && lane == 0) {
-      run_mma_qk<kQ, kFmt, kQ == 2 || kCluster>(p, ms, sbase, tmem);
+      run_mma_qk<kQ, kFmt, kQ == 2 || kCluster, kDual>(p, ms, sbase, tmem);
     } else if (!kCluster && cta_sibling(p) == 0 &&
                (kGather ? warp == kMmaWarp && lane == 1 : warp == kIdleWarp && lane == 0)) {
       write_worker_record<kQ>(p, ms);
