@@ -243,8 +243,9 @@ constexpr int kSoftmaxRegs = 240, kOtherRegs = 128;
 static_assert(128 * kSoftmaxRegs + 256 * kOtherRegs <= kStage1ThreadsGather * 168,
               "register split exceeds the launch allocation");
 // Two softmax warpgroups (12 warps, launched with 168 registers a thread):
-// 192 for each, 120 for the producer and MMA warpgroup.
-constexpr int kDualSoftmaxRegs = 192, kDualOtherRegs = 120;
+// 200 for each, 104 for the producer and MMA warpgroup (192 / 120 spilled
+// three times as many bytes in the softmax).
+constexpr int kDualSoftmaxRegs = 200, kDualOtherRegs = 104;
 static_assert(2 * 128 * kDualSoftmaxRegs + 128 * kDualOtherRegs <= kStage1ThreadsGather * 168,
               "two-warpgroup register split exceeds the launch allocation");
 // MXFP4 (16 warps, launched with 128 registers a thread): 240 for the softmax
@@ -486,6 +487,15 @@ __device__ __forceinline__ void zero_row(const Stage1Params& p, int32_t b) {
 // finds the worker's first row (tile 0's ring slots start empty), so that its
 // copies are in flight while the roles start; the producer begins with the
 // second tile.  Not used for an MXFP4 cache or the stall test hook.
+// L2 policy of the cache copies.  Every cached element is read once per call
+// (by one CTA, or by two siblings a few tiles apart), so its copies leave L2
+// first, before the code, query, index and partial lines that every call
+// touches again; siblings keep the normal priority, so that the second one's
+// copies still find the first one's lines.
+__device__ __forceinline__ uint64_t cache_policy(const Stage1Params& p) {
+  return p.siblings == 2 ? l2_policy_evict_normal() : l2_policy_evict_first();
+}
+
 template <int kQ, Kv kFmt>
 __device__ __forceinline__ void issue_first_tile(const Stage1Params& p, const CUtensorMap* map_v,
                                                  const CUtensorMap* map_r, Misc* ms, uint32_t sbase,
@@ -493,9 +503,10 @@ __device__ __forceinline__ void issue_first_tile(const Stage1Params& p, const CU
   using G = Geo<kQ, kFmt>;
   static_assert(G::kNumV >= 4, "tile 0 takes latent slots 0-3");
   if (!MLA_DCHECK(tok0 >= 0 && tok0 < p.kv_rows, p.err)) return;  // the producer then aborts
+  const uint64_t pol = cache_policy(p);
   const uint32_t rfull = smem_u32(&ms->r_full[0]);
   mbar_arrive_expect_tx(rfull, G::kRSlotBytes);
-  tma_load_2d(sbase + G::kOffR, map_r, kVDim * G::kElem, tok0, rfull);
+  tma_load_2d(sbase + G::kOffR, map_r, kVDim * G::kElem, tok0, rfull, pol);
   constexpr int kBoxes = G::kSplit ? 1 : 2;  // 128-byte-wide boxes per latent slot
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -504,7 +515,7 @@ __device__ __forceinline__ void issue_first_tile(const Stage1Params& p, const CU
 #pragma unroll
     for (int i = 0; i < kBoxes; ++i)
       tma_load_2d(sbase + G::kOffV + c * G::kVSlotBytes + i * kTileTokens * 128, map_v,
-                  128 * c * G::kElem + 128 * i, tok0, full);
+                  128 * c * G::kElem + 128 * i, tok0, full, pol);
   }
   ms->tile0_issued = 1;
 }
@@ -913,6 +924,7 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
   uint32_t tile = 0;
   uint32_t next_k = 0;  // one past the last panel this warp issued
   const bool tile0_issued = !kGather && ms->tile0_issued;  // by the prologue
+  const uint64_t pol = cache_policy(p);
   bool ok = true;
   while (cur.live && ok) {
     if (G::kNumV >= 8 && tile == kStartGateTile) {
@@ -988,7 +1000,7 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
         if (lane == 0) mbar_arrive_expect_tx(full, bytes);
         __syncwarp();
         tma_gather4(dst + lane * 4 * (bytes / kTileTokens), map, x, rows[0], rows[1], rows[2],
-                    rows[3], full);
+                    rows[3], full, pol);
       } else {
         // Boxes of one 128-byte-wide panel each: the whole slot for e4m3; for
         // bf16 64 dims, two per latent slot, 16 KB apart.
@@ -1003,7 +1015,7 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
         if (k == 0) MLA_TRACE_CLK(kTrFirstExpect);
         mbar_arrive_expect_tx(full, bytes);
         for (int i = 0; i < boxes; ++i)
-          tma_load_2d(dst + i * kTileTokens * 128, map, x + 128 * i, tok0, full);
+          tma_load_2d(dst + i * kTileTokens * 128, map, x + 128 * i, tok0, full, pol);
       }
       next_k = k + 1;
       if (k == 0 && lane == 0) MLA_TRACE_CLK(kTrFirstCopy);
@@ -1072,6 +1084,7 @@ __device__ void run_producer_mx(const Stage1Params& p, const CUtensorMap* map_v,
   if (p.stall_stream) cur.live = false;  // test hook: nothing is ever loaded
   uint32_t tile = 0;
   uint32_t v_fills = 0, r_fills = 0;  // latent / rope panels issued
+  const uint64_t pol = cache_policy(p);  // the elements' copies (the scale boxes overlap: unhinted)
   bool ok = true;
   while (cur.live && ok) {
     const int32_t tok0 = cur.kb + cur.j * kTileTokens;
@@ -1087,7 +1100,7 @@ __device__ void run_producer_mx(const Stage1Params& p, const CUtensorMap* map_v,
       const uint32_t full = smem_u32(&ms->rraw_full[slot]);
       mbar_arrive_expect_tx(full, kTileTokens * 32 + kSclSlotBytes);
       tma_load_2d(sbase + G::kOffR + slot * G::kRSlotBytes + G::kRRawOff, map_r, kVDim / 2, tok0,
-                  full);
+                  full, pol);
       const uint32_t sdst = sbase + G::kOffScl + (tile % kNumSclSlots) * kSclSlotBytes;
       const int32_t x0 = (18 * tok0) & ~15;  // the host bounds 18 * kv_rows well below 2^31
 #pragma unroll 1
@@ -1102,7 +1115,8 @@ __device__ void run_producer_mx(const Stage1Params& p, const CUtensorMap* map_v,
       if (!ok) break;
       const uint32_t full = smem_u32(&ms->raw_full[slot]);
       mbar_arrive_expect_tx(full, kTileTokens * 64);
-      tma_load_2d(sbase + G::kOffV + slot * G::kVSlotBytes + G::kVRawOff, map_v, 64 * c, tok0, full);
+      tma_load_2d(sbase + G::kOffV + slot * G::kVSlotBytes + G::kVRawOff, map_v, 64 * c, tok0, full,
+                  pol);
       v_fills = g + 1;
     }
     if (!ok) break;
