@@ -25,8 +25,9 @@ namespace mla {
 constexpr int kNumRSlots = 2;
 // warps 0-3 softmax/epilogue, 4 TMA producer, 5 PV MMA issuer, 6 QK MMA issuer;
 // page-table mode with one query token adds TMA producers in warps 7-11 (12
-// warps), an MXFP4 cache converter warps 8-15 (16 warps); registers rebalanced
-// with setmaxnreg in both.
+// warps), two query tokens on contiguous rows a second softmax warpgroup in
+// warps 8-11 (12 warps), an MXFP4 cache converter warps 8-15 (16 warps);
+// registers rebalanced with setmaxnreg in all three.
 constexpr int kStage1Threads = 256;
 constexpr int kStage1ThreadsGather = 384;
 constexpr int kStage1ThreadsMx = 512;  // MXFP4 cache: warps 8-15 convert its panels
