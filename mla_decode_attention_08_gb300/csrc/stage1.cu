@@ -121,6 +121,16 @@ struct Geo {
                                               : idesc_bf16(128, kN, true, true);
 };
 
+constexpr int kQParts = 5;  // parts of the Q operand, each with a barrier (see q_job)
+// The chunk order of the Q preparation (q_job): by parts on contiguous rows.
+// And whether the operand is published part by part (q_part_done), which
+// needs that order: also only with the QK issuer's loops rolled.  The softmax
+// and the issuer both decide by these.
+__device__ __forceinline__ bool q_panel_order(bool gather, const Stage1Params&) { return !gather; }
+__device__ __forceinline__ bool q_split(bool rolled, bool gather, const Stage1Params& p) {
+  return rolled && q_panel_order(gather, p);
+}
+
 struct Misc {
   uint64_t v_full[kMaxVSlots];
   uint64_t v_empty[kMaxVSlots];
@@ -130,11 +140,11 @@ struct Misc {
   uint64_t s_full[2];   // QK of tile i landed in S[i & 1]
   uint64_t pv_done[2];  // PV of tile i completed (P[i & 1] free again)
   uint64_t q_empty;     // the segment's last QK completed (Q operand free)
+  uint64_t q_part[kQParts];  // a part of the segment's Q operand is written (one phase per segment)
   uint64_t mma_done;
   // Monotonic counters the MMA issuers poll (st.release, then relaxed loads
   // followed by fence.acq_rel once a condition holds), one per softmax
   // warpgroup (the two-token kernels on contiguous rows run two).
-  uint32_t q_ready[2];  // segments whose Q operand is written
   uint32_t s_read[2];   // tiles whose S has been read out by every softmax warp
   uint32_t p_ready[2];  // tiles whose P is published (and O rescaled)
   uint32_t o_free[2];   // segments whose epilogue has read O out of TMEM
@@ -1414,24 +1424,32 @@ __device__ __forceinline__ bool spin_groups(const uint32_t (&ctr)[2], uint32_t t
 // product's issue waits behind the other's (issuing one product blocks the
 // issuing thread for about its execution time, ~1200 cycles).
 //
-// QK issuer (warp 6, lane 0): QK of tile i needs the segment's Q operand
-// (first tile of a segment) and S[i & 1] read out by the softmax of tile i - 2;
-// then each of its five slots is multiplied as soon as its copy has landed (the
-// issuer waits on the TMA barriers itself), so that the products overlap the
-// copies still in flight.
-template <int kQ, Kv kFmt, bool kRolled, bool kDual>
+// QK issuer (warp 6, lane 0): QK of tile i needs S[i & 1] read out by the
+// softmax of tile i - 2; then each of its five slots is multiplied as soon as
+// its copy has landed (the issuer waits on the TMA barriers itself), so that
+// the products overlap the copies still in flight, and, on the first tile of a
+// segment, as soon as the matching part of the segment's Q operand is written.
+template <bool kGather, int kQ, Kv kFmt, bool kRolled, bool kDual>
 __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem) {
   using G = Geo<kQ, kFmt>;
   Cursor qc;
   cursor_start(qc, ms);
   uint32_t qk_n = 0;  // tiles whose QK has been issued
+  const uint32_t qbars = smem_u32(&ms->q_part[0]);
   while (qc.live) {
     bool ok = true;
-    if (qc.j == qc.j0) ok = spin_groups<kDual>(ms->q_ready, static_cast<uint32_t>(qc.seg) + 1, ms, p.err);
+    // The segment's Q operand (one barrier phase per segment), on its first
+    // tile: part by part with the rolled issue loops (each part just before
+    // its products), whole otherwise (the last part's phase).
+    const bool qwait = qc.j == qc.j0;
+    const uint32_t qpar = static_cast<uint32_t>(qc.seg) & 1;
+    const bool by_part = q_split(kRolled, kGather, p);
+    if (!by_part && qwait) ok = wait_phase(qbars + 8 * (kQParts - 1), qpar, ms, p.err);
     if (ok && qk_n >= 2) ok = spin_groups<kDual>(ms->s_read, qk_n - 1, ms, p.err);
     if (ok) fence_acquire_cta();
     if (ok) ok = wait_phase(smem_u32(&ms->r_full[qk_n % kNumRSlots]), (qk_n / kNumRSlots) & 1, ms,
                             p.err);
+    if (by_part && ok && qwait) ok = wait_phase(qbars, qpar, ms, p.err);
     if (!ok) break;
     if (qk_n == 0) MLA_TRACE_CLK(kTrRopeLanded);
     tc_fence_after();
@@ -1440,6 +1458,7 @@ __device__ void run_mma_qk(const Stage1Params& p, Misc* ms, uint32_t sbase, uint
     auto latent = [&](int c) {
       const uint32_t g = qk_n * 4 + c;
       if (!wait_phase(smem_u32(&ms->v_full[g % G::kNumV]), (g / G::kNumV) & 1, ms, p.err)) return false;
+      if (by_part && qwait && !wait_phase(qbars + 8 * (1 + c), qpar, ms, p.err)) return false;
       tc_fence_after();
       issue_qk_latent<kQ, kFmt>(tmem, sbase, qk_n, c);
       return true;
@@ -1540,6 +1559,46 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
   return *reinterpret_cast<const uint16_t*>(&h);
 }
 
+// The Q operand is written in parts, in the order the QK issuer multiplies
+// them: part 0 the rope dims 512..575, part 1 + c the latent dims 128c ..
+// 128c + 127.  Each part has an mbarrier (Misc::q_part, one phase per segment)
+// that every softmax thread arrives on once its share of the part is written
+// and made visible to the tensor core's proxy, so that the first MMAs of a
+// segment run while later parts are still being converted.  In round r thread
+// t (of 128) takes one 16-dim chunk (ch) of one head of each of its tokens.
+// By parts (`panel`): rope chunk 32 + t % 4 of head t / 4 (threads 0-63), or
+// latent chunk 8 (r - 1) + t % 8 of head t / 8.  Otherwise the 16 x 36 chunks
+// in order, t + 128 r, which measured faster for the page-table kernel (the
+// ragged step 76.5 -> 74.4 us).
+__device__ __forceinline__ bool q_job(int t, int r, bool panel, int& head, int& ch) {
+  if (!panel) {
+    const int job = t + 128 * r;
+    head = job / 36;
+    ch = job % 36;
+    return job < 576;
+  }
+  if (r == 0) {
+    head = t >> 2;
+    ch = 32 + (t & 3);
+    return t < 64;
+  }
+  head = t >> 3;
+  ch = 8 * (r - 1) + (t & 7);
+  return true;
+}
+// Arrive on part r's barrier (bars: the first of Misc::q_part, or 0 for none).
+// Without `split` a thread arrives once, on the last part, after all of its
+// share, and the issuer waits for the whole operand: where the issue loops are
+// unrolled (one proxy fence per segment instead of five measured faster
+// there) and with a page table.  A thread arrives on the parts in order, so the
+// last part's phase completes only after every part's.  q_split is the one
+// rule both sides apply.
+__device__ __forceinline__ void q_part_done(uint32_t bars, int r, bool split) {
+  if (bars == 0 || (!split && r != kQParts - 1)) return;
+  fence_proxy_async_smem();
+  mbar_arrive(bars + 8 * r);
+}
+
 // Two-term e4m3 split of 16 floats x (|x| <= 448): hi = e4m3(x), lo = e4m3(16 (x - hi)),
 // so x ~= hi + lo / 16 with about 8 significant bits.  Packs codes 4 per word.
 __device__ __forceinline__ void split_e4m3_16(const float (&x)[16], uint32_t (&hi)[4],
@@ -1563,23 +1622,25 @@ __device__ __forceinline__ void split_e4m3_16(const float (&x)[16], uint32_t (&h
 // Q operand rows of a bf16 cache: the bf16 values themselves, row 16 qi + head.
 template <int kQ, int kQt>
 __device__ __forceinline__ void store_q_bf16(uint32_t sq, const uint4 (&raw)[kQt][5][2],
-                                             float (&qk_scale)[kQt], const SoftmaxGroup& sg) {
+                                             float (&qk_scale)[kQt], const SoftmaxGroup& sg,
+                                             uint32_t bars, bool panel, bool split) {
   const int t = sg.t;
   named_bar_sync(sg.pair, sg.pair_threads);
 #pragma unroll
-  for (int i = 0; i < kQt; ++i) {
-    const int qi = sg.q0 + i;
-    qk_scale[i] = kSmScaleLog2;
+  for (int i = 0; i < kQt; ++i) qk_scale[i] = kSmScaleLog2;
 #pragma unroll
-    for (int r = 0; r < 5; ++r) {
-      const int job = t + 128 * r;
-      if (job < 576) {
-        const int head = job / 36, ch = job % 36;  // ch: 16 dims = two 16-byte chunks
+  for (int r = 0; r < kQParts; ++r) {
+#pragma unroll
+    for (int i = 0; i < kQt; ++i) {
+      const int qi = sg.q0 + i;
+      int head, ch;  // ch: 16 dims = two 16-byte chunks
+      if (q_job(t, r, panel, head, ch)) {
         const uint4 a = raw[i][r][0], b = raw[i][r][1];
         st_shared_v4(q_chunk_addr<kQ, Kv::kBf16>(sq, 16 * qi + head, 2 * ch), a.x, a.y, a.z, a.w);
         st_shared_v4(q_chunk_addr<kQ, Kv::kBf16>(sq, 16 * qi + head, 2 * ch + 1), b.x, b.y, b.z, b.w);
       }
     }
+    q_part_done(bars, r, split);
   }
   fence_proxy_async_smem();
   named_bar_sync(sg.bar, kSoftmaxThreads);
@@ -1591,7 +1652,8 @@ __device__ __forceinline__ void store_q_bf16(uint32_t sq, const uint4 (&raw)[kQt
 template <int kQ, int kQt>
 __device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 (&raw)[kQt][5][2],
                                              float kv_scale, float (&qk_scale)[kQt],
-                                             const SoftmaxGroup& sg) {
+                                             const SoftmaxGroup& sg, uint32_t bars, int seg, bool panel,
+                                             bool split) {
   const int t = sg.t, warp = t >> 5, lane = t & 31;
 #pragma unroll
   for (int i = 0; i < kQt; ++i) {
@@ -1609,11 +1671,12 @@ __device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 
       }
     }
     amax = __reduce_max_sync(0xffffffffu, amax);
-    if (t == 0 && qi == 0 && ms->q_ready[0] == 0 && amax != 0xFFFFFFFFu) MLA_TRACE_CLK(kTrQLoaded);
-    if (t == 0 && qi == 0 && ms->q_ready[0] == 1 && amax != 0xFFFFFFFFu) MLA_TRACE_CLK(kTrQLoaded1);
+    if (t == 0 && qi == 0 && seg == 0 && amax != 0xFFFFFFFFu) MLA_TRACE_CLK(kTrQLoaded);
+    if (t == 0 && qi == 0 && seg == 1 && amax != 0xFFFFFFFFu) MLA_TRACE_CLK(kTrQLoaded1);
     if (lane == 0) ms->red_u32[4 * qi + warp] = amax;
   }
   named_bar_sync(sg.pair, sg.pair_threads);
+  float up[kQt];
 #pragma unroll
   for (int i = 0; i < kQt; ++i) {
     const int qi = sg.q0 + i;
@@ -1627,17 +1690,20 @@ __device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 
       k2 = (f <= 0.875f) ? 9 - e : 8 - e;
       k2 = min(max(k2, -126), 126);
     }
-    const float up = __int_as_float((k2 + 127) << 23);
+    up[i] = __int_as_float((k2 + 127) << 23);
     qk_scale[i] = __int_as_float((127 - k2) << 23) * kv_scale * kSmScaleLog2;
+  }
 #pragma unroll
-    for (int r = 0; r < 5; ++r) {
-      const int job = t + 128 * r;
-      if (job < 576) {
-        const int head = job / 36, ch = job % 36;
+  for (int r = 0; r < kQParts; ++r) {
+#pragma unroll
+    for (int i = 0; i < kQt; ++i) {
+      const int qi = sg.q0 + i;
+      int head, ch;
+      if (q_job(t, r, panel, head, ch)) {
         float x[16];
-        auto unpack = [&](uint32_t w, int i) {
-          x[2 * i] = u2f(w << 16) * up;
-          x[2 * i + 1] = u2f(w & 0xFFFF0000u) * up;
+        auto unpack = [&](uint32_t w, int k) {
+          x[2 * k] = u2f(w << 16) * up[i];
+          x[2 * k + 1] = u2f(w & 0xFFFF0000u) * up[i];
         };
         unpack(raw[i][r][0].x, 0); unpack(raw[i][r][0].y, 1);
         unpack(raw[i][r][0].z, 2); unpack(raw[i][r][0].w, 3);
@@ -1649,7 +1715,9 @@ __device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 
         st_shared_v4(q_chunk_addr<kQ, Kv::kE4m3>(sq, 32 * qi + 16 + head, ch), lo[0], lo[1], lo[2], lo[3]);
       }
     }
+    q_part_done(bars, r, split);
   }
+  // (every thread has read the |q| maxima before red_u32 is used again)
   fence_proxy_async_smem();
   named_bar_sync(sg.bar, kSoftmaxThreads);
 }
@@ -1659,20 +1727,19 @@ __device__ __forceinline__ void store_q_e4m3(Misc* ms, uint32_t sq, const uint4 
 // writes their rows of the Q operand of the cache format (kQ token columns).
 // Sets qk_scale[i], the factor turning the QK accumulator of token q0 + i into
 // base-2 softmax exponent units.  tq < 0 writes a zero query.  This thread's
-// share of each token (16-dim chunks `t + 128 r` of the 16 x 36 per token)
-// goes into registers first.
+// share of each token goes into registers first: in round r (q_job) one
+// 16-dim chunk of one head.
 template <int kQt>
 __device__ __forceinline__ void load_q(const Stage1Params& p, int t, int32_t tq, int32_t nq, int q0,
-                                       uint4 (&raw)[kQt][5][2]) {
+                                       bool panel, uint4 (&raw)[kQt][5][2]) {
 #pragma unroll
   for (int i = 0; i < kQt; ++i) {
     const int qi = q0 + i;
 #pragma unroll
-    for (int r = 0; r < 5; ++r) {
-      const int job = t + 128 * r;
+    for (int r = 0; r < kQParts; ++r) {
       raw[i][r][0] = raw[i][r][1] = make_uint4(0, 0, 0, 0);
-      if (job < 576 && tq >= 0 && qi < nq && MLA_DCHECK(tq + qi < total_tokens(p), p.err)) {
-        const int head = job / 36, ch = job % 36;
+      int head, ch;
+      if (q_job(t, r, panel, head, ch) && tq >= 0 && qi < nq && MLA_DCHECK(tq + qi < total_tokens(p), p.err)) {
         const uint4* src = reinterpret_cast<const uint4*>(
             p.q + (static_cast<size_t>(tq + qi) * kNumHeads + head) * kQkDim + ch * 16);
         raw[i][r][0] = __ldg(src);
@@ -1682,23 +1749,27 @@ __device__ __forceinline__ void load_q(const Stage1Params& p, int t, int32_t tq,
   }
 }
 
+// bars: the first of the Q part barriers to arrive on (0: none); seg: the
+// segment this operand serves (for the trace stamps); panel / split: the chunk
+// order and the publication by parts (q_job, q_part_done).
 template <int kQ, int kQt, Kv kFmt>
 __device__ void prepare_q(const Stage1Params& p, Misc* ms, uint32_t sq, int32_t tq, int32_t nq,
-                          float kv_scale, float (&qk_scale)[kQt], const SoftmaxGroup& sg) {
+                          float kv_scale, float (&qk_scale)[kQt], const SoftmaxGroup& sg,
+                          uint32_t bars, int seg, bool panel, bool split) {
   const bool lead = sg.t == 0 && sg.q0 == 0;
-  if (lead && ms->q_ready[0] == 1) MLA_TRACE_CLK(kTrQStart1);
+  if (lead && seg == 1) MLA_TRACE_CLK(kTrQStart1);
   uint4 raw[kQt][5][2];
-  load_q<kQt>(p, sg.t, tq, nq, sg.q0, raw);
-  if (lead && ms->q_ready[0] == 0) MLA_TRACE_CLK(kTrQIssued);
+  load_q<kQt>(p, sg.t, tq, nq, sg.q0, panel, raw);
+  if (lead && seg == 0) MLA_TRACE_CLK(kTrQIssued);
   // The previous segment's output rows may still be leaving the Q region
   // through bulk stores (the loads above are already in flight); the barrier
   // in the store below (both warpgroups', when there are two) orders every
   // write to it after these waits.
   if (sg.t == 0) bulk_wait_read<0>();
   if constexpr (kFmt == Kv::kBf16)
-    store_q_bf16<kQ, kQt>(sq, raw, qk_scale, sg);
+    store_q_bf16<kQ, kQt>(sq, raw, qk_scale, sg, bars, panel, split);
   else
-    store_q_e4m3<kQ, kQt>(ms, sq, raw, kv_scale, qk_scale, sg);
+    store_q_e4m3<kQ, kQt>(ms, sq, raw, kv_scale, qk_scale, sg, bars, seg, panel, split);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -1771,12 +1842,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // kQ, reads their S columns, writes their P chunks and Q rows and their O
 // columns, and publishes its own progress counters; the MMA issuers wait for
 // every warpgroup's.
-template <int kQ, Kv kFmt, bool kInlineWaits, bool kCluster, int kGroups>
+template <bool kGather, int kQ, Kv kFmt, bool kInlineWaits, bool kCluster, int kGroups>
 __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uint32_t tmem,
                             float kv_scale, int g) {
   using G = Geo<kQ, kFmt>;
   static_assert(kGroups == 1 || (kGroups == 2 && kQ == 2 && !kCluster), "two warpgroups take one token each");
   constexpr int kQt = kQ / kGroups;  // token columns of this warpgroup
+  // The Q operand is published part by part where the QK issuer's loops are
+  // rolled (two tokens, or the cluster split) on contiguous rows, whole
+  // otherwise; its chunks go by parts except with a page table (q_job,
+  // q_part_done).
+  const bool q_panel = q_panel_order(kGather, p);
+  const bool q_by_part = q_split(kQ == 2 || kCluster, kGather, p);
   const SoftmaxGroup sg{static_cast<int>(threadIdx.x) - 256 * g, g * kQt,
                         g ? kBarSoftmaxB : kBarSoftmax, kGroups == 2 ? kBarSoftmaxPair : kBarSoftmax,
                         kGroups == 2 ? 2u * kSoftmaxThreads : kSoftmaxThreads};
@@ -1823,8 +1900,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
     if (!row_ok && t == 0) set_error(p.err, MLA_DERR_QO_INDPTR);
     if (!q_early) {
       if (cur.seg > 0) softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), (cur.seg - 1) & 1, ms, p.err);
-      prepare_q<kQ, kQt, kFmt>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, nq, kv_scale, qk_scale, sg);
-      if (t == 0) st_release_u32(&ms->q_ready[g], static_cast<uint32_t>(cur.seg + 1));
+      prepare_q<kQ, kQt, kFmt>(p, ms, sbase + G::kOffQ, row_ok ? tq : -1, nq, kv_scale, qk_scale, sg,
+                               smem_u32(&ms->q_part[0]), cur.seg, q_panel, q_by_part);
       if (lead && cur.seg == 0) MLA_TRACE_CLK(kTrQReady);
       if (lead && cur.seg == 1) MLA_TRACE_CLK(kTrQReady1);
     }
@@ -2030,8 +2107,8 @@ __device__ void run_softmax(const Stage1Params& p, Misc* ms, uint32_t sbase, uin
         tq_early = row_token(p, q_off, ldg_i32(p.qo_indptr + nxt.b), ldg_i32(p.qo_indptr + nxt.b + 1));
         // the QK of this segment's last tile has released the Q region
         softmax_wait<kInlineWaits>(smem_u32(&ms->q_empty), cur.seg & 1, ms, p.err);
-        prepare_q<kQ, kQt, kFmt>(p, ms, sbase + G::kOffQ, tq_early, nq, kv_scale, qk_scale, sg);
-        if (t == 0) st_release_u32(&ms->q_ready[g], static_cast<uint32_t>(cur.seg + 2));
+        prepare_q<kQ, kQt, kFmt>(p, ms, sbase + G::kOffQ, tq_early, nq, kv_scale, qk_scale, sg,
+                                 smem_u32(&ms->q_part[0]), cur.seg + 1, q_panel, q_by_part);
         if (lead && cur.seg == 0) MLA_TRACE_CLK(kTrQReady1);
         q_early = true;
       }
@@ -2192,7 +2269,8 @@ __global__ void __launch_bounds__(kSoftmaxThreads) debug_q_operand_kernel(const 
   const int32_t tq = static_cast<int32_t>(blockIdx.x) * kQ;
   const int32_t nq = min(kQ, tokens - tq);
   float qk_scale[kQ];
-  prepare_q<kQ, kQ, Kv::kE4m3>(p, ms, sq, tq, nq, __ldg(p.kv_scale), qk_scale, single_softmax_group());
+  prepare_q<kQ, kQ, Kv::kE4m3>(p, ms, sq, tq, nq, __ldg(p.kv_scale), qk_scale, single_softmax_group(), 0, 0,
+                               true, false);
   constexpr int kChunks = kQkDim / 16;  // 16-byte chunks of an operand row
   for (int job = threadIdx.x; job < nq * 32 * kChunks; job += kSoftmaxThreads) {
     const int row = job / kChunks, ch = job % kChunks;  // row = 32 qi + 16 lo + head
@@ -2267,7 +2345,10 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
       mbar_init(smem_u32(&ms->pv_done[i]), 1);
     }
     mbar_init(smem_u32(&ms->q_empty), 1);
-    for (int g = 0; g < 2; ++g) ms->q_ready[g] = ms->s_read[g] = ms->p_ready[g] = ms->o_free[g] = 0;
+    // every thread of each softmax warpgroup arrives on every part
+    for (int i = 0; i < kQParts; ++i)
+      mbar_init(smem_u32(&ms->q_part[i]), kSoftmaxThreads * (dual_softmax<kGather, kQ, kFmt>() ? 2 : 1));
+    for (int g = 0; g < 2; ++g) ms->s_read[g] = ms->p_ready[g] = ms->o_free[g] = 0;
     mbar_init(smem_u32(&ms->mma_done), 2);  // one commit from each MMA issuer
     ms->abort_flag = 0;
     ms->first_row = -1;
@@ -2311,7 +2392,7 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
     if constexpr (kDual) setmaxnreg_inc<kDualSoftmaxRegs>();
     const float kv_scale = G::kMx ? __int_as_float((127 + p.mx_bias) << 23)
                                   : (G::kSplit ? __ldg(p.kv_scale) : 1.0f);
-    run_softmax<kQ, kFmt, kWide || kQ == 2, kCluster, kDual ? 2 : 1>(p, ms, sbase, tmem, kv_scale,
+    run_softmax<kGather, kQ, kFmt, kWide || kQ == 2, kCluster, kDual ? 2 : 1>(p, ms, sbase, tmem, kv_scale,
                                                                       warp >= 8 ? 1 : 0);
   } else {
     if constexpr (G::kMx)
@@ -2332,7 +2413,7 @@ __global__ void __launch_bounds__((stage1_threads<kGather, kQ, kFmt>()), 1)
     } else if (warp == kMmaWarp && lane == 0) {
       run_mma_pv<kQ, kFmt, kQ == 2 || kCluster, kDual>(p, ms, sbase, tmem);
     } else if (warp == kMmaQkWarp && lane == 0) {
-      run_mma_qk<kQ, kFmt, kQ == 2 || kCluster, kDual>(p, ms, sbase, tmem);
+      run_mma_qk<kGather, kQ, kFmt, kQ == 2 || kCluster, kDual>(p, ms, sbase, tmem);
     } else if (!kCluster && cta_sibling(p) == 0 &&
                (kGather ? warp == kMmaWarp && lane == 1 : warp == kIdleWarp && lane == 0)) {
       write_worker_record<kQ>(p, ms);
