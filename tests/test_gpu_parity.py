@@ -285,14 +285,18 @@ COMBINE_CASES = [
 ]
 
 
+@pytest.mark.parametrize("qo_len", [1, 2, 3])
 @pytest.mark.parametrize("name,lengths,paged,sms", COMBINE_CASES, ids=[c[0] for c in COMBINE_CASES])
-def test_combine_edge_cases_and_separate_stages(name, lengths, paged, sms):
+def test_combine_edge_cases_and_separate_stages(name, lengths, paged, sms, qo_len):
     """Rows split over many workers, workers with no tiles, rows without cached
-    tokens: mla_decode_fwd matches the oracle, and launching its two kernels
-    through mla_decode_stage1 / mla_decode_stage2 gives the same bits."""
-    inp = make_from_lengths(lengths, seed=99 + len(lengths), paged=paged, max_kv_len=max(max(lengths), 1))
+    tokens, with one to three query tokens per row (stage 2's four- and
+    eight-head kernels, sibling CTAs): mla_decode_fwd matches the oracle, and
+    launching its two kernels through mla_decode_stage1 / mla_decode_stage2
+    gives the same bits."""
+    inp = make_from_lengths(lengths, seed=99 + len(lengths), paged=paged, max_kv_len=max(max(lengths), 1),
+                            qo_len=qo_len)
     dev = DeviceCase(inp)
-    plan = binding.mla_decode_plan(inp.batch, inp.max_kv_len, sms)
+    plan = binding.mla_decode_plan(inp.batch, inp.max_kv_len, sms, qo_len=qo_len)
     ws = binding.new_workspace(plan)
     dev.out.fill_(float("nan"))
     gpu, err, _, _ = dev.run(plan=plan, workspace=ws)
