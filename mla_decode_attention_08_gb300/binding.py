@@ -321,7 +321,7 @@ TRACE_CTAS, TRACE_EVENTS, TRACE2_BLOCKS = 320, 40, 4096
 
 
 def mla_decode_trace_read(clear: bool = True):
-    """Trace builds only: (stage-1 stamps uint64 [320, 32], stage-2 stamps uint64 [4096, 3])."""
+    """Trace builds only: (stage-1 stamps uint64 [TRACE_CTAS, TRACE_EVENTS], stage-2 stamps uint64 [TRACE2_BLOCKS, 3])."""
     import numpy as np
     s1 = np.zeros((TRACE_CTAS, TRACE_EVENTS), dtype=np.uint64)
     s2 = np.zeros((TRACE2_BLOCKS, 3), dtype=np.uint64)
