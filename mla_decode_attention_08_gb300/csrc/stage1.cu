@@ -945,10 +945,10 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
       // of that slot is the first tile's only while the second tile fits in
       // other slots: a ring of 8 or more latent slots.  A shallower ring
       // bounds the look-ahead by itself.)
-      int w = 1;
-      if (lane == 0) w = wait_phase(smem_u32(&ms->v_full[3 % G::kNumV]), 0, ms, p.err);
-      if (kGather) w = __shfl_sync(0xffffffffu, w, 0);
-      ok = w != 0;
+      // (with a page table every lane of the warp waits: a wait run by lane 0
+      // alone leaves the warp diverged into the lanes' copies that follow)
+      const int w = wait_phase(smem_u32(&ms->v_full[3 % G::kNumV]), 0, ms, p.err);
+      ok = kGather ? __all_sync(0xffffffffu, w != 0) : w != 0;
       if (!ok) break;
     }
     const int32_t tok0 = cur.kb + cur.j * kTileTokens;
@@ -1003,9 +1003,9 @@ __device__ void run_producer(const Stage1Params& p, const CUtensorMap* map_v,
       }
       // The maps address the cache as bytes, so x is a byte offset into the row.
       if (kGather) {  // e4m3 only: one 128- or 64-byte-wide panel per slot
-        int w = 1;
-        if (lane == 0 && use > 0) w = wait_phase(empty, (use - 1) & 1, ms, p.err);
-        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+        int w = 1;  // every lane waits (see the start gate above)
+        if (use > 0) w = wait_phase(empty, (use - 1) & 1, ms, p.err);
+        ok = __all_sync(0xffffffffu, w != 0);
         if (!ok) break;
         if (lane == 0) mbar_arrive_expect_tx(full, bytes);
         __syncwarp();
